@@ -1,0 +1,365 @@
+// C-ABI layer: argument validation, the split-K planner and dispatch.
+//
+// Everything here is host code. Validation happens before the first launch,
+// so an error status means nothing was enqueued (the loud-failure rule of
+// "ROCm/rocm-libraries PR #11188", "Motivation": a silently wrong dW is the
+// failure being designed out). All sizes are 64-bit and checked for overflow.
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "conv_internal.h"
+
+namespace cig {
+namespace {
+
+int g_kernel_override = CONV_KERNEL_AUTO;
+
+bool mul_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_mul_overflow(a, b, out); }
+bool add_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_add_overflow(a, b, out); }
+
+int esize(int dt) { return dt == CONV_F32 ? 4 : 2; }
+
+uint64_t round256(uint64_t v) { return (v + 255u) & ~uint64_t(255u); }
+
+// Output extent floor((in + 2 pad - dil (f - 1) - 1) / stride) + 1, computed
+// with overflow checks; returns -1 on overflow, 0 when nothing fits.
+int64_t out_extent(int64_t in, int64_t pad, int64_t dil, int64_t f, int64_t stride) {
+  int64_t twice_pad, reach, span;
+  if (!mul_ok(2, pad, &twice_pad) || !mul_ok(dil, f - 1, &reach)) return -1;
+  if (!add_ok(in, twice_pad, &span)) return -1;
+  span = span - reach - 1;
+  if (span < 0) return 0;
+  return span / stride + 1;
+}
+
+conv_status validate(const conv_problem* p, Shape* out) {
+  if (!p) return CONV_ERR_INVALID_ARG;
+  if (p->n < 0 || p->h < 1 || p->w < 1 || p->c < 1 || p->k < 1 || p->r < 1 || p->s < 1)
+    return CONV_ERR_INVALID_ARG;
+  if (p->stride_h < 1 || p->stride_w < 1 || p->dil_h < 1 || p->dil_w < 1) return CONV_ERR_INVALID_ARG;
+  if (p->pad_h < 0 || p->pad_w < 0 || p->groups < 1) return CONV_ERR_INVALID_ARG;
+  if (p->c % p->groups != 0 || p->k % p->groups != 0) return CONV_ERR_INVALID_ARG;
+  if (p->in_dtype < CONV_F32 || p->in_dtype > CONV_F16) return CONV_ERR_INVALID_ARG;
+  if (p->out_dtype != CONV_F32 && p->out_dtype != p->in_dtype) return CONV_ERR_INVALID_ARG;
+  Shape s;
+  s.n = p->n; s.h = p->h; s.w = p->w; s.c = p->c; s.k = p->k; s.r = p->r; s.s = p->s;
+  s.sh = p->stride_h; s.sw = p->stride_w; s.ph = p->pad_h; s.pw = p->pad_w;
+  s.dh = p->dil_h; s.dw = p->dil_w; s.groups = p->groups;
+  s.cg = p->c / p->groups; s.kg = p->k / p->groups;
+  s.in_dt = p->in_dtype; s.out_dt = p->out_dtype;
+  s.ho = out_extent(s.h, s.ph, s.dh, s.r, s.sh);
+  s.wo = out_extent(s.w, s.pw, s.dw, s.s, s.sw);
+  if (s.ho < 0 || s.wo < 0) return CONV_ERR_OVERFLOW;
+  if (s.ho == 0 || s.wo == 0) return CONV_ERR_INVALID_ARG;
+  // Every element and byte count used anywhere must fit in int64 (with room
+  // for the 4-byte fp32 slabs).
+  int64_t t;
+  const int64_t xs[4] = {s.n, s.h, s.w, s.c};
+  const int64_t ws_[4] = {s.k, s.r, s.s, s.cg};
+  const int64_t ys[4] = {s.n, s.ho, s.wo, s.k};
+  const int64_t* lists[3] = {xs, ws_, ys};
+  for (auto* l : lists) {
+    t = 4;
+    for (int i = 0; i < 4; ++i)
+      if (!mul_ok(t, l[i], &t)) return CONV_ERR_OVERFLOW;
+  }
+  *out = s;
+  return CONV_OK;
+}
+
+Geometry geometry_of(conv_kernel k, const Shape& s, conv_dir dir) {
+  switch (k) {
+    case CONV_KERNEL_GENERIC: return geometry_generic(s, dir);
+    case CONV_KERNEL_WGRAD_1X1_FFMA: return dir == CONV_DIR_WGRAD ? geometry_wgrad1x1_ffma(s) : Geometry{};
+    case CONV_KERNEL_WGRAD_1X1_TF32X3: return dir == CONV_DIR_WGRAD ? geometry_wgrad1x1_tf32x3(s) : Geometry{};
+    case CONV_KERNEL_FWD_TC: return dir == CONV_DIR_FWD ? geometry_fwd_tc(s) : Geometry{};
+    case CONV_KERNEL_WGRAD_DEPTHWISE: return dir == CONV_DIR_WGRAD ? geometry_wgrad_depthwise(s) : Geometry{};
+    case CONV_KERNEL_WGRAD_GROUPED: return dir == CONV_DIR_WGRAD ? geometry_wgrad_grouped(s) : Geometry{};
+    default: return Geometry{};
+  }
+}
+
+// The kernel a call runs: the override if set, else the first fast kernel
+// that takes the problem, else the generic one.
+conv_status choose_kernel(const Shape& s, conv_dir dir, conv_kernel* kernel, Geometry* geo) {
+  if (g_kernel_override != CONV_KERNEL_AUTO) {
+    Geometry g = geometry_of((conv_kernel)g_kernel_override, s, dir);
+    if (!g.ok) return CONV_ERR_UNSUPPORTED;
+    *kernel = (conv_kernel)g_kernel_override;
+    *geo = g;
+    return CONV_OK;
+  }
+  static const conv_kernel wgrad_order[] = {CONV_KERNEL_WGRAD_1X1_TF32X3, CONV_KERNEL_WGRAD_1X1_FFMA,
+                                            CONV_KERNEL_WGRAD_DEPTHWISE, CONV_KERNEL_WGRAD_GROUPED,
+                                            CONV_KERNEL_GENERIC};
+  static const conv_kernel fwd_order[] = {CONV_KERNEL_FWD_TC, CONV_KERNEL_GENERIC};
+  const conv_kernel* order = dir == CONV_DIR_WGRAD ? wgrad_order : fwd_order;
+  const int count = dir == CONV_DIR_WGRAD ? 5 : 2;
+  for (int i = 0; i < count; ++i) {
+    Geometry g = geometry_of(order[i], s, dir);
+    if (g.ok) {
+      *kernel = order[i];
+      *geo = g;
+      return CONV_OK;
+    }
+  }
+  return CONV_ERR_UNSUPPORTED;
+}
+
+// Split-K degree: see resolve_split_k_for in conv_igemm.h. The forward
+// policy restates "feat(rocke): split-K forward implicit-GEMM convolution on
+// gfx1250" ("Auto-deduced degree"): split only a grid under half the target,
+// over a reduction at least 512 deep; a power of two toward the target, at
+// most 32, with at least 2 reduction blocks per slice; pointwise stays whole.
+conv_status resolve_degree(const Shape& s, conv_dir dir, const Geometry& g, int32_t request,
+                           int32_t sm_count, int32_t* degree) {
+  if (request < -1) return CONV_ERR_INVALID_ARG;
+  if (request == 0) {
+    *degree = 1;
+    return CONV_OK;
+  }
+  if (request > 0) {
+    const int64_t cap = g.blocks > 0 ? g.blocks : 1;
+    if ((int64_t)request > cap) return CONV_ERR_INVALID_ARG;
+    *degree = request;
+    return CONV_OK;
+  }
+  if (sm_count < 1) return CONV_ERR_INVALID_ARG;
+  const int64_t target = (int64_t)sm_count * g.ctas_per_sm;
+  int64_t d = 1;
+  if (dir == CONV_DIR_FWD) {
+    const bool pointwise = s.r == 1 && s.s == 1;
+    if (!pointwise && 2 * g.tiles < target && s.D() >= 512) {
+      while (2 * d <= 32 && g.tiles * (2 * d) <= target) d *= 2;
+      while (d > 1 && g.blocks < 2 * d) d /= 2;
+    }
+  } else if (g.tiles < target) {
+    d = target / g.tiles;
+    if (d > g.blocks / 2) d = g.blocks / 2;
+    if (d > 4096) d = 4096;
+    if (d < 1) d = 1;
+  }
+  *degree = (int32_t)d;
+  return CONV_OK;
+}
+
+conv_status make_plan(const conv_problem* prob, conv_dir dir, int32_t request, bool with_bias,
+                      int32_t sm_count, Plan* plan) {
+  if (dir != CONV_DIR_FWD && dir != CONV_DIR_WGRAD) return CONV_ERR_INVALID_ARG;
+  Plan p;
+  conv_status st = validate(prob, &p.sh);
+  if (st != CONV_OK) return st;
+  if (request < -1) return CONV_ERR_INVALID_ARG;
+  p.dir = dir;
+  p.with_bias = with_bias && dir == CONV_DIR_WGRAD;
+  st = choose_kernel(p.sh, dir, &p.kernel, &p.geo);
+  if (st != CONV_OK) return st;
+  st = resolve_degree(p.sh, dir, p.geo, request, sm_count, &p.split);
+  if (st != CONV_OK) return st;
+  p.out_elems = dir == CONV_DIR_FWD ? p.sh.y_elems() : p.sh.w_elems();
+  p.slab_bytes = p.bias_slab_bytes = 0;
+  if (p.split > 1) {
+    int64_t b;
+    if (!mul_ok(p.out_elems, 4, &b) || !mul_ok(b, p.split, &b)) return CONV_ERR_OVERFLOW;
+    p.slab_bytes = round256((uint64_t)b);
+    if (p.with_bias) p.bias_slab_bytes = round256((uint64_t)p.sh.k * 4u * (uint64_t)p.split);
+  }
+  *plan = p;
+  return CONV_OK;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+// Which stages a call enqueues.
+enum Stages { kStage1 = 1, kStage2 = 2, kBoth = 3 };
+
+conv_status run(const conv_problem* prob, conv_dir dir, const void* x, const void* b, void* out,
+                void* db, void* ws, uint64_t ws_bytes, int32_t split_k, void* stream, bool with_bias,
+                int stages) {
+  Shape sh;
+  conv_status st = validate(prob, &sh);
+  if (st != CONV_OK) return st;
+  if (dir != CONV_DIR_FWD && dir != CONV_DIR_WGRAD) return CONV_ERR_INVALID_ARG;
+  if (split_k < -1) return CONV_ERR_INVALID_ARG;
+  if (with_bias && dir != CONV_DIR_WGRAD) return CONV_ERR_INVALID_ARG;
+  const int64_t b_elems = dir == CONV_DIR_FWD ? sh.w_elems() : sh.y_elems();
+  const int64_t out_elems = dir == CONV_DIR_FWD ? sh.y_elems() : sh.w_elems();
+  const bool needs_inputs = (stages & kStage1) != 0;
+  if ((needs_inputs && sh.x_elems() > 0 && !x) || (needs_inputs && b_elems > 0 && !b) ||
+      (out_elems > 0 && !out) || (with_bias && !db))
+    return CONV_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(b) || !aligned16(out) || !aligned16(db) || !aligned16(ws))
+    return CONV_ERR_ALIGNMENT;
+  const int sms = current_sm_count();
+  if (sms < 1) return CONV_ERR_CUDA;
+  Plan plan;
+  st = make_plan(prob, dir, split_k, with_bias, sms, &plan);
+  if (st != CONV_OK) return st;
+  if (plan.ws_bytes() > 0 && (!ws || ws_bytes < plan.ws_bytes())) return CONV_ERR_WORKSPACE_TOO_SMALL;
+  if (out_elems == 0) return CONV_OK;  // an empty forward batch: nothing to write
+  Args a;
+  a.x = x;
+  a.b = b;
+  a.out = out;
+  a.db = plan.with_bias ? db : nullptr;
+  a.ws = plan.split > 1 ? static_cast<float*>(ws) : nullptr;
+  a.ws_bias = plan.split > 1 && plan.with_bias
+                  ? reinterpret_cast<float*>(static_cast<char*>(ws) + plan.slab_bytes)
+                  : nullptr;
+  a.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t err = cudaSuccess;
+  if (stages & kStage1) {
+    switch (plan.kernel) {
+      case CONV_KERNEL_GENERIC: err = launch_generic(plan, a); break;
+      case CONV_KERNEL_WGRAD_1X1_FFMA: err = launch_wgrad1x1_ffma(plan, a); break;
+      case CONV_KERNEL_WGRAD_1X1_TF32X3: err = launch_wgrad1x1_tf32x3(plan, a); break;
+      case CONV_KERNEL_FWD_TC: err = launch_fwd_tc(plan, a); break;
+      case CONV_KERNEL_WGRAD_DEPTHWISE: err = launch_wgrad_depthwise(plan, a); break;
+      case CONV_KERNEL_WGRAD_GROUPED: err = launch_wgrad_grouped(plan, a); break;
+      default: return CONV_ERR_UNSUPPORTED;
+    }
+    if (err != cudaSuccess) return CONV_ERR_CUDA;
+  }
+  if ((stages & kStage2) && plan.split > 1) {
+    err = launch_fold(plan, a);
+    if (err != cudaSuccess) return CONV_ERR_CUDA;
+  }
+  return CONV_OK;
+}
+
+}  // namespace
+
+int current_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return -1;
+  }
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  if (dev < 64) cached[dev] = sms;
+  return sms;
+}
+
+}  // namespace cig
+
+using namespace cig;
+
+extern "C" {
+
+const char* conv_status_string(conv_status status) {
+  switch (status) {
+    case CONV_OK: return "CONV_OK";
+    case CONV_ERR_INVALID_ARG: return "CONV_ERR_INVALID_ARG";
+    case CONV_ERR_UNSUPPORTED: return "CONV_ERR_UNSUPPORTED";
+    case CONV_ERR_WORKSPACE_TOO_SMALL: return "CONV_ERR_WORKSPACE_TOO_SMALL";
+    case CONV_ERR_OVERFLOW: return "CONV_ERR_OVERFLOW";
+    case CONV_ERR_ALIGNMENT: return "CONV_ERR_ALIGNMENT";
+    case CONV_ERR_CUDA: return "CONV_ERR_CUDA";
+  }
+  return "CONV_ERR_UNKNOWN";
+}
+
+conv_status conv_output_dims(const conv_problem* p, int64_t* ho, int64_t* wo) {
+  Shape s;
+  conv_status st = validate(p, &s);
+  if (st != CONV_OK) return st;
+  if (!ho || !wo) return CONV_ERR_INVALID_ARG;
+  *ho = s.ho;
+  *wo = s.wo;
+  return CONV_OK;
+}
+
+conv_status resolve_split_k_for(const conv_problem* p, conv_dir dir, int32_t request,
+                                int32_t sm_count, int32_t* degree) {
+  if (!degree) return CONV_ERR_INVALID_ARG;
+  Plan plan;
+  conv_status st = make_plan(p, dir, request, false, sm_count, &plan);
+  if (st == CONV_OK) *degree = plan.split;
+  return st;
+}
+
+conv_status resolve_split_k(const conv_problem* p, conv_dir dir, int32_t request, int32_t* degree) {
+  const int sms = current_sm_count();
+  if (sms < 1) return CONV_ERR_CUDA;
+  return resolve_split_k_for(p, dir, request, sms, degree);
+}
+
+conv_status conv_workspace_bytes_for(const conv_problem* p, conv_dir dir, int32_t split_k,
+                                     int32_t with_bias, int32_t sm_count, uint64_t* bytes) {
+  if (!bytes) return CONV_ERR_INVALID_ARG;
+  Plan plan;
+  conv_status st = make_plan(p, dir, split_k, with_bias != 0, sm_count, &plan);
+  if (st == CONV_OK) *bytes = plan.ws_bytes();
+  return st;
+}
+
+conv_status conv_workspace_bytes(const conv_problem* p, conv_dir dir, int32_t split_k,
+                                 int32_t with_bias, uint64_t* bytes) {
+  const int sms = current_sm_count();
+  if (sms < 1) return CONV_ERR_CUDA;
+  return conv_workspace_bytes_for(p, dir, split_k, with_bias, sms, bytes);
+}
+
+conv_status conv_describe_plan(const conv_problem* p, conv_dir dir, int32_t split_k,
+                               int32_t with_bias, int32_t sm_count, conv_plan_info* info) {
+  if (!info) return CONV_ERR_INVALID_ARG;
+  Plan plan;
+  conv_status st = make_plan(p, dir, split_k, with_bias != 0, sm_count, &plan);
+  if (st != CONV_OK) return st;
+  info->kernel = plan.kernel;
+  info->split_k = plan.split;
+  info->needs_fold = plan.split > 1;
+  info->ctas_per_sm = plan.geo.ctas_per_sm;
+  info->tiles = plan.geo.tiles;
+  info->reduction_blocks = plan.geo.blocks;
+  info->ctas = plan.geo.tiles * plan.split;
+  info->workspace_bytes = plan.ws_bytes();
+  return CONV_OK;
+}
+
+conv_status conv_fwd(const conv_problem* p, const void* x, const void* w, void* y, void* ws,
+                     uint64_t ws_bytes, int32_t split_k, void* stream) {
+  return run(p, CONV_DIR_FWD, x, w, y, nullptr, ws, ws_bytes, split_k, stream, false, kBoth);
+}
+
+conv_status conv_wgrad(const conv_problem* p, const void* x, const void* dy, void* dw, void* ws,
+                       uint64_t ws_bytes, int32_t split_k, void* stream) {
+  return run(p, CONV_DIR_WGRAD, x, dy, dw, nullptr, ws, ws_bytes, split_k, stream, false, kBoth);
+}
+
+conv_status conv_wgrad_bias(const conv_problem* p, const void* x, const void* dy, void* dw,
+                            void* db, void* ws, uint64_t ws_bytes, int32_t split_k, void* stream) {
+  return run(p, CONV_DIR_WGRAD, x, dy, dw, db, ws, ws_bytes, split_k, stream, true, kBoth);
+}
+
+conv_status conv_stage1(const conv_problem* p, conv_dir dir, const void* x, const void* b, void* out,
+                        void* db, void* ws, uint64_t ws_bytes, int32_t split_k, void* stream) {
+  return run(p, dir, x, b, out, db, ws, ws_bytes, split_k, stream, db != nullptr, kStage1);
+}
+
+conv_status conv_stage2(const conv_problem* p, conv_dir dir, void* out, void* db, void* ws,
+                        uint64_t ws_bytes, int32_t split_k, void* stream) {
+  return run(p, dir, nullptr, nullptr, out, db, ws, ws_bytes, split_k, stream, db != nullptr, kStage2);
+}
+
+int64_t conv_batch_split_count(int64_t n, int64_t max_n) {
+  if (n < 0 || max_n < 1) return -1;
+  if (n == 0) return 1;
+  return (n - 1) / max_n + 1;  // == (n + max_n - 1) / max_n without the overflow
+}
+
+conv_status conv_set_kernel_override(int32_t kernel) {
+  if (kernel < CONV_KERNEL_AUTO || kernel > CONV_KERNEL_WGRAD_GROUPED) return CONV_ERR_INVALID_ARG;
+  g_kernel_override = kernel;
+  return CONV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,83 @@
+// Internal host/device declarations shared by the C-ABI layer and the kernels.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "conv_igemm.h"
+
+namespace cig {
+
+// A validated problem with its derived extents.
+struct Shape {
+  int64_t n, h, w, c, k, r, s;
+  int64_t sh, sw, ph, pw, dh, dw, groups;
+  int64_t ho, wo, cg, kg;
+  int in_dt, out_dt;
+  __host__ __device__ int64_t P() const { return n * ho * wo; }  // wgrad reduction rows
+  __host__ __device__ int64_t D() const { return r * s * cg; }  // forward reduction depth
+  __host__ __device__ int64_t x_elems() const { return n * h * w * c; }
+  __host__ __device__ int64_t w_elems() const { return k * r * s * cg; }
+  __host__ __device__ int64_t y_elems() const { return n * ho * wo * k; }
+};
+
+// What a kernel needs the planner to know about it.
+struct Geometry {
+  bool ok = false;           // the kernel takes this problem
+  int64_t tiles = 0;         // output tiles (CTAs per slice)
+  int64_t blocks = 0;        // reduction blocks a slice is made of
+  int ctas_per_sm = 1;       // resident CTAs per SM (sets the auto target)
+};
+
+struct Plan {
+  Shape sh;
+  conv_dir dir;
+  conv_kernel kernel;
+  Geometry geo;
+  int32_t split;             // S
+  bool with_bias;
+  int64_t out_elems;         // E: elements of Y or dW
+  uint64_t slab_bytes;       // S*E*4 rounded to 256 (0 when S == 1)
+  uint64_t bias_slab_bytes;  // S*K*4 rounded to 256 (0 when S == 1 or no bias)
+  uint64_t ws_bytes() const { return slab_bytes + bias_slab_bytes; }
+};
+
+struct Args {
+  const void* x;
+  const void* b;   // W (forward) or dY (weight gradient)
+  void* out;       // Y or dW
+  void* db;        // bias gradient or nullptr
+  float* ws;       // slabs [S][E] (nullptr when S == 1)
+  float* ws_bias;  // bias slabs [S][K] (nullptr when S == 1 or no bias)
+  cudaStream_t stream;
+};
+
+// Reduction slice sigma of S over `blocks` blocks: [begin, end), balanced,
+// never empty when S <= blocks.
+__host__ __device__ inline int64_t slice_begin(int64_t blocks, int64_t S, int64_t sigma) {
+  return (blocks * sigma) / S;
+}
+
+// Kernel geometries (pure host functions).
+Geometry geometry_generic(const Shape& s, conv_dir dir);
+Geometry geometry_wgrad1x1_ffma(const Shape& s);
+Geometry geometry_wgrad1x1_tf32x3(const Shape& s);
+Geometry geometry_fwd_tc(const Shape& s);
+Geometry geometry_wgrad_depthwise(const Shape& s);
+Geometry geometry_wgrad_grouped(const Shape& s);
+
+// Launchers: enqueue stage 1 on a.stream. Return the launch status.
+cudaError_t launch_generic(const Plan& p, const Args& a);
+cudaError_t launch_wgrad1x1_ffma(const Plan& p, const Args& a);
+cudaError_t launch_wgrad1x1_tf32x3(const Plan& p, const Args& a);
+cudaError_t launch_fwd_tc(const Plan& p, const Args& a);
+cudaError_t launch_wgrad_depthwise(const Plan& p, const Args& a);
+cudaError_t launch_wgrad_grouped(const Plan& p, const Args& a);
+// Stage 2: out = cast(sum of slabs) (and the bias slabs into db).
+cudaError_t launch_fold(const Plan& p, const Args& a);
+
+// SM count of the current device (cached per device), or -1.
+int current_sm_count();
+
+}  // namespace cig

@@ -1,0 +1,194 @@
+/*
+ * conv_igemm.h — C ABI of the GB300 (sm_103a) NHWC implicit-GEMM convolution
+ * library: forward Y = conv(X, W), weight gradient dW and bias gradient db,
+ * each with deterministic two-stage split-K.
+ *
+ * Sources of the operations (web pages, cited by title and section):
+ *  [P1] "ROCm/rocm-libraries PR #11188" (MIOpen NHWC wgrad batch split):
+ *       "Motivation", "Technical Details", "Test Plan".
+ *  [P2] "feat(rocke): split-K forward implicit-GEMM convolution on gfx1250"
+ *       (PR #14393): "Two-stage split-K", "Auto-deduced degree",
+ *       "ABI, AOT and runtime", "Review follow-ups".
+ *  [P3] "perf(rocke): depthwise 7x7 and grouped cpg4/8 wgrad on batched
+ *       mfma 4x4x4" (PR #14157): "Technical Details".
+ *
+ * Conventions shared by every entry point
+ *  - Layouts are dense and contiguous: X [n][h][w][c], W and dW
+ *    [k][r][s][c/groups] (channels-last weight), Y and dY [n][ho][wo][k],
+ *    db [k]. Output channel k reads input channels g*Cg .. g*Cg+Cg-1 with
+ *    g = k / (k/groups) (contiguous groups; depthwise is groups = c = k).
+ *  - The operation is a cross-correlation:
+ *      Y[n,ho,wo,k]  = sum_{r,s,c<Cg} X[n, ho*sh + r*dh - ph, wo*sw + s*dw - pw, g*Cg + c] * W[k,r,s,c]
+ *      dW[k,r,s,c]   = sum_{n,ho,wo}  dY[n,ho,wo,k] * X[n, ho*sh + r*dh - ph, wo*sw + s*dw - pw, g*Cg + c]
+ *      db[k]         = sum_{n,ho,wo}  dY[n,ho,wo,k]
+ *    with X = 0 outside [0,h) x [0,w), and
+ *      ho extent = floor((h + 2 ph - dh (r - 1) - 1) / sh) + 1 (likewise wo).
+ *  - Every index and byte offset is 64-bit. A tensor larger than 4 GB is
+ *    handled in one call; there is no batch split and nothing wraps [P1].
+ *    A size whose byte count does not fit in int64 is rejected.
+ *  - Ownership: the caller owns every buffer (device memory for tensors and
+ *    workspace). The library allocates nothing, never synchronises, and
+ *    enqueues its kernels on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream). Pointers must be 16-byte aligned device pointers.
+ *  - Errors are loud [P1 "Motivation"]: every argument is checked before the
+ *    first launch, so a non-OK status means nothing was enqueued, except
+ *    CONV_ERR_CUDA, which reports a failed launch.
+ *  - Split-K [P2 "Two-stage split-K"]: the reduction (N*Ho*Wo for the weight
+ *    gradient, R*S*Cg for the forward) is cut into S slices. Stage 1 writes
+ *    one fp32 partial slab per slice into the caller's workspace, each
+ *    element exactly once, so the workspace needs no clearing and its
+ *    contents on entry do not matter. Stage 2 (the fold) sums the slabs in
+ *    the fixed order 0..S-1 and rounds once (round-to-nearest-even) into the
+ *    output type. No atomics are used: a call repeated with the same inputs
+ *    and the same degree gives bit-identical outputs. With S = 1 stage 1
+ *    writes the output directly and no workspace is needed.
+ *  - The degree request: -1 = auto (the policy of resolve_split_k), 0 = no
+ *    split (S = 1), n >= 1 = exactly n slices, which must not exceed the
+ *    number of reduction blocks of the chosen kernel (else
+ *    CONV_ERR_INVALID_ARG). Values below -1 are rejected [P2 "Review
+ *    follow-ups": split_k <= 0 is rejected there; this ABI keeps 0 = none].
+ */
+#ifndef CONV_IGEMM_H
+#define CONV_IGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum conv_status {
+  CONV_OK = 0,
+  CONV_ERR_INVALID_ARG = 1,          /* a NULL pointer, a bad size, dtype or degree */
+  CONV_ERR_UNSUPPORTED = 2,          /* a valid problem no kernel here takes */
+  CONV_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes < conv_workspace_bytes(...) */
+  CONV_ERR_OVERFLOW = 4,             /* a byte size does not fit in int64 */
+  CONV_ERR_ALIGNMENT = 5,            /* a pointer is not 16-byte aligned */
+  CONV_ERR_CUDA = 6                  /* a CUDA call failed (no device, launch error) */
+} conv_status;
+
+typedef enum conv_dtype { CONV_F32 = 0, CONV_BF16 = 1, CONV_F16 = 2 } conv_dtype;
+
+typedef enum conv_dir { CONV_DIR_FWD = 0, CONV_DIR_WGRAD = 1 } conv_dir;
+
+/* One convolution. in_dtype is the type of X and W (forward) or X and dY
+ * (weight gradient). out_dtype is the type of Y, or of dW and db; it must be
+ * CONV_F32 or in_dtype (the pages require a non-NULL output type [P2 "Review
+ * follow-ups"]). Sizes: n >= 0 (n = 0 gives dW = db = 0); h, w, c, k, r, s,
+ * strides, dilations, groups >= 1; pads >= 0; groups divides c and k; the
+ * output extent must be >= 1. */
+typedef struct conv_problem {
+  int64_t n, h, w, c, k, r, s;
+  int64_t stride_h, stride_w, pad_h, pad_w, dil_h, dil_w, groups;
+  int32_t in_dtype, out_dtype;
+} conv_problem;
+
+/* The kernels stage 1 can run. Chosen from the problem alone (never from
+ * timing), so a degree and a workspace size resolved ahead of a call hold for
+ * that call. */
+typedef enum conv_kernel {
+  CONV_KERNEL_AUTO = 0,
+  CONV_KERNEL_GENERIC = 1,           /* direct, CUDA cores: any shape and type */
+  CONV_KERNEL_WGRAD_1X1_FFMA = 2,    /* fp32 1x1 weight gradient, FFMA tiles */
+  CONV_KERNEL_WGRAD_1X1_TF32X3 = 3,  /* fp32 1x1 weight gradient, tcgen05 3xTF32 */
+  CONV_KERNEL_FWD_TC = 4,            /* 16-bit forward, tcgen05 + TMA im2col */
+  CONV_KERNEL_WGRAD_DEPTHWISE = 5,   /* depthwise weight gradient, CUDA cores */
+  CONV_KERNEL_WGRAD_GROUPED = 6      /* 4/8 channels per group, CUDA cores */
+} conv_kernel;
+
+/* What a call with these arguments would run. */
+typedef struct conv_plan_info {
+  int32_t kernel;            /* conv_kernel of stage 1 */
+  int32_t split_k;           /* resolved degree S >= 1 */
+  int32_t needs_fold;        /* 1 when stage 2 runs (S > 1) */
+  int32_t ctas_per_sm;       /* resident stage-1 CTAs per SM the policy assumes */
+  int64_t tiles;             /* output tiles of stage 1 */
+  int64_t reduction_blocks;  /* reduction blocks; a pinned degree may not exceed it */
+  int64_t ctas;              /* stage-1 CTAs = tiles * S */
+  uint64_t workspace_bytes;  /* bytes the call needs (0 when S = 1) */
+} conv_plan_info;
+
+/* Human-readable name of a status. Never NULL. */
+const char* conv_status_string(conv_status status);
+
+/* Output extent (ho, wo) of a problem after validation. */
+conv_status conv_output_dims(const conv_problem* p, int64_t* ho, int64_t* wo);
+
+/* Resolve a degree request for this problem on a GPU with sm_count SMs
+ * (pure host function). request -1 runs the auto policy
+ * [P2 "Auto-deduced degree"], restated for this hardware:
+ *  - target = sm_count x (resident stage-1 CTAs per SM of the chosen kernel);
+ *  - forward: split only when the unsplit grid is under half the target and
+ *    the reduction R*S*Cg is at least 512 deep, and never for a pointwise
+ *    (1x1) forward; the degree is the largest power of two <= 32 with
+ *    tiles x degree <= target, halved until every slice has >= 2 reduction
+ *    blocks;
+ *  - weight gradient (no policy on the pages): degree = floor(target / tiles)
+ *    when tiles < target, at most half the reduction blocks (>= 2 blocks per
+ *    slice) and at most 4096, else 1.
+ * request 0 gives 1; request n >= 1 gives n if n <= reduction blocks. */
+conv_status resolve_split_k_for(const conv_problem* p, conv_dir dir, int32_t request,
+                                int32_t sm_count, int32_t* degree);
+
+/* resolve_split_k_for on the current CUDA device (CONV_ERR_CUDA without one). */
+conv_status resolve_split_k(const conv_problem* p, conv_dir dir, int32_t request, int32_t* degree);
+
+/* Workspace bytes a call with this degree request needs: 0 when the degree
+ * resolves to 1, else S x E x 4 rounded up to 256 bytes (E = output elements),
+ * plus S x k x 4 (rounded up to 256) when with_bias and dir is the weight
+ * gradient. */
+conv_status conv_workspace_bytes_for(const conv_problem* p, conv_dir dir, int32_t split_k,
+                                     int32_t with_bias, int32_t sm_count, uint64_t* bytes);
+conv_status conv_workspace_bytes(const conv_problem* p, conv_dir dir, int32_t split_k,
+                                 int32_t with_bias, uint64_t* bytes);
+
+/* The full plan for a call (kernel, degree, grid, workspace) on sm_count SMs. */
+conv_status conv_describe_plan(const conv_problem* p, conv_dir dir, int32_t split_k,
+                               int32_t with_bias, int32_t sm_count, conv_plan_info* info);
+
+/* Forward [P2 "Two-stage split-K"]: y = conv(x, w). x, w in in_dtype, y in
+ * out_dtype. ws may be NULL when the resolved degree is 1. */
+conv_status conv_fwd(const conv_problem* p, const void* x, const void* w, void* y, void* ws,
+                     uint64_t ws_bytes, int32_t split_k, void* stream);
+
+/* Weight gradient [P1 "Motivation"; P3 "Technical Details"]: dw from x and
+ * dy, in out_dtype. */
+conv_status conv_wgrad(const conv_problem* p, const void* x, const void* dy, void* dw, void* ws,
+                       uint64_t ws_bytes, int32_t split_k, void* stream);
+
+/* Weight and bias gradient together [P1 "Motivation": weight.grad and
+ * bias.grad]: dw as conv_wgrad, db[k] = sum of dy over n, ho, wo, both in
+ * out_dtype, from one pass over dy. */
+conv_status conv_wgrad_bias(const conv_problem* p, const void* x, const void* dy, void* dw,
+                            void* db, void* ws, uint64_t ws_bytes, int32_t split_k, void* stream);
+
+/* The two stages of a call, enqueued separately [P2 "Two-stage split-K";
+ * "Benchmark": both stages are bound and launched one after the other].
+ * conv_stage1 followed by conv_stage2 on the same stream, with the same
+ * arguments, is exactly conv_fwd (dir = FWD, b = w, db = NULL), conv_wgrad
+ * (dir = WGRAD, b = dy, db = NULL) or conv_wgrad_bias (db != NULL).
+ * conv_stage1 writes the slabs (or, at degree 1, the outputs);
+ * conv_stage2 folds the slabs into out (and db) and enqueues nothing when the
+ * degree resolves to 1. Each validates all of its arguments. */
+conv_status conv_stage1(const conv_problem* p, conv_dir dir, const void* x, const void* b, void* out,
+                        void* db, void* ws, uint64_t ws_bytes, int32_t split_k, void* stream);
+conv_status conv_stage2(const conv_problem* p, conv_dir dir, void* out, void* db, void* ws,
+                        uint64_t ws_bytes, int32_t split_k, void* stream);
+
+/* Batch split count [P1 "Technical Details"]: the smallest m with
+ * m * max_n >= n, i.e. the integer ceiling (n + max_n - 1) / max_n, or 1 for
+ * n = 0. Returns -1 when n < 0 or max_n < 1. The library itself never splits
+ * a batch (all indexing is 64-bit); this is the exact form of the count for
+ * callers that must. */
+int64_t conv_batch_split_count(int64_t n, int64_t max_n);
+
+/* Testing aid: force stage 1 to one kernel (CONV_KERNEL_AUTO restores the
+ * normal choice). A forced kernel that cannot take a problem makes the call
+ * fail with CONV_ERR_UNSUPPORTED. Process-wide, not thread-safe. */
+conv_status conv_set_kernel_override(int32_t kernel);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONV_IGEMM_H */

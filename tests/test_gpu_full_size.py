@@ -1,0 +1,99 @@
+"""Full-size parity of the >4 GB 1x1 fp32 weight + bias gradient, in the launch
+configuration the bench times (auto split-K).
+
+The oracle computes a sample of the outputs one by one (16 of the 64 output
+channels, every input channel) plus the whole bias gradient, streaming the
+inputs sample by sample from the seeded generator. The last batch sample is
+also run alone at its >6 GB offset: the failure on the pages was a silently
+zero or wrong weight gradient once a dispatch addressed more than ~4 GB
+("ROCm/rocm-libraries PR #11188", "Motivation")."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import implicit_gemm_convolution_nhwc_gb300 as cig
+from gpu_util import oproblem, relerr
+
+pytestmark = pytest.mark.gpu
+
+C, K, HW = 96, 64, 512
+K_SAMPLE = (0, 16)
+
+
+def device_inputs(n, seed=1):
+    """X [n,512,512,96] and dY [n,512,512,64] fp32 ~ N(0,1), streamed to the device."""
+    x = torch.empty((n, HW, HW, C), dtype=torch.float32, device="cuda")
+    dy = torch.empty((n, HW, HW, K), dtype=torch.float32, device="cuda")
+    for t, tid in ((x, synth.X_ID), (dy, synth.DY_ID)):
+        per = t[0].numel()
+        stage = torch.empty(per, dtype=torch.float32, pin_memory=True)
+        for i in range(n):
+            synth.fill(stage, "normal", 0.0, 1.0, seed, tid, offset=i * per)
+            t[i].view(-1).copy_(stage)
+    return x, dy
+
+
+def oracle_rows(n_begin, n_end, seed=1, dw=None, db=None):
+    """Oracle dW rows K_SAMPLE and db over samples [n_begin, n_end), added into dw / db."""
+    orc = oracle.get()
+    p1 = oracle.Problem(n=1, h=HW, w=HW, c=C, k=K)
+    dw = np.zeros((K, 1, 1, C)) if dw is None else dw
+    db = np.zeros(K) if db is None else db
+    x = np.empty((1, HW, HW, C), np.float32)
+    dy = np.empty((1, HW, HW, K), np.float32)
+    for i in range(n_begin, n_end):
+        synth.fill(x, "normal", 0.0, 1.0, seed, synth.X_ID, offset=i * x.size)
+        synth.fill(dy, "normal", 0.0, 1.0, seed, synth.DY_ID, offset=i * dy.size)
+        orc.wgrad_acc(p1, x, dy, dw, K_SAMPLE)
+        orc.bgrad_acc(p1, dy, db)
+    return dw, db
+
+
+def gpu_wgrad(x, dy, n):
+    p = cig.Problem(n=n, h=HW, w=HW, c=C, k=K)
+    dw = torch.empty((K, 1, 1, C), device="cuda")
+    db = torch.empty(K, device="cuda")
+    ws = cig.workspace(p, cig.DIR_WGRAD, -1, True)
+    cig.conv_wgrad_bias(p, x, dy, dw, db, ws, -1)
+    torch.cuda.synchronize()
+    return dw.cpu(), db.cpu()
+
+
+def test_config2_n64_sampled_rows_and_last_sample():
+    x, dy = device_inputs(64)
+    assert x.numel() * 4 > 2 ** 32 and dy.numel() * 4 > 2 ** 32
+    dw, db = gpu_wgrad(x, dy, 64)
+    ref_w, ref_b = oracle_rows(0, 64)
+    k0, k1 = K_SAMPLE
+    assert relerr(dw[k0:k1], ref_w[k0:k1]) <= 1e-5
+    assert relerr(db, ref_b) <= 1e-5
+    # run-to-run bit identity at the same (auto) degree
+    dw2, db2 = gpu_wgrad(x, dy, 64)
+    assert torch.equal(dw, dw2) and torch.equal(db, db2)
+    # the last sample alone, read at its offset past 6 GB: non-zero and correct
+    last_w, last_b = gpu_wgrad(x[63:], dy[63:], 1)
+    ref_lw, ref_lb = oracle_rows(63, 64)
+    assert float(last_w[k0:k1].abs().max()) > 100.0
+    assert relerr(last_w[k0:k1], ref_lw[k0:k1]) <= 1e-5
+    assert relerr(last_b, ref_lb) <= 1e-5
+
+
+def test_config2_batch_sweep():
+    """N = 43, 59, ..., 187 (the pages' sweep range, step 16): every N against the oracle."""
+    ns = list(range(43, 193, 16))
+    free, _ = torch.cuda.mem_get_info()
+    need = ns[-1] * HW * HW * (C + K) * 4
+    if need > free * 0.9:
+        pytest.skip(f"needs {need / 1e9:.1f} GB of device memory")
+    x, dy = device_inputs(ns[-1])
+    dw_ref, db_ref = np.zeros((K, 1, 1, C)), np.zeros(K)
+    done = 0
+    k0, k1 = K_SAMPLE
+    for n in ns:
+        oracle_rows(done, n, dw=dw_ref, db=db_ref)  # the prefix sums, extended
+        done = n
+        dw, db = gpu_wgrad(x[:n], dy[:n], n)
+        assert relerr(dw[k0:k1], dw_ref[k0:k1]) <= 1e-5, n
+        assert relerr(db, db_ref) <= 1e-5, n

@@ -1,0 +1,162 @@
+"""GPU parity through the C ABI against the CPU oracle, element by element,
+on seeded inputs spanning several tiles with ragged tails; determinism;
+workspace needing no clearing; canaries around every output."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import implicit_gemm_convolution_nhwc_gb300 as cig
+from gpu_util import inputs, oproblem, relerr, run_fwd, run_wgrad, tol
+
+pytestmark = pytest.mark.gpu
+
+BF16, F16, F32 = cig.BF16, cig.F16, cig.F32
+
+
+@pytest.fixture(autouse=True)
+def _reset_override():
+    cig.set_kernel_override("auto")
+    yield
+    cig.set_kernel_override("auto")
+
+
+def _max_degree(p, d):
+    return cig.describe_plan(p, d, 1, sm_count=torch.cuda.get_device_properties(0).multi_processor_count)[
+        "reduction_blocks"]
+
+
+def check_wgrad(p, seed, kernels, splits, dist="normal", a=0.0, b=1.0, bias=True):
+    orc = oracle.get()
+    x, dy = inputs(p, seed, dist, a, b)
+    ref_w = orc.wgrad(oproblem(p), x, dy)
+    ref_b = orc.bgrad(oproblem(p), dy) if bias else None
+    for kern in kernels:
+        cig.set_kernel_override(kern)
+        for sk in splits:
+            if sk == "max":
+                sk = _max_degree(p, cig.DIR_WGRAD)
+            dw, db = run_wgrad(p, x, dy, sk, bias)
+            e = relerr(dw, ref_w)
+            assert e <= tol(p), f"{kern} split {sk}: dW err {e:.3e}"
+            if bias:
+                eb = relerr(db, ref_b)
+                assert eb <= tol(p), f"{kern} split {sk}: db err {eb:.3e}"
+    cig.set_kernel_override("auto")
+
+
+def check_fwd(p, seed, kernels, splits, dist="normal", a=0.0, b=1.0):
+    orc = oracle.get()
+    x, w = inputs(p, seed, dist, a, b, cig.DIR_FWD)
+    ref = orc.fwd(oproblem(p), x, w)
+    for kern in kernels:
+        cig.set_kernel_override(kern)
+        for sk in splits:
+            if sk == "max":
+                sk = _max_degree(p, cig.DIR_FWD)
+            y = run_fwd(p, x, w, sk)
+            e = relerr(y, ref)
+            assert e <= tol(p), f"{kern} split {sk}: Y err {e:.3e}"
+    cig.set_kernel_override("auto")
+
+
+# ---------------------------------------------------------------- 1x1 fp32
+
+
+def test_config1_exact():
+    """1x1 wgrad+db fp32, N=4, 16x16, C=8 -> K=16, uniform [-1, 1], seed 0."""
+    p = cig.Problem(n=4, h=16, w=16, c=8, k=16)
+    check_wgrad(p, 0, ["auto", "generic", "wgrad_1x1_ffma"], [-1, 0, 1, 2, 5, "max"], "uniform", -1.0, 1.0)
+
+
+@pytest.mark.parametrize("shape", [
+    dict(n=3, h=37, w=29, c=100, k=68),     # ragged rows, one c tile with a tail, two k tiles
+    dict(n=2, h=19, w=23, c=196, k=16),     # two c tiles (128 + 68)
+    dict(n=1, h=5, w=7, c=4, k=4),          # fewer rows than one block
+    dict(n=5, h=16, w=16, c=96, k=64),      # the large config's channels on a small image
+])
+def test_1x1_fp32_ragged(shape):
+    p = cig.Problem(**shape)
+    check_wgrad(p, 1, ["auto", "wgrad_1x1_ffma", "generic"], [-1, 1, 3, 17])
+
+
+def test_1x1_without_bias_and_empty_batch():
+    p = cig.Problem(n=2, h=9, w=9, c=32, k=32)
+    check_wgrad(p, 3, ["auto"], [-1, 1], bias=False)
+    empty = cig.Problem(n=0, h=9, w=9, c=32, k=32)
+    x, dy = inputs(empty, 3)
+    dw, db = run_wgrad(empty, x, dy, -1, True)
+    assert not dw.any() and not db.any()
+
+
+# ------------------------------------------------------------ generic path
+
+GENERIC_SHAPES = [
+    dict(n=2, h=7, w=9, c=6, k=4, r=3, s=2, stride_h=1, stride_w=2, pad_h=1, pad_w=0),
+    dict(n=1, h=8, w=8, c=8, k=6, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1, dil_h=2, groups=2),
+    dict(n=3, h=5, w=6, c=4, k=4, r=5, s=3, pad_h=2, pad_w=3, dil_w=2, groups=4),
+    dict(n=2, h=9, w=7, c=12, k=8, r=1, s=4, stride_h=3, pad_w=2, groups=4),
+]
+DTYPES = [(F32, F32), (BF16, BF16), (BF16, F32), (F16, F16), (F16, F32)]
+
+
+@pytest.mark.parametrize("shape", GENERIC_SHAPES)
+@pytest.mark.parametrize("dt", DTYPES, ids=lambda d: f"{d[0]}{d[1]}")
+def test_generic_wgrad(shape, dt):
+    p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
+    check_wgrad(p, 4, ["generic"], [-1, 0, 3])
+
+
+@pytest.mark.parametrize("shape", GENERIC_SHAPES)
+@pytest.mark.parametrize("dt", DTYPES, ids=lambda d: f"{d[0]}{d[1]}")
+def test_generic_fwd(shape, dt):
+    p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
+    check_fwd(p, 5, ["generic"], [-1, 0, 2])
+
+
+# ------------------------------------------------------------ determinism
+
+
+def test_repeated_runs_are_bit_identical():
+    for p, direction in [(cig.Problem(n=3, h=37, w=29, c=100, k=68), cig.DIR_WGRAD),
+                         (cig.Problem(n=2, h=9, w=7, c=12, k=8, r=3, s=3, pad_h=1, pad_w=1, groups=4,
+                                      in_dtype=BF16, out_dtype=BF16), cig.DIR_WGRAD),
+                         (cig.Problem(n=1, h=8, w=8, c=64, k=32, r=3, s=3, pad_h=1, pad_w=1,
+                                      in_dtype=BF16, out_dtype=BF16), cig.DIR_FWD)]:
+        x, other = inputs(p, 9, direction=direction)
+        for sk in (-1, 3):
+            if direction == cig.DIR_WGRAD:
+                outs = [run_wgrad(p, x, other, sk, True) for _ in range(3)]
+                for o in outs[1:]:
+                    assert torch.equal(o[0], outs[0][0]) and torch.equal(o[1], outs[0][1])
+            else:
+                outs = [run_fwd(p, x, other, sk) for _ in range(3)]
+                for o in outs[1:]:
+                    assert torch.equal(o, outs[0])
+
+
+# ---------------------------------------------------------------- errors
+
+
+def test_device_call_errors():
+    p = cig.Problem(n=2, h=16, w=16, c=8, k=16)
+    x, dy = inputs(p, 0)
+    xd, dyd = x.cuda(), dy.cuda()
+    dw = torch.empty((16, 1, 1, 8), device="cuda")
+    db = torch.empty(16, device="cuda")
+    need = cig.workspace_bytes(p, cig.DIR_WGRAD, 4, True)
+    small = torch.empty(need - 1, dtype=torch.uint8, device="cuda")
+    with pytest.raises(cig.ConvError) as e:
+        cig.conv_wgrad_bias(p, xd, dyd, dw, db, small, 4)
+    assert e.value.status == 3
+    with pytest.raises(cig.ConvError) as e:
+        cig.conv_wgrad_bias(p, xd, dyd, dw, db, None, 4)
+    assert e.value.status == 3
+    big = torch.empty(need + 4, dtype=torch.uint8, device="cuda")
+    with pytest.raises(cig.ConvError) as e:
+        cig.conv_wgrad_bias(p, xd, dyd, dw, db, big[4:], 4)
+    assert e.value.status == 5
+    flat = torch.empty(2 * 16 * 16 * 8 + 1, device="cuda")
+    with pytest.raises(cig.ConvError) as e:
+        cig.conv_wgrad_bias(p, flat[1:], dyd, dw, db, big[:need], 4)
+    assert e.value.status == 5

@@ -1,0 +1,187 @@
+"""Host-side logic of the C ABI, run without a GPU: exports, validation, the
+split-K planner, workspace arithmetic and the batch-split count."""
+import ctypes
+
+import pytest
+
+import implicit_gemm_convolution_nhwc_gb300 as cig
+from implicit_gemm_convolution_nhwc_gb300 import BF16, DIR_FWD, DIR_WGRAD, F16, F32, Problem
+
+SMS = 152
+
+CONFIG1 = Problem(n=4, h=16, w=16, c=8, k=16)
+CONFIG2 = Problem(n=64, h=512, w=512, c=96, k=64)
+CONFIG3 = Problem(n=1, h=14, w=14, c=2048, k=512, r=3, s=3, pad_h=1, pad_w=1, in_dtype=BF16, out_dtype=BF16)
+CONFIG4 = Problem(n=32, h=56, w=56, c=384, k=384, r=7, s=7, pad_h=3, pad_w=3, groups=384,
+                  in_dtype=BF16, out_dtype=BF16)
+CONFIG5A = Problem(n=64, h=28, w=28, c=512, k=512, r=3, s=3, pad_h=1, pad_w=1, groups=64,
+                   in_dtype=F16, out_dtype=F16)
+CONFIG5B = Problem(n=64, h=28, w=28, c=512, k=512, r=3, s=3, pad_h=1, pad_w=1, groups=128,
+                   in_dtype=F16, out_dtype=F16)
+CONFIGS = [(CONFIG1, DIR_WGRAD), (CONFIG2, DIR_WGRAD), (CONFIG3, DIR_FWD), (CONFIG4, DIR_WGRAD),
+           (CONFIG5A, DIR_WGRAD), (CONFIG5B, DIR_WGRAD)]
+
+
+@pytest.fixture(autouse=True)
+def _no_override():
+    cig.set_kernel_override("auto")
+    yield
+    cig.set_kernel_override("auto")
+
+
+def test_library_exports_every_declared_symbol():
+    import re
+    import os
+    lib = cig.load()
+    header = open(os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "conv_igemm.h")).read()
+    declared = set(re.findall(r"^\S.*?\b(\w+)\s*\(", header, re.M)) - {"if", "while"}
+    declared = {d for d in declared if d.startswith(("conv_", "resolve_"))}
+    assert declared == set(cig.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name)
+    assert lib.conv_status_string(0) == b"CONV_OK"
+    assert lib.conv_status_string(99) == b"CONV_ERR_UNKNOWN"
+
+
+def test_output_dims():
+    assert cig.output_dims(CONFIG3) == (14, 14)
+    assert cig.output_dims(CONFIG4) == (56, 56)
+    assert cig.output_dims(Problem(n=1, h=9, w=10, c=1, k=1, r=3, s=2, stride_h=2, stride_w=3,
+                                   pad_h=1, pad_w=0, dil_h=2, dil_w=1)) == (4, 3)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(n=-1), dict(h=0), dict(c=0), dict(k=0), dict(r=0), dict(stride_h=0), dict(dil_w=0),
+    dict(pad_h=-1), dict(groups=0), dict(groups=3), dict(in_dtype=3), dict(in_dtype=F16, out_dtype=BF16),
+    dict(h=2, w=2, r=5, s=5),
+])
+def test_validation_rejects(bad):
+    base = dict(n=2, h=8, w=8, c=8, k=4, r=3, s=3, pad_h=1, pad_w=1, groups=2)
+    base.update(bad)
+    with pytest.raises(cig.ConvError) as e:
+        cig.resolve_split_k(Problem(**base), DIR_WGRAD, -1, sm_count=SMS)
+    assert e.value.status == 1
+
+
+def test_overflow_is_loud():
+    huge = Problem(n=1 << 30, h=1 << 20, w=1 << 20, c=64, k=64)
+    with pytest.raises(cig.ConvError) as e:
+        cig.resolve_split_k(huge, DIR_WGRAD, -1, sm_count=SMS)
+    assert e.value.status == 4
+    with pytest.raises(cig.ConvError) as e:
+        cig.resolve_split_k(Problem(n=1, h=1 << 62, w=1, c=1, k=1, pad_h=1 << 62), DIR_FWD, 0, sm_count=SMS)
+    assert e.value.status == 4
+
+
+def test_degree_request_semantics():
+    p = CONFIG1
+    plan = cig.describe_plan(p, DIR_WGRAD, 1, sm_count=SMS)
+    assert cig.resolve_split_k(p, DIR_WGRAD, 0, sm_count=SMS) == 1
+    assert cig.resolve_split_k(p, DIR_WGRAD, 3, sm_count=SMS) == 3
+    blocks = plan["reduction_blocks"]
+    assert cig.resolve_split_k(p, DIR_WGRAD, blocks, sm_count=SMS) == blocks
+    for bad in (blocks + 1, -2, -100):
+        with pytest.raises(cig.ConvError) as e:
+            cig.resolve_split_k(p, DIR_WGRAD, bad, sm_count=SMS)
+        assert e.value.status == 1
+    with pytest.raises(cig.ConvError):
+        cig.resolve_split_k(p, 7, -1, sm_count=SMS)
+
+
+def test_auto_is_deterministic_and_within_bounds():
+    for p, d in CONFIGS:
+        for sms in (1, 2, 16, 148, 152, 160):
+            a = cig.describe_plan(p, d, -1, sm_count=sms)
+            b = cig.describe_plan(p, d, -1, sm_count=sms)
+            assert a == b
+            S = a["split_k"]
+            assert 1 <= S <= max(1, a["reduction_blocks"])
+            assert a["ctas"] == a["tiles"] * S
+            assert a["needs_fold"] == (S > 1)
+
+
+def test_forward_policy_properties():
+    """Forward auto degree ("Auto-deduced degree" of the split-K forward page):
+    power of two <= 32, 1 for a grid >= half the target, a reduction < 512 or
+    a pointwise problem, >= 2 reduction blocks per slice."""
+    shapes = [CONFIG3,
+              Problem(n=1, h=7, w=7, c=512, k=512, r=7, s=7, pad_h=3, pad_w=3, in_dtype=BF16, out_dtype=BF16),
+              Problem(n=1, h=14, w=14, c=2048, k=512, in_dtype=BF16, out_dtype=BF16),   # pointwise
+              Problem(n=1, h=14, w=14, c=16, k=64, r=3, s=3, pad_h=1, pad_w=1, in_dtype=BF16, out_dtype=BF16),
+              Problem(n=64, h=56, w=56, c=256, k=256, r=3, s=3, pad_h=1, pad_w=1, in_dtype=BF16, out_dtype=BF16)]
+    for p in shapes:
+        for sms in (8, 76, 152):
+            info = cig.describe_plan(p, DIR_FWD, -1, sm_count=sms)
+            S, tiles, blocks = info["split_k"], info["tiles"], info["reduction_blocks"]
+            target = sms * info["ctas_per_sm"]
+            depth = p.r * p.s * (p.c // p.groups)
+            assert S & (S - 1) == 0 and S <= 32
+            if p.r == 1 and p.s == 1 or 2 * tiles >= target or depth < 512:
+                assert S == 1
+            else:
+                assert tiles * S <= target and blocks >= 2 * S
+                assert S == 32 or tiles * 2 * S > target or blocks < 4 * S
+
+
+def test_wgrad_policy_fills_the_gpu_in_whole_waves():
+    info = cig.describe_plan(CONFIG2, DIR_WGRAD, -1, with_bias=True, sm_count=SMS)
+    target = SMS * info["ctas_per_sm"]
+    assert info["ctas"] <= target and info["ctas"] > target - info["tiles"]
+    assert info["reduction_blocks"] >= 2 * info["split_k"]
+
+
+def test_workspace_bytes_arithmetic():
+    for p, d in CONFIGS:
+        for req in (-1, 0, 1, 2, 5):
+            for bias in (False, True):
+                info = cig.describe_plan(p, d, req, with_bias=bias, sm_count=SMS)
+                S = info["split_k"]
+                ho, wo = p.out_hw
+                E = p.n * ho * wo * p.k if d == DIR_FWD else p.k * p.r * p.s * (p.c // p.groups)
+                r256 = lambda v: (v + 255) // 256 * 256  # noqa: E731
+                want = 0 if S == 1 else r256(S * E * 4) + (r256(S * p.k * 4) if bias and d == DIR_WGRAD else 0)
+                assert info["workspace_bytes"] == want
+                assert cig.workspace_bytes(p, d, req, bias, sm_count=SMS) == want
+
+
+def test_empty_batch_plans_one_slice():
+    p = Problem(n=0, h=8, w=8, c=8, k=8)
+    assert cig.resolve_split_k(p, DIR_WGRAD, -1, sm_count=SMS) == 1
+    assert cig.resolve_split_k(p, DIR_WGRAD, 1, sm_count=SMS) == 1
+    with pytest.raises(cig.ConvError):
+        cig.resolve_split_k(p, DIR_WGRAD, 2, sm_count=SMS)
+
+
+def test_batch_split_count_exhaustive():
+    """Exact integer ceiling (PR #11188, "Technical Details"): minimal m with m * max_n >= n."""
+    for n in range(0, 2001):
+        for max_n in range(1, 2001, 7):
+            m = cig.batch_split_count(n, max_n)
+            assert m * max_n >= n and (m == 1 or (m - 1) * max_n < n)
+    assert cig.batch_split_count(-1, 3) == -1 and cig.batch_split_count(3, 0) == -1
+    big = (1 << 62) + 1
+    assert cig.batch_split_count(big, 1 << 61) == 3
+
+
+def test_kernel_override():
+    assert cig.describe_plan(CONFIG1, DIR_WGRAD, -1, sm_count=SMS)["kernel_name"] != "generic"
+    cig.set_kernel_override("generic")
+    assert cig.describe_plan(CONFIG1, DIR_WGRAD, -1, sm_count=SMS)["kernel_name"] == "generic"
+    cig.set_kernel_override("wgrad_1x1_ffma")
+    with pytest.raises(cig.ConvError) as e:
+        cig.describe_plan(CONFIG3, DIR_FWD, -1, sm_count=SMS)
+    assert e.value.status == 2
+    with pytest.raises(cig.ConvError):
+        cig.set_kernel_override(42)
+
+
+def test_calls_validate_before_touching_the_device():
+    lib = cig.load()
+    p = cig._cp(CONFIG1)
+    null = ctypes.c_void_p(0)
+    # NULL problem, NULL tensors, misaligned pointer: rejected without a device
+    assert lib.conv_wgrad(None, null, null, null, null, 0, -1, null) == 1
+    assert lib.conv_wgrad(p, null, null, null, null, 0, -1, null) == 1
+    assert lib.conv_wgrad_bias(p, 16, 16, 16, None, None, 0, -1, None) == 1
+    assert lib.conv_fwd(p, 18, 32, 32, None, 0, -1, None) == 5
+    assert lib.conv_wgrad(p, 16, 16, 16, None, 0, -3, None) == 1
