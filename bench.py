@@ -278,6 +278,9 @@ def run_ours(a, rank, world, local_rank):
     if a.kernel != "auto":
         cig.set_kernel_override(a.kernel)
     kw, direction, dist, args, seed, desc = WORKLOADS[a.workload]
+    if a.batch:
+        kw = dict(kw, n=a.batch)
+        desc = f"{desc} [batch overridden to N={a.batch}]"
     p = cig.Problem(**kw)
     d = cig.DIR_FWD if direction == "fwd" else cig.DIR_WGRAD
     bias = direction == "wgrad"
@@ -493,6 +496,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--batch", type=int, default=0, help="override N (small cases for profiling)")
     a = ap.parse_args()
     if a.warmup < 3:
         a.warmup = 3

@@ -25,7 +25,7 @@ STATUS = ["CONV_OK", "CONV_ERR_INVALID_ARG", "CONV_ERR_UNSUPPORTED", "CONV_ERR_W
 EXPORTS = ["conv_status_string", "conv_output_dims", "resolve_split_k_for", "resolve_split_k",
            "conv_workspace_bytes_for", "conv_workspace_bytes", "conv_describe_plan", "conv_fwd",
            "conv_wgrad", "conv_wgrad_bias", "conv_stage1", "conv_stage2", "conv_batch_split_count",
-           "conv_set_kernel_override"]
+           "conv_device_errors", "conv_set_kernel_override"]
 
 
 class ConvError(RuntimeError):
@@ -117,6 +117,7 @@ def load(build_if_missing: bool = True):
         "conv_stage2": ([P, ctypes.c_int, V, V, V, U64, I32, V], ctypes.c_int),
         "conv_batch_split_count": ([I64, I64], I64),
         "conv_set_kernel_override": ([I32], ctypes.c_int),
+        "conv_device_errors": ([ctypes.POINTER(ctypes.c_uint32), I32], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -268,3 +269,10 @@ def conv_stage2(p: Problem, direction: int, out, db=None, ws=None, split_k: int 
     st = load().conv_stage2(_cp(p), direction, _ptr(out), _ptr(db), _ptr(ws), 0 if ws is None else ws.numel(),
                             split_k, _stream(stream))
     _check(st, "conv_stage2")
+
+
+def device_errors(clear: bool = True) -> int:
+    """The device error word (bit 0: a pipeline wait timed out); synchronous."""
+    v = ctypes.c_uint32()
+    _check(load().conv_device_errors(ctypes.byref(v), int(clear)), "conv_device_errors")
+    return v.value

@@ -182,6 +182,12 @@ conv_status conv_stage2(const conv_problem* p, conv_dir dir, void* out, void* db
  * callers that must. */
 int64_t conv_batch_split_count(int64_t n, int64_t max_n);
 
+/* Device-side error word of the current device (synchronous read). The
+ * tensor-core kernels bound every pipeline wait; a wait that gives up sets
+ * bit 0 (1 = a pipeline wait timed out; that call's outputs are invalid) and
+ * the kernel ends early instead of hanging. clear != 0 resets the word. */
+conv_status conv_device_errors(uint32_t* flags, int32_t clear);
+
 /* Testing aid: force stage 1 to one kernel (CONV_KERNEL_AUTO restores the
  * normal choice). A forced kernel that cannot take a problem makes the call
  * fail with CONV_ERR_UNSUPPORTED. Process-wide, not thread-safe. */

@@ -33,9 +33,11 @@ def check_wgrad(p, seed, kernels, splits, dist="normal", a=0.0, b=1.0, bias=True
     ref_b = orc.bgrad(oproblem(p), dy) if bias else None
     for kern in kernels:
         cig.set_kernel_override(kern)
+        top = _max_degree(p, cig.DIR_WGRAD)
         for sk in splits:
-            if sk == "max":
-                sk = _max_degree(p, cig.DIR_WGRAD)
+            sk = top if sk == "max" else sk
+            if sk > top:  # more slices than reduction blocks: rejected, checked elsewhere
+                continue
             dw, db = run_wgrad(p, x, dy, sk, bias)
             e = relerr(dw, ref_w)
             assert e <= tol(p), f"{kern} split {sk}: dW err {e:.3e}"
@@ -51,9 +53,11 @@ def check_fwd(p, seed, kernels, splits, dist="normal", a=0.0, b=1.0):
     ref = orc.fwd(oproblem(p), x, w)
     for kern in kernels:
         cig.set_kernel_override(kern)
+        top = _max_degree(p, cig.DIR_FWD)
         for sk in splits:
-            if sk == "max":
-                sk = _max_degree(p, cig.DIR_FWD)
+            sk = top if sk == "max" else sk
+            if sk > top:
+                continue
             y = run_fwd(p, x, w, sk)
             e = relerr(y, ref)
             assert e <= tol(p), f"{kern} split {sk}: Y err {e:.3e}"
@@ -67,6 +71,7 @@ def test_config1_exact():
     """1x1 wgrad+db fp32, N=4, 16x16, C=8 -> K=16, uniform [-1, 1], seed 0."""
     p = cig.Problem(n=4, h=16, w=16, c=8, k=16)
     check_wgrad(p, 0, ["auto", "generic", "wgrad_1x1_ffma"], [-1, 0, 1, 2, 5, "max"], "uniform", -1.0, 1.0)
+    assert cig.device_errors() == 0
 
 
 @pytest.mark.parametrize("shape", [
@@ -74,10 +79,16 @@ def test_config1_exact():
     dict(n=2, h=19, w=23, c=196, k=16),     # two c tiles (128 + 68)
     dict(n=1, h=5, w=7, c=4, k=4),          # fewer rows than one block
     dict(n=5, h=16, w=16, c=96, k=64),      # the large config's channels on a small image
+    dict(n=2, h=33, w=31, c=40, k=36),      # tensor-core tile with channel tails in both operands
+    dict(n=3, h=8, w=8, c=128, k=128),      # two k tiles, one full 128-wide c tile
 ])
 def test_1x1_fp32_ragged(shape):
     p = cig.Problem(**shape)
-    check_wgrad(p, 1, ["auto", "wgrad_1x1_ffma", "generic"], [-1, 1, 3, 17])
+    kernels = ["auto", "wgrad_1x1_ffma", "generic"]
+    if p.c >= 32 and p.k >= 32 and p.h * p.w >= 32:
+        kernels.append("wgrad_1x1_tf32x3")
+    check_wgrad(p, 1, kernels, [-1, 1, 3, 17])
+    assert cig.device_errors() == 0
 
 
 def test_1x1_without_bias_and_empty_batch():
@@ -124,7 +135,7 @@ def test_repeated_runs_are_bit_identical():
                          (cig.Problem(n=1, h=8, w=8, c=64, k=32, r=3, s=3, pad_h=1, pad_w=1,
                                       in_dtype=BF16, out_dtype=BF16), cig.DIR_FWD)]:
         x, other = inputs(p, 9, direction=direction)
-        for sk in (-1, 3):
+        for sk in (-1, min(3, _max_degree(p, direction))):
             if direction == cig.DIR_WGRAD:
                 outs = [run_wgrad(p, x, other, sk, True) for _ in range(3)]
                 for o in outs[1:]:
