@@ -10,62 +10,64 @@
 //
 // Precision: a tf32 operand keeps 10 explicit mantissa bits. Every fp32 input
 // v is split as hi = v with its low 13 mantissa bits cleared (exact in tf32)
-// and lo = v - hi (exact in fp32, then rounded to tf32 by the unit). The tile
-// computes [dY_hi; dY_lo]^T x [X_hi | X_lo] as ONE M=128 x N=2*BC MMA per 8
-// rows: rows 0..63 of the accumulator are hi(dY) times (hi|lo)(X), rows
-// 64..127 are lo(dY) times (hi|lo)(X), so
+// and lo = v - hi (exact in fp32, rounded to tf32 by the unit). One
+// M=128 x N=2*BC MMA per 8 rows computes [dY_hi; dY_lo]^T x [X_hi | X_lo]:
+// accumulator rows 0..63 are hi(dY) times (hi|lo)(X), rows 64..127 lo(dY)
+// times (hi|lo)(X), so
 //   dW[k,c] = (D[k,c] + D[k,BC+c]) + (D[64+k,c] + D[64+k,BC+c]),
-// all four products of the split, with fp32 accumulation in TMEM.
+// every product of the split, accumulated in fp32 in TMEM.
 //
-// Data path (per CTA, one 64 x BC output tile, one slice of rows):
-//   TMA (3-D maps over [N][H*W][ch], 128-byte swizzle, 32 channels x 32 rows
-//   per box) lands raw dY and X rows in shared memory in exactly the
-//   MN-major SW128 layout the MMA reads -> 4 converter warps split each value
-//   into hi (in place) and lo (a parallel chunk), summing db from the raw dY on
-//   the way -> one thread issues the MMAs -> tcgen05.commit frees the stage.
-//   Warp roles: 0 TMA producer, 1 MMA issuer, 2 TMEM owner, 4-7 converters
-//   and epilogue (TMEM lane quarters 0-3).
+// Layouts: the tf32 MMA takes K-major operands only (the reduction index
+// contiguous), while NHWC rows hold channels contiguously. So:
+//  - A = the dY split lives in TMEM (lane = row m, one column per row p),
+//    written with tcgen05.st: a warp reads one 128-byte swizzled row of the
+//    raw dY chunk per load (conflict-free) and each lane keeps its channel;
+//  - B = the X split is transposed into a K-major 128B-swizzled shared tile
+//    (row = channel, 32 rows p per 128 bytes): each lane owns one row p, and
+//    every store writes one full 128-byte row (conflict-free).
+// Data path: TMA (3-D maps over [N][H*W][ch], 32 channels x 32 rows per box,
+// 128B swizzle) -> raw ring -> 8 converter warps (split, transpose, db) ->
+// operand ring (B in smem, A in TMEM) -> one thread issues the MMAs ->
+// tcgen05.commit frees the operand stage. Warp roles: 0 TMA producer, 1 MMA
+// issuer, 2 TMEM owner, 4-11 converters; 4-7 also run the epilogue.
 #include "tc_common.cuh"
 
 namespace cig {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+constexpr int kConv = 256;                // converter threads (warps 4..11)
 constexpr int kBP = 32;                   // rows per stage = one reduction block
-constexpr int kChunk = kBP * 128;         // bytes of one 32-channel x kBP-row swizzled chunk
+constexpr int kChunk = kBP * 128;         // bytes of one 32-channel x kBP-row raw chunk
 constexpr int kBK = 64;                   // k rows of an output tile (M = 2 x 64 with the split)
 constexpr int kSmemBudget = 200 * 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAcol = 256;           // first TMEM column of the A ring
 
 template <int BC>
 struct Cfg {
-  static constexpr int NC = BC / 32;                     // raw X chunks per stage
-  static constexpr int A_BYTES = 4 * kChunk;             // dY: hi k0-31, hi k32-63, lo, lo
-  static constexpr int B_BYTES = 2 * NC * kChunk;        // X: hi chunks then lo chunks
-  static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = kSmemBudget / STAGE < 6 ? kSmemBudget / STAGE : 6;
-  static constexpr int N = 2 * BC;                       // MMA N
-  static constexpr int TMEM_COLS = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
-  static constexpr uint32_t TX = (2 + NC) * kChunk;      // raw bytes TMA lands per stage
+  static constexpr int NC = BC / 32;                      // raw X chunks per stage
+  static constexpr int RAW = (2 + NC) * kChunk;           // raw dY (2 chunks) + raw X
+  static constexpr int OPB = 2 * BC * 128;                // K-major B: 2*BC rows x 128 B
+  static constexpr int Q = BC >= 128 ? 3 : 4;             // operand stages
+  static constexpr int R0 = (kSmemBudget - Q * OPB) / RAW;
+  static constexpr int R = R0 > 8 ? 8 : R0;               // raw stages
+  static constexpr int N = 2 * BC;
+  static constexpr uint32_t TX = (uint32_t)RAW;
   static constexpr int BAR_BYTES = 256;
-  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + BAR_BYTES;
-  static constexpr uint32_t IDESC = mma_idesc(2u, 1u, 1u, (uint32_t)N, 128u);
-  static_assert(STAGES >= 2, "pipeline too shallow");
+  static constexpr size_t SMEM = 1024 + (size_t)R * RAW + (size_t)Q * OPB + BAR_BYTES;
+  static constexpr uint32_t IDESC = mma_idesc(2u, 0u, 0u, (uint32_t)N, 128u);
+  static_assert(R >= 2, "raw pipeline too shallow");
   static_assert(N % 16 == 0 && N >= 16 && N <= 256, "invalid MMA N for M=128");
+  static_assert(kAcol + 32 * Q <= kTmemCols, "TMEM overflow");
 };
 
 __device__ __forceinline__ float tf32_hi(float v) { return __uint_as_float(__float_as_uint(v) & 0xFFFFE000u); }
 
-// Split one 16-byte unit (4 values) in place: hi stays, lo goes to `lo_dst`.
-__device__ __forceinline__ float4 split_unit(float4* unit, float4* lo_dst) {
-  const float4 v = *unit;
-  float4 hi, lo;
-  hi.x = tf32_hi(v.x); lo.x = v.x - hi.x;
-  hi.y = tf32_hi(v.y); lo.y = v.y - hi.y;
-  hi.z = tf32_hi(v.z); lo.z = v.z - hi.z;
-  hi.w = tf32_hi(v.w); lo.w = v.w - hi.w;
-  *unit = hi;
-  *lo_dst = lo;
-  return v;
+// Byte offset of element (row n, reduction index p) of a K-major, 128B-swizzled
+// fp32 tile with 32 reduction elements per 128-byte row.
+__device__ __forceinline__ int kmajor_off(int n, int p) {
+  return (n >> 3) * 1024 + (n & 7) * 128 + ((((p >> 2) ^ (n & 7)) << 4) | ((p & 3) << 2));
 }
 
 template <int BC>
@@ -77,10 +79,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   using G = Cfg<BC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)G::STAGES * G::STAGE);
-  uint64_t* conv = full + G::STAGES;
-  uint64_t* empty = conv + G::STAGES;
-  uint64_t* tmem_full = empty + G::STAGES;
+  uint8_t* raw = smem;                                   // R raw stages
+  uint8_t* opb = smem + (size_t)G::R * G::RAW;           // Q operand (B) stages
+  uint64_t* raw_full = reinterpret_cast<uint64_t*>(opb + (size_t)G::Q * G::OPB);
+  uint64_t* raw_empty = raw_full + G::R;
+  uint64_t* op_full = raw_empty + G::R;
+  uint64_t* op_empty = op_full + G::Q;
+  uint64_t* tmem_full = op_empty + G::Q;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_full + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -93,10 +98,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t nblk = slice_begin(blocks, S, sigma + 1) - b0;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < G::STAGES; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&conv[i], 128);
-      mbar_init(&empty[i], 1);
+    for (int i = 0; i < G::R; ++i) {
+      mbar_init(&raw_full[i], 1);
+      mbar_init(&raw_empty[i], kConv);
+    }
+    for (int i = 0; i < G::Q; ++i) {
+      mbar_init(&op_full[i], kConv);
+      mbar_init(&op_empty[i], 1);
     }
     mbar_init(tmem_full, 1);
     *abort_flag = 0u;
@@ -105,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch(&tm_x);
   }
   if (warp == 2) {
-    tmem_alloc(tmem_slot, G::TMEM_COLS);
+    tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -118,94 +126,109 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int64_t it = 0;
       for (; it < nblk; ++it) {
-        const int s = (int)(it % G::STAGES);
-        const uint32_t round = (uint32_t)(it / G::STAGES);
-        if (it >= G::STAGES && !mbar_wait(&empty[s], (round - 1) & 1u, abort_flag, err)) break;
+        const int s = (int)(it % G::R);
+        const uint32_t round = (uint32_t)(it / G::R);
+        if (it >= G::R && !mbar_wait(&raw_empty[s], (round - 1) & 1u, abort_flag, err)) break;
         const int64_t b = b0 + it;
         const int32_t n = (int32_t)(b / blocks_per_sample);
         const int32_t row = (int32_t)((b % blocks_per_sample) * kBP);
-        uint8_t* st = smem + (size_t)s * G::STAGE;
-        mbar_arrive_expect_tx(&full[s], G::TX);
-        tma_load_3d(st, &tm_dy, (int32_t)k0, row, n, &full[s]);
-        tma_load_3d(st + kChunk, &tm_dy, (int32_t)k0 + 32, row, n, &full[s]);
+        uint8_t* st = raw + (size_t)s * G::RAW;
+        mbar_arrive_expect_tx(&raw_full[s], G::TX);
+        tma_load_3d(st, &tm_dy, (int32_t)k0, row, n, &raw_full[s]);
+        tma_load_3d(st + kChunk, &tm_dy, (int32_t)k0 + 32, row, n, &raw_full[s]);
 #pragma unroll
         for (int j = 0; j < G::NC; ++j)
-          tma_load_3d(st + G::A_BYTES + j * kChunk, &tm_x, (int32_t)(c0 + 32 * j), row, n, &full[s]);
+          tma_load_3d(st + (2 + j) * kChunk, &tm_x, (int32_t)(c0 + 32 * j), row, n, &raw_full[s]);
       }
       // Before the CTA can exit, every copy it started must have landed.
-      for (int64_t q = it > G::STAGES ? it - G::STAGES : 0; q < it; ++q)
-        mbar_wait(&full[q % G::STAGES], (uint32_t)(q / G::STAGES) & 1u, nullptr, err);
+      for (int64_t q = it > G::R ? it - G::R : 0; q < it; ++q)
+        mbar_wait(&raw_full[q % G::R], (uint32_t)(q / G::R) & 1u, nullptr, err);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t sbase = smem_u32(smem);
+      const uint32_t bbase = smem_u32(opb);
       for (int64_t it = 0; it < nblk; ++it) {
-        const int s = (int)(it % G::STAGES);
-        if (!mbar_wait(&conv[s], (uint32_t)(it / G::STAGES) & 1u, abort_flag, err)) break;
+        const int s = (int)(it % G::Q);
+        if (!mbar_wait(&op_full[s], (uint32_t)(it / G::Q) & 1u, abort_flag, err)) break;
         tc_fence_after();
-        const uint32_t a = sbase + (uint32_t)(s * G::STAGE);
-        const uint32_t bb = a + G::A_BYTES;
+        const uint32_t b = bbase + (uint32_t)(s * G::OPB);
+        const uint32_t a = tmem + kAcol + 32u * (uint32_t)s;
 #pragma unroll
         for (int kk = 0; kk < kBP / 8; ++kk) {
-          // MN-major, 128B swizzle: 32-channel chunks kChunk bytes apart (LBO),
-          // 8-row groups 1024 bytes apart (SBO); one MMA consumes one group.
-          const uint64_t da = smem_desc_sw128(a + kk * 1024, kChunk, 1024);
-          const uint64_t db_ = smem_desc_sw128(bb + kk * 1024, kChunk, 1024);
-          mma_tf32(tmem, da, db_, G::IDESC, (it > 0 || kk > 0) ? 1u : 0u);
+          // K-major SW128 B: 8-row groups 1024 B apart; the k step of 8 rows p
+          // is a 32-byte advance inside the swizzled 128-byte row.
+          const uint64_t bd = smem_desc_sw128(b + 32u * kk, 16, 1024);
+          mma_tf32_ts(tmem, a + 8u * kk, bd, G::IDESC, (it > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&empty[s]);
+        mma_commit(&op_empty[s]);
       }
       // Arrives once every MMA issued above has completed (or at once if none).
       if (nblk > 0) mma_commit(tmem_full);
       else mbar_arrive(tmem_full);
     }
   } else if (warp >= 4) {
-    // ---------------------------------------------------- converters + epilogue
-    const int ct = threadIdx.x - 128;  // 0..127
-    const int u = ct % 8;              // logical 16-byte unit (4 channels) this thread owns
-    const int r0 = ct / 8;             // first row (0..15); rows r0 and r0 + 16
-    float bsum[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // ---------------------------------------------------- converters
+    const int cw = warp - 4;          // 0..7
+    const int q = cw & 3;             // TMEM lane quarter (= warp % 4)
+    const int hh = cw >> 2;           // which 16 rows p of the stage this warp puts in TMEM
+    const int jdy = q & 1;            // raw dY chunk (channels 32 jdy ..) of this warp's lanes
+    const bool lo_rows = q >= 2;      // lanes 64..127 hold lo(dY)
+    float bsum = 0.f;                 // db partial of channel k0 + 32 jdy + lane (hi warps only)
     for (int64_t it = 0; it < nblk; ++it) {
-      const int s = (int)(it % G::STAGES);
-      if (!mbar_wait(&full[s], (uint32_t)(it / G::STAGES) & 1u, abort_flag, err)) break;
-      uint8_t* st = smem + (size_t)s * G::STAGE;
+      const int rs = (int)(it % G::R);
+      const int qs = (int)(it % G::Q);
+      if (!mbar_wait(&raw_full[rs], (uint32_t)(it / G::R) & 1u, abort_flag, err)) break;
+      if (it >= G::Q && !mbar_wait(&op_empty[qs], (uint32_t)(it / G::Q - 1) & 1u, abort_flag, err)) break;
+      tc_fence_after();
+      const uint8_t* st = raw + (size_t)rs * G::RAW;
+      // dY -> TMEM A: lane = channel, 16 rows p per warp.
+      {
+        const uint8_t* cd = st + jdy * kChunk;
+        float v[16];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
+        for (int i = 0; i < 16; ++i) {
+          const int p = 16 * hh + i;
+          const float f = *reinterpret_cast<const float*>(cd + p * 128 + ((((lane >> 2) ^ (p & 7)) << 4) |
+                                                                            ((lane & 3) << 2)));
+          const float h = tf32_hi(f);
+          v[i] = lo_rows ? f - h : h;
+          bsum += f;
+        }
+        tmem_st16(tmem + ((uint32_t)(32 * q) << 16) + kAcol + 32u * (uint32_t)qs + 16u * (uint32_t)hh, v);
+      }
+      // X -> K-major B: lane = row p, 4 channels per item, hi and lo rows.
+      uint8_t* ob = opb + (size_t)qs * G::OPB;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int row = r0 + 16 * h;
-          const int off = row * 128 + ((u ^ (row & 7)) << 4);
-          float4* unit = reinterpret_cast<float4*>(st + j * kChunk + off);
-          const float4 v = split_unit(unit, reinterpret_cast<float4*>(st + (2 + j) * kChunk + off));
-          bsum[j][0] += v.x; bsum[j][1] += v.y; bsum[j][2] += v.z; bsum[j][3] += v.w;
+      for (int item = cw; item < G::NC * 8; item += 8) {
+        const int j = item >> 3, u = item & 7, p = lane;
+        const float4 f = *reinterpret_cast<const float4*>(st + (2 + j) * kChunk + p * 128 + ((u ^ (p & 7)) << 4));
+        const float fv[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = 32 * j + 4 * u + i;
+          const float h = tf32_hi(fv[i]);
+          *reinterpret_cast<float*>(ob + kmajor_off(c, p)) = h;
+          *reinterpret_cast<float*>(ob + kmajor_off(BC + c, p)) = fv[i] - h;
         }
       }
-#pragma unroll
-      for (int j = 0; j < G::NC; ++j) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int row = r0 + 16 * h;
-          const int off = row * 128 + ((u ^ (row & 7)) << 4);
-          uint8_t* xb = st + G::A_BYTES;
-          split_unit(reinterpret_cast<float4*>(xb + j * kChunk + off),
-                     reinterpret_cast<float4*>(xb + (G::NC + j) * kChunk + off));
-        }
-      }
-      fence_proxy_async_smem();  // these writes -> visible to the tensor core
-      mbar_arrive(&conv[s]);
+      tmem_wait_st();
+      tc_fence_before();
+      fence_proxy_async_smem();  // B writes -> visible to the tensor core
+      mbar_arrive(&raw_empty[rs]);
+      mbar_arrive(&op_full[qs]);
     }
 
-    // All MMAs done: the stage buffers are free for the epilogue's scratch.
+    // ---------------------------------------------------- epilogue
     const bool ok = mbar_wait(tmem_full, 0u, nullptr, err) && *abort_flag == 0u;
     tc_fence_after();
-    float* comb = reinterpret_cast<float*>(smem);                      // [64][BC + 4]
-    float* bred = reinterpret_cast<float*>(smem + 64 * (BC + 4) * 4);  // [16][64]
     constexpr int LD = BC + 4;
-    const int q = warp - 4;  // TMEM lane quarter
-    const int m = 32 * q + lane;
+    float* comb = reinterpret_cast<float*>(raw);                      // [64][LD]
+    float* bred = reinterpret_cast<float*>(raw + 64 * LD * 4);        // [2][64]
+    if (!lo_rows) bred[hh * 64 + 32 * jdy + lane] = bsum;
     const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
-    if (q >= 2) {
+    if (hh == 0 && lo_rows) {
+      // rows 64..127: lo(dY) products, parked in shared memory by channel k
 #pragma unroll 1
       for (int j = 0; j < G::NC; ++j) {
         float hi[32], lo[32];
@@ -216,22 +239,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) hi[i] = lo[i] = 0.f;
         }
-        float* dst = comb + (m - 64) * LD + 32 * j;
+        float* dst = comb + (32 * jdy + lane) * LD + 32 * j;
 #pragma unroll
         for (int i = 0; i < 32; i += 4)
           *reinterpret_cast<float4*>(dst + i) =
               make_float4(hi[i] + lo[i], hi[i + 1] + lo[i + 1], hi[i + 2] + lo[i + 2], hi[i + 3] + lo[i + 3]);
       }
     }
-    // db partials of this thread: k = 32 j + 4 u + i
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) bred[r0 * 64 + 32 * j + 4 * u + i] = bsum[j][i];
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    asm volatile("bar.sync 1, 256;" ::: "memory");
     const int64_t E = K * C;
-    if (q < 2) {
-      const int64_t k = k0 + m;
+    if (hh == 0 && !lo_rows) {
+      const int kl = 32 * jdy + lane;
+      const int64_t k = k0 + kl;
 #pragma unroll 1
       for (int j = 0; j < G::NC; ++j) {
         float hi[32], lo[32];
@@ -242,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) hi[i] = lo[i] = 0.f;
         }
-        const float* cb = comb + m * LD + 32 * j;
+        const float* cb = comb + kl * LD + 32 * j;
         const int64_t cc = c0 + 32 * j;
         if (ok && k < K) {
           float* dst = ws ? ws + (int64_t)sigma * E + k * C + cc : out + k * C + cc;
@@ -257,13 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-    }
-    if (db && (tile % tiles_c) == 0 && ct < 64 && ok) {
-      float v = 0.f;
-#pragma unroll
-      for (int g = 0; g < 16; ++g) v += bred[g * 64 + ct];
-      const int64_t k = k0 + ct;
-      if (k < K) {
+      if (db && (tile % tiles_c) == 0 && ok && k < K) {
+        const float v = bred[kl] + bred[64 + kl];  // rows 0-15 then 16-31 of every stage
         if (ws_bias) ws_bias[(int64_t)sigma * K + k] = v;
         else db[k] = v;
       }
@@ -274,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, G::TMEM_COLS);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -320,9 +334,9 @@ Geometry geometry_wgrad1x1_tf32x3(const Shape& s) {
   Geometry g;
   const bool pointwise = s.r == 1 && s.s == 1 && s.sh == 1 && s.sw == 1 && s.ph == 0 && s.pw == 0;
   if (!pointwise || s.groups != 1 || s.in_dt != CONV_F32 || s.out_dt != CONV_F32) return g;
-  if (s.c % 4 != 0 || s.k % 4 != 0) return g;         // 16-byte row strides for TMA
-  if (s.n < 1) return g;                               // an empty batch takes the other kernels
-  if (s.k < 32 || s.c < 32 || s.h * s.w < kBP) return g;  // no TMA box larger than its tensor
+  if (s.c % 4 != 0 || s.k % 4 != 0) return g;              // 16-byte row strides for TMA
+  if (s.n < 1) return g;                                    // an empty batch takes the other kernels
+  if (s.k < 32 || s.c < 32 || s.h * s.w < kBP) return g;    // no TMA box larger than its tensor
   if (s.h * s.w > 0x7fffffffLL || s.n > 0x7fffffffLL) return g;  // 32-bit TMA coordinates
   const int bc = pick_bc(s.c);
   g.ok = true;
