@@ -15,7 +15,11 @@
 // accumulator rows 0..63 are hi(dY) times (hi|lo)(X), rows 64..127 lo(dY)
 // times (hi|lo)(X), so
 //   dW[k,c] = (D[k,c] + D[k,BC+c]) + (D[64+k,c] + D[64+k,BC+c]),
-// every product of the split, accumulated in fp32 in TMEM.
+// every product of the split. The tensor core's fp32 accumulation is not an
+// IEEE round-to-nearest sum and its error grows with the number of rows added
+// into one accumulator, so the accumulator is double-buffered in TMEM and
+// drained every kPeriod blocks (512 rows) into fp32 registers with ordinary
+// round-to-nearest adds.
 //
 // Layouts: the tf32 MMA takes K-major operands only (the reduction index
 // contiguous), while NHWC rows hold channels contiguously. So:
@@ -29,7 +33,8 @@
 // 128B swizzle) -> raw ring -> 8 converter warps (split, transpose, db) ->
 // operand ring (B in smem, A in TMEM) -> one thread issues the MMAs ->
 // tcgen05.commit frees the operand stage. Warp roles: 0 TMA producer, 1 MMA
-// issuer, 2 TMEM owner, 4-11 converters; 4-7 also run the epilogue.
+// issuer, 2 TMEM owner, 4-11 converters, which also drain the accumulators
+// and run the epilogue.
 #include "tc_common.cuh"
 
 namespace cig {
@@ -41,34 +46,32 @@ constexpr int kBP = 32;                   // rows per stage = one reduction bloc
 constexpr int kChunk = kBP * 128;         // bytes of one 32-channel x kBP-row raw chunk
 constexpr int kBK = 64;                   // k rows of an output tile (M = 2 x 64 with the split)
 constexpr int kSmemBudget = 200 * 1024;
+constexpr int kPeriod = 16;               // blocks accumulated in TMEM before a drain
+constexpr int kQ = 4;                     // operand stages
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAcol = 256;           // first TMEM column of the A ring
+constexpr uint32_t kDcol = 192;           // accumulator buffer b at column kDcol * b
+constexpr uint32_t kAcol = 384;           // operand A ring at columns 384 + 32 * stage
 
 template <int BC>
 struct Cfg {
   static constexpr int NC = BC / 32;                      // raw X chunks per stage
   static constexpr int RAW = (2 + NC) * kChunk;           // raw dY (2 chunks) + raw X
   static constexpr int OPB = 2 * BC * 128;                // K-major B: 2*BC rows x 128 B
-  static constexpr int Q = BC >= 128 ? 3 : 4;             // operand stages
-  static constexpr int R0 = (kSmemBudget - Q * OPB) / RAW;
+  static constexpr int R0 = (kSmemBudget - kQ * OPB) / RAW;
   static constexpr int R = R0 > 8 ? 8 : R0;               // raw stages
   static constexpr int N = 2 * BC;
+  static constexpr int HALF = BC / 2;                     // output columns per converter thread
   static constexpr uint32_t TX = (uint32_t)RAW;
   static constexpr int BAR_BYTES = 256;
-  static constexpr size_t SMEM = 1024 + (size_t)R * RAW + (size_t)Q * OPB + BAR_BYTES;
+  static constexpr size_t SMEM = 1024 + (size_t)R * RAW + (size_t)kQ * OPB + BAR_BYTES;
   static constexpr uint32_t IDESC = mma_idesc(2u, 0u, 0u, (uint32_t)N, 128u);
   static_assert(R >= 2, "raw pipeline too shallow");
-  static_assert(N % 16 == 0 && N >= 16 && N <= 256, "invalid MMA N for M=128");
-  static_assert(kAcol + 32 * Q <= kTmemCols, "TMEM overflow");
+  static_assert(N % 16 == 0 && N >= 16 && N <= (int)kDcol, "invalid MMA N for M=128");
+  static_assert(kAcol + 32 * kQ <= kTmemCols && kDcol * 2 <= kAcol, "TMEM overflow");
+  static_assert(kQ < kPeriod, "a drain must come before its buffer is reused");
 };
 
 __device__ __forceinline__ float tf32_hi(float v) { return __uint_as_float(__float_as_uint(v) & 0xFFFFE000u); }
-
-// Byte offset of element (row n, reduction index p) of a K-major, 128B-swizzled
-// fp32 tile with 32 reduction elements per 128-byte row.
-__device__ __forceinline__ int kmajor_off(int n, int p) {
-  return (n >> 3) * 1024 + (n & 7) * 128 + ((((p >> 2) ^ (n & 7)) << 4) | ((p & 3) << 2));
-}
 
 template <int BC>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -80,13 +83,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* raw = smem;                                   // R raw stages
-  uint8_t* opb = smem + (size_t)G::R * G::RAW;           // Q operand (B) stages
-  uint64_t* raw_full = reinterpret_cast<uint64_t*>(opb + (size_t)G::Q * G::OPB);
+  uint8_t* opb = smem + (size_t)G::R * G::RAW;           // kQ operand (B) stages
+  uint64_t* raw_full = reinterpret_cast<uint64_t*>(opb + (size_t)kQ * G::OPB);
   uint64_t* raw_empty = raw_full + G::R;
   uint64_t* op_full = raw_empty + G::R;
-  uint64_t* op_empty = op_full + G::Q;
-  uint64_t* tmem_full = op_empty + G::Q;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_full + 1);
+  uint64_t* op_empty = op_full + kQ;
+  uint64_t* acc_full = op_empty + kQ;                    // [2]
+  uint64_t* acc_empty = acc_full + 2;                    // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -96,17 +100,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t c0 = (tile % tiles_c) * BC;
   const int64_t b0 = slice_begin(blocks, S, sigma);
   const int64_t nblk = slice_begin(blocks, S, sigma + 1) - b0;
+  const int64_t nper = (nblk + kPeriod - 1) / kPeriod;   // accumulation periods
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < G::R; ++i) {
       mbar_init(&raw_full[i], 1);
       mbar_init(&raw_empty[i], kConv);
     }
-    for (int i = 0; i < G::Q; ++i) {
+    for (int i = 0; i < kQ; ++i) {
       mbar_init(&op_full[i], kConv);
       mbar_init(&op_empty[i], 1);
     }
-    mbar_init(tmem_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kConv);
+    }
     *abort_flag = 0u;
     mbar_fence_init();
     tma_prefetch(&tm_dy);
@@ -149,8 +157,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t bbase = smem_u32(opb);
       for (int64_t it = 0; it < nblk; ++it) {
-        const int s = (int)(it % G::Q);
-        if (!mbar_wait(&op_full[s], (uint32_t)(it / G::Q) & 1u, abort_flag, err)) break;
+        const int s = (int)(it % kQ);
+        const int64_t per = it / kPeriod;
+        const int within = (int)(it % kPeriod);
+        const uint32_t d = tmem + kDcol * (uint32_t)(per & 1);
+        if (within == 0 && per >= 2 && !mbar_wait(&acc_empty[per & 1], (uint32_t)((per >> 1) - 1) & 1u, abort_flag, err))
+          break;
+        if (!mbar_wait(&op_full[s], (uint32_t)(it / kQ) & 1u, abort_flag, err)) break;
         tc_fence_after();
         const uint32_t b = bbase + (uint32_t)(s * G::OPB);
         const uint32_t a = tmem + kAcol + 32u * (uint32_t)s;
@@ -159,57 +172,105 @@ __global__ void __launch_bounds__(kThreads, 1)
           // K-major SW128 B: 8-row groups 1024 B apart; the k step of 8 rows p
           // is a 32-byte advance inside the swizzled 128-byte row.
           const uint64_t bd = smem_desc_sw128(b + 32u * kk, 16, 1024);
-          mma_tf32_ts(tmem, a + 8u * kk, bd, G::IDESC, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_tf32_ts(d, a + 8u * kk, bd, G::IDESC, (within > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&op_empty[s]);
+        if (within == kPeriod - 1 || it == nblk - 1) mma_commit(&acc_full[per & 1]);
       }
-      // Arrives once every MMA issued above has completed (or at once if none).
-      if (nblk > 0) mma_commit(tmem_full);
-      else mbar_arrive(tmem_full);
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------- converters
     const int cw = warp - 4;          // 0..7
     const int q = cw & 3;             // TMEM lane quarter (= warp % 4)
-    const int hh = cw >> 2;           // which 16 rows p of the stage this warp puts in TMEM
+    const int hh = cw >> 2;           // rows p 16 hh .. 16 hh + 15 of a stage go to TMEM from this warp;
+                                      // output columns hh * BC/2 .. of the tile are drained by it
     const int jdy = q & 1;            // raw dY chunk (channels 32 jdy ..) of this warp's lanes
     const bool lo_rows = q >= 2;      // lanes 64..127 hold lo(dY)
-    float bsum = 0.f;                 // db partial of channel k0 + 32 jdy + lane (hi warps only)
+    // dY loads: row p = 16 hh + i, element = lane (channel), 128B swizzle
+    int dsw[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) dsw[t] = ((((lane >> 2) ^ t) << 4) | ((lane & 3) << 2)) + (16 * hh + t) * 128;
+    const int dbase = jdy * kChunk;
+    // X loads: row p = lane, unit (4 channels) cw of each 32-channel chunk
+    const int xoff = 2 * kChunk + lane * 128 + ((cw ^ (lane & 7)) << 4);
+    // B stores: channel c = 32 j + 4 cw + i -> K-major row c, column p = lane
+    int sofs[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      sofs[i] = (4 * cw + i) * 128 + ((((lane >> 2) ^ (((cw & 1) << 2) + i)) << 4) | ((lane & 3) << 2));
+
+    float acc[G::HALF];
+#pragma unroll
+    for (int i = 0; i < G::HALF; ++i) acc[i] = 0.f;
+    float bsum = 0.f;  // db partial of channel k0 + 32 jdy + lane (hi warps only)
+    int64_t drained = 0;
+    bool alive = true;
+
+    // Adds accumulator period `pd` (buffer pd & 1) into the registers.
+    auto drain = [&](int64_t pd) -> bool {
+      if (!mbar_wait(&acc_full[pd & 1], (uint32_t)(pd >> 1) & 1u, abort_flag, err)) return false;
+      tc_fence_after();
+      const uint32_t t = tmem + ((uint32_t)(32 * q) << 16) + kDcol * (uint32_t)(pd & 1) + (uint32_t)(hh * G::HALF);
+#pragma unroll
+      for (int j = 0; j < G::HALF / 16; ++j) {
+        float part[16];
+        tmem_ld16(t + 16u * j, part);  // products with X_hi
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[16 * j + i] += part[i];
+        tmem_ld16(t + BC + 16u * j, part);  // products with X_lo
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[16 * j + i] += part[i];
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[pd & 1]);
+      return true;
+    };
+
     for (int64_t it = 0; it < nblk; ++it) {
       const int rs = (int)(it % G::R);
-      const int qs = (int)(it % G::Q);
-      if (!mbar_wait(&raw_full[rs], (uint32_t)(it / G::R) & 1u, abort_flag, err)) break;
-      if (it >= G::Q && !mbar_wait(&op_empty[qs], (uint32_t)(it / G::Q - 1) & 1u, abort_flag, err)) break;
+      const int qs = (int)(it % kQ);
+      if (it >= kPeriod + kQ && (it - kQ) % kPeriod == 0) {
+        if (!drain(drained)) { alive = false; break; }
+        ++drained;
+      }
+      if (!mbar_wait(&raw_full[rs], (uint32_t)(it / G::R) & 1u, abort_flag, err)) { alive = false; break; }
+      if (it >= kQ && !mbar_wait(&op_empty[qs], (uint32_t)(it / kQ - 1) & 1u, abort_flag, err)) {
+        alive = false;
+        break;
+      }
       tc_fence_after();
       const uint8_t* st = raw + (size_t)rs * G::RAW;
       // dY -> TMEM A: lane = channel, 16 rows p per warp.
       {
-        const uint8_t* cd = st + jdy * kChunk;
+        const uint8_t* cd = st + dbase;
         float v[16];
+        if (lo_rows) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int p = 16 * hh + i;
-          const float f = *reinterpret_cast<const float*>(cd + p * 128 + ((((lane >> 2) ^ (p & 7)) << 4) |
-                                                                            ((lane & 3) << 2)));
-          const float h = tf32_hi(f);
-          v[i] = lo_rows ? f - h : h;
-          bsum += f;
+          for (int i = 0; i < 16; ++i) {
+            const float f = *reinterpret_cast<const float*>(cd + dsw[i & 7] + (i >> 3) * 1024);
+            v[i] = f - tf32_hi(f);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float f = *reinterpret_cast<const float*>(cd + dsw[i & 7] + (i >> 3) * 1024);
+            v[i] = tf32_hi(f);
+            bsum += f;
+          }
         }
         tmem_st16(tmem + ((uint32_t)(32 * q) << 16) + kAcol + 32u * (uint32_t)qs + 16u * (uint32_t)hh, v);
       }
-      // X -> K-major B: lane = row p, 4 channels per item, hi and lo rows.
+      // X -> K-major B: lane = row p, 4 channels per chunk, hi and lo rows.
       uint8_t* ob = opb + (size_t)qs * G::OPB;
 #pragma unroll
-      for (int item = cw; item < G::NC * 8; item += 8) {
-        const int j = item >> 3, u = item & 7, p = lane;
-        const float4 f = *reinterpret_cast<const float4*>(st + (2 + j) * kChunk + p * 128 + ((u ^ (p & 7)) << 4));
+      for (int j = 0; j < G::NC; ++j) {
+        const float4 f = *reinterpret_cast<const float4*>(st + xoff + j * kChunk);
         const float fv[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int c = 32 * j + 4 * u + i;
           const float h = tf32_hi(fv[i]);
-          *reinterpret_cast<float*>(ob + kmajor_off(c, p)) = h;
-          *reinterpret_cast<float*>(ob + kmajor_off(BC + c, p)) = fv[i] - h;
+          *reinterpret_cast<float*>(ob + j * 4096 + sofs[i]) = h;
+          *reinterpret_cast<float*>(ob + BC * 128 + j * 4096 + sofs[i]) = fv[i] - h;
         }
       }
       tmem_wait_st();
@@ -218,65 +279,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&raw_empty[rs]);
       mbar_arrive(&op_full[qs]);
     }
+    while (alive && drained < nper) {
+      if (!drain(drained)) alive = false;
+      ++drained;
+    }
 
     // ---------------------------------------------------- epilogue
-    const bool ok = mbar_wait(tmem_full, 0u, nullptr, err) && *abort_flag == 0u;
-    tc_fence_after();
+    const bool ok = alive && *abort_flag == 0u;
     constexpr int LD = BC + 4;
     float* comb = reinterpret_cast<float*>(raw);                      // [64][LD]
     float* bred = reinterpret_cast<float*>(raw + 64 * LD * 4);        // [2][64]
-    if (!lo_rows) bred[hh * 64 + 32 * jdy + lane] = bsum;
-    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
-    if (hh == 0 && lo_rows) {
-      // rows 64..127: lo(dY) products, parked in shared memory by channel k
-#pragma unroll 1
-      for (int j = 0; j < G::NC; ++j) {
-        float hi[32], lo[32];
-        if (nblk > 0) {
-          tmem_ld32(trow + 32 * j, hi);
-          tmem_ld32(trow + BC + 32 * j, lo);
-        } else {
+    const int kl = 32 * jdy + lane;
+    if (!lo_rows) bred[hh * 64 + kl] = bsum;
+    if (lo_rows) {
+      float* dst = comb + kl * LD + hh * G::HALF;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) hi[i] = lo[i] = 0.f;
-        }
-        float* dst = comb + (32 * jdy + lane) * LD + 32 * j;
-#pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(dst + i) =
-              make_float4(hi[i] + lo[i], hi[i + 1] + lo[i + 1], hi[i + 2] + lo[i + 2], hi[i + 3] + lo[i + 3]);
-      }
+      for (int i = 0; i < G::HALF; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
     }
     asm volatile("bar.sync 1, 256;" ::: "memory");
     const int64_t E = K * C;
-    if (hh == 0 && !lo_rows) {
-      const int kl = 32 * jdy + lane;
-      const int64_t k = k0 + kl;
-#pragma unroll 1
-      for (int j = 0; j < G::NC; ++j) {
-        float hi[32], lo[32];
-        if (nblk > 0) {
-          tmem_ld32(trow + 32 * j, hi);
-          tmem_ld32(trow + BC + 32 * j, lo);
-        } else {
+    const int64_t k = k0 + kl;
+    if (!lo_rows && ok && k < K) {
+      const float* cb = comb + kl * LD + hh * G::HALF;
+      const int64_t cc = c0 + hh * G::HALF;
+      float* dst = ws ? ws + (int64_t)sigma * E + k * C + cc : out + k * C + cc;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) hi[i] = lo[i] = 0.f;
-        }
-        const float* cb = comb + kl * LD + 32 * j;
-        const int64_t cc = c0 + 32 * j;
-        if (ok && k < K) {
-          float* dst = ws ? ws + (int64_t)sigma * E + k * C + cc : out + k * C + cc;
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            if (cc + i < C) {  // C % 4 == 0: a 4-wide group is all in or all out
-              const float4 o = *reinterpret_cast<const float4*>(cb + i);
-              *reinterpret_cast<float4*>(dst + i) =
-                  make_float4((hi[i] + lo[i]) + o.x, (hi[i + 1] + lo[i + 1]) + o.y,
-                              (hi[i + 2] + lo[i + 2]) + o.z, (hi[i + 3] + lo[i + 3]) + o.w);
-            }
-          }
+      for (int i = 0; i < G::HALF; i += 4) {
+        if (cc + i < C) {  // C % 4 == 0: a 4-wide group is all in or all out
+          const float4 o = *reinterpret_cast<const float4*>(cb + i);
+          *reinterpret_cast<float4*>(dst + i) =
+              make_float4(acc[i] + o.x, acc[i + 1] + o.y, acc[i + 2] + o.z, acc[i + 3] + o.w);
         }
       }
-      if (db && (tile % tiles_c) == 0 && ok && k < K) {
+      if (hh == 0 && db && (tile % tiles_c) == 0) {
         const float v = bred[kl] + bred[64 + kl];  // rows 0-15 then 16-31 of every stage
         if (ws_bias) ws_bias[(int64_t)sigma * K + k] = v;
         else db[k] = v;
@@ -295,8 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 int pick_bc(int64_t C) {
   if (C <= 32) return 32;
   if (C <= 64) return 64;
-  if (C <= 96) return 96;
-  return 128;
+  return 96;
 }
 
 template <int BC>
@@ -350,8 +384,7 @@ cudaError_t launch_wgrad1x1_tf32x3(const Plan& p, const Args& a) {
   switch (pick_bc(p.sh.c)) {
     case 32: return launch_bc<32>(p, a);
     case 64: return launch_bc<64>(p, a);
-    case 96: return launch_bc<96>(p, a);
-    default: return launch_bc<128>(p, a);
+    default: return launch_bc<96>(p, a);
   }
 }
 

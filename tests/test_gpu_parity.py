@@ -171,3 +171,27 @@ def test_device_call_errors():
     with pytest.raises(cig.ConvError) as e:
         cig.conv_wgrad_bias(p, flat[1:], dyd, dw, db, big[:need], 4)
     assert e.value.status == 5
+
+
+# ------------------------------------------------------- tensor-core forward
+
+
+def test_config3_forward_split_sweep():
+    """3x3 fwd bf16, N=1, 14x14, C=2048 -> K=512, pad 1, N(0, 0.02) seed 2; split auto and 1..32."""
+    p = cig.Problem(n=1, h=14, w=14, c=2048, k=512, r=3, s=3, pad_h=1, pad_w=1, in_dtype=BF16, out_dtype=BF16)
+    assert cig.describe_plan(p, cig.DIR_FWD, -1)["kernel_name"] == "fwd_tc"
+    check_fwd(p, 2, ["auto"], [-1, 1, 2, 4, 8, 16, 32], "normal", 0.0, 0.02)
+    assert cig.device_errors() == 0
+
+
+@pytest.mark.parametrize("shape", [
+    dict(n=2, h=10, w=12, c=128, k=136, r=3, s=3, pad_h=1, pad_w=1),           # K tail, 2 M tiles per image
+    dict(n=1, h=9, w=11, c=64, k=128, r=5, s=5, pad_h=4, pad_w=4, dil_h=2, dil_w=2),  # dilation, wide pad
+    dict(n=3, h=9, w=9, c=64, k=128),                                           # pointwise
+    dict(n=1, h=20, w=40, c=192, k=256, r=3, s=1, pad_h=1, pad_w=0),           # non-square filter
+])
+@pytest.mark.parametrize("dt", [(BF16, BF16), (F16, F32), (F16, F16)], ids=lambda d: f"{d[0]}{d[1]}")
+def test_forward_tc_ragged(shape, dt):
+    p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
+    check_fwd(p, 6, ["fwd_tc", "generic"], [-1, 1, 3])
+    assert cig.device_errors() == 0
