@@ -25,7 +25,7 @@ STATUS = ["CONV_OK", "CONV_ERR_INVALID_ARG", "CONV_ERR_UNSUPPORTED", "CONV_ERR_W
 EXPORTS = ["conv_status_string", "conv_output_dims", "resolve_split_k_for", "resolve_split_k",
            "conv_workspace_bytes_for", "conv_workspace_bytes", "conv_describe_plan", "conv_fwd",
            "conv_wgrad", "conv_wgrad_bias", "conv_stage1", "conv_stage2", "conv_batch_split_count",
-           "conv_device_errors", "conv_set_kernel_override"]
+           "conv_wgrad_bias_static_ws", "conv_device_errors", "conv_set_kernel_override"]
 
 
 class ConvError(RuntimeError):
@@ -118,6 +118,7 @@ def load(build_if_missing: bool = True):
         "conv_batch_split_count": ([I64, I64], I64),
         "conv_set_kernel_override": ([I32], ctypes.c_int),
         "conv_device_errors": ([ctypes.POINTER(ctypes.c_uint32), I32], ctypes.c_int),
+        "conv_wgrad_bias_static_ws": ([P, V, V, V, V, I32, V], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -276,3 +277,20 @@ def device_errors(clear: bool = True) -> int:
     v = ctypes.c_uint32()
     _check(load().conv_device_errors(ctypes.byref(v), int(clear)), "conv_device_errors")
     return v.value
+
+
+STATIC_WS_BYTES = 8 << 20
+
+
+def conv_wgrad_bias_static_ws(p: Problem, x, dy, dw, db, split_k: int = -1, stream=None):
+    """conv_wgrad_bias with the split-K slabs in the library's fixed 8 MiB device
+    array: for callers that cannot allocate device memory (or hold no workspace)
+    where they run. Calls that overlap on the GPU share that array and race."""
+    ho, wo = p.out_hw
+    _need(x, "x", p.n * p.h * p.w * p.c, p.in_dtype)
+    _need(dy, "dy", p.n * ho * wo * p.k, p.in_dtype)
+    _need(dw, "dw", p.k * p.r * p.s * (p.c // p.groups), p.out_dtype)
+    _need(db, "db", p.k, p.out_dtype)
+    st = load().conv_wgrad_bias_static_ws(_cp(p), _ptr(x), _ptr(dy), _ptr(dw), _ptr(db), split_k, _stream(stream))
+    _check(st, "conv_wgrad_bias_static_ws")
+    return dw, db

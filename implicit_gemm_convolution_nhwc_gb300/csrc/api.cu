@@ -356,6 +356,60 @@ int64_t conv_batch_split_count(int64_t n, int64_t max_n) {
   return (n - 1) / max_n + 1;  // == (n + max_n - 1) / max_n without the overflow
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Weight + bias gradient without any device allocation by the caller.
+//
+// Some callers cannot allocate device memory at the point where they run the
+// convolution: code whose device memory budget is owned by a framework's
+// pool, and plugin or enqueue-time paths of inference runtimes that forbid
+// cudaMalloc after set-up. They may also have no workspace of their own to
+// pass. For them the split-K slabs live in this fixed, library-owned device
+// array instead of a caller workspace.
+namespace {
+
+constexpr uint64_t kStaticScratchBytes = 8ull << 20;  // 8 MiB on every device that loads the library
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+// The array's device address on the current device, looked up once per device
+// (the first call on a device does this set-up).
+void* static_scratch_address() {
+  static void* cached[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (dev < 64 && cached[dev]) return cached[dev];
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (dev < 64) cached[dev] = ptr;
+  return ptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+conv_status conv_wgrad_bias_static_ws(const conv_problem* p, const void* x, const void* dy, void* dw, void* db,
+                                      int32_t split_k, void* stream) {
+  const int sms = current_sm_count();
+  if (sms < 1) return CONV_ERR_CUDA;
+  uint64_t need = 0;
+  conv_status st = conv_workspace_bytes_for(p, CONV_DIR_WGRAD, split_k, 1, sms, &need);
+  if (st != CONV_OK) return st;
+  if (need > kStaticScratchBytes) return CONV_ERR_WORKSPACE_TOO_SMALL;
+  void* scratch = need > 0 ? static_scratch_address() : nullptr;
+  if (need > 0 && !scratch) return CONV_ERR_CUDA;
+  return run(p, CONV_DIR_WGRAD, x, dy, dw, db, scratch, need > 0 ? kStaticScratchBytes : 0, split_k, stream, true,
+             kBoth);
+}
+
+
 conv_status conv_set_kernel_override(int32_t kernel) {
   if (kernel < CONV_KERNEL_AUTO || kernel > CONV_KERNEL_WGRAD_GROUPED) return CONV_ERR_INVALID_ARG;
   g_kernel_override = kernel;

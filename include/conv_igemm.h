@@ -182,6 +182,29 @@ conv_status conv_stage2(const conv_problem* p, conv_dir dir, void* out, void* db
  * callers that must. */
 int64_t conv_batch_split_count(int64_t n, int64_t max_n);
 
+/* Weight + bias gradient for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point; it exists for users of
+ * this library. Some callers cannot call cudaMalloc where they run the
+ * convolution: their device memory is owned by a framework's pool, or they
+ * run at plugin/enqueue time in a runtime that forbids allocation after
+ * set-up, and they may hold no spare workspace either. This call computes
+ * exactly what conv_wgrad_bias computes, with the split-K slabs placed in
+ * one fixed device array owned by the library (8 MiB on every GPU that loads
+ * the library, held until the process exits) instead of a caller workspace.
+ *  - The caller still passes x, dy, dw and db (device pointers, 16-byte
+ *    aligned); nothing is allocated or freed by this call.
+ *  - A degree whose slabs need more than 8 MiB (conv_workspace_bytes with
+ *    with_bias = 1 above 8388608) is rejected with
+ *    CONV_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *  - The first call on a device looks up the array's device address on that
+ *    device (once); make that first call before any stream capture.
+ *  - Every call shares the one array. Its contents between calls do not
+ *    matter (every slab element is written before it is read), but two calls
+ *    whose kernels overlap on the GPU (different streams, no ordering) race
+ *    on it; order such calls on one stream or with events. */
+conv_status conv_wgrad_bias_static_ws(const conv_problem* p, const void* x, const void* dy, void* dw,
+                                      void* db, int32_t split_k, void* stream);
+
 /* Device-side error word of the current device (synchronous read). The
  * tensor-core kernels bound every pipeline wait; a wait that gives up sets
  * bit 0 (1 = a pipeline wait timed out; that call's outputs are invalid) and
