@@ -335,15 +335,17 @@ def run_ours(a, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     sampler.mark(False)
     clocks = sampler.stop()
-    total_ms = start.elapsed_time(end)
+    s1 = [e[0].elapsed_time(e[1]) for e in evs]
+    s2 = [e[1].elapsed_time(e[2]) for e in evs]
+    # With an L2 flush between steps, only stage 1 + fold of each step is timed;
+    # otherwise the whole back-to-back region is.
+    total_ms = sum(e[0].elapsed_time(e[2]) for e in evs) if flush is not None else start.elapsed_time(end)
     if world > 1:
         import torch.distributed as dist_
         t = torch.tensor([total_ms], device=dev)
         dist_.all_reduce(t, op=dist_.ReduceOp.MAX)
         total_ms = float(t.item())
         dist_.barrier()
-    s1 = [e[0].elapsed_time(e[1]) for e in evs]
-    s2 = [e[1].elapsed_time(e[2]) for e in evs]
     ms_step = total_ms / a.steps
     flops = p.flops()
     value = flops * world / (ms_step * 1e-3) / 1e12

@@ -3,75 +3,82 @@
 // round-to-nearest-even into the output type ("feat(rocke): split-K forward
 // implicit-GEMM convolution on gfx1250", "Two-stage split-K": the reduce
 // kernel folds the slabs and casts into D). The bias slabs fold the same way
-// in the same launch. Bandwidth-bound: every slab byte is read once with
-// 16-byte streaming loads, four slabs in flight per step.
+// in the same launch.
+//
+// Bandwidth- and latency-bound: the slabs were just written by stage 1 and
+// usually sit in L2. Each thread owns kVec consecutive elements and issues
+// the loads of kBatch slabs before it adds any of them, so a warp keeps
+// kBatch independent 4- or 16-byte loads in flight per slab batch; the adds
+// still happen strictly in slice order.
 #include "common.cuh"
 
 namespace cig {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kBatch = 16;
 
-__device__ __forceinline__ float4 ldcs4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+template <int V>
+struct Vec;
+template <>
+struct Vec<1> {
+  using T = float;
+  static __device__ __forceinline__ T load(const float* p) { return __ldcs(p); }
+  static __device__ __forceinline__ void add(T& a, const T& b) { a += b; }
+};
+template <>
+struct Vec<4> {
+  using T = float4;
+  static __device__ __forceinline__ T load(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+  static __device__ __forceinline__ void add(T& a, const T& b) {
+    a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+  }
+};
+
+// Sum of S slabs (stride E floats) at element e, in slice order.
+template <int V>
+__device__ __forceinline__ typename Vec<V>::T fold_at(const float* ws, int64_t E, int32_t S, int64_t e) {
+  using T = typename Vec<V>::T;
+  T acc = Vec<V>::load(ws + e);
+  int32_t s = 1;
+  for (; s + kBatch <= S; s += kBatch) {
+    T v[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) v[i] = Vec<V>::load(ws + (int64_t)(s + i) * E + e);
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) Vec<V>::add(acc, v[i]);
+  }
+  for (; s < S; ++s) Vec<V>::add(acc, Vec<V>::load(ws + (int64_t)s * E + e));
+  return acc;
+}
 
 template <typename TO>
-__device__ __forceinline__ void store4(TO* out, int64_t e, float4 v) {
+__device__ __forceinline__ void store_vec(TO* out, int64_t e, float v) { store_out(out + e, v); }
+template <typename TO>
+__device__ __forceinline__ void store_vec(TO* out, int64_t e, float4 v) {
   store_out(out + e + 0, v.x);
   store_out(out + e + 1, v.y);
   store_out(out + e + 2, v.z);
   store_out(out + e + 3, v.w);
 }
-template <>
-__device__ __forceinline__ void store4<float>(float* out, int64_t e, float4 v) {
+__device__ __forceinline__ void store_vec(float* out, int64_t e, float4 v) {
   *reinterpret_cast<float4*>(out + e) = v;
 }
 
-// Sum of S slabs at element e (vector of 4), in slice order.
-__device__ __forceinline__ float4 fold4(const float* ws, int64_t E, int32_t S, int64_t e) {
-  float4 acc = ldcs4(ws + e);
-  int32_t s = 1;
-  for (; s + 4 <= S; s += 4) {
-    const float4 a = ldcs4(ws + (int64_t)(s + 0) * E + e);
-    const float4 b = ldcs4(ws + (int64_t)(s + 1) * E + e);
-    const float4 c = ldcs4(ws + (int64_t)(s + 2) * E + e);
-    const float4 d = ldcs4(ws + (int64_t)(s + 3) * E + e);
-    acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
-    acc.x += b.x; acc.y += b.y; acc.z += b.z; acc.w += b.w;
-    acc.x += c.x; acc.y += c.y; acc.z += c.z; acc.w += c.w;
-    acc.x += d.x; acc.y += d.y; acc.z += d.z; acc.w += d.w;
-  }
-  for (; s < S; ++s) {
-    const float4 a = ldcs4(ws + (int64_t)s * E + e);
-    acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
-  }
-  return acc;
-}
-
-__device__ __forceinline__ float fold1(const float* ws, int64_t E, int32_t S, int64_t e) {
-  float acc = __ldcs(ws + e);
-  for (int32_t s = 1; s < S; ++s) acc += __ldcs(ws + (int64_t)s * E + e);
-  return acc;
-}
-
-// Elements [0, E) of the main slabs, then [0, K) of the bias slabs (if any).
-// vec4: E is a multiple of 4 (the main region runs 4 elements per unit).
-template <typename TO, bool kVec4>
+// Units [0, E / V) cover the main slabs, then [0, K) the bias slabs (if any).
+template <typename TO, int V>
 __global__ void __launch_bounds__(kThreads) fold_kernel(const float* __restrict__ ws, TO* out, int64_t E,
                                                         const float* __restrict__ wsb, TO* db, int64_t K,
                                                         int32_t S) {
-  const int64_t main_units = kVec4 ? E / 4 : E;
+  const int64_t main_units = E / V;
   const int64_t units = main_units + (db ? K : 0);
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   for (int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x; u < units; u += stride) {
     if (u < main_units) {
-      if (kVec4) {
-        store4(out, u * 4, fold4(ws, E, S, u * 4));
-      } else {
-        store_out(out + u, fold1(ws, E, S, u));
-      }
+      store_vec(out, u * V, fold_at<V>(ws, E, S, u * V));
     } else {
       const int64_t k = u - main_units;
-      store_out(db + k, fold1(wsb, K, S, k));
+      store_out(db + k, fold_at<1>(wsb, K, S, k));
     }
   }
 }
@@ -79,16 +86,21 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const float* __restrict_
 template <typename TO>
 cudaError_t launch_typed(const Plan& p, const Args& a) {
   const int64_t E = p.out_elems;
-  const bool vec4 = (E % 4) == 0;
-  const int64_t units = (vec4 ? E / 4 : E) + (p.with_bias ? p.sh.k : 0);
   const int sms = current_sm_count();
-  const int grid = launch_grid_cap(units, kThreads, sms > 0 ? sms : 148, 8);
+  const int cap = (sms > 0 ? sms : 148) * 16;
   TO* out = static_cast<TO*>(a.out);
   TO* db = p.with_bias ? static_cast<TO*>(a.db) : nullptr;
-  if (vec4)
-    fold_kernel<TO, true><<<grid, kThreads, 0, a.stream>>>(a.ws, out, E, a.ws_bias, db, p.sh.k, p.split);
-  else
-    fold_kernel<TO, false><<<grid, kThreads, 0, a.stream>>>(a.ws, out, E, a.ws_bias, db, p.sh.k, p.split);
+  const int64_t bias_units = p.with_bias ? p.sh.k : 0;
+  // 16-byte units when they still give every SM several CTAs; else one float
+  // per thread for more loads in flight.
+  const bool vec4 = (E % 4) == 0 && (E / 4) >= (int64_t)(sms > 0 ? sms : 148) * kThreads * 4;
+  if (vec4) {
+    const int grid = launch_grid_cap(E / 4 + bias_units, kThreads, cap / 8 > 0 ? cap / 8 : 1, 8);
+    fold_kernel<TO, 4><<<grid, kThreads, 0, a.stream>>>(a.ws, out, E, a.ws_bias, db, p.sh.k, p.split);
+  } else {
+    const int grid = launch_grid_cap(E + bias_units, kThreads, cap / 8 > 0 ? cap / 8 : 1, 8);
+    fold_kernel<TO, 1><<<grid, kThreads, 0, a.stream>>>(a.ws, out, E, a.ws_bias, db, p.sh.k, p.split);
+  }
   return cudaGetLastError();
 }
 

@@ -195,3 +195,53 @@ def test_forward_tc_ragged(shape, dt):
     p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
     check_fwd(p, 6, ["fwd_tc", "generic"], [-1, 1, 3])
     assert cig.device_errors() == 0
+
+
+# ------------------------------------------------------- depthwise / grouped
+
+
+def test_config4_depthwise_full():
+    """Depthwise 7x7 wgrad bf16, N=32, 56x56, C=K=384 (groups=384), pad 3, N(0,1) seed 3."""
+    p = cig.Problem(n=32, h=56, w=56, c=384, k=384, r=7, s=7, pad_h=3, pad_w=3, groups=384,
+                    in_dtype=BF16, out_dtype=BF16)
+    assert cig.describe_plan(p, cig.DIR_WGRAD, -1)["kernel_name"] == "wgrad_depthwise"
+    check_wgrad(p, 3, ["auto"], [-1, 1, 7], bias=False)
+    assert cig.device_errors() == 0
+
+
+@pytest.mark.parametrize("shape", [
+    dict(n=3, h=13, w=17, c=128, k=128, groups=128, r=5, s=5, pad_h=2, pad_w=2),
+    dict(n=2, h=9, w=30, c=64, k=64, groups=64, r=3, s=3, pad_h=1, pad_w=1),
+    dict(n=1, h=12, w=20, c=64, k=64, groups=64, r=3, s=11, pad_h=1, pad_w=5),
+    dict(n=2, h=10, w=12, c=64, k=64, groups=64, r=7, s=7),                  # no padding: Wo = W - 6
+    dict(n=3, h=5, w=9, c=192, k=192, groups=192, r=7, s=7, pad_h=3, pad_w=3),  # fewer rows than taps
+])
+@pytest.mark.parametrize("dt", [(BF16, BF16), (BF16, F32), (F16, F16)], ids=lambda d: f"{d[0]}{d[1]}")
+def test_depthwise_ragged(shape, dt):
+    p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
+    check_wgrad(p, 8, ["wgrad_depthwise", "generic"], [-1, 1, 4], bias=True)
+    assert cig.device_errors() == 0
+
+
+@pytest.mark.parametrize("groups", [64, 128], ids=["cpg8", "cpg4"])
+def test_config5_grouped_full(groups):
+    """Grouped 3x3 wgrad fp16, N=64, 28x28, C=K=512, groups 64 / 128, pad 1, N(0,1) seed 4."""
+    p = cig.Problem(n=64, h=28, w=28, c=512, k=512, r=3, s=3, pad_h=1, pad_w=1, groups=groups,
+                    in_dtype=F16, out_dtype=F16)
+    assert cig.describe_plan(p, cig.DIR_WGRAD, -1)["kernel_name"] == "wgrad_grouped"
+    check_wgrad(p, 4, ["auto"], [-1, 1, 9], bias=False)
+    assert cig.device_errors() == 0
+
+
+@pytest.mark.parametrize("shape", [
+    dict(n=3, h=11, w=13, c=128, k=128, groups=16, r=3, s=3, pad_h=1, pad_w=1),   # cpg 8
+    dict(n=2, h=9, w=30, c=64, k=64, groups=16, r=3, s=3, pad_h=1, pad_w=1),      # cpg 4
+    dict(n=2, h=7, w=9, c=64, k=64, groups=16, r=5, s=5, pad_h=2, pad_w=2),       # cpg 4, 5x5
+    dict(n=4, h=6, w=6, c=192, k=192, groups=24, r=1, s=1),                         # cpg 8, pointwise
+    dict(n=1, h=4, w=5, c=64, k=64, groups=8, r=3, s=3),                            # no padding
+])
+@pytest.mark.parametrize("dt", [(F16, F16), (BF16, F32)], ids=lambda d: f"{d[0]}{d[1]}")
+def test_grouped_ragged(shape, dt):
+    p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
+    check_wgrad(p, 9, ["wgrad_grouped", "generic"], [-1, 1, 3], bias=True)
+    assert cig.device_errors() == 0
