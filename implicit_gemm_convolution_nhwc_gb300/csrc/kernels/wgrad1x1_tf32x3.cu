@@ -47,48 +47,52 @@ constexpr int kChunk = kBP * 128;         // bytes of one 32-channel x kBP-row r
 constexpr int kBK = 64;                   // k rows of an output tile (M = 2 x 64 with the split)
 constexpr int kSmemBudget = 200 * 1024;
 constexpr int kPeriod = 16;               // blocks accumulated in TMEM before a drain
-constexpr int kQ = 4;                     // operand stages
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDcol = 192;           // accumulator buffer b at column kDcol * b
 constexpr uint32_t kAcol = 384;           // operand A ring at columns 384 + 32 * stage
+constexpr int kMaxRaw = 12;               // raw stages at most (barrier area)
 
-template <int BC>
+// BC: output channels c of a tile; Q: operand stages (the raw ring gets the
+// rest of the shared-memory budget).
+template <int BC, int Q>
 struct Cfg {
+  static constexpr int QS = Q;
   static constexpr int NC = BC / 32;                      // raw X chunks per stage
   static constexpr int RAW = (2 + NC) * kChunk;           // raw dY (2 chunks) + raw X
   static constexpr int OPB = 2 * BC * 128;                // K-major B: 2*BC rows x 128 B
-  static constexpr int R0 = (kSmemBudget - kQ * OPB) / RAW;
-  static constexpr int R = R0 > 8 ? 8 : R0;               // raw stages
+  static constexpr int R0 = (kSmemBudget - QS * OPB) / RAW;
+  static constexpr int R = R0 > kMaxRaw ? kMaxRaw : R0;   // raw stages
   static constexpr int N = 2 * BC;
   static constexpr int HALF = BC / 2;                     // output columns per converter thread
   static constexpr uint32_t TX = (uint32_t)RAW;
-  static constexpr int BAR_BYTES = 256;
-  static constexpr size_t SMEM = 1024 + (size_t)R * RAW + (size_t)kQ * OPB + BAR_BYTES;
+  static constexpr int BAR_BYTES = 512;
+  static constexpr size_t SMEM = 1024 + (size_t)R * RAW + (size_t)QS * OPB + BAR_BYTES;
   static constexpr uint32_t IDESC = mma_idesc(2u, 0u, 0u, (uint32_t)N, 128u);
   static_assert(R >= 2, "raw pipeline too shallow");
+  static_assert((2 * R + 2 * QS + 4) * 8 + 8 <= BAR_BYTES, "barrier area too small");
   static_assert(N % 16 == 0 && N >= 16 && N <= (int)kDcol, "invalid MMA N for M=128");
-  static_assert(kAcol + 32 * kQ <= kTmemCols && kDcol * 2 <= kAcol, "TMEM overflow");
-  static_assert(kQ < kPeriod, "a drain must come before its buffer is reused");
+  static_assert(kAcol + 32 * QS <= kTmemCols && kDcol * 2 <= kAcol, "TMEM overflow");
+  static_assert(QS < kPeriod, "a drain must come before its buffer is reused");
 };
 
 __device__ __forceinline__ float tf32_hi(float v) { return __uint_as_float(__float_as_uint(v) & 0xFFFFE000u); }
 
-template <int BC>
+template <int BC, int Q>
 __global__ void __launch_bounds__(kThreads, 1)
     wgrad1x1_tf32x3_kernel(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_x,
                            float* __restrict__ out, float* __restrict__ ws, float* __restrict__ db,
                            float* __restrict__ ws_bias, int64_t K, int64_t C, int64_t blocks_per_sample,
                            int64_t tiles_c, int64_t tiles, int32_t S, int64_t blocks, unsigned* err) {
-  using G = Cfg<BC>;
+  using G = Cfg<BC, Q>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* raw = smem;                                   // R raw stages
-  uint8_t* opb = smem + (size_t)G::R * G::RAW;           // kQ operand (B) stages
-  uint64_t* raw_full = reinterpret_cast<uint64_t*>(opb + (size_t)kQ * G::OPB);
+  uint8_t* opb = smem + (size_t)G::R * G::RAW;           // G::QS operand (B) stages
+  uint64_t* raw_full = reinterpret_cast<uint64_t*>(opb + (size_t)G::QS * G::OPB);
   uint64_t* raw_empty = raw_full + G::R;
   uint64_t* op_full = raw_empty + G::R;
-  uint64_t* op_empty = op_full + kQ;
-  uint64_t* acc_full = op_empty + kQ;                    // [2]
+  uint64_t* op_empty = op_full + G::QS;
+  uint64_t* acc_full = op_empty + G::QS;                    // [2]
   uint64_t* acc_empty = acc_full + 2;                    // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -107,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&raw_full[i], 1);
       mbar_init(&raw_empty[i], kConv);
     }
-    for (int i = 0; i < kQ; ++i) {
+    for (int i = 0; i < G::QS; ++i) {
       mbar_init(&op_full[i], kConv);
       mbar_init(&op_empty[i], 1);
     }
@@ -157,13 +161,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t bbase = smem_u32(opb);
       for (int64_t it = 0; it < nblk; ++it) {
-        const int s = (int)(it % kQ);
+        const int s = (int)(it % G::QS);
         const int64_t per = it / kPeriod;
         const int within = (int)(it % kPeriod);
         const uint32_t d = tmem + kDcol * (uint32_t)(per & 1);
         if (within == 0 && per >= 2 && !mbar_wait(&acc_empty[per & 1], (uint32_t)((per >> 1) - 1) & 1u, abort_flag, err))
           break;
-        if (!mbar_wait(&op_full[s], (uint32_t)(it / kQ) & 1u, abort_flag, err)) break;
+        if (!mbar_wait(&op_full[s], (uint32_t)(it / G::QS) & 1u, abort_flag, err)) break;
         tc_fence_after();
         const uint32_t b = bbase + (uint32_t)(s * G::OPB);
         const uint32_t a = tmem + kAcol + 32u * (uint32_t)s;
@@ -228,13 +232,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     for (int64_t it = 0; it < nblk; ++it) {
       const int rs = (int)(it % G::R);
-      const int qs = (int)(it % kQ);
-      if (it >= kPeriod + kQ && (it - kQ) % kPeriod == 0) {
+      const int qs = (int)(it % G::QS);
+      if (it >= kPeriod + G::QS && (it - G::QS) % kPeriod == 0) {
         if (!drain(drained)) { alive = false; break; }
         ++drained;
       }
       if (!mbar_wait(&raw_full[rs], (uint32_t)(it / G::R) & 1u, abort_flag, err)) { alive = false; break; }
-      if (it >= kQ && !mbar_wait(&op_empty[qs], (uint32_t)(it / kQ - 1) & 1u, abort_flag, err)) {
+      if (it >= G::QS && !mbar_wait(&op_empty[qs], (uint32_t)(it / G::QS - 1) & 1u, abort_flag, err)) {
         alive = false;
         break;
       }
@@ -333,9 +337,9 @@ int pick_bc(int64_t C) {
   return 96;
 }
 
-template <int BC>
+template <int BC, int Q>
 cudaError_t launch_bc(const Plan& p, const Args& a) {
-  using G = Cfg<BC>;
+  using G = Cfg<BC, Q>;
   const Shape& s = p.sh;
   const int64_t hw = s.h * s.w;
   CUtensorMap tm_dy, tm_x;
@@ -349,14 +353,14 @@ cudaError_t launch_bc(const Plan& p, const Args& a) {
       !encode_tmap(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.x, x_dims, x_strides, box,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  cudaError_t err = cudaFuncSetAttribute(wgrad1x1_tf32x3_kernel<BC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t err = cudaFuncSetAttribute(wgrad1x1_tf32x3_kernel<BC, Q>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)G::SMEM);
   if (err != cudaSuccess) return err;
   const int64_t ctas = p.geo.tiles * p.split;
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const int64_t tiles_c = (s.c + BC - 1) / BC;
   const int64_t bps = (hw + kBP - 1) / kBP;
-  wgrad1x1_tf32x3_kernel<BC><<<(unsigned)ctas, kThreads, G::SMEM, a.stream>>>(
+  wgrad1x1_tf32x3_kernel<BC, Q><<<(unsigned)ctas, kThreads, G::SMEM, a.stream>>>(
       tm_dy, tm_x, static_cast<float*>(a.out), a.ws, p.with_bias ? static_cast<float*>(a.db) : nullptr, a.ws_bias,
       s.k, s.c, bps, tiles_c, p.geo.tiles, p.split, p.geo.blocks, device_error_word());
   return cudaGetLastError();
@@ -381,10 +385,12 @@ Geometry geometry_wgrad1x1_tf32x3(const Shape& s) {
 }
 
 cudaError_t launch_wgrad1x1_tf32x3(const Plan& p, const Args& a) {
+  // Three operand stages (the rest of shared memory feeds the raw ring):
+  // measured best of 2, 3 and 4 on the N=64 512x512 C=96 K=64 problem.
   switch (pick_bc(p.sh.c)) {
-    case 32: return launch_bc<32>(p, a);
-    case 64: return launch_bc<64>(p, a);
-    default: return launch_bc<96>(p, a);
+    case 32: return launch_bc<32, 3>(p, a);
+    case 64: return launch_bc<64, 3>(p, a);
+    default: return launch_bc<96, 3>(p, a);
   }
 }
 
