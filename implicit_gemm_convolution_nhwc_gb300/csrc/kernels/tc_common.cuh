@@ -221,8 +221,11 @@ __host__ __device__ constexpr uint32_t mma_idesc(uint32_t fmt, uint32_t a_mn, ui
   return (1u << 4) | (fmt << 7) | (fmt << 10) | (a_mn << 15) | (b_mn << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
+// Rounds a pointer into dynamic shared memory up to 1024 bytes by pointer
+// arithmetic (not through an integer), so the compiler still knows it points
+// to shared memory and emits shared loads/stores rather than generic ones.
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+  return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
 }
 
 // Host: encode a tiled tensor map (through the driver entry point, no -lcuda).
