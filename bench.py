@@ -209,13 +209,20 @@ def recorded_traffic(kernel_name: str, workload: str):
     entry = table.get(f"{kernel_name}:{workload}")
     if not entry:
         return None
-    src = os.path.join(ROOT, "implicit_gemm_convolution_nhwc_gb300", "csrc", "kernels", entry["source"])
-    if not os.path.exists(src):
-        return None
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if digest != entry.get("source_sha256_16"):
+    if sources_digest(entry["sources"]) != entry.get("sources_sha256_16"):
         return None
     return entry["dram_bytes_per_launch"]
+
+
+def sources_digest(rel_paths) -> str | None:
+    """sha256 (first 16 hex digits) over the listed csrc files, in order."""
+    h = hashlib.sha256()
+    for rel in rel_paths:
+        path = os.path.join(ROOT, "implicit_gemm_convolution_nhwc_gb300", "csrc", rel)
+        if not os.path.exists(path):
+            return None
+        h.update(open(path, "rb").read())
+    return h.hexdigest()[:16]
 
 
 # ------------------------------------------------------------------ oracle
