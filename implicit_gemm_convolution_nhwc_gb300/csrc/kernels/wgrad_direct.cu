@@ -11,21 +11,21 @@
 // FP32-FMA bound (18-36 flop per byte of input), not HBM bound.
 //
 // CTA: 64 channels (= 64/Cg whole groups) and one slice of the batch's output
-// rows (n, ho); 16 warps. Rows come in with 16-byte global loads issued two
-// rows ahead into registers, are widened ONCE to fp32 and stored in a shared
-// ring (R + 1 input rows, padded with pw zero columns on each side; 2 dY
-// rows), so the inner loop is only shared loads and packed FMAs
-// (__ffma2_rn). Warp w < R*WS owns filter row r = w % R and part w / R of
-// every output row (WS = 16 / R parts). Lane l owns output channels
-// c0 + 2l and c0 + 2l + 1:
+// rows (n, ho); 16 warps. A step covers RB output rows at once. Rows come in
+// with 16-byte global loads issued two steps ahead into registers, are
+// widened ONCE to fp32 and stored in a shared ring (R + 2 RB - 1 input rows,
+// padded with pw zero columns on each side; 2 RB dY rows), so the inner loop
+// is only shared loads and packed FMAs (__ffma2_rn). Warp w < R*RB*WS owns
+// filter row r = w % R, row q = (w / R) % RB of the step and part w / (R RB)
+// of that output row. Lane l owns output channels c0 + 2l and c0 + 2l + 1:
 //  - depthwise: per pixel one float2 of dY and one float2 of X (the same two
 //    channels); S packed FMAs on a register window of S input pixels that
 //    rotates without moves (the loop is unrolled by S);
 //  - grouped: per pixel the dY pair (broadcast once into two register pairs)
 //    and the group's Cg input channels as Cg/2 pairs; S*Cg packed FMAs.
-// The filter-row-0 warps also sum db. One __syncthreads per output row.
-// The parts of a filter row are added in part order at the end, and the
-// slice's partial sums go to an fp32 slab ("feat(rocke): split-K forward
+// The filter-row-0 warps also sum db. One __syncthreads per step. At the end
+// the warps of each filter row are added in warp order, and the slice's
+// partial sums go to an fp32 slab ("feat(rocke): split-K forward
 // implicit-GEMM convolution on gfx1250", "Two-stage split-K") or, with one
 // slice, straight to dW / db.
 #include "common.cuh"
@@ -36,22 +36,25 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCG = 64;            // channels per CTA
-constexpr int kPixIn = kCG * 2;    // bytes per pixel in global memory (16-bit)
 constexpr int kPix = kCG * 4;      // bytes per pixel in the fp32 ring
-constexpr int kMaxItems = 2;       // 16-byte loads per thread per row step
+// 16-byte loads per thread per step (prefetch registers): fewer where the
+// 8-channel groups need the registers for accumulators.
+__host__ __device__ constexpr int load_slots(int cpg) { return cpg == 8 ? 2 : 4; }
 constexpr int kMaxW = 256;
-constexpr int kSmemLimit = 200 * 1024;
+constexpr int kSmemLimit = 220 * 1024;
 
 struct DirParams {
   int64_t N, H, W, C, Ho, Wo;
   int32_t R, ph, pw;
+  int32_t RB;          // output rows per step
   int32_t WS;          // parts per output row
+  int32_t XR;          // input rows in the ring: R + 2 RB - 1
   int64_t rows;        // N * Ho: the reduction blocks
   int64_t groups;      // C / 64: the tiles
   int32_t split;
-  int32_t xrow_bytes;  // (W + 2 pw + S) * 256
+  int32_t xrow_bytes;  // (W + 2 pw + 1) * 256
   int32_t dyrow_bytes; // Wo * 256
-  int32_t items;       // 16-byte global loads per row step: (W + Wo) * 8
+  int32_t row_items;   // 16-byte loads per output row: (W + Wo) * 8
 };
 
 template <typename TI>
@@ -65,6 +68,9 @@ __device__ __forceinline__ float2 unpack2<__half>(uint32_t u) {
   __half2 h = *reinterpret_cast<__half2*>(&u);
   return __half22float2(h);
 }
+
+// c + a * b on both halves of a register pair (one packed FP32 FMA).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
 // Accumulators of one lane: depthwise (CPG = 1) v[s][0][0] = (dW[c][r][s], dW[c+1][r][s]);
 // grouped v[s][ki][cp] = (dW[k+ki][r][s][2cp], dW[k+ki][r][s][2cp+1]).
@@ -92,25 +98,27 @@ __device__ __forceinline__ void row_pass(const uint8_t* xrow, const uint8_t* dyr
 #pragma unroll
   for (int j = 0; j < S; ++j) load_x(wo_a + j, win[j]);
   int wo = wo_a;
-  for (; wo + S <= wo_b; wo += S) {
+  {
+    for (; wo + S <= wo_b; wo += S) {
 #pragma unroll
-    for (int t = 0; t < S; ++t) {
-      const float2 d = *reinterpret_cast<const float2*>(dp + (wo + t) * kPix);
-      if constexpr (CPG == 1) {
+      for (int t = 0; t < S; ++t) {
+        const float2 d = *reinterpret_cast<const float2*>(dp + (wo + t) * kPix);
+        if constexpr (CPG == 1) {
 #pragma unroll
-        for (int j = 0; j < S; ++j) acc.v[j][0][0] = __ffma2_rn(d, win[(t + j) % S][0], acc.v[j][0][0]);
-      } else {
-        const float2 d0 = make_float2(d.x, d.x), d1 = make_float2(d.y, d.y);
+          for (int j = 0; j < S; ++j) acc.v[j][0][0] = fma2(d, win[(t + j) % S][0], acc.v[j][0][0]);
+        } else {
+          const float2 d0 = make_float2(d.x, d.x), d1 = make_float2(d.y, d.y);
 #pragma unroll
-        for (int j = 0; j < S; ++j)
+          for (int j = 0; j < S; ++j)
 #pragma unroll
-          for (int c = 0; c < CP; ++c) {
-            acc.v[j][0][c] = __ffma2_rn(d0, win[(t + j) % S][c], acc.v[j][0][c]);
-            acc.v[j][1][c] = __ffma2_rn(d1, win[(t + j) % S][c], acc.v[j][1][c]);
-          }
+            for (int c = 0; c < CP; ++c) {
+              acc.v[j][0][c] = fma2(d0, win[(t + j) % S][c], acc.v[j][0][c]);
+              acc.v[j][1][c] = fma2(d1, win[(t + j) % S][c], acc.v[j][1][c]);
+            }
+        }
+        if (BIAS) bsum = __fadd2_rn(bsum, d);
+        if (t + 1 < S || wo + S < wo_b) load_x(wo + t + S, win[t]);
       }
-      if (BIAS) bsum = __fadd2_rn(bsum, d);
-      load_x(wo + t + S, win[t]);
     }
   }
   for (; wo < wo_b; ++wo) {  // the last (wo_b - wo_a) % S pixels
@@ -121,13 +129,13 @@ __device__ __forceinline__ void row_pass(const uint8_t* xrow, const uint8_t* dyr
       float2 v[CP];
       load_x(wo + j, v);
       if constexpr (CPG == 1) {
-        acc.v[j][0][0] = __ffma2_rn(d, v[0], acc.v[j][0][0]);
+        acc.v[j][0][0] = fma2(d, v[0], acc.v[j][0][0]);
       } else {
         const float2 d0 = make_float2(d.x, d.x), d1 = make_float2(d.y, d.y);
 #pragma unroll
         for (int c = 0; c < CP; ++c) {
-          acc.v[j][0][c] = __ffma2_rn(d0, v[c], acc.v[j][0][c]);
-          acc.v[j][1][c] = __ffma2_rn(d1, v[c], acc.v[j][1][c]);
+          acc.v[j][0][c] = fma2(d0, v[c], acc.v[j][0][c]);
+          acc.v[j][1][c] = fma2(d1, v[c], acc.v[j][1][c]);
         }
       }
     }
@@ -139,22 +147,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     direct_wgrad_kernel(const TI* __restrict__ x, const TI* __restrict__ dy, TO* out, float* ws, TO* db,
                         float* ws_bias, DirParams p) {
   using A = Acc<S, CPG>;
+  constexpr int MI = load_slots(CPG);
   extern __shared__ __align__(16) uint8_t smem[];
-  const int ring = p.R + 1;
-  uint8_t* xring = smem;                                   // ring rows of (W + 2 pw + S) pixels, fp32
-  uint8_t* dyring = smem + (size_t)ring * p.xrow_bytes;    // 2 rows of Wo pixels, fp32
+  uint8_t* xring = smem;                                      // XR rows of (W + 2 pw + 1) pixels, fp32
+  uint8_t* dyring = smem + (size_t)p.XR * p.xrow_bytes;       // 2 RB rows of Wo pixels, fp32
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, tid = threadIdx.x;
   const int64_t g = blockIdx.x % p.groups;
   const int32_t sigma = (int32_t)(blockIdx.x / p.groups);
   const int64_t c0 = g * kCG;
   const int64_t row_b = slice_begin(p.rows, p.split, sigma), row_e = slice_begin(p.rows, p.split, sigma + 1);
-  const bool compute = warp < p.R * p.WS;
-  const int r = warp % p.R, part = warp / p.R;
+  const bool compute = warp < p.R * p.RB * p.WS;
+  const int r = warp % p.R, q = (warp / p.R) % p.RB, part = warp / (p.R * p.RB);
   const int wo_a = compute ? (int)((p.Wo * part) / p.WS) : 0;
   const int wo_b = compute ? (int)((p.Wo * (part + 1)) / p.WS) : 0;
   const bool bias_warp = compute && r == 0 && db != nullptr;
+  const int x_items = (int)p.W * 8;
 
-  for (int i = tid * 16; i < ring * p.xrow_bytes; i += kThreads * 16)
+  for (int i = tid * 16; i < p.XR * p.xrow_bytes; i += kThreads * 16)
     *reinterpret_cast<uint4*>(xring + i) = make_uint4(0, 0, 0, 0);
 
   A acc;
@@ -166,131 +175,124 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < A::CP; ++c) acc.v[j][ki][c] = make_float2(0.f, 0.f);
   float2 bsum = make_float2(0.f, 0.f);
 
-  // Row-step data of output row ho of image n: X row ho - ph + R - 1 (the row
-  // that enters the window) and dY row ho, as 16-byte items per thread.
-  uint4 buf[2][kMaxItems];
-  auto fetch = [&](int64_t n, int64_t ho, uint4* b) {
-    const int64_t h = ho - p.ph + p.R - 1;
-    const bool inside = h >= 0 && h < p.H;
+  auto xslot = [&](int64_t h) -> uint8_t* {
+    return xring + (size_t)(((h % p.XR) + p.XR) % p.XR) * p.xrow_bytes + p.pw * kPix;
+  };
+  auto dyslot = [&](int64_t ho) -> uint8_t* { return dyring + (size_t)(ho % (2 * p.RB)) * p.dyrow_bytes; };
+  auto widen_to = [&](uint8_t* dst, uint4 u) {
+    const float2 a = unpack2<TI>(u.x), b = unpack2<TI>(u.y), c = unpack2<TI>(u.z), d = unpack2<TI>(u.w);
+    reinterpret_cast<float4*>(dst)[0] = make_float4(a.x, a.y, b.x, b.y);
+    reinterpret_cast<float4*>(dst)[1] = make_float4(c.x, c.y, d.x, d.y);
+  };
+  // The data a step brings in: for output rows ho0 .. ho0 + nr - 1, the input
+  // rows that enter the window (ho - ph + R - 1) and the dY rows.
+  auto fetch = [&](int64_t n, int64_t ho0, int nr, uint4* b) {
 #pragma unroll
-    for (int m = 0; m < kMaxItems; ++m) {
+    for (int m = 0; m < MI; ++m) {
       const int i = tid + m * kThreads;
       b[m] = make_uint4(0, 0, 0, 0);
-      if (i < p.W * 8) {
-        if (inside) b[m] = __ldg(reinterpret_cast<const uint4*>(x + ((n * p.H + h) * p.W + (i >> 3)) * p.C + c0 + (i & 7) * 8));
-      } else if (i < p.items) {
-        const int j = i - (int)p.W * 8;
+      const int qq = i / p.row_items, rem = i - qq * p.row_items;
+      if (qq >= nr) continue;
+      const int64_t ho = ho0 + qq;
+      if (rem < x_items) {
+        const int64_t h = ho - p.ph + p.R - 1;
+        if (h >= 0 && h < p.H)
+          b[m] = __ldg(reinterpret_cast<const uint4*>(x + ((n * p.H + h) * p.W + (rem >> 3)) * p.C + c0 + (rem & 7) * 8));
+      } else {
+        const int j = rem - x_items;
         b[m] = __ldg(reinterpret_cast<const uint4*>(dy + ((n * p.Ho + ho) * p.Wo + (j >> 3)) * p.C + c0 + (j & 7) * 8));
       }
     }
   };
-  auto widen_store = [&](int64_t ho, const uint4* b) {
-    const int64_t h = ho - p.ph + p.R - 1;
-    uint8_t* xdst = xring + (size_t)(((h % ring) + ring) % ring) * p.xrow_bytes + p.pw * kPix;
-    uint8_t* ddst = dyring + (size_t)(ho & 1) * p.dyrow_bytes;
+  auto store = [&](int64_t ho0, int nr, const uint4* b) {
 #pragma unroll
-    for (int m = 0; m < kMaxItems; ++m) {
+    for (int m = 0; m < MI; ++m) {
       const int i = tid + m * kThreads;
-      if (i >= p.items) break;
-      const uint4 u = b[m];
-      const float2 a = unpack2<TI>(u.x), bb = unpack2<TI>(u.y), c = unpack2<TI>(u.z), d = unpack2<TI>(u.w);
-      uint8_t* dst = i < p.W * 8 ? xdst + (i >> 3) * kPix + (i & 7) * 32
-                                 : ddst + ((i - (int)p.W * 8) >> 3) * kPix + ((i - (int)p.W * 8) & 7) * 32;
-      reinterpret_cast<float4*>(dst)[0] = make_float4(a.x, a.y, bb.x, bb.y);
-      reinterpret_cast<float4*>(dst)[1] = make_float4(c.x, c.y, d.x, d.y);
-    }
-  };
-  // The first R - 1 input rows of a window (ho_a - ph .. ho_a - ph + R - 2).
-  auto prologue_rows = [&](int64_t n, int64_t ho_a) {
-    for (int rr = 0; rr + 1 < p.R; ++rr) {
-      uint4 b[kMaxItems];
-      const int64_t h = ho_a - p.ph + rr;
-      const bool inside = h >= 0 && h < p.H;
-      uint8_t* xdst = xring + (size_t)(((h % ring) + ring) % ring) * p.xrow_bytes + p.pw * kPix;
-#pragma unroll
-      for (int m = 0; m < kMaxItems; ++m) {
-        const int i = tid + m * kThreads;
-        b[m] = make_uint4(0, 0, 0, 0);
-        if (inside && i < p.W * 8)
-          b[m] = __ldg(reinterpret_cast<const uint4*>(x + ((n * p.H + h) * p.W + (i >> 3)) * p.C + c0 + (i & 7) * 8));
-      }
-#pragma unroll
-      for (int m = 0; m < kMaxItems; ++m) {
-        const int i = tid + m * kThreads;
-        if (i >= p.W * 8) break;
-        const uint4 u = b[m];
-        const float2 a = unpack2<TI>(u.x), bb = unpack2<TI>(u.y), c = unpack2<TI>(u.z), d = unpack2<TI>(u.w);
-        uint8_t* dst = xdst + (i >> 3) * kPix + (i & 7) * 32;
-        reinterpret_cast<float4*>(dst)[0] = make_float4(a.x, a.y, bb.x, bb.y);
-        reinterpret_cast<float4*>(dst)[1] = make_float4(c.x, c.y, d.x, d.y);
-      }
+      const int qq = i / p.row_items, rem = i - qq * p.row_items;
+      if (qq >= nr) continue;
+      const int64_t ho = ho0 + qq;
+      if (rem < x_items) widen_to(xslot(ho - p.ph + p.R - 1) + (rem >> 3) * kPix + (rem & 7) * 32, b[m]);
+      else widen_to(dyslot(ho) + ((rem - x_items) >> 3) * kPix + ((rem - x_items) & 7) * 32, b[m]);
     }
   };
 
+  uint4 bufA[MI], bufB[MI];
   for (int64_t row = row_b; row < row_e;) {
     const int64_t n = row / p.Ho;
     const int64_t ho_a = row % p.Ho;
     const int64_t ho_b = (n + 1) * p.Ho <= row_e ? p.Ho : row_e - n * p.Ho;
+    auto rows_at = [&](int64_t ho0) -> int { return (int)(ho0 + p.RB <= ho_b ? p.RB : ho_b - ho0); };
     __syncthreads();  // the previous image's rows are no longer read
-    prologue_rows(n, ho_a);
-    fetch(n, ho_a, buf[0]);
-    widen_store(ho_a, buf[0]);
-    if (ho_a + 1 < ho_b) fetch(n, ho_a + 1, buf[1]);
-    if (ho_a + 2 < ho_b) fetch(n, ho_a + 2, buf[0]);
-    // One output row: nxt holds row step ho + 1 on entry and is refilled with
-    // step ho + 3 (the other buffer holds step ho + 2).
-    auto step = [&](int64_t ho, uint4* nxt) {
-      __syncthreads();  // row step ho is in shared memory; step ho - 1 is done
-      if (ho + 1 < ho_b) widen_store(ho + 1, nxt);
-      if (ho + 3 < ho_b) fetch(n, ho + 3, nxt);
-      if (compute) {
-        const int64_t h = ho - p.ph + r;
-        const uint8_t* xr = xring + (size_t)(((h % ring) + ring) % ring) * p.xrow_bytes;
-        const uint8_t* dr = dyring + (size_t)(ho & 1) * p.dyrow_bytes;
+    // Prologue: the first R - 1 input rows of the window, straight to the ring.
+    for (int rr = 0; rr + 1 < p.R; ++rr) {
+      const int64_t h = ho_a - p.ph + rr;
+      for (int i = tid; i < x_items; i += kThreads) {
+        uint4 u = make_uint4(0, 0, 0, 0);
+        if (h >= 0 && h < p.H)
+          u = __ldg(reinterpret_cast<const uint4*>(x + ((n * p.H + h) * p.W + (i >> 3)) * p.C + c0 + (i & 7) * 8));
+        widen_to(xslot(h) + (i >> 3) * kPix + (i & 7) * 32, u);
+      }
+    }
+    fetch(n, ho_a, rows_at(ho_a), bufA);
+    store(ho_a, rows_at(ho_a), bufA);
+    if (ho_a + p.RB < ho_b) fetch(n, ho_a + p.RB, rows_at(ho_a + p.RB), bufB);
+    if (ho_a + 2 * p.RB < ho_b) fetch(n, ho_a + 2 * p.RB, rows_at(ho_a + 2 * p.RB), bufA);
+    // One step: rows ho0 .. ho0 + RB - 1. nxt holds step ho0 + RB on entry and is
+    // refilled with step ho0 + 3 RB (the other buffer holds step ho0 + 2 RB).
+    auto step = [&](int64_t ho0, uint4* nxt) {
+      __syncthreads();  // this step's rows are in shared memory; the previous step is done
+      const int64_t h1 = ho0 + p.RB, h3 = ho0 + 3 * p.RB;
+      if (h1 < ho_b) store(h1, rows_at(h1), nxt);
+      if (h3 < ho_b) fetch(n, h3, rows_at(h3), nxt);
+      const int64_t ho = ho0 + q;
+      if (compute && ho < ho_b) {
+        const uint8_t* xr = xslot(ho - p.ph + r) - p.pw * kPix;
+        const uint8_t* dr = dyslot(ho);
         if (bias_warp) row_pass<S, CPG, true>(xr, dr, wo_a, wo_b, lane, acc, bsum);
         else row_pass<S, CPG, false>(xr, dr, wo_a, wo_b, lane, acc, bsum);
       }
     };
     // Unrolled by two so each buffer is named at compile time (kept in registers).
-    for (int64_t ho = ho_a; ho < ho_b; ho += 2) {
-      step(ho, buf[1]);
-      if (ho + 1 < ho_b) step(ho + 1, buf[0]);
+    for (int64_t ho0 = ho_a; ho0 < ho_b; ho0 += 2 * p.RB) {
+      step(ho0, bufB);
+      if (ho0 + p.RB < ho_b) step(ho0 + p.RB, bufA);
     }
     row = n * p.Ho + ho_b;
   }
 
-  // Add the WS parts of each filter row in part order, then store.
+  // Add the warps of each filter row in warp order, then store.
   constexpr int PER = S * A::KI * A::CP * 2 + 2;  // dW partials, then the db pair
   __syncthreads();
   float* red = reinterpret_cast<float*>(smem);
-  if (compute && part > 0) {
+  const bool leader = compute && warp < p.R;
+  if (compute && !leader) {
     float* dst = red + ((size_t)warp * 32 + lane) * PER;
-    int q = 0;
+    int o = 0;
 #pragma unroll
     for (int j = 0; j < S; ++j)
 #pragma unroll
       for (int ki = 0; ki < A::KI; ++ki)
 #pragma unroll
         for (int c = 0; c < A::CP; ++c) {
-          dst[q++] = acc.v[j][ki][c].x;
-          dst[q++] = acc.v[j][ki][c].y;
+          dst[o++] = acc.v[j][ki][c].x;
+          dst[o++] = acc.v[j][ki][c].y;
         }
     dst[PER - 2] = bsum.x;
     dst[PER - 1] = bsum.y;
   }
   __syncthreads();
-  if (!(compute && part == 0)) return;
-  for (int pt = 1; pt < p.WS; ++pt) {
-    const float* src = red + ((size_t)(pt * p.R + r) * 32 + lane) * PER;
-    int q = 0;
+  if (!leader) return;
+  for (int w = warp + p.R; w < p.R * p.RB * p.WS; w += p.R) {
+    const float* src = red + ((size_t)w * 32 + lane) * PER;
+    int o = 0;
 #pragma unroll
     for (int j = 0; j < S; ++j)
 #pragma unroll
       for (int ki = 0; ki < A::KI; ++ki)
 #pragma unroll
         for (int c = 0; c < A::CP; ++c) {
-          acc.v[j][ki][c].x += src[q++];
-          acc.v[j][ki][c].y += src[q++];
+          acc.v[j][ki][c].x += src[o++];
+          acc.v[j][ki][c].y += src[o++];
         }
     bsum.x += src[PER - 2];
     bsum.y += src[PER - 1];
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
   }
-  if (bias_warp) {
+  if (r == 0 && db) {
     if (ws_bias) {
       ws_bias[(int64_t)sigma * p.C + k] = bsum.x;
       ws_bias[(int64_t)sigma * p.C + k + 1] = bsum.y;
@@ -329,40 +331,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-DirParams make_params(const Shape& s, int32_t split) {
+size_t smem_bytes(const DirParams& p, int S, int cpg) {
+  const size_t ringb = (size_t)p.XR * p.xrow_bytes + 2 * (size_t)p.RB * p.dyrow_bytes;
+  const int per = S * (cpg == 1 ? 2 : 2 * cpg) + 2;
+  const size_t red = (size_t)(p.R * p.RB * p.WS) * 32 * per * 4;
+  return ringb > red ? ringb : red;
+}
+
+// Rows per step: as many as the warps, the shared-memory budget and the
+// per-thread load slots allow.
+DirParams make_params(const Shape& s, int32_t split, int cpg) {
   DirParams p;
   p.N = s.n; p.H = s.h; p.W = s.w; p.C = s.c; p.Ho = s.ho; p.Wo = s.wo;
   p.R = (int32_t)s.r; p.ph = (int32_t)s.ph; p.pw = (int32_t)s.pw;
-  p.WS = kWarps / p.R;
   p.rows = s.n * s.ho;
   p.groups = s.c / kCG;
   p.split = split;
-  p.xrow_bytes = (int32_t)((s.w + 2 * s.pw + s.s) * kPix);
+  p.xrow_bytes = (int32_t)((s.w + 2 * s.pw + 1) * kPix);
   p.dyrow_bytes = (int32_t)(s.wo * kPix);
-  p.items = (int32_t)((s.w + s.wo) * 8);
+  p.row_items = (int32_t)((s.w + s.wo) * 8);
+  p.RB = 1;
+  for (int rb = kWarps / p.R; rb >= 1; --rb) {
+    DirParams t = p;
+    t.RB = rb;
+    t.WS = kWarps / (p.R * rb);
+    t.XR = p.R + 2 * rb - 1;
+    if ((int64_t)rb * p.row_items <= (int64_t)load_slots(cpg) * kThreads && smem_bytes(t, (int)s.s, cpg) <= kSmemLimit) {
+      p.RB = rb;
+      break;
+    }
+  }
+  p.WS = kWarps / (p.R * p.RB);
+  p.XR = p.R + 2 * p.RB - 1;
   return p;
-}
-
-size_t smem_bytes(const DirParams& p, int S, int cpg) {
-  const size_t ringb = (size_t)(p.R + 1) * p.xrow_bytes + 2 * (size_t)p.dyrow_bytes;
-  const int per = S * (cpg == 1 ? 2 : 2 * cpg) + 2;
-  const size_t red = (size_t)(p.R * p.WS) * 32 * per * 4;
-  return ringb > red ? ringb : red;
 }
 
 // Shapes both kernels share: stride 1, dilation 1, 16-bit inputs, whole
 // 64-channel CTAs, rows that fit the ring and the per-thread load slots.
-bool common_ok(const Shape& s) {
+bool common_ok(const Shape& s, int cpg) {
   if (s.in_dt == CONV_F32 || s.sh != 1 || s.sw != 1 || s.dh != 1 || s.dw != 1 || s.n < 1) return false;
-  if (s.c % kCG != 0 || s.c != s.k || s.r > kWarps / 2 || s.w > kMaxW) return false;
+  if (s.c % kCG != 0 || s.c != s.k || s.r > kWarps || s.w > kMaxW) return false;
   if (s.pw > s.s || s.ph > s.r) return false;
-  if ((s.w + s.wo) * 8 > (int64_t)kMaxItems * kThreads) return false;
-  return true;
+  if ((s.w + s.wo) * 8 > (int64_t)load_slots(cpg) * kThreads) return false;
+  const DirParams p = make_params(s, 1, cpg);
+  return smem_bytes(p, (int)s.s, cpg) <= kSmemLimit;
 }
 
 template <typename TI, typename TO, int S, int CPG>
 cudaError_t launch_s(const Plan& pl, const Args& a) {
-  const DirParams p = make_params(pl.sh, pl.split);
+  const DirParams p = make_params(pl.sh, pl.split, CPG);
   const size_t smem = smem_bytes(p, S, CPG);
   cudaError_t err = cudaFuncSetAttribute(direct_wgrad_kernel<TI, TO, S, CPG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -399,10 +416,8 @@ cudaError_t launch_grouped_t(const Plan& pl, const Args& a) {
   }
 }
 
-Geometry direct_geometry(const Shape& s, int cpg) {
+Geometry direct_geometry(const Shape& s) {
   Geometry g;
-  const DirParams p = make_params(s, 1);
-  if (smem_bytes(p, (int)s.s, cpg) > kSmemLimit) return g;
   g.ok = true;
   g.ctas_per_sm = 1;
   g.tiles = s.c / kCG;
@@ -414,15 +429,15 @@ Geometry direct_geometry(const Shape& s, int cpg) {
 
 Geometry geometry_wgrad_depthwise(const Shape& s) {
   const bool depthwise = s.groups == s.c && s.groups == s.k;
-  if (!depthwise || !common_ok(s)) return Geometry{};
+  if (!depthwise || !common_ok(s, 1)) return Geometry{};
   if (!(s.s == 3 || s.s == 5 || s.s == 7 || s.s == 9 || s.s == 11)) return Geometry{};
-  return direct_geometry(s, 1);
+  return direct_geometry(s);
 }
 
 Geometry geometry_wgrad_grouped(const Shape& s) {
-  if (!(s.cg == 4 || s.cg == 8) || s.kg != s.cg || !common_ok(s)) return Geometry{};
+  if (!(s.cg == 4 || s.cg == 8) || s.kg != s.cg || !common_ok(s, (int)s.cg)) return Geometry{};
   if (!(s.s == 1 || s.s == 3 || (s.s == 5 && s.cg == 4))) return Geometry{};
-  return direct_geometry(s, (int)s.cg);
+  return direct_geometry(s);
 }
 
 cudaError_t launch_wgrad_depthwise(const Plan& p, const Args& a) {
