@@ -49,6 +49,10 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
+// This CTA's main work is done: the fold, launched as a programmatic
+// dependent, may be scheduled (it still waits for this grid to complete).
+__device__ __forceinline__ void signal_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 inline int launch_grid_cap(int64_t units, int threads, int sms, int per_sm) {
   int64_t blocks = (units + threads - 1) / threads;
   const int64_t cap = (int64_t)sms * per_sm;

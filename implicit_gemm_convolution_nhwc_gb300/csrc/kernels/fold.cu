@@ -70,6 +70,9 @@ template <typename TO, int V>
 __global__ void __launch_bounds__(kThreads) fold_kernel(const float* __restrict__ ws, TO* out, int64_t E,
                                                         const float* __restrict__ wsb, TO* db, int64_t K,
                                                         int32_t S) {
+  // Launched as a programmatic dependent of stage 1: wait here until stage 1
+  // has completed and its slab writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t main_units = E / V;
   const int64_t units = main_units + (db ? K : 0);
   const int64_t stride = (int64_t)gridDim.x * kThreads;
@@ -94,14 +97,26 @@ cudaError_t launch_typed(const Plan& p, const Args& a) {
   // 16-byte units when they still give every SM several CTAs; else one float
   // per thread for more loads in flight.
   const bool vec4 = (E % 4) == 0 && (E / 4) >= (int64_t)(sms > 0 ? sms : 148) * kThreads * 4;
-  if (vec4) {
-    const int grid = launch_grid_cap(E / 4 + bias_units, kThreads, cap / 8 > 0 ? cap / 8 : 1, 8);
-    fold_kernel<TO, 4><<<grid, kThreads, 0, a.stream>>>(a.ws, out, E, a.ws_bias, db, p.sh.k, p.split);
-  } else {
-    const int grid = launch_grid_cap(E + bias_units, kThreads, cap / 8 > 0 ? cap / 8 : 1, 8);
-    fold_kernel<TO, 1><<<grid, kThreads, 0, a.stream>>>(a.ws, out, E, a.ws_bias, db, p.sh.k, p.split);
-  }
-  return cudaGetLastError();
+  const int grid = launch_grid_cap((vec4 ? E / 4 : E) + bias_units, kThreads, cap / 8 > 0 ? cap / 8 : 1, 8);
+  // Programmatic dependent launch: the fold may be scheduled as soon as the
+  // stage-1 CTAs signal (griddepcontrol.launch_dependents) and then waits in
+  // griddepcontrol.wait for stage 1 to finish, hiding its launch latency.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const float* ws = a.ws;
+  const float* wsb = a.ws_bias;
+  const int64_t K = p.sh.k;
+  const int32_t S = p.split;
+  if (vec4) return cudaLaunchKernelEx(&cfg, fold_kernel<TO, 4>, ws, out, E, wsb, db, K, S);
+  return cudaLaunchKernelEx(&cfg, fold_kernel<TO, 1>, ws, out, E, wsb, db, K, S);
 }
 
 }  // namespace

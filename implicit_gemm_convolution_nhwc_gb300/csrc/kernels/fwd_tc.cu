@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   } else if (warp >= 4) {
     const bool ok = mbar_wait(tmem_full, 0u, nullptr, err) && *abort_flag == 0u;
+    signal_dependents();
     tc_fence_after();
     const int q = warp - 4;
     const int m = 32 * q + lane;  // tile row = output pixel within the tile

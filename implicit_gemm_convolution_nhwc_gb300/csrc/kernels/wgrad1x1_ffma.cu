@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   }
   cp_async_wait<0>();
+  signal_dependents();
 
   // Epilogue: this CTA's partial tile (or the final values when S == 1).
   const int64_t E = K * C;

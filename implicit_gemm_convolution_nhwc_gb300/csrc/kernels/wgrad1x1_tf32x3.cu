@@ -289,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------- epilogue
+    signal_dependents();
     const bool ok = alive && *abort_flag == 0u;
     constexpr int LD = BC + 4;
     float* comb = reinterpret_cast<float*>(raw);                      // [64][LD]

@@ -260,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     row = n * p.Ho + ho_b;
   }
 
+  signal_dependents();
   // Add the warps of each filter row in warp order, then store.
   constexpr int PER = S * A::KI * A::CP * 2 + 2;  // dW partials, then the db pair
   __syncthreads();
