@@ -194,6 +194,19 @@ def make_inputs_on_device(p, direction, dist, args, seed, device, pinned_copy=Fa
     return x, b, hosts
 
 
+# --------------------------------------------------------------- replicas
+
+def max_over_ranks(value: float, device) -> float:
+    """The largest of every rank's value (all ranks get it), then a barrier.
+    Used for the step time of replicas: the job is as slow as its slowest rank."""
+    import torch
+    import torch.distributed as dist_
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist_.all_reduce(t, op=dist_.ReduceOp.MAX)
+    dist_.barrier()
+    return float(t.item())
+
+
 # --------------------------------------------------------------- traffic
 
 def recorded_traffic(kernel_name: str, workload: str):
@@ -249,8 +262,9 @@ def oracle_sample(p, direction, dist, args, seed, n_samples: int):
 
 
 def time_oracle(p, direction, dist, args, seed, target_s: float):
-    """Run the oracle on growing batch samples until one run takes >= target_s / 4,
-    then report that run. Returns (flops/s, seconds, samples, threads)."""
+    """Run the oracle on growing batch samples until one run takes >= 0.6 target_s
+    (or covers the whole batch), then report that run.
+    Returns (flops/s, seconds, samples, threads)."""
     import oracle
     orc = oracle.get()
     threads = max(1, len(os.sched_getaffinity(0)))
@@ -268,10 +282,10 @@ def time_oracle(p, direction, dist, args, seed, target_s: float):
             orc.bgrad(op, b)
         dt = time.perf_counter() - t0
         flops = 2 * n * p.out_hw[0] * p.out_hw[1] * p.k * (p.c // p.groups) * p.r * p.s
-        if dt >= target_s / 4 or n >= p.n:
+        if dt >= 0.6 * target_s or n >= p.n:
             used = min(threads, p.k) if direction == "wgrad" else min(threads, n * p.out_hw[0])
             return flops / dt, dt, n, used
-        n = min(p.n, max(n + 1, int(n * (target_s / 4) / max(dt, 1e-3)) + 1))
+        n = min(p.n, max(n + 1, int(n * target_s / max(dt, 1e-3))))
 
 
 # --------------------------------------------------------------- our arm
@@ -357,11 +371,7 @@ def run_ours(a, rank, world, local_rank):
     # otherwise the whole back-to-back region is.
     total_ms = sum(e[0].elapsed_time(e[1]) for e in evs) if flush is not None else start.elapsed_time(end)
     if world > 1:
-        import torch.distributed as dist_
-        t = torch.tensor([total_ms], device=dev)
-        dist_.all_reduce(t, op=dist_.ReduceOp.MAX)
-        total_ms = float(t.item())
-        dist_.barrier()
+        total_ms = max_over_ranks(total_ms, dev)
     # Per-kernel durations (stage 1 is the roofline's kernel), from a second
     # loop with an event between the stages.
     sev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.steps)]
@@ -477,8 +487,8 @@ def run_reference(a, rank, world):
     orc = oracle.get()
     threads = max(1, len(os.sched_getaffinity(0)))
     # calibrate a bounded sample so the whole run stays within a few minutes
-    budget = max(20.0, 150.0 / max(1, a.steps + a.warmup))
-    fps, secs, n_s, used = time_oracle(p, direction, dist, args, seed, min(budget, 8.0))
+    budget = min(8.0, max(0.5, 150.0 / max(1, a.steps + a.warmup)))  # seconds per step
+    fps, secs, n_s, used = time_oracle(p, direction, dist, args, seed, budget)
     x, b = oracle_sample(p, direction, dist, args, seed, n_s)
     op = oracle.Problem(n=n_s, h=p.h, w=p.w, c=p.c, k=p.k, r=p.r, s=p.s, stride_h=p.stride_h,
                         stride_w=p.stride_w, pad_h=p.pad_h, pad_w=p.pad_w, dil_h=p.dil_h, dil_w=p.dil_w,
