@@ -136,14 +136,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------- TMA producer
     if (lane == 0) {
+      // Ring stage s and the parity ph of its current round advance by
+      // increments (no divisions in the loop); so do the sample and row.
+      int s = 0;
+      uint32_t ph = 0;
+      int32_t n = (int32_t)(b0 / blocks_per_sample);
+      int32_t row = (int32_t)((b0 % blocks_per_sample) * kBP);
+      const int32_t row_end = (int32_t)(blocks_per_sample * kBP);
       int64_t it = 0;
       for (; it < nblk; ++it) {
-        const int s = (int)(it % G::R);
-        const uint32_t round = (uint32_t)(it / G::R);
-        if (it >= G::R && !mbar_wait(&raw_empty[s], (round - 1) & 1u, abort_flag, err)) break;
-        const int64_t b = b0 + it;
-        const int32_t n = (int32_t)(b / blocks_per_sample);
-        const int32_t row = (int32_t)((b % blocks_per_sample) * kBP);
+        if (it >= G::R && !mbar_wait(&raw_empty[s], ph ^ 1u, abort_flag, err)) break;
         uint8_t* st = raw + (size_t)s * G::RAW;
         mbar_arrive_expect_tx(&raw_full[s], G::TX);
         tma_load_3d(st, &tm_dy, (int32_t)k0, row, n, &raw_full[s]);
@@ -151,6 +153,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < G::NC; ++j)
           tma_load_3d(st + (2 + j) * kChunk, &tm_x, (int32_t)(c0 + 32 * j), row, n, &raw_full[s]);
+        if ((row += kBP) == row_end) {
+          row = 0;
+          ++n;
+        }
+        if (++s == G::R) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       // Before the CTA can exit, every copy it started must have landed.
       for (int64_t q = it > G::R ? it - G::R : 0; q < it; ++q)
@@ -160,14 +170,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t bbase = smem_u32(opb);
+      int s = 0;
+      uint32_t ph = 0;
       for (int64_t it = 0; it < nblk; ++it) {
-        const int s = (int)(it % G::QS);
         const int64_t per = it / kPeriod;
         const int within = (int)(it % kPeriod);
         const uint32_t d = tmem + kDcol * (uint32_t)(per & 1);
         if (within == 0 && per >= 2 && !mbar_wait(&acc_empty[per & 1], (uint32_t)((per >> 1) - 1) & 1u, abort_flag, err))
           break;
-        if (!mbar_wait(&op_full[s], (uint32_t)(it / G::QS) & 1u, abort_flag, err)) break;
+        if (!mbar_wait(&op_full[s], ph, abort_flag, err)) break;
         tc_fence_after();
         const uint32_t b = bbase + (uint32_t)(s * G::OPB);
         const uint32_t a = tmem + kAcol + 32u * (uint32_t)s;
@@ -180,6 +191,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(&op_empty[s]);
         if (within == kPeriod - 1 || it == nblk - 1) mma_commit(&acc_full[per & 1]);
+        if (++s == G::QS) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
     }
   } else if (warp >= 4) {
@@ -230,15 +245,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
 
+    int rs = 0, qs = 0;          // raw and operand ring stages
+    uint32_t rph = 0, qph = 0;   // parities of their current rounds
     for (int64_t it = 0; it < nblk; ++it) {
-      const int rs = (int)(it % G::R);
-      const int qs = (int)(it % G::QS);
       if (it >= kPeriod + G::QS && (it - G::QS) % kPeriod == 0) {
         if (!drain(drained)) { alive = false; break; }
         ++drained;
       }
-      if (!mbar_wait(&raw_full[rs], (uint32_t)(it / G::R) & 1u, abort_flag, err)) { alive = false; break; }
-      if (it >= G::QS && !mbar_wait(&op_empty[qs], (uint32_t)(it / G::QS - 1) & 1u, abort_flag, err)) {
+      if (!mbar_wait(&raw_full[rs], rph, abort_flag, err)) { alive = false; break; }
+      if (it >= G::QS && !mbar_wait(&op_empty[qs], qph ^ 1u, abort_flag, err)) {
         alive = false;
         break;
       }
@@ -282,6 +297,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();  // B writes -> visible to the tensor core
       mbar_arrive(&raw_empty[rs]);
       mbar_arrive(&op_full[qs]);
+      if (++rs == G::R) {
+        rs = 0;
+        rph ^= 1u;
+      }
+      if (++qs == G::QS) {
+        qs = 0;
+        qph ^= 1u;
+      }
     }
     while (alive && drained < nper) {
       if (!drain(drained)) alive = false;
