@@ -16,7 +16,7 @@ from . import _build
 F32, BF16, F16 = 0, 1, 2
 DIR_FWD, DIR_WGRAD = 0, 1
 KERNELS = {"auto": 0, "generic": 1, "wgrad_1x1_ffma": 2, "wgrad_1x1_tf32x3": 3, "fwd_tc": 4,
-           "wgrad_depthwise": 5, "wgrad_grouped": 6}
+           "wgrad_depthwise": 5, "wgrad_grouped": 6, "fwd_tc_cluster": 7}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 STATUS = ["CONV_OK", "CONV_ERR_INVALID_ARG", "CONV_ERR_UNSUPPORTED", "CONV_ERR_WORKSPACE_TOO_SMALL",
           "CONV_ERR_OVERFLOW", "CONV_ERR_ALIGNMENT", "CONV_ERR_CUDA"]
@@ -75,7 +75,7 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("split_k", ctypes.c_int32), ("needs_fold", ctypes.c_int32),
                 ("ctas_per_sm", ctypes.c_int32), ("tiles", ctypes.c_int64),
                 ("reduction_blocks", ctypes.c_int64), ("ctas", ctypes.c_int64),
-                ("workspace_bytes", ctypes.c_uint64)]
+                ("workspace_bytes", ctypes.c_uint64), ("max_split", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         d = {f[0]: getattr(self, f[0]) for f in self._fields_}

@@ -75,6 +75,7 @@ Geometry geometry_of(conv_kernel k, const Shape& s, conv_dir dir) {
     case CONV_KERNEL_WGRAD_1X1_FFMA: return dir == CONV_DIR_WGRAD ? geometry_wgrad1x1_ffma(s) : Geometry{};
     case CONV_KERNEL_WGRAD_1X1_TF32X3: return dir == CONV_DIR_WGRAD ? geometry_wgrad1x1_tf32x3(s) : Geometry{};
     case CONV_KERNEL_FWD_TC: return dir == CONV_DIR_FWD ? geometry_fwd_tc(s) : Geometry{};
+    case CONV_KERNEL_FWD_TC_CLUSTER: return dir == CONV_DIR_FWD ? geometry_fwd_tc_cluster(s) : Geometry{};
     case CONV_KERNEL_WGRAD_DEPTHWISE: return dir == CONV_DIR_WGRAD ? geometry_wgrad_depthwise(s) : Geometry{};
     case CONV_KERNEL_WGRAD_GROUPED: return dir == CONV_DIR_WGRAD ? geometry_wgrad_grouped(s) : Geometry{};
     default: return Geometry{};
@@ -94,6 +95,8 @@ conv_status choose_kernel(const Shape& s, conv_dir dir, conv_kernel* kernel, Geo
   static const conv_kernel wgrad_order[] = {CONV_KERNEL_WGRAD_1X1_TF32X3, CONV_KERNEL_WGRAD_1X1_FFMA,
                                             CONV_KERNEL_WGRAD_DEPTHWISE, CONV_KERNEL_WGRAD_GROUPED,
                                             CONV_KERNEL_GENERIC};
+  // The cluster form of the forward is reached only through the override:
+  // on the 3x3 small-M layer it measured slower than the two-stage form.
   static const conv_kernel fwd_order[] = {CONV_KERNEL_FWD_TC, CONV_KERNEL_GENERIC};
   const conv_kernel* order = dir == CONV_DIR_WGRAD ? wgrad_order : fwd_order;
   const int count = dir == CONV_DIR_WGRAD ? 5 : 2;
@@ -112,7 +115,8 @@ conv_status choose_kernel(const Shape& s, conv_dir dir, conv_kernel* kernel, Geo
 // policy restates "feat(rocke): split-K forward implicit-GEMM convolution on
 // gfx1250" ("Auto-deduced degree"): split only a grid under half the target,
 // over a reduction at least 512 deep; a power of two toward the target, at
-// most 32, with at least 2 reduction blocks per slice; pointwise stays whole.
+// most 32 (at most the kernel's own limit, 16 for the cluster form), with at
+// least 2 reduction blocks per slice; pointwise stays whole.
 conv_status resolve_degree(const Shape& s, conv_dir dir, const Geometry& g, int32_t request,
                            int32_t sm_count, int32_t* degree) {
   if (request < -1) return CONV_ERR_INVALID_ARG;
@@ -131,8 +135,9 @@ conv_status resolve_degree(const Shape& s, conv_dir dir, const Geometry& g, int3
   int64_t d = 1;
   if (dir == CONV_DIR_FWD) {
     const bool pointwise = s.r == 1 && s.s == 1;
+    const int64_t cap = g.max_split > 0 && g.max_split < 32 ? g.max_split : 32;
     if (!pointwise && 2 * g.tiles < target && s.D() >= 512) {
-      while (2 * d <= 32 && g.tiles * (2 * d) <= target) d *= 2;
+      while (2 * d <= cap && g.tiles * (2 * d) <= target) d *= 2;
       while (d > 1 && g.blocks < 2 * d) d /= 2;
     }
   } else if (g.tiles < target) {
@@ -156,11 +161,15 @@ conv_status make_plan(const conv_problem* prob, conv_dir dir, int32_t request, b
   p.with_bias = with_bias && dir == CONV_DIR_WGRAD;
   st = choose_kernel(p.sh, dir, &p.kernel, &p.geo);
   if (st != CONV_OK) return st;
+  // The cluster form takes at most 16 slices (one cluster per tile).
+  if (p.kernel == CONV_KERNEL_FWD_TC_CLUSTER && request > p.geo.max_split && request <= p.geo.blocks)
+    return CONV_ERR_UNSUPPORTED;
   st = resolve_degree(p.sh, dir, p.geo, request, sm_count, &p.split);
   if (st != CONV_OK) return st;
+  p.fold = p.split > 1 && p.kernel != CONV_KERNEL_FWD_TC_CLUSTER;
   p.out_elems = dir == CONV_DIR_FWD ? p.sh.y_elems() : p.sh.w_elems();
   p.slab_bytes = p.bias_slab_bytes = 0;
-  if (p.split > 1) {
+  if (p.fold) {
     int64_t b;
     if (!mul_ok(p.out_elems, 4, &b) || !mul_ok(b, p.split, &b)) return CONV_ERR_OVERFLOW;
     p.slab_bytes = round256((uint64_t)b);
@@ -204,8 +213,8 @@ conv_status run(const conv_problem* prob, conv_dir dir, const void* x, const voi
   a.b = b;
   a.out = out;
   a.db = plan.with_bias ? db : nullptr;
-  a.ws = plan.split > 1 ? static_cast<float*>(ws) : nullptr;
-  a.ws_bias = plan.split > 1 && plan.with_bias
+  a.ws = plan.fold ? static_cast<float*>(ws) : nullptr;
+  a.ws_bias = plan.fold && plan.with_bias
                   ? reinterpret_cast<float*>(static_cast<char*>(ws) + plan.slab_bytes)
                   : nullptr;
   a.stream = static_cast<cudaStream_t>(stream);
@@ -216,13 +225,14 @@ conv_status run(const conv_problem* prob, conv_dir dir, const void* x, const voi
       case CONV_KERNEL_WGRAD_1X1_FFMA: err = launch_wgrad1x1_ffma(plan, a); break;
       case CONV_KERNEL_WGRAD_1X1_TF32X3: err = launch_wgrad1x1_tf32x3(plan, a); break;
       case CONV_KERNEL_FWD_TC: err = launch_fwd_tc(plan, a); break;
+      case CONV_KERNEL_FWD_TC_CLUSTER: err = launch_fwd_tc_cluster(plan, a); break;
       case CONV_KERNEL_WGRAD_DEPTHWISE: err = launch_wgrad_depthwise(plan, a); break;
       case CONV_KERNEL_WGRAD_GROUPED: err = launch_wgrad_grouped(plan, a); break;
       default: return CONV_ERR_UNSUPPORTED;
     }
     if (err != cudaSuccess) return CONV_ERR_CUDA;
   }
-  if ((stages & kStage2) && plan.split > 1) {
+  if ((stages & kStage2) && plan.fold) {
     err = launch_fold(plan, a);
     if (err != cudaSuccess) return CONV_ERR_CUDA;
   }
@@ -316,12 +326,15 @@ conv_status conv_describe_plan(const conv_problem* p, conv_dir dir, int32_t spli
   if (st != CONV_OK) return st;
   info->kernel = plan.kernel;
   info->split_k = plan.split;
-  info->needs_fold = plan.split > 1;
+  info->needs_fold = plan.fold ? 1 : 0;
   info->ctas_per_sm = plan.geo.ctas_per_sm;
   info->tiles = plan.geo.tiles;
   info->reduction_blocks = plan.geo.blocks;
   info->ctas = plan.geo.tiles * plan.split;
   info->workspace_bytes = plan.ws_bytes();
+  info->max_split = plan.geo.max_split > 0 && plan.geo.max_split < plan.geo.blocks
+                        ? plan.geo.max_split
+                        : (int32_t)(plan.geo.blocks < 0x7fffffff ? plan.geo.blocks : 0x7fffffff);
   return CONV_OK;
 }
 
@@ -411,7 +424,7 @@ conv_status conv_wgrad_bias_static_ws(const conv_problem* p, const void* x, cons
 
 
 conv_status conv_set_kernel_override(int32_t kernel) {
-  if (kernel < CONV_KERNEL_AUTO || kernel > CONV_KERNEL_WGRAD_GROUPED) return CONV_ERR_INVALID_ARG;
+  if (kernel < CONV_KERNEL_AUTO || kernel > CONV_KERNEL_FWD_TC_CLUSTER) return CONV_ERR_INVALID_ARG;
   g_kernel_override = kernel;
   return CONV_OK;
 }

@@ -28,7 +28,12 @@ struct Geometry {
   int64_t tiles = 0;         // output tiles (CTAs per slice)
   int64_t blocks = 0;        // reduction blocks a slice is made of
   int ctas_per_sm = 1;       // resident CTAs per SM (sets the auto target)
+  int32_t max_split = 0;     // largest degree the kernel takes (0: any up to `blocks`)
 };
+
+// Largest thread-block cluster (non-portable size) the single-launch
+// split-K forward forms from the S slices of a tile.
+constexpr int kMaxClusterSplit = 16;
 
 struct Plan {
   Shape sh;
@@ -40,6 +45,7 @@ struct Plan {
   int64_t out_elems;         // E: elements of Y or dW
   uint64_t slab_bytes;       // S*E*4 rounded to 256 (0 when S == 1)
   uint64_t bias_slab_bytes;  // S*K*4 rounded to 256 (0 when S == 1 or no bias)
+  bool fold;                 // stage 2 runs (S > 1 and the slices do not fold in-launch)
   uint64_t ws_bytes() const { return slab_bytes + bias_slab_bytes; }
 };
 
@@ -64,6 +70,7 @@ Geometry geometry_generic(const Shape& s, conv_dir dir);
 Geometry geometry_wgrad1x1_ffma(const Shape& s);
 Geometry geometry_wgrad1x1_tf32x3(const Shape& s);
 Geometry geometry_fwd_tc(const Shape& s);
+Geometry geometry_fwd_tc_cluster(const Shape& s);
 Geometry geometry_wgrad_depthwise(const Shape& s);
 Geometry geometry_wgrad_grouped(const Shape& s);
 
@@ -72,6 +79,7 @@ cudaError_t launch_generic(const Plan& p, const Args& a);
 cudaError_t launch_wgrad1x1_ffma(const Plan& p, const Args& a);
 cudaError_t launch_wgrad1x1_tf32x3(const Plan& p, const Args& a);
 cudaError_t launch_fwd_tc(const Plan& p, const Args& a);
+cudaError_t launch_fwd_tc_cluster(const Plan& p, const Args& a);
 cudaError_t launch_wgrad_depthwise(const Plan& p, const Args& a);
 cudaError_t launch_wgrad_grouped(const Plan& p, const Args& a);
 // Stage 2: out = cast(sum of slabs) (and the bias slabs into db).

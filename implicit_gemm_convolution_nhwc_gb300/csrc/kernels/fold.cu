@@ -6,9 +6,9 @@
 // in the same launch.
 //
 // Bandwidth- and latency-bound: the slabs were just written by stage 1 and
-// usually sit in L2. Each thread owns kVec consecutive elements and issues
-// the loads of kBatch slabs before it adds any of them, so a warp keeps
-// kBatch independent 4- or 16-byte loads in flight per slab batch; the adds
+// usually sit in L2. Each thread owns 1 or 4 consecutive elements and issues
+// the loads of a batch of slabs (32 or 16) before it adds any of them, so a
+// warp keeps a batch of independent 4- or 16-byte loads in flight; the adds
 // still happen strictly in slice order.
 #include "common.cuh"
 
@@ -16,39 +16,43 @@ namespace cig {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kBatch = 16;
 
 template <int V>
 struct Vec;
 template <>
 struct Vec<1> {
   using T = float;
+  static constexpr int kBatch = 32;  // slabs whose loads are in flight together
   static __device__ __forceinline__ T load(const float* p) { return __ldcs(p); }
   static __device__ __forceinline__ void add(T& a, const T& b) { a += b; }
 };
 template <>
 struct Vec<4> {
   using T = float4;
+  static constexpr int kBatch = 16;
   static __device__ __forceinline__ T load(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
   static __device__ __forceinline__ void add(T& a, const T& b) {
     a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
   }
 };
 
-// Sum of S slabs (stride E floats) at element e, in slice order.
+// Sum of S slabs (stride E floats) at element e, in slice order. Each batch
+// issues all of its (predicated) loads before its first add, the last,
+// partial batch included, so no slab load waits on the previous add.
 template <int V>
 __device__ __forceinline__ typename Vec<V>::T fold_at(const float* ws, int64_t E, int32_t S, int64_t e) {
   using T = typename Vec<V>::T;
+  constexpr int B = Vec<V>::kBatch;
   T acc = Vec<V>::load(ws + e);
-  int32_t s = 1;
-  for (; s + kBatch <= S; s += kBatch) {
-    T v[kBatch];
+  for (int32_t s = 1; s < S; s += B) {
+    T v[B];
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) v[i] = Vec<V>::load(ws + (int64_t)(s + i) * E + e);
+    for (int i = 0; i < B; ++i)
+      if (s + i < S) v[i] = Vec<V>::load(ws + (int64_t)(s + i) * E + e);
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) Vec<V>::add(acc, v[i]);
+    for (int i = 0; i < B; ++i)
+      if (s + i < S) Vec<V>::add(acc, v[i]);
   }
-  for (; s < S; ++s) Vec<V>::add(acc, Vec<V>::load(ws + (int64_t)s * E + e));
   return acc;
 }
 

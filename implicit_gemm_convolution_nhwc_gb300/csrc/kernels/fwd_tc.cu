@@ -20,6 +20,16 @@
 // into Y. No fused epilogue is applied under split-K ("Review follow-ups":
 // a bias or activation cannot be applied per slice).
 //
+// Single-launch form (same page, "Changes": single-launch split-K; its
+// testing notes: each slice folds 1/S of the tile's rows): the S slices of a
+// tile are one thread-block cluster (S <= 16). Each CTA stages its fp32
+// partial tile in its own shared memory; after a cluster barrier, CTA sigma
+// sums rows [128 sigma / S, 128 (sigma + 1) / S) of all S partial tiles over
+// distributed shared memory, in slice order 0..S-1 (the fold's order, so Y is
+// bit-identical to the two-stage form at the same S), and rounds into Y. No
+// workspace and no fold launch. A second cluster barrier keeps every CTA (and
+// its shared memory) alive until its peers have read it.
+//
 // Warp roles: 0 TMA producer, 1 MMA issuer, 2 TMEM owner, 4-7 epilogue.
 #include "tc_common.cuh"
 
@@ -30,12 +40,18 @@ constexpr int kThreads = 256;
 constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kBK = 64;                     // channels per reduction block (128 bytes of 16-bit)
-constexpr int kStages = 3;
 constexpr int kA = kBM * 128;               // A tile bytes (128 rows x 128 B)
 constexpr int kB = kBN * 128;
 constexpr int kStage = kA + kB;
-constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + 256;
 constexpr uint32_t kTmemCols = 128;
+constexpr int kLD = kBN + 4;                // staged partial tile: row stride in floats (conflict-free float4s)
+
+// Ring depth: 3 stages, 2 CTAs per SM. (A deeper ring for the cluster form
+// would hold one CTA per SM, and then only 7 clusters of 16 fit on the GPU at
+// once, fewer than the 8 tiles of the 3x3 small-M layer.)
+constexpr int kStages = 3;
+constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + 256;
+static_assert(kBM * kLD * 4 <= kStages * kStage, "staged partial tile must fit in the ring");
 
 struct FwdParams {
   int64_t K, Ho, Wo, Cg, S_f;   // S_f: filter width
@@ -72,7 +88,24 @@ __device__ __forceinline__ void store8<__half>(__half* dst, const float* v) {
   *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<uint4*>(h);
 }
 
-template <typename TO, uint32_t FMT>
+template <typename TO>
+__device__ __forceinline__ void store4(TO* dst, float4 v);
+template <>
+__device__ __forceinline__ void store4<float>(float* dst, float4 v) {
+  *reinterpret_cast<float4*>(dst) = v;
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float4 v) {
+  __nv_bfloat162 h[2] = {__floats2bfloat162_rn(v.x, v.y), __floats2bfloat162_rn(v.z, v.w)};
+  *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<uint2*>(h);
+}
+template <>
+__device__ __forceinline__ void store4<__half>(__half* dst, float4 v) {
+  __half2 h[2] = {__floats2half2_rn(v.x, v.y), __floats2half2_rn(v.z, v.w)};
+  *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<uint2*>(h);
+}
+
+template <typename TO, uint32_t FMT, bool CL>
 __global__ void __launch_bounds__(kThreads, 2)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, TO* out,
                   float* ws, FwdParams fp, unsigned* err) {
@@ -86,8 +119,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   constexpr uint32_t IDESC = mma_idesc(FMT, 0u, 0u, (uint32_t)kBN, (uint32_t)kBM);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int64_t tile = blockIdx.x % fp.tiles;
-  const int32_t sigma = (int32_t)(blockIdx.x / fp.tiles);
+  // Two-stage form: CTA = sigma * tiles + tile. Cluster form: the S CTAs of
+  // a tile are consecutive, sigma = rank in the cluster.
+  const int64_t tile = CL ? (int64_t)(blockIdx.x / (uint32_t)fp.split) : (int64_t)(blockIdx.x % fp.tiles);
+  const int32_t sigma = CL ? (int32_t)cluster_ctarank() : (int32_t)(blockIdx.x / fp.tiles);
   const int64_t tn = tile % fp.tiles_n;
   const int64_t tm = tile / fp.tiles_n;
   const int64_t img = tm / fp.tiles_m_per_img;
@@ -96,6 +131,33 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int64_t b0 = slice_begin(fp.blocks, fp.split, sigma);
   const int64_t nblk = slice_begin(fp.blocks, fp.split, sigma + 1) - b0;
   const uint32_t tx = (uint32_t)(fp.TR * fp.Wo * 128 + kB);
+
+  // Producer state (thread 0): the ring stage and its round's parity, and
+  // the next block's (r, s, c-block), all advanced by increments.
+  int ps = 0;
+  uint32_t pph = 0;
+  int32_t cb = 0, rs = 0, r = 0, sx = 0;
+  int64_t it = 0;
+  const int32_t cblocks = (int32_t)fp.cblocks, cg = (int32_t)fp.Cg, sf = (int32_t)fp.S_f;
+  auto issue = [&]() {
+    uint8_t* st = smem + (size_t)ps * kStage;
+    mbar_arrive_expect_tx(&full[ps], tx);
+    tma_load_4d(st, &tm_x, cb * kBK, sx * fp.dw - fp.pw, (int32_t)ho0 + r * fp.dh - fp.ph, (int32_t)img,
+                &full[ps]);
+    tma_load_2d(st + kA, &tm_w, rs * cg + cb * kBK, (int32_t)k0, &full[ps]);
+    if (++cb == cblocks) {
+      cb = 0;
+      ++rs;
+      if (++sx == sf) {
+        sx = 0;
+        ++r;
+      }
+    }
+    if (++ps == kStages) {
+      ps = 0;
+      pph ^= 1u;
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -107,6 +169,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_fence_init();
     tma_prefetch(&tm_x);
     tma_prefetch(&tm_w);
+    cb = (int32_t)(b0 % fp.cblocks);
+    rs = (int32_t)(b0 / fp.cblocks);
+    r = rs / sf;
+    sx = rs % sf;
+    // The first ring of loads goes out before the CTA-wide sync (which waits
+    // for the TMEM allocation), so its latency overlaps the set-up.
+    for (; it < nblk && it < kStages; ++it) issue();
   }
   if (warp == 2) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -119,20 +188,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (warp == 0) {
     if (lane == 0) {
-      int64_t it = 0;
       for (; it < nblk; ++it) {
-        const int s = (int)(it % kStages);
-        const uint32_t round = (uint32_t)(it / kStages);
-        if (it >= kStages && !mbar_wait(&empty[s], (round - 1) & 1u, abort_flag, err)) break;
-        const int64_t b = b0 + it;
-        const int64_t cb = b % fp.cblocks;
-        const int64_t rs = b / fp.cblocks;
-        const int32_t r = (int32_t)(rs / fp.S_f), sx = (int32_t)(rs % fp.S_f);
-        uint8_t* st = smem + (size_t)s * kStage;
-        mbar_arrive_expect_tx(&full[s], tx);
-        tma_load_4d(st, &tm_x, (int32_t)(cb * kBK), sx * fp.dw - fp.pw, (int32_t)ho0 + r * fp.dh - fp.ph,
-                    (int32_t)img, &full[s]);
-        tma_load_2d(st + kA, &tm_w, (int32_t)(rs * fp.Cg + cb * kBK), (int32_t)k0, &full[s]);
+        if (!mbar_wait(&empty[ps], pph ^ 1u, abort_flag, err)) break;
+        issue();
       }
       for (int64_t q = it > kStages ? it - kStages : 0; q < it; ++q)
         mbar_wait(&full[q % kStages], (uint32_t)(q / kStages) & 1u, nullptr, err);
@@ -140,9 +198,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t base = smem_u32(smem);
-      for (int64_t it = 0; it < nblk; ++it) {
-        const int s = (int)(it % kStages);
-        if (!mbar_wait(&full[s], (uint32_t)(it / kStages) & 1u, abort_flag, err)) break;
+      int s = 0;
+      uint32_t ph = 0;
+      for (int64_t j = 0; j < nblk; ++j) {
+        if (!mbar_wait(&full[s], ph, abort_flag, err)) break;
         tc_fence_after();
         const uint32_t a = base + (uint32_t)(s * kStage), b = a + kA;
 #pragma unroll
@@ -150,47 +209,102 @@ __global__ void __launch_bounds__(kThreads, 2)
           // K-major SW128: 8-row groups 1024 B apart; a K step of 16 elements is
           // a 32-byte advance inside the swizzled 128-byte row.
           mma_f16(tmem, smem_desc_sw128(a + 32u * kk, 16, 1024), smem_desc_sw128(b + 32u * kk, 16, 1024), IDESC,
-                  (it > 0 || kk > 0) ? 1u : 0u);
+                  (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&empty[s]);
+        if (++s == kStages) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       if (nblk > 0) mma_commit(tmem_full);
       else mbar_arrive(tmem_full);
     }
   } else if (warp >= 4) {
     const bool ok = mbar_wait(tmem_full, 0u, nullptr, err) && *abort_flag == 0u;
-    signal_dependents();
+    if (!CL) signal_dependents();
     tc_fence_after();
     const int q = warp - 4;
     const int m = 32 * q + lane;  // tile row = output pixel within the tile
-    const int64_t ho = ho0 + m / fp.Wo, wo = m % fp.Wo;
-    const bool row_ok = ok && m < fp.TR * fp.Wo && ho < fp.Ho;
-    const int64_t pix = (img * fp.Ho + ho) * fp.Wo + wo;
-    float* slab = ws ? ws + (int64_t)sigma * fp.E : nullptr;
+    if (CL) {
+      // Stage this slice's partial tile: row m at part + m * kLD (the ring is
+      // idle: every copy landed and every MMA that read it has completed).
+      float* part = reinterpret_cast<float*>(smem) + m * kLD;
 #pragma unroll 1
-    for (int j = 0; j < kBN / 32; ++j) {
-      float v[32];
-      if (nblk > 0) {
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32u * j, v);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0.f;
-      }
-      if (!row_ok) continue;
-#pragma unroll
-      for (int i = 0; i < 32; i += 8) {
-        const int64_t k = k0 + 32 * j + i;
-        if (k >= fp.K) continue;  // K % 8 == 0: an 8-wide group is all in or all out
-        if (slab) {
-          store8<float>(slab + pix * fp.K + k, v + i);
+      for (int j = 0; j < kBN / 32; ++j) {
+        float v[32];
+        if (nblk > 0) {
+          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32u * j, v);
         } else {
-          store8<TO>(out + pix * fp.K + k, v + i);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4*>(part + 32 * j + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+      }
+    } else {
+      const int64_t ho = ho0 + m / fp.Wo, wo = m % fp.Wo;
+      const bool row_ok = ok && m < fp.TR * fp.Wo && ho < fp.Ho;
+      const int64_t pix = (img * fp.Ho + ho) * fp.Wo + wo;
+      float* slab = ws ? ws + (int64_t)sigma * fp.E : nullptr;
+#pragma unroll 1
+      for (int j = 0; j < kBN / 32; ++j) {
+        float v[32];
+        if (nblk > 0) {
+          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32u * j, v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        }
+        if (!row_ok) continue;
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) {
+          const int64_t k = k0 + 32 * j + i;
+          if (k >= fp.K) continue;  // K % 8 == 0: an 8-wide group is all in or all out
+          if (slab) {
+            store8<float>(slab + pix * fp.K + k, v + i);
+          } else {
+            store8<TO>(out + pix * fp.K + k, v + i);
+          }
         }
       }
     }
   }
 
   tc_fence_before();
+  if (CL) {
+    cluster_sync();  // every slice's partial tile is staged
+    const int S = fp.split;
+    const int r0 = (sigma * kBM) / S, r1 = ((sigma + 1) * kBM) / S;
+    const int64_t rows_here = fp.Ho - ho0 < fp.TR ? fp.Ho - ho0 : fp.TR;
+    const int valid = (int)(rows_here * fp.Wo);  // rows m < valid are output pixels
+    const bool ok = *abort_flag == 0u;
+    const uint32_t base = smem_u32(smem);
+#pragma unroll 1
+    for (int w = threadIdx.x; w < (r1 - r0) * (kBN / 4); w += kThreads) {
+      const int m = r0 + w / (kBN / 4), c4 = w % (kBN / 4);
+      const int64_t k = k0 + 4 * c4;
+      if (!ok || m >= valid || k >= fp.K) continue;  // K % 8 == 0: 4-wide groups are all in or all out
+      const uint32_t la = base + (uint32_t)((m * kLD + 4 * c4) * 4);
+      float4 part[kMaxClusterSplit];
+#pragma unroll
+      for (int j = 0; j < kMaxClusterSplit; ++j)
+        if (j < S) part[j] = ld_cluster_f4(cluster_map(la, (uint32_t)j));
+      float4 acc = part[0];
+#pragma unroll
+      for (int j = 1; j < kMaxClusterSplit; ++j)
+        if (j < S) {
+          acc.x += part[j].x;
+          acc.y += part[j].y;
+          acc.z += part[j].z;
+          acc.w += part[j].w;
+        }
+      const int64_t pix = (img * fp.Ho + ho0 + m / fp.Wo) * fp.Wo + m % fp.Wo;
+      store4<TO>(out + pix * fp.K + k, acc);
+    }
+    cluster_sync();  // peers are done reading this CTA's shared memory
+  }
   __syncthreads();
   if (warp == 2) {
     tc_fence_after();
@@ -232,7 +346,7 @@ FwdParams make_params(const Plan& p) {
   return fp;
 }
 
-template <typename TO, uint32_t FMT>
+template <typename TO, uint32_t FMT, bool CL>
 cudaError_t launch_typed(const Plan& p, const Args& a, CUtensorMapDataType dt) {
   const Shape& s = p.sh;
   FwdParams fp = make_params(p);
@@ -246,15 +360,46 @@ cudaError_t launch_typed(const Plan& p, const Args& a, CUtensorMapDataType dt) {
   if (!encode_tmap(&tm_x, dt, 4, a.x, x_dims, x_strides, x_box, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tmap(&tm_w, dt, 2, a.b, w_dims, w_strides, w_box, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  cudaError_t err =
-      cudaFuncSetAttribute(fwd_tc_kernel<TO, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
-  if (err != cudaSuccess) return err;
   const int64_t ctas = fp.tiles * p.split;
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  // Slab sigma starts at ws + sigma * E; the kernel indexes pixels within it.
-  fwd_tc_kernel<TO, FMT><<<(unsigned)ctas, kThreads, kSmem, a.stream>>>(tm_x, tm_w, static_cast<TO*>(a.out), a.ws,
-                                                                        fp, device_error_word());
-  return cudaGetLastError();
+  if (!CL) {
+    auto kern = fwd_tc_kernel<TO, FMT, false>;
+    constexpr size_t smem = kSmem;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    // Slab sigma starts at ws + sigma * E; the kernel indexes pixels within it.
+    kern<<<(unsigned)ctas, kThreads, smem, a.stream>>>(tm_x, tm_w, static_cast<TO*>(a.out), a.ws, fp,
+                                                      device_error_word());
+    return cudaGetLastError();
+  }
+  if (p.split < 1 || p.split > kMaxClusterSplit) return cudaErrorInvalidConfiguration;
+  auto kern = fwd_tc_kernel<TO, FMT, true>;
+  constexpr size_t smem = kSmem;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  if (p.split > 8) {  // above the portable cluster size
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (err != cudaSuccess) return err;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // A cluster shape the device cannot place fails here, before any launch.
+  int clusters = 0;
+  err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+  if (err != cudaSuccess) return err;
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  return cudaLaunchKernelEx(&cfg, kern, tm_x, tm_w, static_cast<TO*>(a.out), (float*)nullptr, fp,
+                            device_error_word());
 }
 
 }  // namespace
@@ -270,13 +415,25 @@ Geometry geometry_fwd_tc(const Shape& s) {
   return g;
 }
 
-cudaError_t launch_fwd_tc(const Plan& p, const Args& a) {
-  if (p.sh.in_dt == CONV_BF16) {
-    if (p.sh.out_dt == CONV_F32) return launch_typed<float, 1u>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
-    return launch_typed<__nv_bfloat16, 1u>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
-  }
-  if (p.sh.out_dt == CONV_F32) return launch_typed<float, 0u>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
-  return launch_typed<__half, 0u>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+Geometry geometry_fwd_tc_cluster(const Shape& s) {
+  Geometry g = geometry_fwd_tc(s);
+  g.max_split = kMaxClusterSplit;
+  return g;
 }
+
+namespace {
+template <bool CL>
+cudaError_t launch_any(const Plan& p, const Args& a) {
+  if (p.sh.in_dt == CONV_BF16) {
+    if (p.sh.out_dt == CONV_F32) return launch_typed<float, 1u, CL>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+    return launch_typed<__nv_bfloat16, 1u, CL>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+  }
+  if (p.sh.out_dt == CONV_F32) return launch_typed<float, 0u, CL>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+  return launch_typed<__half, 0u, CL>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+}
+}  // namespace
+
+cudaError_t launch_fwd_tc(const Plan& p, const Args& a) { return launch_any<false>(p, a); }
+cudaError_t launch_fwd_tc_cluster(const Plan& p, const Args& a) { return launch_any<true>(p, a); }
 
 }  // namespace cig

@@ -83,9 +83,11 @@ typedef struct conv_problem {
   int32_t in_dtype, out_dtype;
 } conv_problem;
 
-/* The kernels stage 1 can run. Chosen from the problem alone (never from
- * timing), so a degree and a workspace size resolved ahead of a call hold for
- * that call. */
+/* The kernels stage 1 can run. Chosen from the problem and the degree
+ * request alone (never from timing), so a degree and a workspace size
+ * resolved ahead of a call hold for that call. Automatic choice never takes
+ * CONV_KERNEL_FWD_TC_CLUSTER (on the 3x3 small-M layer it measured slower than
+ * the two-stage form); the override selects it. */
 typedef enum conv_kernel {
   CONV_KERNEL_AUTO = 0,
   CONV_KERNEL_GENERIC = 1,           /* direct, CUDA cores: any shape and type */
@@ -93,19 +95,24 @@ typedef enum conv_kernel {
   CONV_KERNEL_WGRAD_1X1_TF32X3 = 3,  /* fp32 1x1 weight gradient, tcgen05 3xTF32 */
   CONV_KERNEL_FWD_TC = 4,            /* 16-bit forward, tcgen05 + TMA im2col */
   CONV_KERNEL_WGRAD_DEPTHWISE = 5,   /* depthwise weight gradient, CUDA cores */
-  CONV_KERNEL_WGRAD_GROUPED = 6      /* 4/8 channels per group, CUDA cores */
+  CONV_KERNEL_WGRAD_GROUPED = 6,     /* 4/8 channels per group, CUDA cores */
+  CONV_KERNEL_FWD_TC_CLUSTER = 7     /* 16-bit forward, the S <= 16 slices of a tile as one
+                                        thread-block cluster folding through distributed
+                                        shared memory [P2 "Changes": single-launch split-K]:
+                                        no workspace, no stage 2 */
 } conv_kernel;
 
 /* What a call with these arguments would run. */
 typedef struct conv_plan_info {
   int32_t kernel;            /* conv_kernel of stage 1 */
   int32_t split_k;           /* resolved degree S >= 1 */
-  int32_t needs_fold;        /* 1 when stage 2 runs (S > 1) */
+  int32_t needs_fold;        /* 1 when stage 2 runs (S > 1, slices not folded in-launch) */
   int32_t ctas_per_sm;       /* resident stage-1 CTAs per SM the policy assumes */
   int64_t tiles;             /* output tiles of stage 1 */
   int64_t reduction_blocks;  /* reduction blocks; a pinned degree may not exceed it */
   int64_t ctas;              /* stage-1 CTAs = tiles * S */
-  uint64_t workspace_bytes;  /* bytes the call needs (0 when S = 1) */
+  uint64_t workspace_bytes;  /* bytes the call needs (0 without stage 2) */
+  int32_t max_split;         /* largest degree a pinned request may ask of this kernel */
 } conv_plan_info;
 
 /* Human-readable name of a status. Never NULL. */
@@ -120,13 +127,14 @@ conv_status conv_output_dims(const conv_problem* p, int64_t* ho, int64_t* wo);
  *  - target = sm_count x (resident stage-1 CTAs per SM of the chosen kernel);
  *  - forward: split only when the unsplit grid is under half the target and
  *    the reduction R*S*Cg is at least 512 deep, and never for a pointwise
- *    (1x1) forward; the degree is the largest power of two <= 32 with
- *    tiles x degree <= target, halved until every slice has >= 2 reduction
- *    blocks;
+ *    (1x1) forward; the degree is the largest power of two <= 32 (<= 16,
+ *    the largest cluster, for the cluster form) with tiles x degree <=
+ *    target, halved until every slice has >= 2 reduction blocks;
  *  - weight gradient (no policy on the pages): degree = floor(target / tiles)
  *    when tiles < target, at most half the reduction blocks (>= 2 blocks per
  *    slice) and at most 4096, else 1.
- * request 0 gives 1; request n >= 1 gives n if n <= reduction blocks. */
+ * request 0 gives 1; request n >= 1 gives n if n <= reduction blocks (and
+ * n <= 16 for the cluster form, else CONV_ERR_UNSUPPORTED). */
 conv_status resolve_split_k_for(const conv_problem* p, conv_dir dir, int32_t request,
                                 int32_t sm_count, int32_t* degree);
 

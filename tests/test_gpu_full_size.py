@@ -97,3 +97,26 @@ def test_config2_batch_sweep():
         dw, db = gpu_wgrad(x[:n], dy[:n], n)
         assert relerr(dw[k0:k1], dw_ref[k0:k1]) <= 1e-5, n
         assert relerr(db, db_ref) <= 1e-5, n
+
+
+def test_fwd3x3_compute_bound_supplement_sampled_images():
+    """3x3 fwd bf16, N=64, 56x56, C=K=256, pad 1, in the bench's launch
+    configuration (auto). An image's output depends on that image alone, so the
+    oracle runs images 0, 31 and 63 as N=1 problems on the same W."""
+    n, hw, c, k = 64, 56, 256, 256
+    p = cig.Problem(n=n, h=hw, w=hw, c=c, k=k, r=3, s=3, pad_h=1, pad_w=1, in_dtype=cig.BF16, out_dtype=cig.BF16)
+    x = synth.tensor((n, hw, hw, c), torch.bfloat16, "normal", 0.0, 0.02, 5, synth.X_ID)
+    w = synth.tensor((k, 3, 3, c), torch.bfloat16, "normal", 0.0, 0.02, 5, synth.W_ID)
+    y = torch.empty((n, hw, hw, k), dtype=torch.bfloat16, device="cuda")
+    ws = cig.workspace(p, cig.DIR_FWD, -1, False)
+    assert cig.describe_plan(p, cig.DIR_FWD, -1)["kernel_name"] == "fwd_tc"
+    cig.conv_fwd(p, x.cuda(), w.cuda(), y, ws, -1)
+    torch.cuda.synchronize()
+    yc = y.cpu()
+    orc = oracle.get()
+    p1 = cig.Problem(n=1, h=hw, w=hw, c=c, k=k, r=3, s=3, pad_h=1, pad_w=1, in_dtype=cig.BF16, out_dtype=cig.BF16)
+    for i in (0, 31, 63):
+        ref = orc.fwd(oproblem(p1), x[i:i + 1], w)
+        e = relerr(yc[i:i + 1], ref)
+        assert e <= 1e-2, f"image {i}: err {e:.3e}"
+    assert cig.device_errors() == 0

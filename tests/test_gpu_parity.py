@@ -22,8 +22,10 @@ def _reset_override():
 
 
 def _max_degree(p, d):
+    """The largest degree the current kernel takes: the reduction blocks, or
+    the cluster limit of the single-launch forward."""
     return cig.describe_plan(p, d, 1, sm_count=torch.cuda.get_device_properties(0).multi_processor_count)[
-        "reduction_blocks"]
+        "max_split"]
 
 
 def check_wgrad(p, seed, kernels, splits, dist="normal", a=0.0, b=1.0, bias=True):
@@ -181,6 +183,35 @@ def test_config3_forward_split_sweep():
     p = cig.Problem(n=1, h=14, w=14, c=2048, k=512, r=3, s=3, pad_h=1, pad_w=1, in_dtype=BF16, out_dtype=BF16)
     assert cig.describe_plan(p, cig.DIR_FWD, -1)["kernel_name"] == "fwd_tc"
     check_fwd(p, 2, ["auto"], [-1, 1, 2, 4, 8, 16, 32], "normal", 0.0, 0.02)
+    check_fwd(p, 2, ["fwd_tc_cluster"], [-1, 2, 16], "normal", 0.0, 0.02)
+    assert cig.device_errors() == 0
+
+
+@pytest.mark.parametrize("shape", [
+    dict(n=1, h=14, w=14, c=2048, k=512, r=3, s=3, pad_h=1, pad_w=1),          # the 3x3 small-M layer
+    dict(n=2, h=10, w=12, c=128, k=136, r=3, s=3, pad_h=1, pad_w=1),           # K tail, 2 M tiles per image
+    dict(n=1, h=9, w=11, c=64, k=128, r=5, s=5, pad_h=4, pad_w=4, dil_h=2, dil_w=2),
+])
+def test_forward_cluster_equals_two_stage(shape):
+    """The single-launch form folds the same per-slice partial tiles in the
+    same slice order as the fold kernel ("feat(rocke): split-K forward
+    implicit-GEMM convolution on gfx1250", "Changes"), so Y is bit-identical
+    to the two-stage form at every degree, and reruns are bit-identical."""
+    p = cig.Problem(**shape, in_dtype=BF16, out_dtype=BF16)
+    x, w = inputs(p, 2, "normal", 0.0, 0.02, cig.DIR_FWD)
+    top = cig.describe_plan(p, cig.DIR_FWD, 1)["reduction_blocks"]
+    for sk in (2, 3, 5, 8, 13, 16):
+        if sk > top:
+            continue
+        cig.set_kernel_override("fwd_tc_cluster")
+        assert cig.describe_plan(p, cig.DIR_FWD, sk)["workspace_bytes"] == 0
+        y1 = run_fwd(p, x, w, sk)
+        y2 = run_fwd(p, x, w, sk)
+        cig.set_kernel_override("fwd_tc")
+        y0 = run_fwd(p, x, w, sk)
+        cig.set_kernel_override("auto")
+        assert torch.equal(y1.view(torch.int16), y0.view(torch.int16)), f"split {sk}: cluster != two-stage"
+        assert torch.equal(y1.view(torch.int16), y2.view(torch.int16)), f"split {sk}: rerun differs"
     assert cig.device_errors() == 0
 
 
@@ -193,7 +224,8 @@ def test_config3_forward_split_sweep():
 @pytest.mark.parametrize("dt", [(BF16, BF16), (F16, F32), (F16, F16)], ids=lambda d: f"{d[0]}{d[1]}")
 def test_forward_tc_ragged(shape, dt):
     p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
-    check_fwd(p, 6, ["fwd_tc", "generic"], [-1, 1, 3])
+    check_fwd(p, 6, ["fwd_tc", "fwd_tc_cluster", "generic"], [-1, 1, 3])
+    check_fwd(p, 6, ["fwd_tc", "fwd_tc_cluster"], ["max"])
     assert cig.device_errors() == 0
 
 

@@ -97,13 +97,14 @@ def test_auto_is_deterministic_and_within_bounds():
             S = a["split_k"]
             assert 1 <= S <= max(1, a["reduction_blocks"])
             assert a["ctas"] == a["tiles"] * S
-            assert a["needs_fold"] == (S > 1)
+            assert a["needs_fold"] == (S > 1 and a["kernel_name"] != "fwd_tc_cluster")
 
 
 def test_forward_policy_properties():
     """Forward auto degree ("Auto-deduced degree" of the split-K forward page):
-    power of two <= 32, 1 for a grid >= half the target, a reduction < 512 or
-    a pointwise problem, >= 2 reduction blocks per slice."""
+    power of two <= 32 (<= 16 for the cluster form), 1 for a grid >= half the
+    target, a reduction < 512 or a pointwise problem, >= 2 reduction blocks
+    per slice."""
     shapes = [CONFIG3,
               Problem(n=1, h=7, w=7, c=512, k=512, r=7, s=7, pad_h=3, pad_w=3, in_dtype=BF16, out_dtype=BF16),
               Problem(n=1, h=14, w=14, c=2048, k=512, in_dtype=BF16, out_dtype=BF16),   # pointwise
@@ -115,12 +116,13 @@ def test_forward_policy_properties():
             S, tiles, blocks = info["split_k"], info["tiles"], info["reduction_blocks"]
             target = sms * info["ctas_per_sm"]
             depth = p.r * p.s * (p.c // p.groups)
-            assert S & (S - 1) == 0 and S <= 32
+            cap = 16 if info["kernel_name"] == "fwd_tc_cluster" else 32
+            assert S & (S - 1) == 0 and S <= cap
             if p.r == 1 and p.s == 1 or 2 * tiles >= target or depth < 512:
                 assert S == 1
             else:
                 assert tiles * S <= target and blocks >= 2 * S
-                assert S == 32 or tiles * 2 * S > target or blocks < 4 * S
+                assert S == cap or tiles * 2 * S > target or blocks < 4 * S
 
 
 def test_wgrad_policy_fills_the_gpu_in_whole_waves():
@@ -139,9 +141,36 @@ def test_workspace_bytes_arithmetic():
                 ho, wo = p.out_hw
                 E = p.n * ho * wo * p.k if d == DIR_FWD else p.k * p.r * p.s * (p.c // p.groups)
                 r256 = lambda v: (v + 255) // 256 * 256  # noqa: E731
-                want = 0 if S == 1 else r256(S * E * 4) + (r256(S * p.k * 4) if bias and d == DIR_WGRAD else 0)
+                fold = S > 1 and info["kernel_name"] != "fwd_tc_cluster"
+                want = 0 if not fold else r256(S * E * 4) + (r256(S * p.k * 4) if bias and d == DIR_WGRAD else 0)
                 assert info["workspace_bytes"] == want
                 assert cig.workspace_bytes(p, d, req, bias, sm_count=SMS) == want
+
+
+def test_forward_cluster_form_selection():
+    """Single-launch split-K ("feat(rocke): split-K forward implicit-GEMM
+    convolution on gfx1250", "Changes"): only through the override; degrees
+    1..16, no workspace and no fold; past 16 it is refused. Automatic choice
+    keeps the two-stage form."""
+    auto = cig.describe_plan(CONFIG3, DIR_FWD, -1, sm_count=SMS)
+    assert auto["kernel_name"] == "fwd_tc" and auto["split_k"] == 32 and auto["needs_fold"] == 1
+    assert auto["max_split"] == auto["reduction_blocks"] == 288
+    cig.set_kernel_override("fwd_tc_cluster")
+    info = cig.describe_plan(CONFIG3, DIR_FWD, -1, sm_count=SMS)
+    assert (info["kernel_name"], info["split_k"], info["workspace_bytes"], info["needs_fold"]) == (
+        "fwd_tc_cluster", 16, 0, 0)
+    assert info["max_split"] == 16
+    for req in (0, 1, 2, 3, 9, 16):
+        info = cig.describe_plan(CONFIG3, DIR_FWD, req, sm_count=SMS)
+        assert (info["kernel_name"], info["split_k"], info["workspace_bytes"]) == ("fwd_tc_cluster", max(req, 1), 0)
+        assert cig.workspace_bytes(p=CONFIG3, direction=DIR_FWD, split_k=req, sm_count=SMS) == 0
+    for req, status in ((17, 2), (288, 2), (289, 1)):
+        with pytest.raises(cig.ConvError) as e:
+            cig.describe_plan(CONFIG3, DIR_FWD, req, sm_count=SMS)
+        assert e.value.status == status
+    with pytest.raises(cig.ConvError) as e:
+        cig.describe_plan(CONFIG4, DIR_WGRAD, -1, sm_count=SMS)
+    assert e.value.status == 2
 
 
 def test_empty_batch_plans_one_slice():
