@@ -38,23 +38,29 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kBM = 128;
-constexpr int kBN = 128;
 constexpr int kBK = 64;                     // channels per reduction block (128 bytes of 16-bit)
 constexpr int kA = kBM * 128;               // A tile bytes (128 rows x 128 B)
-constexpr int kB = kBN * 128;
-constexpr int kStage = kA + kB;
-constexpr uint32_t kTmemCols = 128;
-constexpr int kLD = kBN + 4;                // staged partial tile: row stride in floats (conflict-free float4s)
 
-// Ring depth: 3 stages, 2 CTAs per SM. (A deeper ring for the cluster form
-// would hold one CTA per SM, and then only 7 clusters of 16 fit on the GPU at
-// once, fewer than the 8 tiles of the 3x3 small-M layer.)
-constexpr int kStages = 3;
-constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + 256;
-static_assert(kBM * kLD * 4 <= kStages * kStage, "staged partial tile must fit in the ring");
+// Tile of BN output channels (128, or 256 when K >= 256: an SM then loads
+// 48 KB per 2 M multiply-adds instead of 32 KB per 1 M, and its L2 -> shared
+// bandwidth, not the tensor pipe, is what bounds a block). Ring: 3 stages for
+// BN = 128 (2 CTAs per SM), 4 for BN = 256 (1 CTA per SM). (A deeper ring for
+// the cluster form would hold one CTA per SM, and then only 7 clusters of 16
+// fit on the GPU at once, fewer than the 8 tiles of the 3x3 small-M layer.)
+template <int BN>
+struct Tile {
+  static constexpr int kB = BN * 128;              // B tile bytes (BN rows x 128 B)
+  static constexpr int kStage = kA + kB;
+  static constexpr int kStages = BN == 256 ? 4 : 3;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + 256;
+  static constexpr uint32_t kTmemCols = BN;
+  static constexpr int kLD = BN + 4;                // staged partial tile row stride, floats (conflict-free float4s)
+  static_assert(BN == 128 || BN == 256, "tile width");
+  static_assert(kBM * kLD * 4 <= kStages * kStage, "staged partial tile must fit in the ring");
+};
 
 struct FwdParams {
-  int64_t K, Ho, Wo, Cg, S_f;   // S_f: filter width
+  int64_t N, K, Ho, Wo, Cg, S_f;   // S_f: filter width
   int64_t E;                    // output elements N*Ho*Wo*K (one slab)
   int64_t cblocks;              // Cg / 64
   int64_t tiles_m_per_img;      // ceil(Ho / TR)
@@ -66,26 +72,77 @@ struct FwdParams {
   int32_t split;
 };
 
-template <typename TO>
-__device__ __forceinline__ void store8(TO* dst, const float* v);
+// 16 bytes of TE from 4 (fp32) or 8 (16-bit) values, rounded to nearest even.
+template <typename TE>
+__device__ __forceinline__ uint4 pack16(const float* v);
 template <>
-__device__ __forceinline__ void store8<float>(float* dst, const float* v) {
-  reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
-  reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
+__device__ __forceinline__ uint4 pack16<float>(const float* v) {
+  return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
 }
 template <>
-__device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* dst, const float* v) {
+__device__ __forceinline__ uint4 pack16<__nv_bfloat16>(const float* v) {
+  uint4 r;
   __nv_bfloat162 h[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-  *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<uint4*>(h);
+  memcpy(&r, h, 16);
+  return r;
 }
 template <>
-__device__ __forceinline__ void store8<__half>(__half* dst, const float* v) {
+__device__ __forceinline__ uint4 pack16<__half>(const float* v) {
+  uint4 r;
   __half2 h[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
-  *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<uint4*>(h);
+  memcpy(&r, h, 16);
+  return r;
+}
+
+// Epilogue of the two-stage form: the tile's rows go through shared memory
+// and TMA tensor stores. For each 128-byte column chunk (32 fp32 or 64 16-bit
+// channels) the thread of row m writes its 128 bytes into a 128B-swizzled
+// staging buffer (8 conflict-free 16-byte stores; two 16 KB buffers in the
+// idle ring, alternating), and one thread stores the box {chunk, TR*Wo
+// pixels, 1}; the tensor map clips it at K and at the image's Ho*Wo pixels.
+// Few instructions per thread: the four epilogue warps issue every one of
+// them, one CTA per SM.
+template <typename TE, int BN>
+__device__ __forceinline__ void store_tile_tma(uint32_t trow, uint8_t* stage, const CUtensorMap* tm, int32_t kx0,
+                                               int32_t kx_end, int32_t py, int32_t pz, int m, bool have_acc,
+                                               bool leader, bool do_store) {
+  constexpr int CW = 128 / (int)sizeof(TE);  // channels per 128-byte chunk
+  constexpr int VPU = 16 / (int)sizeof(TE);  // values per 16-byte unit
+#pragma unroll 1
+  for (int c = 0; c < BN / CW; ++c) {
+    uint8_t* buf = stage + (c & 1) * (kBM * 128);
+    if (c >= 2) {  // the store that last read this buffer must be done reading
+      if (leader) bulk_wait_read<1>();
+      named_bar_sync(1, 128);
+    }
+    float v[CW];
+#pragma unroll
+    for (int h = 0; h < CW / 32; ++h) {
+      if (have_acc) {
+        tmem_ld32(trow + (uint32_t)(c * CW + 32 * h), v + 32 * h);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[32 * h + i] = 0.f;
+      }
+    }
+    uint8_t* row = buf + m * 128;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint4 pk = pack16<TE>(v + u * VPU);
+      st_shared_v4(row + ((u ^ (m & 7)) << 4), pk.x, pk.y, pk.z, pk.w);
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, 128);
+    if (leader && do_store && kx0 + c * CW < kx_end) {  // no box starting past K
+      tma_store_3d(tm, buf, kx0 + c * CW, py, pz);
+      bulk_commit();
+    }
+  }
+  if (leader) bulk_wait<0>();
 }
 
 template <typename TO>
@@ -105,10 +162,13 @@ __device__ __forceinline__ void store4<__half>(__half* dst, float4 v) {
   *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<uint2*>(h);
 }
 
-template <typename TO, uint32_t FMT, bool CL>
-__global__ void __launch_bounds__(kThreads, 2)
-    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, TO* out,
-                  float* ws, FwdParams fp, unsigned* err) {
+template <typename TO, uint32_t FMT, bool CL, int BN>
+__global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                  const __grid_constant__ CUtensorMap tm_y, TO* out, float* ws, FwdParams fp, unsigned* err) {
+  using T = Tile<BN>;
+  constexpr int kStages = T::kStages, kStage = T::kStage, kB = T::kB, kLD = T::kLD;
+  constexpr uint32_t kTmemCols = T::kTmemCols;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * kStage);
@@ -116,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint64_t* tmem_full = empty + kStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_full + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
-  constexpr uint32_t IDESC = mma_idesc(FMT, 0u, 0u, (uint32_t)kBN, (uint32_t)kBM);
+  constexpr uint32_t IDESC = mma_idesc(FMT, 0u, 0u, (uint32_t)BN, (uint32_t)kBM);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // Two-stage form: CTA = sigma * tiles + tile. Cluster form: the S CTAs of
@@ -127,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int64_t tm = tile / fp.tiles_n;
   const int64_t img = tm / fp.tiles_m_per_img;
   const int64_t ho0 = (tm % fp.tiles_m_per_img) * fp.TR;
-  const int64_t k0 = tn * kBN;
+  const int64_t k0 = tn * BN;
   const int64_t b0 = slice_begin(fp.blocks, fp.split, sigma);
   const int64_t nblk = slice_begin(fp.blocks, fp.split, sigma + 1) - b0;
   const uint32_t tx = (uint32_t)(fp.TR * fp.Wo * 128 + kB);
@@ -231,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       // idle: every copy landed and every MMA that read it has completed).
       float* part = reinterpret_cast<float*>(smem) + m * kLD;
 #pragma unroll 1
-      for (int j = 0; j < kBN / 32; ++j) {
+      for (int j = 0; j < BN / 32; ++j) {
         float v[32];
         if (nblk > 0) {
           tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32u * j, v);
@@ -244,31 +304,16 @@ __global__ void __launch_bounds__(kThreads, 2)
           *reinterpret_cast<float4*>(part + 32 * j + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
       }
     } else {
-      const int64_t ho = ho0 + m / fp.Wo, wo = m % fp.Wo;
-      const bool row_ok = ok && m < fp.TR * fp.Wo && ho < fp.Ho;
-      const int64_t pix = (img * fp.Ho + ho) * fp.Wo + wo;
-      float* slab = ws ? ws + (int64_t)sigma * fp.E : nullptr;
-#pragma unroll 1
-      for (int j = 0; j < kBN / 32; ++j) {
-        float v[32];
-        if (nblk > 0) {
-          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32u * j, v);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0.f;
-        }
-        if (!row_ok) continue;
-#pragma unroll
-        for (int i = 0; i < 32; i += 8) {
-          const int64_t k = k0 + 32 * j + i;
-          if (k >= fp.K) continue;  // K % 8 == 0: an 8-wide group is all in or all out
-          if (slab) {
-            store8<float>(slab + pix * fp.K + k, v + i);
-          } else {
-            store8<TO>(out + pix * fp.K + k, v + i);
-          }
-        }
-      }
+      // Y (or slab sigma of the workspace, fp32) as [N (x S)][Ho*Wo][K].
+      const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+      uint8_t* stage = smem;  // the ring is idle: every copy landed, every MMA completed
+      const int32_t py = (int32_t)(ho0 * fp.Wo);
+      if (ws)
+        store_tile_tma<float, BN>(trow, stage, &tm_y, (int32_t)k0, (int32_t)fp.K, py, (int32_t)(sigma * fp.N + img),
+                                  m, nblk > 0, threadIdx.x == 128, ok);
+      else
+        store_tile_tma<TO, BN>(trow, stage, &tm_y, (int32_t)k0, (int32_t)fp.K, py, (int32_t)img, m, nblk > 0,
+                               threadIdx.x == 128, ok);
     }
   }
 
@@ -282,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     const bool ok = *abort_flag == 0u;
     const uint32_t base = smem_u32(smem);
 #pragma unroll 1
-    for (int w = threadIdx.x; w < (r1 - r0) * (kBN / 4); w += kThreads) {
-      const int m = r0 + w / (kBN / 4), c4 = w % (kBN / 4);
+    for (int w = threadIdx.x; w < (r1 - r0) * (BN / 4); w += kThreads) {
+      const int m = r0 + w / (BN / 4), c4 = w % (BN / 4);
       const int64_t k = k0 + 4 * c4;
       if (!ok || m >= valid || k >= fp.K) continue;  // K % 8 == 0: 4-wide groups are all in or all out
       const uint32_t la = base + (uint32_t)((m * kLD + 4 * c4) * 4);
@@ -314,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 bool fwd_tc_admissible(const Shape& s) {
   if (s.in_dt == CONV_F32 || s.groups != 1 || s.sh != 1 || s.sw != 1) return false;
-  if (s.cg % kBK != 0 || s.k % 8 != 0 || s.k < kBN) return false;
+  if (s.cg % kBK != 0 || s.k % 8 != 0 || s.k < 128) return false;
   if (s.wo > kBM || s.wo > s.w) return false;    // one TMA box spans a whole output row
   if (s.n < 1 || s.n > 0x7fffffffLL || s.h > 0x7fffffffLL || s.w > 0x7fffffffLL) return false;
   const int64_t tr = kBM / s.wo;
@@ -323,9 +368,13 @@ bool fwd_tc_admissible(const Shape& s) {
   return true;
 }
 
-FwdParams make_params(const Plan& p) {
+// Tile width: 256 output channels when K >= 256 (the two-stage form), else 128.
+int tile_bn(const Shape& s, bool cluster) { return !cluster && s.k >= 256 ? 256 : 128; }
+
+FwdParams make_params(const Plan& p, int bn) {
   const Shape& s = p.sh;
   FwdParams fp;
+  fp.N = s.n;
   fp.K = s.k;
   fp.E = s.y_elems();
   fp.Ho = s.ho;
@@ -335,7 +384,7 @@ FwdParams make_params(const Plan& p) {
   fp.cblocks = s.cg / kBK;
   fp.TR = (int32_t)(kBM / s.wo < s.ho ? kBM / s.wo : s.ho);
   fp.tiles_m_per_img = (s.ho + fp.TR - 1) / fp.TR;
-  fp.tiles_n = (s.k + kBN - 1) / kBN;
+  fp.tiles_n = (s.k + bn - 1) / bn;
   fp.tiles = s.n * fp.tiles_m_per_img * fp.tiles_n;
   fp.blocks = s.r * s.s * fp.cblocks;
   fp.ph = (int32_t)s.ph;
@@ -346,35 +395,51 @@ FwdParams make_params(const Plan& p) {
   return fp;
 }
 
-template <typename TO, uint32_t FMT, bool CL>
+template <typename TO, uint32_t FMT, bool CL, int BN>
 cudaError_t launch_typed(const Plan& p, const Args& a, CUtensorMapDataType dt) {
   const Shape& s = p.sh;
-  FwdParams fp = make_params(p);
+  FwdParams fp = make_params(p, BN);
+  constexpr size_t smem = Tile<BN>::kSmem;
   CUtensorMap tm_x, tm_w;
   const uint64_t x_dims[4] = {(uint64_t)s.c, (uint64_t)s.w, (uint64_t)s.h, (uint64_t)s.n};
   const uint64_t x_strides[3] = {(uint64_t)s.c * 2u, (uint64_t)(s.w * s.c) * 2u, (uint64_t)(s.h * s.w * s.c) * 2u};
   const uint32_t x_box[4] = {(uint32_t)kBK, (uint32_t)s.wo, (uint32_t)fp.TR, 1u};
   const uint64_t w_dims[2] = {(uint64_t)(s.r * s.s * s.cg), (uint64_t)s.k};
   const uint64_t w_strides[1] = {(uint64_t)(s.r * s.s * s.cg) * 2u};
-  const uint32_t w_box[2] = {(uint32_t)kBK, (uint32_t)kBN};
+  const uint32_t w_box[2] = {(uint32_t)kBK, (uint32_t)BN};
   if (!encode_tmap(&tm_x, dt, 4, a.x, x_dims, x_strides, x_box, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tmap(&tm_w, dt, 2, a.b, w_dims, w_strides, w_box, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  // Output map of the two-stage form's epilogue: the slabs (fp32) under
+  // split-K, else Y, as [N (x S)][Ho*Wo][K], boxes of 128 bytes x TR*Wo pixels.
+  CUtensorMap tm_y;
+  if (!CL) {
+    const bool slabs = a.ws != nullptr;
+    const uint64_t es = slabs ? 4u : (uint64_t)sizeof(TO);
+    const CUtensorMapDataType ydt = slabs || sizeof(TO) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : dt;
+    const uint64_t y_dims[3] = {(uint64_t)s.k, (uint64_t)(s.ho * s.wo), (uint64_t)s.n * (slabs ? (uint64_t)p.split : 1u)};
+    const uint64_t y_strides[2] = {(uint64_t)s.k * es, (uint64_t)(s.ho * s.wo * s.k) * es};
+    const uint32_t y_box[3] = {(uint32_t)(128 / es), (uint32_t)(fp.TR * s.wo), 1u};
+    if (s.n * (int64_t)p.split > 0x7fffffffLL ||
+        !encode_tmap(&tm_y, ydt, 3, slabs ? (const void*)a.ws : a.out, y_dims, y_strides, y_box,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  } else {
+    tm_y = tm_w;  // unused by the cluster form
+  }
   const int64_t ctas = fp.tiles * p.split;
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (!CL) {
-    auto kern = fwd_tc_kernel<TO, FMT, false>;
-    constexpr size_t smem = kSmem;
+    auto kern = fwd_tc_kernel<TO, FMT, false, BN>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     // Slab sigma starts at ws + sigma * E; the kernel indexes pixels within it.
-    kern<<<(unsigned)ctas, kThreads, smem, a.stream>>>(tm_x, tm_w, static_cast<TO*>(a.out), a.ws, fp,
+    kern<<<(unsigned)ctas, kThreads, smem, a.stream>>>(tm_x, tm_w, tm_y, static_cast<TO*>(a.out), a.ws, fp,
                                                       device_error_word());
     return cudaGetLastError();
   }
   if (p.split < 1 || p.split > kMaxClusterSplit) return cudaErrorInvalidConfiguration;
-  auto kern = fwd_tc_kernel<TO, FMT, true>;
-  constexpr size_t smem = kSmem;
+  auto kern = fwd_tc_kernel<TO, FMT, true, BN>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   if (p.split > 8) {  // above the portable cluster size
@@ -398,42 +463,45 @@ cudaError_t launch_typed(const Plan& p, const Args& a, CUtensorMapDataType dt) {
   err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
   if (err != cudaSuccess) return err;
   if (clusters < 1) return cudaErrorInvalidConfiguration;
-  return cudaLaunchKernelEx(&cfg, kern, tm_x, tm_w, static_cast<TO*>(a.out), (float*)nullptr, fp,
+  return cudaLaunchKernelEx(&cfg, kern, tm_x, tm_w, tm_y, static_cast<TO*>(a.out), (float*)nullptr, fp,
                             device_error_word());
 }
 
 }  // namespace
 
-Geometry geometry_fwd_tc(const Shape& s) {
+namespace {
+Geometry geometry_of(const Shape& s, bool cluster) {
   Geometry g;
   if (!fwd_tc_admissible(s)) return g;
   const int64_t tr = kBM / s.wo < s.ho ? kBM / s.wo : s.ho;
+  const int bn = tile_bn(s, cluster);
   g.ok = true;
-  g.ctas_per_sm = 2;
-  g.tiles = s.n * ((s.ho + tr - 1) / tr) * ((s.k + kBN - 1) / kBN);
+  g.ctas_per_sm = bn == 256 ? 1 : 2;
+  g.tiles = s.n * ((s.ho + tr - 1) / tr) * ((s.k + bn - 1) / bn);
   g.blocks = s.r * s.s * (s.cg / kBK);
+  if (cluster) g.max_split = kMaxClusterSplit;
   return g;
-}
-
-Geometry geometry_fwd_tc_cluster(const Shape& s) {
-  Geometry g = geometry_fwd_tc(s);
-  g.max_split = kMaxClusterSplit;
-  return g;
-}
-
-namespace {
-template <bool CL>
-cudaError_t launch_any(const Plan& p, const Args& a) {
-  if (p.sh.in_dt == CONV_BF16) {
-    if (p.sh.out_dt == CONV_F32) return launch_typed<float, 1u, CL>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
-    return launch_typed<__nv_bfloat16, 1u, CL>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
-  }
-  if (p.sh.out_dt == CONV_F32) return launch_typed<float, 0u, CL>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
-  return launch_typed<__half, 0u, CL>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
 }
 }  // namespace
 
-cudaError_t launch_fwd_tc(const Plan& p, const Args& a) { return launch_any<false>(p, a); }
-cudaError_t launch_fwd_tc_cluster(const Plan& p, const Args& a) { return launch_any<true>(p, a); }
+Geometry geometry_fwd_tc(const Shape& s) { return geometry_of(s, false); }
+Geometry geometry_fwd_tc_cluster(const Shape& s) { return geometry_of(s, true); }
+
+namespace {
+template <bool CL, int BN>
+cudaError_t launch_bn(const Plan& p, const Args& a) {
+  if (p.sh.in_dt == CONV_BF16) {
+    if (p.sh.out_dt == CONV_F32) return launch_typed<float, 1u, CL, BN>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+    return launch_typed<__nv_bfloat16, 1u, CL, BN>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+  }
+  if (p.sh.out_dt == CONV_F32) return launch_typed<float, 0u, CL, BN>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+  return launch_typed<__half, 0u, CL, BN>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+}
+}  // namespace
+
+cudaError_t launch_fwd_tc(const Plan& p, const Args& a) {
+  return tile_bn(p.sh, false) == 256 ? launch_bn<false, 256>(p, a) : launch_bn<false, 128>(p, a);
+}
+cudaError_t launch_fwd_tc_cluster(const Plan& p, const Args& a) { return launch_bn<true, 128>(p, a); }
 
 }  // namespace cig
