@@ -1,4 +1,4 @@
-"""CPU fp64 oracle for NHWC convolution (forward, weight gradient, bias gradient).
+"""CPU fp64 oracle for NHWC convolution (forward, weight, bias and data gradients).
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
 bench's CPU-baseline leg are the only code allowed to import this package.
@@ -90,6 +90,8 @@ class Oracle:
         lib.oracle_conv_wgrad_acc.argtypes = [ctypes.POINTER(_CProblem), _P, _P, ctypes.c_int64,
                                               ctypes.c_int64, _P, ctypes.c_int]
         lib.oracle_conv_wgrad_acc.restype = None
+        lib.oracle_conv_dgrad.argtypes = [ctypes.POINTER(_CProblem), _P, _P, _P, ctypes.c_int]
+        lib.oracle_conv_dgrad.restype = None
         lib.oracle_conv_bgrad_acc.argtypes = [ctypes.POINTER(_CProblem), _P, _P]
         lib.oracle_conv_bgrad_acc.restype = None
         lib.oracle_batch_split_count.argtypes = [ctypes.c_int64, ctypes.c_int64]
@@ -116,6 +118,16 @@ class Oracle:
         self._lib.oracle_conv_fwd(self._cp(p), x.ctypes.data, w.ctypes.data, y.ctypes.data,
                                   nthreads or _threads())
         return y
+
+    def dgrad(self, p: Problem, dy, w, nthreads: int | None = None) -> np.ndarray:
+        """dX [n, h, w, c] in float64: the gradient of the forward with respect to X."""
+        ho, wo = self.out_hw(p)
+        dy, w = _f32(dy), _f32(w)
+        assert dy.size == p.n * ho * wo * p.k and w.size == p.k * p.r * p.s * (p.c // p.groups)
+        dx = np.zeros((p.n, p.h, p.w, p.c), dtype=np.float64)
+        self._lib.oracle_conv_dgrad(self._cp(p), dy.ctypes.data, w.ctypes.data, dx.ctypes.data,
+                                    nthreads or _threads())
+        return dx
 
     def wgrad_acc(self, p: Problem, x, dy, dw: np.ndarray, k_range=None, nthreads: int | None = None):
         """dw += the weight gradient of the samples in x / dy (p.n of them)."""

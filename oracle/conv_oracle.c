@@ -1,6 +1,7 @@
 /*
- * CPU oracle for NHWC 2-D convolution: forward, weight gradient and bias
- * gradient, written as the plain nested-loop definitions in fp64.
+ * CPU oracle for NHWC 2-D convolution: forward, weight gradient, bias
+ * gradient and data gradient, written as the plain nested-loop definitions in
+ * fp64.
  *
  * TEST INFRASTRUCTURE ONLY. Only the tests, the smoke check and the bench's
  * CPU-baseline leg may load this library. The product path never calls it and
@@ -31,7 +32,8 @@
  *
  * Every product of two inputs is formed in double, where it is exact (two
  * 24-bit significands), and summed in double in the loop order written here:
- * wgrad sums over (n, ho, wo) in increasing order, forward over (r, s, c).
+ * wgrad sums over (n, ho, wo) in increasing order, forward over (r, s, c),
+ * dgrad over (r, s, k).
  * Threads split the OUTPUTS among themselves; no output's sum is reordered.
  * Build with -ffp-contract=off so no multiply-add is fused.
  */
@@ -180,6 +182,58 @@ void oracle_conv_wgrad_acc(const oracle_problem* p, const float* x, const float*
   if (k_end <= k_begin) return;
   work base = {p, x, NULL, dy, dw, 0, 0};
   run_parallel(wgrad_worker, &base, k_begin, k_end - k_begin, nthreads);
+}
+
+/* -------------------------------------------------------------- data grad */
+
+/* dX[n,h,w,g*Cg + c] = sum over k = g*Kg .. g*Kg + Kg - 1, r, s of
+ *   dY[n,ho,wo,k] * W[k,r,s,c]
+ * for the one (ho, wo) per tap with ho*sh + r*dh - ph = h and
+ * wo*sw + s*dw - pw = w inside [0,Ho) x [0,Wo): the forward output positions
+ * that read input (h, w) through tap (r, s). This is the gradient of the
+ * forward with respect to X (the "dgrad" direction the split-K resolver of
+ * "feat(rocke): split-K forward implicit-GEMM convolution on gfx1250",
+ * "Auto-deduced degree", also covers). Summed over r, then s, then k.
+ * This worker owns input rows (n, h) in [lo, hi). */
+static void* dgrad_worker(void* arg) {
+  const work* j = (const work*)arg;
+  const oracle_problem* p = j->p;
+  const int64_t Ho = oracle_out_extent(p->h, p->pad_h, p->dil_h, p->r, p->stride_h);
+  const int64_t Wo = oracle_out_extent(p->w, p->pad_w, p->dil_w, p->s, p->stride_w);
+  const int64_t Cg = p->c / p->groups, Kg = p->k / p->groups;
+  for (int64_t row = j->lo; row < j->hi; ++row) {
+    const int64_t n = row / p->h, h = row % p->h;
+    for (int64_t w = 0; w < p->w; ++w) {
+      for (int64_t ci = 0; ci < p->c; ++ci) {
+        const int64_t g = ci / Cg, c = ci % Cg;
+        double acc = 0.0;
+        for (int64_t r = 0; r < p->r; ++r) {
+          const int64_t hn = h + p->pad_h - r * p->dil_h; /* = ho * sh */
+          if (hn < 0 || hn % p->stride_h != 0) continue;
+          const int64_t ho = hn / p->stride_h;
+          if (ho >= Ho) continue;
+          for (int64_t s = 0; s < p->s; ++s) {
+            const int64_t wn = w + p->pad_w - s * p->dil_w; /* = wo * sw */
+            if (wn < 0 || wn % p->stride_w != 0) continue;
+            const int64_t wo = wn / p->stride_w;
+            if (wo >= Wo) continue;
+            const float* dyp = j->dy + ((n * Ho + ho) * Wo + wo) * p->k + g * Kg;
+            const float* wp = j->wt + ((g * Kg * p->r + r) * p->s + s) * Cg + c;
+            for (int64_t kk = 0; kk < Kg; ++kk)
+              acc += (double)dyp[kk] * (double)wp[kk * p->r * p->s * Cg];
+          }
+        }
+        j->out[((n * p->h + h) * p->w + w) * p->c + ci] = acc;
+      }
+    }
+  }
+  return NULL;
+}
+
+void oracle_conv_dgrad(const oracle_problem* p, const float* dy, const float* wt, double* dx,
+                       int nthreads) {
+  work base = {p, NULL, wt, dy, dx, 0, 0};
+  run_parallel(dgrad_worker, &base, 0, p->n * p->h, nthreads);
 }
 
 /* -------------------------------------------------------------- bias grad */

@@ -144,7 +144,47 @@ def pin_adjoint(orc: Oracle):
     return True
 
 
-PINS = [pin_1x1_gemm, pin_bias_sum, pin_torch_fwd, pin_torch_wgrad, pin_all_ones, pin_adjoint]
+def torch_dgrad(p: Problem, w, dy):
+    """dX via autograd of torch's float64 conv2d with respect to its input."""
+    xt = torch.zeros((p.n, p.c, p.h, p.w), dtype=torch.float64, requires_grad=True)
+    wt = torch.from_numpy(np.asarray(w, np.float64)).permute(0, 3, 1, 2)
+    y = torch.nn.functional.conv2d(xt, wt, stride=(p.stride_h, p.stride_w),
+                                   padding=(p.pad_h, p.pad_w), dilation=(p.dil_h, p.dil_w),
+                                   groups=p.groups)
+    y.backward(torch.from_numpy(np.asarray(dy, np.float64)).permute(0, 3, 1, 2))
+    return xt.grad.permute(0, 2, 3, 1).numpy()
+
+
+def pin_torch_dgrad(orc: Oracle):
+    for p in SHAPES:
+        _, w, dy = _inputs(p, orc)
+        if relerr(orc.dgrad(p, dy, w), torch_dgrad(p, w, dy)) > 1e-12:
+            return False
+    return True
+
+
+def pin_adjoint_dgrad(orc: Oracle):
+    """<conv(X, W), dY> = <X, dgrad(dY, W)> (exact in real arithmetic)."""
+    for p in SHAPES:
+        x, w, dy = _inputs(p, orc)
+        lhs = float((orc.fwd(p, x, w) * dy.astype(np.float64)).sum())
+        rhs = float((orc.dgrad(p, dy, w) * x.astype(np.float64)).sum())
+        if abs(lhs - rhs) > 1e-12 * max(1.0, abs(lhs)):
+            return False
+    return True
+
+
+def pin_1x1_dgrad_gemm(orc: Oracle):
+    """A 1x1, stride-1 data gradient is dY W on the [N*H*W, K] view."""
+    p = Problem(n=3, h=5, w=7, c=12, k=10)
+    dy = rand((3, 5, 7, 10), 3, synth.DY_ID)
+    w = rand((10, 1, 1, 12), 3, synth.W_ID)
+    ref = dy.reshape(-1, 10).astype(np.float64) @ w.reshape(10, 12).astype(np.float64)
+    return relerr(orc.dgrad(p, dy, w).reshape(-1, 12), ref) <= 1e-12
+
+
+PINS = [pin_1x1_gemm, pin_bias_sum, pin_torch_fwd, pin_torch_wgrad, pin_all_ones, pin_adjoint,
+        pin_torch_dgrad, pin_adjoint_dgrad, pin_1x1_dgrad_gemm]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -288,6 +328,15 @@ MUTANTS = {
     "fwd_stride_ignored": ("const int64_t h = ho * p->stride_h + r * p->dil_h - p->pad_h;\n          if (h < 0 || h >= p->h) continue;\n          for (int64_t s = 0; s < p->s; ++s) {\n            const int64_t w = wo * p->stride_w",
                            "const int64_t h = ho + r * p->dil_h - p->pad_h;\n          if (h < 0 || h >= p->h) continue;\n          for (int64_t s = 0; s < p->s; ++s) {\n            const int64_t w = wo * p->stride_w"),
     "extent_off_by_one": ("return span / stride + 1;", "return span / stride;"),
+    # data gradient: a wrong sign, a dropped stride test, a transposed tap, the
+    # wrong group block
+    "dgrad_pad_sign": ("const int64_t hn = h + p->pad_h - r * p->dil_h;",
+                       "const int64_t hn = h - p->pad_h + r * p->dil_h;"),
+    "dgrad_stride_not_checked": ("if (wn < 0 || wn % p->stride_w != 0) continue;", "if (wn < 0) continue;"),
+    "dgrad_taps_transposed": ("const float* wp = j->wt + ((g * Kg * p->r + r) * p->s + s) * Cg + c;",
+                              "const float* wp = j->wt + ((g * Kg * p->s + s) * p->r + r) * Cg + c;"),
+    "dgrad_group_block": ("const int64_t g = ci / Cg, c = ci % Cg;", "const int64_t g = ci % p->groups, c = ci / p->groups;"),
+    "dgrad_dropped_last_k": ("for (int64_t kk = 0; kk < Kg; ++kk)", "for (int64_t kk = 0; kk + 1 < Kg; ++kk)"),
 }
 
 
