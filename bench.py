@@ -45,6 +45,12 @@ WORKLOADS = {
     "fwd3x3_bf16_n64_c256": (dict(n=64, h=56, w=56, c=256, k=256, r=3, s=3, pad_h=1, pad_w=1, in_dtype=1,
                                   out_dtype=1), "fwd", "normal", (0.0, 0.02), 5,
                              "3x3 fwd bf16 NHWC N=64 H=W=56 C=K=256 pad 1 (compute-bound supplement)"),
+    "dgrad3x3_bf16_n1": (dict(n=1, h=14, w=14, c=2048, k=512, r=3, s=3, pad_h=1, pad_w=1, in_dtype=1, out_dtype=1),
+                         "dgrad", "normal", (0.0, 0.02), 2,
+                         "3x3 dgrad bf16 NHWC N=1 H=W=14 C=2048 K=512 pad 1 (the small-M layer backwards), split-K"),
+    "dgrad3x3_bf16_n64_c256": (dict(n=64, h=56, w=56, c=256, k=256, r=3, s=3, pad_h=1, pad_w=1, in_dtype=1,
+                                    out_dtype=1), "dgrad", "normal", (0.0, 0.02), 5,
+                               "3x3 dgrad bf16 NHWC N=64 H=W=56 C=K=256 pad 1 (compute-bound supplement backwards)"),
     "dw7x7_wgrad_bf16": (dict(n=32, h=56, w=56, c=384, k=384, r=7, s=7, pad_h=3, pad_w=3, groups=384,
                               in_dtype=1, out_dtype=1), "wgrad", "normal", (0.0, 1.0), 3,
                          "depthwise 7x7 wgrad bf16 NHWC N=32 H=W=56 C=K=384 pad 3"),
@@ -84,6 +90,8 @@ def problem_bytes(p, direction):
     y = p.n * ho * wo * p.k
     if direction == "wgrad":
         return x + y * es + (w + p.k) * eo
+    if direction == "dgrad":  # dY and W in, dX out
+        return y * es + w * es + p.n * p.h * p.w * p.c * eo
     return x + w * es + y * eo
 
 
@@ -171,7 +179,13 @@ def make_inputs_on_device(p, direction, dist, args, seed, device, pinned_copy=Fa
     dt = {0: torch.float32, 1: torch.bfloat16, 2: torch.float16}[p.in_dtype]
     ho, wo = p.out_hw
     x = torch.empty((p.n, p.h, p.w, p.c), dtype=dt, device=device)
+    x_id = synth.X_ID
     if direction == "fwd":
+        b = torch.empty((p.k, p.r, p.s, p.c // p.groups), dtype=dt, device=device)
+        b_id = synth.W_ID
+    elif direction == "dgrad":  # the first input is dY, the second W
+        x = torch.empty((p.n, ho, wo, p.k), dtype=dt, device=device)
+        x_id = synth.DY_ID
         b = torch.empty((p.k, p.r, p.s, p.c // p.groups), dtype=dt, device=device)
         b_id = synth.W_ID
     else:
@@ -180,12 +194,12 @@ def make_inputs_on_device(p, direction, dist, args, seed, device, pinned_copy=Fa
     hosts = None
     if pinned_copy:
         hosts = (torch.empty(x.shape, dtype=dt, pin_memory=True), torch.empty(b.shape, dtype=dt, pin_memory=True))
-        synth.fill(hosts[0], dist, args[0], args[1], seed, synth.X_ID)
+        synth.fill(hosts[0], dist, args[0], args[1], seed, x_id)
         synth.fill(hosts[1], dist, args[0], args[1], seed, b_id)
         x.copy_(hosts[0])
         b.copy_(hosts[1])
         return x, b, hosts
-    for t, tid in ((x, synth.X_ID), (b, b_id)):
+    for t, tid in ((x, x_id), (b, b_id)):
         flat = t.view(-1)
         chunk = max(1, min(flat.numel(), 64 << 20))
         stage = torch.empty(chunk, dtype=dt, pin_memory=True)
@@ -250,7 +264,12 @@ def oracle_sample(p, direction, dist, args, seed, n_samples: int):
     ho, wo = p.out_hw
     x = np.empty((n_samples, p.h, p.w, p.c), np.float32)
     synth.fill(x, dist, args[0], args[1], seed, synth.X_ID)
-    if direction == "fwd":
+    if direction == "dgrad":  # (dY, W)
+        x = np.empty((n_samples, ho, wo, p.k), np.float32)
+        synth.fill(x, dist, args[0], args[1], seed, synth.DY_ID)
+        b = np.empty((p.k, p.r, p.s, p.c // p.groups), np.float32)
+        synth.fill(b, dist, args[0], args[1], seed, synth.W_ID)
+    elif direction == "fwd":
         b = np.empty((p.k, p.r, p.s, p.c // p.groups), np.float32)
         synth.fill(b, dist, args[0], args[1], seed, synth.W_ID)
     else:
@@ -280,13 +299,16 @@ def time_oracle(p, direction, dist, args, seed, target_s: float):
         t0 = time.perf_counter()
         if direction == "fwd":
             orc.fwd(op, x, b, threads)
+        elif direction == "dgrad":
+            orc.dgrad(op, x, b, threads)
         else:
             orc.wgrad(op, x, b, None, threads)
             orc.bgrad(op, b)
         dt = time.perf_counter() - t0
         flops = 2 * n * p.out_hw[0] * p.out_hw[1] * p.k * (p.c // p.groups) * p.r * p.s
         if dt >= 0.6 * target_s or n >= p.n:
-            used = min(threads, p.k) if direction == "wgrad" else min(threads, n * p.out_hw[0])
+            used = min(threads, p.k) if direction == "wgrad" else \
+                min(threads, n * (p.h if direction == "dgrad" else p.out_hw[0]))
             return flops / dt, dt, n, used
         n = min(p.n, max(n + 1, int(n * target_s / max(dt, 1e-3))))
 
@@ -306,13 +328,16 @@ def run_ours(a, rank, world, local_rank):
         kw = dict(kw, n=a.batch)
         desc = f"{desc} [batch overridden to N={a.batch}]"
     p = cig.Problem(**kw)
-    d = cig.DIR_FWD if direction == "fwd" else cig.DIR_WGRAD
+    d = {"fwd": cig.DIR_FWD, "wgrad": cig.DIR_WGRAD, "dgrad": cig.DIR_DGRAD}[direction]
     bias = direction == "wgrad"
     x, b, _ = make_inputs_on_device(p, direction, dist, args, seed, dev)
     ho, wo = p.out_hw
     odt = {0: torch.float32, 1: torch.bfloat16, 2: torch.float16}[p.out_dtype]
     if direction == "fwd":
         out = torch.empty((p.n, ho, wo, p.k), dtype=odt, device=dev)
+        db = None
+    elif direction == "dgrad":
+        out = torch.empty((p.n, p.h, p.w, p.c), dtype=odt, device=dev)
         db = None
     else:
         out = torch.empty((p.k, p.r, p.s, p.c // p.groups), dtype=odt, device=dev)
@@ -334,6 +359,8 @@ def run_ours(a, rank, world, local_rank):
             ev[0].record(stream)
         if direction == "fwd":
             cig.conv_fwd(p, x, b, out, ws, a.split_k, stream)
+        elif direction == "dgrad":
+            cig.conv_dgrad(p, x, b, out, ws, a.split_k, stream)
         else:
             cig.conv_wgrad_bias(p, x, b, out, db, ws, a.split_k, stream)
         if ev is not None:
@@ -391,7 +418,7 @@ def run_ours(a, rank, world, local_rank):
     kname = plan["kernel_name"]
     if kname in ("wgrad_1x1_tf32x3", "wgrad_1x1_ffma") or direction == "wgrad" and kname == "generic" and p.r == 1:
         bound = "hbm"
-    elif kname in ("fwd_tc", "fwd_tc_cluster"):
+    elif kname in ("fwd_tc", "fwd_tc_cluster", "dgrad_tc"):
         # past the ridge point (flop per byte of the measured peaks) the tensor
         # pipe bounds it, else HBM
         bound = "tensor" if flops / in_bytes > pk["bf16"] * 1e12 / (pk["hbm"] * 1e9) else "hbm"
@@ -435,6 +462,8 @@ def run_ours(a, rank, world, local_rank):
             bh_d.copy_(hosts[1], non_blocking=True)
             if direction == "fwd":
                 cig.conv_fwd(p, xh_d, bh_d, out, ws, a.split_k, stream)
+            elif direction == "dgrad":
+                cig.conv_dgrad(p, xh_d, bh_d, out, ws, a.split_k, stream)
             else:
                 cig.conv_wgrad_bias(p, xh_d, bh_d, out, db, ws, a.split_k, stream)
             out_h.copy_(out, non_blocking=True)
@@ -475,8 +504,8 @@ def run_ours(a, rank, world, local_rank):
                    "algorithmic_bytes": in_bytes, "flops_per_step": flops},
         "roofline": roof, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
         "gpu_launches": a.steps * (1 + (1 if plan["needs_fold"] else 0) +
-                                   (1 if kname == "generic" and bias else 0)),
-        "timing": "value: the timed steps through conv_wgrad_bias / conv_fwd; stage_ms: a second loop of "
+                                   (1 if kname == "generic" and bias else 0) + (1 if kname == "dgrad_tc" else 0)),
+        "timing": "value: the timed steps through conv_wgrad_bias / conv_fwd / conv_dgrad; stage_ms: a second loop of "
                   "conv_stage1 + conv_stage2 with an event between them",
         "stage_ms": {"stage1_mean": round(stage1_ms, 5), "stage1_min": round(min(s1), 5),
                      "fold_mean": round(statistics.mean(s2), 5)},
@@ -507,6 +536,8 @@ def run_reference(a, rank, world):
     def step():
         if direction == "fwd":
             orc.fwd(op, x, b, threads)
+        elif direction == "dgrad":
+            orc.dgrad(op, x, b, threads)
         else:
             orc.wgrad(op, x, b, None, threads)
             orc.bgrad(op, b)

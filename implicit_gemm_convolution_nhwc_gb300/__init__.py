@@ -14,9 +14,9 @@ from dataclasses import dataclass, fields
 from . import _build
 
 F32, BF16, F16 = 0, 1, 2
-DIR_FWD, DIR_WGRAD = 0, 1
+DIR_FWD, DIR_WGRAD, DIR_DGRAD = 0, 1, 2
 KERNELS = {"auto": 0, "generic": 1, "wgrad_1x1_ffma": 2, "wgrad_1x1_tf32x3": 3, "fwd_tc": 4,
-           "wgrad_depthwise": 5, "wgrad_grouped": 6, "fwd_tc_cluster": 7}
+           "wgrad_depthwise": 5, "wgrad_grouped": 6, "fwd_tc_cluster": 7, "dgrad_tc": 8}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 STATUS = ["CONV_OK", "CONV_ERR_INVALID_ARG", "CONV_ERR_UNSUPPORTED", "CONV_ERR_WORKSPACE_TOO_SMALL",
           "CONV_ERR_OVERFLOW", "CONV_ERR_ALIGNMENT", "CONV_ERR_CUDA"]
@@ -24,7 +24,7 @@ STATUS = ["CONV_OK", "CONV_ERR_INVALID_ARG", "CONV_ERR_UNSUPPORTED", "CONV_ERR_W
 # Every symbol include/conv_igemm.h declares.
 EXPORTS = ["conv_status_string", "conv_output_dims", "resolve_split_k_for", "resolve_split_k",
            "conv_workspace_bytes_for", "conv_workspace_bytes", "conv_describe_plan", "conv_fwd",
-           "conv_wgrad", "conv_wgrad_bias", "conv_stage1", "conv_stage2", "conv_batch_split_count",
+           "conv_dgrad", "conv_wgrad", "conv_wgrad_bias", "conv_stage1", "conv_stage2", "conv_batch_split_count",
            "conv_wgrad_bias_static_ws", "conv_device_errors", "conv_set_kernel_override"]
 
 
@@ -111,6 +111,7 @@ def load(build_if_missing: bool = True):
         "conv_workspace_bytes": ([P, ctypes.c_int, I32, I32, ctypes.POINTER(U64)], ctypes.c_int),
         "conv_describe_plan": ([P, ctypes.c_int, I32, I32, I32, ctypes.POINTER(PlanInfo)], ctypes.c_int),
         "conv_fwd": ([P, V, V, V, V, U64, I32, V], ctypes.c_int),
+        "conv_dgrad": ([P, V, V, V, V, U64, I32, V], ctypes.c_int),
         "conv_wgrad": ([P, V, V, V, V, U64, I32, V], ctypes.c_int),
         "conv_wgrad_bias": ([P, V, V, V, V, V, U64, I32, V], ctypes.c_int),
         "conv_stage1": ([P, ctypes.c_int, V, V, V, V, V, U64, I32, V], ctypes.c_int),
@@ -235,6 +236,17 @@ def conv_fwd(p: Problem, x, w, y, ws=None, split_k: int = -1, stream=None):
     return y
 
 
+def conv_dgrad(p: Problem, dy, w, dx, ws=None, split_k: int = -1, stream=None):
+    ho, wo = p.out_hw
+    _need(dy, "dy", p.n * ho * wo * p.k, p.in_dtype)
+    _need(w, "w", p.k * p.r * p.s * (p.c // p.groups), p.in_dtype)
+    _need(dx, "dx", p.n * p.h * p.w * p.c, p.out_dtype)
+    st = load().conv_dgrad(_cp(p), _ptr(dy), _ptr(w), _ptr(dx), _ptr(ws), 0 if ws is None else ws.numel(),
+                           split_k, _stream(stream))
+    _check(st, "conv_dgrad")
+    return dx
+
+
 def conv_wgrad(p: Problem, x, dy, dw, ws=None, split_k: int = -1, stream=None):
     ho, wo = p.out_hw
     _need(x, "x", p.n * p.h * p.w * p.c, p.in_dtype)
@@ -259,7 +271,8 @@ def conv_wgrad_bias(p: Problem, x, dy, dw, db, ws=None, split_k: int = -1, strea
 
 
 def conv_stage1(p: Problem, direction: int, x, b, out, db=None, ws=None, split_k: int = -1, stream=None):
-    """Stage 1 only (slabs, or the outputs at degree 1). b is w (forward) or dy."""
+    """Stage 1 only (slabs, or the outputs at degree 1). x is dy for the data
+    gradient; b is w (forward, data gradient) or dy (weight gradient)."""
     st = load().conv_stage1(_cp(p), direction, _ptr(x), _ptr(b), _ptr(out), _ptr(db), _ptr(ws),
                             0 if ws is None else ws.numel(), split_k, _stream(stream))
     _check(st, "conv_stage1")

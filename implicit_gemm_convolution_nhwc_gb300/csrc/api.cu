@@ -76,6 +76,7 @@ Geometry geometry_of(conv_kernel k, const Shape& s, conv_dir dir) {
     case CONV_KERNEL_WGRAD_1X1_TF32X3: return dir == CONV_DIR_WGRAD ? geometry_wgrad1x1_tf32x3(s) : Geometry{};
     case CONV_KERNEL_FWD_TC: return dir == CONV_DIR_FWD ? geometry_fwd_tc(s) : Geometry{};
     case CONV_KERNEL_FWD_TC_CLUSTER: return dir == CONV_DIR_FWD ? geometry_fwd_tc_cluster(s) : Geometry{};
+    case CONV_KERNEL_DGRAD_TC: return dir == CONV_DIR_DGRAD ? geometry_dgrad_tc(s) : Geometry{};
     case CONV_KERNEL_WGRAD_DEPTHWISE: return dir == CONV_DIR_WGRAD ? geometry_wgrad_depthwise(s) : Geometry{};
     case CONV_KERNEL_WGRAD_GROUPED: return dir == CONV_DIR_WGRAD ? geometry_wgrad_grouped(s) : Geometry{};
     default: return Geometry{};
@@ -98,7 +99,8 @@ conv_status choose_kernel(const Shape& s, conv_dir dir, conv_kernel* kernel, Geo
   // The cluster form of the forward is reached only through the override:
   // on the 3x3 small-M layer it measured slower than the two-stage form.
   static const conv_kernel fwd_order[] = {CONV_KERNEL_FWD_TC, CONV_KERNEL_GENERIC};
-  const conv_kernel* order = dir == CONV_DIR_WGRAD ? wgrad_order : fwd_order;
+  static const conv_kernel dgrad_order[] = {CONV_KERNEL_DGRAD_TC, CONV_KERNEL_GENERIC};
+  const conv_kernel* order = dir == CONV_DIR_WGRAD ? wgrad_order : dir == CONV_DIR_FWD ? fwd_order : dgrad_order;
   const int count = dir == CONV_DIR_WGRAD ? 5 : 2;
   for (int i = 0; i < count; ++i) {
     Geometry g = geometry_of(order[i], s, dir);
@@ -133,10 +135,13 @@ conv_status resolve_degree(const Shape& s, conv_dir dir, const Geometry& g, int3
   if (sm_count < 1) return CONV_ERR_INVALID_ARG;
   const int64_t target = (int64_t)sm_count * g.ctas_per_sm;
   int64_t d = 1;
-  if (dir == CONV_DIR_FWD) {
+  if (dir == CONV_DIR_FWD || dir == CONV_DIR_DGRAD) {
+    // The data gradient takes the forward's policy over its own reduction
+    // depth R*S*Kg (the pages name a dgrad policy but do not describe it).
     const bool pointwise = s.r == 1 && s.s == 1;
+    const int64_t depth = dir == CONV_DIR_DGRAD ? s.r * s.s * s.kg : s.D();
     const int64_t cap = g.max_split > 0 && g.max_split < 32 ? g.max_split : 32;
-    if (!pointwise && 2 * g.tiles < target && s.D() >= 512) {
+    if (!pointwise && 2 * g.tiles < target && depth >= 512) {
       while (2 * d <= cap && g.tiles * (2 * d) <= target) d *= 2;
       while (d > 1 && g.blocks < 2 * d) d /= 2;
     }
@@ -152,7 +157,7 @@ conv_status resolve_degree(const Shape& s, conv_dir dir, const Geometry& g, int3
 
 conv_status make_plan(const conv_problem* prob, conv_dir dir, int32_t request, bool with_bias,
                       int32_t sm_count, Plan* plan) {
-  if (dir != CONV_DIR_FWD && dir != CONV_DIR_WGRAD) return CONV_ERR_INVALID_ARG;
+  if (dir != CONV_DIR_FWD && dir != CONV_DIR_WGRAD && dir != CONV_DIR_DGRAD) return CONV_ERR_INVALID_ARG;
   Plan p;
   conv_status st = validate(prob, &p.sh);
   if (st != CONV_OK) return st;
@@ -167,8 +172,11 @@ conv_status make_plan(const conv_problem* prob, conv_dir dir, int32_t request, b
   st = resolve_degree(p.sh, dir, p.geo, request, sm_count, &p.split);
   if (st != CONV_OK) return st;
   p.fold = p.split > 1 && p.kernel != CONV_KERNEL_FWD_TC_CLUSTER;
-  p.out_elems = dir == CONV_DIR_FWD ? p.sh.y_elems() : p.sh.w_elems();
+  p.out_elems = dir == CONV_DIR_FWD ? p.sh.y_elems() : dir == CONV_DIR_WGRAD ? p.sh.w_elems() : p.sh.x_elems();
   p.slab_bytes = p.bias_slab_bytes = 0;
+  // The data gradient's tensor-core path writes the transformed filter (as
+  // many in_dtype elements as W) at the start of the workspace.
+  p.aux_bytes = p.kernel == CONV_KERNEL_DGRAD_TC ? round256((uint64_t)p.sh.w_elems() * (uint64_t)esize(p.sh.in_dt)) : 0;
   if (p.fold) {
     int64_t b;
     if (!mul_ok(p.out_elems, 4, &b) || !mul_ok(b, p.split, &b)) return CONV_ERR_OVERFLOW;
@@ -190,13 +198,16 @@ conv_status run(const conv_problem* prob, conv_dir dir, const void* x, const voi
   Shape sh;
   conv_status st = validate(prob, &sh);
   if (st != CONV_OK) return st;
-  if (dir != CONV_DIR_FWD && dir != CONV_DIR_WGRAD) return CONV_ERR_INVALID_ARG;
+  if (dir != CONV_DIR_FWD && dir != CONV_DIR_WGRAD && dir != CONV_DIR_DGRAD) return CONV_ERR_INVALID_ARG;
   if (split_k < -1) return CONV_ERR_INVALID_ARG;
   if (with_bias && dir != CONV_DIR_WGRAD) return CONV_ERR_INVALID_ARG;
-  const int64_t b_elems = dir == CONV_DIR_FWD ? sh.w_elems() : sh.y_elems();
-  const int64_t out_elems = dir == CONV_DIR_FWD ? sh.y_elems() : sh.w_elems();
+  // Elements of the two inputs and the output, per direction.
+  const int64_t x_elems = dir == CONV_DIR_DGRAD ? sh.y_elems() : sh.x_elems();
+  const int64_t b_elems = dir == CONV_DIR_WGRAD ? sh.y_elems() : sh.w_elems();
+  const int64_t out_elems =
+      dir == CONV_DIR_FWD ? sh.y_elems() : dir == CONV_DIR_WGRAD ? sh.w_elems() : sh.x_elems();
   const bool needs_inputs = (stages & kStage1) != 0;
-  if ((needs_inputs && sh.x_elems() > 0 && !x) || (needs_inputs && b_elems > 0 && !b) ||
+  if ((needs_inputs && x_elems > 0 && !x) || (needs_inputs && b_elems > 0 && !b) ||
       (out_elems > 0 && !out) || (with_bias && !db))
     return CONV_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(b) || !aligned16(out) || !aligned16(db) || !aligned16(ws))
@@ -213,9 +224,10 @@ conv_status run(const conv_problem* prob, conv_dir dir, const void* x, const voi
   a.b = b;
   a.out = out;
   a.db = plan.with_bias ? db : nullptr;
-  a.ws = plan.fold ? static_cast<float*>(ws) : nullptr;
+  a.aux = plan.aux_bytes > 0 ? ws : nullptr;
+  a.ws = plan.fold ? reinterpret_cast<float*>(static_cast<char*>(ws) + plan.aux_bytes) : nullptr;
   a.ws_bias = plan.fold && plan.with_bias
-                  ? reinterpret_cast<float*>(static_cast<char*>(ws) + plan.slab_bytes)
+                  ? reinterpret_cast<float*>(static_cast<char*>(ws) + plan.aux_bytes + plan.slab_bytes)
                   : nullptr;
   a.stream = static_cast<cudaStream_t>(stream);
   cudaError_t err = cudaSuccess;
@@ -226,6 +238,7 @@ conv_status run(const conv_problem* prob, conv_dir dir, const void* x, const voi
       case CONV_KERNEL_WGRAD_1X1_TF32X3: err = launch_wgrad1x1_tf32x3(plan, a); break;
       case CONV_KERNEL_FWD_TC: err = launch_fwd_tc(plan, a); break;
       case CONV_KERNEL_FWD_TC_CLUSTER: err = launch_fwd_tc_cluster(plan, a); break;
+      case CONV_KERNEL_DGRAD_TC: err = launch_dgrad_tc(plan, a); break;
       case CONV_KERNEL_WGRAD_DEPTHWISE: err = launch_wgrad_depthwise(plan, a); break;
       case CONV_KERNEL_WGRAD_GROUPED: err = launch_wgrad_grouped(plan, a); break;
       default: return CONV_ERR_UNSUPPORTED;
@@ -343,6 +356,11 @@ conv_status conv_fwd(const conv_problem* p, const void* x, const void* w, void* 
   return run(p, CONV_DIR_FWD, x, w, y, nullptr, ws, ws_bytes, split_k, stream, false, kBoth);
 }
 
+conv_status conv_dgrad(const conv_problem* p, const void* dy, const void* w, void* dx, void* ws,
+                       uint64_t ws_bytes, int32_t split_k, void* stream) {
+  return run(p, CONV_DIR_DGRAD, dy, w, dx, nullptr, ws, ws_bytes, split_k, stream, false, kBoth);
+}
+
 conv_status conv_wgrad(const conv_problem* p, const void* x, const void* dy, void* dw, void* ws,
                        uint64_t ws_bytes, int32_t split_k, void* stream) {
   return run(p, CONV_DIR_WGRAD, x, dy, dw, nullptr, ws, ws_bytes, split_k, stream, false, kBoth);
@@ -424,7 +442,7 @@ conv_status conv_wgrad_bias_static_ws(const conv_problem* p, const void* x, cons
 
 
 conv_status conv_set_kernel_override(int32_t kernel) {
-  if (kernel < CONV_KERNEL_AUTO || kernel > CONV_KERNEL_FWD_TC_CLUSTER) return CONV_ERR_INVALID_ARG;
+  if (kernel < CONV_KERNEL_AUTO || kernel > CONV_KERNEL_DGRAD_TC) return CONV_ERR_INVALID_ARG;
   g_kernel_override = kernel;
   return CONV_OK;
 }

@@ -46,13 +46,15 @@ struct Plan {
   uint64_t slab_bytes;       // S*E*4 rounded to 256 (0 when S == 1)
   uint64_t bias_slab_bytes;  // S*K*4 rounded to 256 (0 when S == 1 or no bias)
   bool fold;                 // stage 2 runs (S > 1 and the slices do not fold in-launch)
-  uint64_t ws_bytes() const { return slab_bytes + bias_slab_bytes; }
+  uint64_t aux_bytes;        // kernel-private bytes at the start of ws (the data gradient's filter)
+  uint64_t ws_bytes() const { return aux_bytes + slab_bytes + bias_slab_bytes; }
 };
 
 struct Args {
-  const void* x;
-  const void* b;   // W (forward) or dY (weight gradient)
-  void* out;       // Y or dW
+  const void* x;   // X, or dY (data gradient)
+  const void* b;   // W (forward, data gradient) or dY (weight gradient)
+  void* out;       // Y, dW or dX
+  void* aux;       // the first aux_bytes of ws (nullptr when none)
   void* db;        // bias gradient or nullptr
   float* ws;       // slabs [S][E] (nullptr when S == 1)
   float* ws_bias;  // bias slabs [S][K] (nullptr when S == 1 or no bias)
@@ -71,6 +73,10 @@ Geometry geometry_wgrad1x1_ffma(const Shape& s);
 Geometry geometry_wgrad1x1_tf32x3(const Shape& s);
 Geometry geometry_fwd_tc(const Shape& s);
 Geometry geometry_fwd_tc_cluster(const Shape& s);
+Geometry geometry_dgrad_tc(const Shape& s);
+// The forward problem a stride-1, ungrouped data gradient equals (dY as the
+// input, the transformed filter, padding dil * (f - 1) - pad).
+Shape dgrad_as_forward(const Shape& s);
 Geometry geometry_wgrad_depthwise(const Shape& s);
 Geometry geometry_wgrad_grouped(const Shape& s);
 
@@ -80,6 +86,7 @@ cudaError_t launch_wgrad1x1_ffma(const Plan& p, const Args& a);
 cudaError_t launch_wgrad1x1_tf32x3(const Plan& p, const Args& a);
 cudaError_t launch_fwd_tc(const Plan& p, const Args& a);
 cudaError_t launch_fwd_tc_cluster(const Plan& p, const Args& a);
+cudaError_t launch_dgrad_tc(const Plan& p, const Args& a);
 cudaError_t launch_wgrad_depthwise(const Plan& p, const Args& a);
 cudaError_t launch_wgrad_grouped(const Plan& p, const Args& a);
 // Stage 2: out = cast(sum of slabs) (and the bias slabs into db).

@@ -112,10 +112,13 @@ __device__ __forceinline__ void store_tile_tma(uint32_t trow, uint8_t* stage, co
                                                bool leader, bool do_store) {
   constexpr int CW = 128 / (int)sizeof(TE);  // channels per 128-byte chunk
   constexpr int VPU = 16 / (int)sizeof(TE);  // values per 16-byte unit
+  // Only chunks that start below K: each one then commits exactly one bulk
+  // group, which the buffer-reuse wait below counts on.
+  const int nch = min(BN / CW, (kx_end - kx0 + CW - 1) / CW);
 #pragma unroll 1
-  for (int c = 0; c < BN / CW; ++c) {
+  for (int c = 0; c < nch; ++c) {
     uint8_t* buf = stage + (c & 1) * (kBM * 128);
-    if (c >= 2) {  // the store that last read this buffer must be done reading
+    if (c >= 2) {  // the store that last read this buffer (chunk c - 2) must be done reading
       if (leader) bulk_wait_read<1>();
       named_bar_sync(1, 128);
     }
@@ -137,7 +140,7 @@ __device__ __forceinline__ void store_tile_tma(uint32_t trow, uint8_t* stage, co
     }
     fence_proxy_async_smem();
     named_bar_sync(1, 128);
-    if (leader && do_store && kx0 + c * CW < kx_end) {  // no box starting past K
+    if (leader && do_store) {
       tma_store_3d(tm, buf, kx0 + c * CW, py, pz);
       bulk_commit();
     }

@@ -1,4 +1,5 @@
-// Generic direct kernels (CUDA cores): every shape, stride, dilation, padding,
+// Generic direct kernels (CUDA cores) for the forward, weight gradient and
+// data gradient: every shape, stride, dilation, padding,
 // group count and storage type the ABI accepts. One thread owns one output
 // element of one reduction slice and walks the slice in order, so the result
 // of a slice is deterministic. These are the correctness floor under the fast
@@ -10,7 +11,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int64_t kRowsPerBlock = 64;   // weight-gradient reduction block (rows of N*Ho*Wo)
-constexpr int64_t kDepthPerBlock = 32;  // forward reduction block (of R*S*Cg)
+constexpr int64_t kDepthPerBlock = 32;  // forward / data-gradient reduction block (of R*S*Cg / R*S*Kg)
 
 // dW[k,r,s,c] over the rows of slice sigma:
 //   sum dY[n,ho,wo,k] * X[n, ho*sh + r*dh - ph, wo*sw + s*dw - pw, g*Cg + c].
@@ -117,6 +118,47 @@ __global__ void __launch_bounds__(kThreads) generic_fwd_kernel(Shape sh, const T
   store_result(out, ws, E, sigma, e, acc);
 }
 
+// dX[n,h,w,g*Cg + c] over the reduction (r, s, k in group g) of slice sigma:
+//   sum dY[n,ho,wo,k] * W[k,r,s,c] for ho*sh + r*dh - ph = h, wo*sw + s*dw - pw = w.
+template <typename TI, typename TO>
+__global__ void __launch_bounds__(kThreads) generic_dgrad_kernel(Shape sh, const TI* __restrict__ dy,
+                                                                 const TI* __restrict__ wt, TO* out, float* ws,
+                                                                 int32_t S, int64_t tiles, int64_t blocks) {
+  const int64_t tile = blockIdx.x % tiles;
+  const int32_t sigma = (int32_t)(blockIdx.x / tiles);
+  const int64_t E = sh.x_elems();
+  const int64_t e = tile * kThreads + threadIdx.x;
+  if (e >= E) return;
+  const int64_t ci = e % sh.c;
+  int64_t t = e / sh.c;
+  const int64_t w = t % sh.w;
+  t /= sh.w;
+  const int64_t h = t % sh.h;
+  const int64_t n = t / sh.h;
+  const int64_t g = ci / sh.cg, c = ci % sh.cg;
+  const int64_t D = sh.r * sh.s * sh.kg;
+  int64_t d = slice_begin(blocks, S, sigma) * kDepthPerBlock;
+  int64_t d_end = slice_begin(blocks, S, sigma + 1) * kDepthPerBlock;
+  if (d_end > D) d_end = D;
+  float acc = 0.f;
+  while (d < d_end) {
+    // one (r, s) tap: its k range within the slice
+    const int64_t rs = d / sh.kg, k_lo = d % sh.kg;
+    const int64_t r = rs / sh.s, s = rs % sh.s;
+    const int64_t k_hi = (rs + 1) * sh.kg <= d_end ? sh.kg : d_end - rs * sh.kg;
+    d += k_hi - k_lo;
+    const int64_t hn = h + sh.ph - r * sh.dh, wn = w + sh.pw - s * sh.dw;
+    if (hn < 0 || wn < 0 || hn % sh.sh != 0 || wn % sh.sw != 0) continue;
+    const int64_t ho = hn / sh.sh, wo = wn / sh.sw;
+    if (ho >= sh.ho || wo >= sh.wo) continue;
+    const TI* dyp = dy + ((n * sh.ho + ho) * sh.wo + wo) * sh.k + g * sh.kg;
+    const TI* wp = wt + ((g * sh.kg * sh.r + r) * sh.s + s) * sh.cg + c;
+    const int64_t wstride = sh.r * sh.s * sh.cg;
+    for (int64_t kk = k_lo; kk < k_hi; ++kk) acc = fmaf(to_f32(dyp[kk]), to_f32(wp[kk * wstride]), acc);
+  }
+  store_result(out, ws, E, sigma, e, acc);
+}
+
 template <typename TI, typename TO>
 cudaError_t launch_typed(const Plan& p, const Args& a) {
   const int64_t ctas = p.geo.tiles * p.split;
@@ -134,6 +176,11 @@ cudaError_t launch_typed(const Plan& p, const Args& a) {
         p.sh, b, static_cast<TO*>(a.db), a.ws_bias, p.split, ktiles, p.geo.blocks);
     return cudaGetLastError();
   }
+  if (p.dir == CONV_DIR_DGRAD) {
+    generic_dgrad_kernel<TI, TO><<<(unsigned)ctas, kThreads, 0, a.stream>>>(p.sh, x, b, out, a.ws, p.split,
+                                                                             p.geo.tiles, p.geo.blocks);
+    return cudaGetLastError();
+  }
   generic_fwd_kernel<TI, TO><<<(unsigned)ctas, kThreads, 0, a.stream>>>(p.sh, x, b, out, a.ws, p.split,
                                                                          p.geo.tiles, p.geo.blocks);
   return cudaGetLastError();
@@ -145,11 +192,12 @@ Geometry geometry_generic(const Shape& s, conv_dir dir) {
   Geometry g;
   g.ok = true;
   g.ctas_per_sm = 8;
-  const int64_t E = dir == CONV_DIR_FWD ? s.y_elems() : s.w_elems();
+  const int64_t E = dir == CONV_DIR_FWD ? s.y_elems() : dir == CONV_DIR_WGRAD ? s.w_elems() : s.x_elems();
   g.tiles = (E + kThreads - 1) / kThreads;
   if (g.tiles < 1) g.tiles = 1;
-  g.blocks = dir == CONV_DIR_FWD ? (s.D() + kDepthPerBlock - 1) / kDepthPerBlock
-                                 : (s.P() + kRowsPerBlock - 1) / kRowsPerBlock;
+  if (dir == CONV_DIR_FWD) g.blocks = (s.D() + kDepthPerBlock - 1) / kDepthPerBlock;
+  else if (dir == CONV_DIR_WGRAD) g.blocks = (s.P() + kRowsPerBlock - 1) / kRowsPerBlock;
+  else g.blocks = (s.r * s.s * s.kg + kDepthPerBlock - 1) / kDepthPerBlock;
   return g;
 }
 

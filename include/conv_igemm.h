@@ -69,10 +69,15 @@ typedef enum conv_status {
 
 typedef enum conv_dtype { CONV_F32 = 0, CONV_BF16 = 1, CONV_F16 = 2 } conv_dtype;
 
-typedef enum conv_dir { CONV_DIR_FWD = 0, CONV_DIR_WGRAD = 1 } conv_dir;
+/* Direction: forward (Y from X, W), weight gradient (dW, db from X, dY) or
+ * data gradient (dX from dY, W: the gradient of the forward with respect to
+ * X, the "dgrad" the split-K resolver of [P2 "Auto-deduced degree"] also
+ * covers). */
+typedef enum conv_dir { CONV_DIR_FWD = 0, CONV_DIR_WGRAD = 1, CONV_DIR_DGRAD = 2 } conv_dir;
 
-/* One convolution. in_dtype is the type of X and W (forward) or X and dY
- * (weight gradient). out_dtype is the type of Y, or of dW and db; it must be
+/* One convolution. in_dtype is the type of X and W (forward), X and dY
+ * (weight gradient) or dY and W (data gradient). out_dtype is the type of Y,
+ * of dW and db, or of dX; it must be
  * CONV_F32 or in_dtype (the pages require a non-NULL output type [P2 "Review
  * follow-ups"]). Sizes: n >= 0 (n = 0 gives dW = db = 0); h, w, c, k, r, s,
  * strides, dilations, groups >= 1; pads >= 0; groups divides c and k; the
@@ -96,10 +101,14 @@ typedef enum conv_kernel {
   CONV_KERNEL_FWD_TC = 4,            /* 16-bit forward, tcgen05 + TMA im2col */
   CONV_KERNEL_WGRAD_DEPTHWISE = 5,   /* depthwise weight gradient, CUDA cores */
   CONV_KERNEL_WGRAD_GROUPED = 6,     /* 4/8 channels per group, CUDA cores */
-  CONV_KERNEL_FWD_TC_CLUSTER = 7     /* 16-bit forward, the S <= 16 slices of a tile as one
+  CONV_KERNEL_FWD_TC_CLUSTER = 7,    /* 16-bit forward, the S <= 16 slices of a tile as one
                                         thread-block cluster folding through distributed
                                         shared memory [P2 "Changes": single-launch split-K]:
                                         no workspace, no stage 2 */
+  CONV_KERNEL_DGRAD_TC = 8           /* 16-bit, stride-1, ungrouped data gradient: the filter
+                                        rotated 180 degrees with k and c swapped (written into
+                                        the workspace), then the forward tensor-core kernel
+                                        over dY */
 } conv_kernel;
 
 /* What a call with these arguments would run. */
@@ -111,7 +120,8 @@ typedef struct conv_plan_info {
   int64_t tiles;             /* output tiles of stage 1 */
   int64_t reduction_blocks;  /* reduction blocks; a pinned degree may not exceed it */
   int64_t ctas;              /* stage-1 CTAs = tiles * S */
-  uint64_t workspace_bytes;  /* bytes the call needs (0 without stage 2) */
+  uint64_t workspace_bytes;  /* bytes the call needs (0 without stage 2, except the data
+                                gradient's transformed filter) */
   int32_t max_split;         /* largest degree a pinned request may ask of this kernel */
 } conv_plan_info;
 
@@ -144,7 +154,9 @@ conv_status resolve_split_k(const conv_problem* p, conv_dir dir, int32_t request
 /* Workspace bytes a call with this degree request needs: 0 when the degree
  * resolves to 1, else S x E x 4 rounded up to 256 bytes (E = output elements),
  * plus S x k x 4 (rounded up to 256) when with_bias and dir is the weight
- * gradient. */
+ * gradient; the data gradient's tensor-core path adds the transformed filter
+ * (k x r x s x c elements of in_dtype, rounded up to 256) in front, at every
+ * degree. */
 conv_status conv_workspace_bytes_for(const conv_problem* p, conv_dir dir, int32_t split_k,
                                      int32_t with_bias, int32_t sm_count, uint64_t* bytes);
 conv_status conv_workspace_bytes(const conv_problem* p, conv_dir dir, int32_t split_k,
@@ -164,6 +176,15 @@ conv_status conv_fwd(const conv_problem* p, const void* x, const void* w, void* 
 conv_status conv_wgrad(const conv_problem* p, const void* x, const void* dy, void* dw, void* ws,
                        uint64_t ws_bytes, int32_t split_k, void* stream);
 
+/* Data gradient: dx[n,h,w,c] = sum over k, r, s of dy[n,ho,wo,k] * w[k,r,s,c]
+ * for the (ho, wo) with ho*sh + r*dh - ph = h and wo*sw + s*dw - pw = w (the
+ * forward's taps read backwards). dy and w in in_dtype, dx [n,h,w,c] in
+ * out_dtype. The reduction (r, s, k) splits like the forward's. The
+ * tensor-core path keeps the transformed filter at the start of ws, so it
+ * needs a workspace even at degree 1 (conv_workspace_bytes says how much). */
+conv_status conv_dgrad(const conv_problem* p, const void* dy, const void* w, void* dx, void* ws,
+                       uint64_t ws_bytes, int32_t split_k, void* stream);
+
 /* Weight and bias gradient together [P1 "Motivation": weight.grad and
  * bias.grad]: dw as conv_wgrad, db[k] = sum of dy over n, ho, wo, both in
  * out_dtype, from one pass over dy. */
@@ -174,7 +195,8 @@ conv_status conv_wgrad_bias(const conv_problem* p, const void* x, const void* dy
  * "Benchmark": both stages are bound and launched one after the other].
  * conv_stage1 followed by conv_stage2 on the same stream, with the same
  * arguments, is exactly conv_fwd (dir = FWD, b = w, db = NULL), conv_wgrad
- * (dir = WGRAD, b = dy, db = NULL) or conv_wgrad_bias (db != NULL).
+ * (dir = WGRAD, b = dy, db = NULL), conv_wgrad_bias (db != NULL) or
+ * conv_dgrad (dir = DGRAD, x = dy, b = w, out = dx, db = NULL).
  * conv_stage1 writes the slabs (or, at degree 1, the outputs);
  * conv_stage2 folds the slabs into out (and db) and enqueues nothing when the
  * degree resolves to 1. Each validates all of its arguments. */

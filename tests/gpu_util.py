@@ -29,12 +29,15 @@ def oproblem(p: cig.Problem) -> oracle.Problem:
 
 
 def inputs(p: cig.Problem, seed: int, dist: str = "normal", a: float = 0.0, b: float = 1.0, direction=cig.DIR_WGRAD):
-    """Seeded CPU tensors: x, and w (forward) or dy (weight gradient)."""
+    """Seeded CPU tensors: (x, w) forward, (x, dy) weight gradient, (dy, w) data gradient."""
     dt = TORCH_DT[p.in_dtype]
     ho, wo = p.out_hw
     x = synth.tensor((p.n, p.h, p.w, p.c), dt, dist, a, b, seed, synth.X_ID)
     if direction == cig.DIR_FWD:
         other = synth.tensor((p.k, p.r, p.s, p.c // p.groups), dt, dist, a, b, seed, synth.W_ID)
+    elif direction == cig.DIR_DGRAD:  # (dy, w)
+        dy = synth.tensor((p.n, ho, wo, p.k), dt, dist, a, b, seed, synth.DY_ID)
+        return dy, synth.tensor((p.k, p.r, p.s, p.c // p.groups), dt, dist, a, b, seed, synth.W_ID)
     else:
         other = synth.tensor((p.n, ho, wo, p.k), dt, dist, a, b, seed, synth.DY_ID)
     return x, other
@@ -99,6 +102,18 @@ def run_fwd(p: cig.Problem, x, w, split_k=-1, check_guards=True):
     if check_guards:
         assert y.intact() and ws.intact(), "a write left its buffer"
     return y.view.cpu().reshape(p.n, ho, wo, p.k)
+
+
+def run_dgrad(p: cig.Problem, dy, w, split_k=-1, check_guards=True):
+    """dX from the GPU as a CPU tensor [n, h, w, c], with guard and workspace checks."""
+    dev = torch.device("cuda")
+    dx = Guarded(p.n * p.h * p.w * p.c, TORCH_DT[p.out_dtype])
+    ws = GuardedWs(cig.workspace_bytes(p, cig.DIR_DGRAD, split_k, False))
+    cig.conv_dgrad(p, dy.to(dev), w.to(dev), dx.view, ws.view, split_k)
+    torch.cuda.synchronize()
+    if check_guards:
+        assert dx.intact() and ws.intact(), "a write left its buffer"
+    return dx.view.cpu().reshape(p.n, p.h, p.w, p.c)
 
 
 def relerr(gpu, ref) -> float:

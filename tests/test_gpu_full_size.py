@@ -120,3 +120,25 @@ def test_fwd3x3_compute_bound_supplement_sampled_images():
         e = relerr(yc[i:i + 1], ref)
         assert e <= 1e-2, f"image {i}: err {e:.3e}"
     assert cig.device_errors() == 0
+
+
+def test_dgrad3x3_compute_bound_supplement_sampled_images():
+    """The supplement backwards (dX of the 3x3 bf16 N=64, 56x56, C=K=256
+    layer, auto): images 0 and 63 against the oracle as N=1 problems."""
+    n, hw, c, k = 64, 56, 256, 256
+    p = cig.Problem(n=n, h=hw, w=hw, c=c, k=k, r=3, s=3, pad_h=1, pad_w=1, in_dtype=cig.BF16, out_dtype=cig.BF16)
+    dy = synth.tensor((n, hw, hw, k), torch.bfloat16, "normal", 0.0, 0.02, 5, synth.DY_ID)
+    w = synth.tensor((k, 3, 3, c), torch.bfloat16, "normal", 0.0, 0.02, 5, synth.W_ID)
+    dx = torch.empty((n, hw, hw, c), dtype=torch.bfloat16, device="cuda")
+    assert cig.describe_plan(p, cig.DIR_DGRAD, -1)["kernel_name"] == "dgrad_tc"
+    ws = cig.workspace(p, cig.DIR_DGRAD, -1, False)
+    cig.conv_dgrad(p, dy.cuda(), w.cuda(), dx, ws, -1)
+    torch.cuda.synchronize()
+    dxc = dx.cpu()
+    orc = oracle.get()
+    p1 = cig.Problem(n=1, h=hw, w=hw, c=c, k=k, r=3, s=3, pad_h=1, pad_w=1, in_dtype=cig.BF16, out_dtype=cig.BF16)
+    for i in (0, 63):
+        ref = orc.dgrad(oproblem(p1), dy[i:i + 1], w)
+        e = relerr(dxc[i:i + 1], ref)
+        assert e <= 1e-2, f"image {i}: err {e:.3e}"
+    assert cig.device_errors() == 0

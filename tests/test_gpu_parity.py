@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import implicit_gemm_convolution_nhwc_gb300 as cig
-from gpu_util import inputs, oproblem, relerr, run_fwd, run_wgrad, tol
+from gpu_util import inputs, oproblem, relerr, run_dgrad, run_fwd, run_wgrad, tol
 
 pytestmark = pytest.mark.gpu
 
@@ -191,6 +191,7 @@ def test_config3_forward_split_sweep():
     dict(n=1, h=14, w=14, c=2048, k=512, r=3, s=3, pad_h=1, pad_w=1),          # the 3x3 small-M layer
     dict(n=2, h=10, w=12, c=128, k=136, r=3, s=3, pad_h=1, pad_w=1),           # K tail, 2 M tiles per image
     dict(n=1, h=9, w=11, c=64, k=128, r=5, s=5, pad_h=4, pad_w=4, dil_h=2, dil_w=2),
+    dict(n=1, h=20, w=40, c=256, k=192, r=3, s=1, pad_h=1, pad_w=0),           # last N tile half empty
 ])
 def test_forward_cluster_equals_two_stage(shape):
     """The single-launch form folds the same per-slice partial tiles in the
@@ -220,12 +221,75 @@ def test_forward_cluster_equals_two_stage(shape):
     dict(n=1, h=9, w=11, c=64, k=128, r=5, s=5, pad_h=4, pad_w=4, dil_h=2, dil_w=2),  # dilation, wide pad
     dict(n=3, h=9, w=9, c=64, k=128),                                           # pointwise
     dict(n=1, h=20, w=40, c=192, k=256, r=3, s=1, pad_h=1, pad_w=0),           # non-square filter
+    dict(n=1, h=20, w=40, c=256, k=192, r=3, s=1, pad_h=1, pad_w=0),           # last N tile half empty
 ])
 @pytest.mark.parametrize("dt", [(BF16, BF16), (F16, F32), (F16, F16)], ids=lambda d: f"{d[0]}{d[1]}")
 def test_forward_tc_ragged(shape, dt):
     p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
     check_fwd(p, 6, ["fwd_tc", "fwd_tc_cluster", "generic"], [-1, 1, 3])
     check_fwd(p, 6, ["fwd_tc", "fwd_tc_cluster"], ["max"])
+    assert cig.device_errors() == 0
+
+
+# ------------------------------------------------------------- data gradient
+
+
+def check_dgrad(p, seed, kernels, splits, dist="normal", a=0.0, b=1.0):
+    orc = oracle.get()
+    dy, w = inputs(p, seed, dist, a, b, cig.DIR_DGRAD)
+    ref = orc.dgrad(oproblem(p), dy, w)
+    for kern in kernels:
+        cig.set_kernel_override(kern)
+        top = _max_degree(p, cig.DIR_DGRAD)
+        for sk in splits:
+            sk = top if sk == "max" else sk
+            if sk > top:
+                continue
+            dx = run_dgrad(p, dy, w, sk)
+            e = relerr(dx, ref)
+            assert e <= tol(p), f"{kern} split {sk}: dX err {e:.3e}"
+    cig.set_kernel_override("auto")
+
+
+@pytest.mark.parametrize("shape", [
+    dict(n=2, h=9, w=11, c=12, k=8, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1),   # stride 2
+    dict(n=1, h=13, w=10, c=6, k=9, r=3, s=2, stride_h=3, stride_w=1, pad_h=2, pad_w=0, dil_h=2, dil_w=1),
+    dict(n=2, h=8, w=8, c=16, k=24, r=3, s=3, pad_h=1, pad_w=1, groups=4),                # groups
+    dict(n=3, h=7, w=9, c=32, k=32, r=5, s=5, pad_h=2, pad_w=2, groups=32),               # depthwise
+    dict(n=2, h=6, w=5, c=40, k=20, r=1, s=1),                                              # pointwise
+])
+@pytest.mark.parametrize("dt", [(F32, F32), (BF16, BF16), (F16, F32)], ids=lambda d: f"{d[0]}{d[1]}")
+def test_dgrad_generic(shape, dt):
+    p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
+    check_dgrad(p, 11, ["auto", "generic"], [-1, 1, 3, "max"])
+    assert cig.device_errors() == 0
+
+
+@pytest.mark.parametrize("shape", [
+    dict(n=2, h=10, w=12, c=136, k=128, r=3, s=3, pad_h=1, pad_w=1),          # C tail (the output channels)
+    dict(n=1, h=9, w=11, c=128, k=192, r=5, s=5, pad_h=4, pad_w=4, dil_h=2, dil_w=2),
+    dict(n=3, h=9, w=9, c=256, k=64),                                          # pointwise
+    dict(n=1, h=20, w=40, c=192, k=256, r=3, s=1, pad_h=1, pad_w=0),          # non-square filter
+])
+@pytest.mark.parametrize("dt", [(BF16, BF16), (F16, F32), (F16, F16)], ids=lambda d: f"{d[0]}{d[1]}")
+def test_dgrad_tc_ragged(shape, dt):
+    p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
+    assert cig.describe_plan(p, cig.DIR_DGRAD, -1)["kernel_name"] == "dgrad_tc"
+    check_dgrad(p, 12, ["dgrad_tc", "generic"], [-1, 1, 3])
+    check_dgrad(p, 12, ["dgrad_tc"], ["max"])
+    assert cig.device_errors() == 0
+
+
+def test_dgrad_config3_layer():
+    """The 3x3 small-M layer (N=1, 14x14, C=2048, K=512, pad 1, bf16) run
+    backwards: dX [1,14,14,2048] from dY [1,14,14,512]; auto and pinned
+    degrees; reruns bit-identical."""
+    p = cig.Problem(n=1, h=14, w=14, c=2048, k=512, r=3, s=3, pad_h=1, pad_w=1, in_dtype=BF16, out_dtype=BF16)
+    assert cig.describe_plan(p, cig.DIR_DGRAD, -1)["kernel_name"] == "dgrad_tc"
+    check_dgrad(p, 2, ["auto"], [-1, 1, 8, 32], "normal", 0.0, 0.02)
+    dy, w = inputs(p, 2, "normal", 0.0, 0.02, cig.DIR_DGRAD)
+    a, b = run_dgrad(p, dy, w, -1), run_dgrad(p, dy, w, -1)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     assert cig.device_errors() == 0
 
 

@@ -173,6 +173,34 @@ def test_forward_cluster_form_selection():
     assert e.value.status == 2
 
 
+def test_dgrad_plans():
+    """Data gradient: the tensor-core path (16-bit, stride 1, one group) keeps
+    the transformed filter at the start of the workspace at every degree;
+    strided or grouped problems take the generic kernel."""
+    r256 = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    p = CONFIG3
+    wbytes = r256(p.k * p.r * p.s * p.c * 2)
+    E = p.n * p.h * p.w * p.c
+    for req in (-1, 1, 2, 8):
+        info = cig.describe_plan(p, cig.DIR_DGRAD, req, sm_count=SMS)
+        S = info["split_k"]
+        assert info["kernel_name"] == "dgrad_tc" and info["needs_fold"] == (S > 1)
+        assert info["workspace_bytes"] == wbytes + (r256(S * E * 4) if S > 1 else 0)
+        assert cig.workspace_bytes(p, cig.DIR_DGRAD, req, sm_count=SMS) == info["workspace_bytes"]
+    auto = cig.describe_plan(p, cig.DIR_DGRAD, -1, sm_count=SMS)
+    assert auto["split_k"] & (auto["split_k"] - 1) == 0 and auto["ctas"] <= SMS * auto["ctas_per_sm"]
+    strided = Problem(n=2, h=9, w=11, c=128, k=128, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1,
+                      in_dtype=BF16, out_dtype=BF16)
+    info = cig.describe_plan(strided, cig.DIR_DGRAD, 1, sm_count=SMS)
+    assert info["kernel_name"] == "generic" and info["workspace_bytes"] == 0
+    assert cig.describe_plan(CONFIG5A, cig.DIR_DGRAD, -1, sm_count=SMS)["kernel_name"] == "generic"
+    # the planner ignores with_bias outside the weight gradient
+    assert cig.describe_plan(p, cig.DIR_DGRAD, -1, with_bias=True, sm_count=SMS) == auto
+    with pytest.raises(cig.ConvError) as e:
+        cig.describe_plan(p, 3, -1, sm_count=SMS)
+    assert e.value.status == 1
+
+
 def test_empty_batch_plans_one_slice():
     p = Problem(n=0, h=8, w=8, c=8, k=8)
     assert cig.resolve_split_k(p, DIR_WGRAD, -1, sm_count=SMS) == 1
