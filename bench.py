@@ -343,8 +343,17 @@ def run_ours(a, rank, world, local_rank):
         out = torch.empty((p.k, p.r, p.s, p.c // p.groups), dtype=odt, device=dev)
         db = torch.empty(p.k, dtype=odt, device=dev)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    plan = cig.describe_plan(p, d, a.split_k, bias, sm_count=sms)
-    ws = cig.workspace(p, d, a.split_k, bias, dev)
+    fused = bool(a.bias_relu)
+    if fused and direction != "fwd":
+        raise SystemExit("--bias-relu applies to forward workloads only")
+    ep_bias = None
+    if fused:  # the fused bias + ReLU epilogue runs unsplit
+        import synth
+        ep_bias = synth.tensor((p.k,), odt, "normal", 0.0, 0.1, seed, synth.BIAS_ID).to(dev)
+        if a.split_k > 1:
+            raise SystemExit("--bias-relu runs unsplit: use --split-k -1, 0 or 1")
+    plan = cig.describe_plan(p, d, 1 if fused else a.split_k, bias, sm_count=sms)
+    ws = None if fused else cig.workspace(p, d, a.split_k, bias, dev)
     in_bytes = problem_bytes(p, direction)
     flush = None
     if in_bytes - 0 < 4 * L2_BYTES:  # small inputs: flush L2 between steps
@@ -357,7 +366,9 @@ def run_ours(a, rank, world, local_rank):
             flush.fill_(1.0)
         if ev is not None:
             ev[0].record(stream)
-        if direction == "fwd":
+        if fused:
+            cig.conv_fwd_epilogue(p, x, b, out, ep_bias, 0.0, float("inf"), None, a.split_k, stream)
+        elif direction == "fwd":
             cig.conv_fwd(p, x, b, out, ws, a.split_k, stream)
         elif direction == "dgrad":
             cig.conv_dgrad(p, x, b, out, ws, a.split_k, stream)
@@ -371,9 +382,13 @@ def run_ours(a, rank, world, local_rank):
         if flush is not None:
             flush.fill_(1.0)
         ev[0].record(stream)
-        cig.conv_stage1(p, d, x, b, out, db, ws, a.split_k, stream)
-        ev[1].record(stream)
-        cig.conv_stage2(p, d, out, db, ws, a.split_k, stream)
+        if fused:  # one unsplit launch: all of it is stage 1
+            cig.conv_fwd_epilogue(p, x, b, out, ep_bias, 0.0, float("inf"), None, a.split_k, stream)
+            ev[1].record(stream)
+        else:
+            cig.conv_stage1(p, d, x, b, out, db, ws, a.split_k, stream)
+            ev[1].record(stream)
+            cig.conv_stage2(p, d, out, db, ws, a.split_k, stream)
         ev[2].record(stream)
 
     for _ in range(a.warmup):
@@ -460,7 +475,9 @@ def run_ours(a, rank, world, local_rank):
         def e2e_step():
             xh_d.copy_(hosts[0], non_blocking=True)
             bh_d.copy_(hosts[1], non_blocking=True)
-            if direction == "fwd":
+            if fused:
+                cig.conv_fwd_epilogue(p, xh_d, bh_d, out, ep_bias, 0.0, float("inf"), None, a.split_k, stream)
+            elif direction == "fwd":
                 cig.conv_fwd(p, xh_d, bh_d, out, ws, a.split_k, stream)
             elif direction == "dgrad":
                 cig.conv_dgrad(p, xh_d, bh_d, out, ws, a.split_k, stream)
@@ -496,7 +513,8 @@ def run_ours(a, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 4), "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": DT_NAME[p.in_dtype], "data": "synthetic (seeded counter-based generator)",
-        "config": {"workload": desc, "name": a.workload, "kernel": kname, "split_k": plan["split_k"],
+        "config": {"workload": desc + (" + fused bias/ReLU epilogue" if fused else ""), "name": a.workload,
+                   "kernel": kname, "split_k": plan["split_k"],
                    "split_k_request": a.split_k, "ctas": plan["ctas"], "workspace_bytes": plan["workspace_bytes"],
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                    "l2": "flushed between steps (2x L2 buffer written)" if flush is not None
@@ -572,6 +590,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT)
     ap.add_argument("--split-k", type=int, default=-1)
     ap.add_argument("--kernel", default="auto")
+    ap.add_argument("--bias-relu", action="store_true",
+                    help="forward workloads: fuse a bias + ReLU epilogue (runs unsplit)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

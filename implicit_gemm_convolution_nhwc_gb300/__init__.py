@@ -24,7 +24,7 @@ STATUS = ["CONV_OK", "CONV_ERR_INVALID_ARG", "CONV_ERR_UNSUPPORTED", "CONV_ERR_W
 # Every symbol include/conv_igemm.h declares.
 EXPORTS = ["conv_status_string", "conv_output_dims", "resolve_split_k_for", "resolve_split_k",
            "conv_workspace_bytes_for", "conv_workspace_bytes", "conv_describe_plan", "conv_fwd",
-           "conv_dgrad", "conv_wgrad", "conv_wgrad_bias", "conv_stage1", "conv_stage2", "conv_batch_split_count",
+           "conv_fwd_epilogue", "conv_dgrad", "conv_wgrad", "conv_wgrad_bias", "conv_stage1", "conv_stage2", "conv_batch_split_count",
            "conv_wgrad_bias_static_ws", "conv_device_errors", "conv_set_kernel_override"]
 
 
@@ -64,6 +64,10 @@ class Problem:
     def flops(self) -> int:
         ho, wo = self.out_hw
         return 2 * self.n * ho * wo * self.k * (self.c // self.groups) * self.r * self.s
+
+
+class _CEpilogue(ctypes.Structure):
+    _fields_ = [("bias", ctypes.c_void_p), ("lo", ctypes.c_float), ("hi", ctypes.c_float)]
 
 
 class _CProblem(ctypes.Structure):
@@ -112,6 +116,7 @@ def load(build_if_missing: bool = True):
         "conv_describe_plan": ([P, ctypes.c_int, I32, I32, I32, ctypes.POINTER(PlanInfo)], ctypes.c_int),
         "conv_fwd": ([P, V, V, V, V, U64, I32, V], ctypes.c_int),
         "conv_dgrad": ([P, V, V, V, V, U64, I32, V], ctypes.c_int),
+        "conv_fwd_epilogue": ([P, V, V, ctypes.POINTER(_CEpilogue), V, V, U64, I32, V], ctypes.c_int),
         "conv_wgrad": ([P, V, V, V, V, U64, I32, V], ctypes.c_int),
         "conv_wgrad_bias": ([P, V, V, V, V, V, U64, I32, V], ctypes.c_int),
         "conv_stage1": ([P, ctypes.c_int, V, V, V, V, V, U64, I32, V], ctypes.c_int),
@@ -233,6 +238,22 @@ def conv_fwd(p: Problem, x, w, y, ws=None, split_k: int = -1, stream=None):
     st = load().conv_fwd(_cp(p), _ptr(x), _ptr(w), _ptr(y), _ptr(ws), 0 if ws is None else ws.numel(),
                          split_k, _stream(stream))
     _check(st, "conv_fwd")
+    return y
+
+
+def conv_fwd_epilogue(p: Problem, x, w, y, bias=None, lo: float = float("-inf"), hi: float = float("inf"),
+                      ws=None, split_k: int = -1, stream=None):
+    """Forward with a fused y = min(max(conv + bias[k], lo), hi) (ReLU: lo = 0). bias: [k] in out_dtype or None."""
+    ho, wo = p.out_hw
+    _need(x, "x", p.n * p.h * p.w * p.c, p.in_dtype)
+    _need(w, "w", p.k * p.r * p.s * (p.c // p.groups), p.in_dtype)
+    _need(y, "y", p.n * ho * wo * p.k, p.out_dtype)
+    if bias is not None:
+        _need(bias, "bias", p.k, p.out_dtype)
+    ep = _CEpilogue(_ptr(bias), lo, hi)
+    st = load().conv_fwd_epilogue(_cp(p), _ptr(x), _ptr(w), ctypes.byref(ep), _ptr(y), _ptr(ws),
+                                  0 if ws is None else ws.numel(), split_k, _stream(stream))
+    _check(st, "conv_fwd_epilogue")
     return y
 
 

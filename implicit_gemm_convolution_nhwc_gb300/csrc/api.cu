@@ -4,6 +4,7 @@
 // so an error status means nothing was enqueued (the loud-failure rule of
 // "ROCm/rocm-libraries PR #11188", "Motivation": a silently wrong dW is the
 // failure being designed out). All sizes are 64-bit and checked for overflow.
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 
@@ -155,8 +156,12 @@ conv_status resolve_degree(const Shape& s, conv_dir dir, const Geometry& g, int3
   return CONV_OK;
 }
 
+// epilogue: a non-identity fused forward epilogue, which runs unsplit
+// ("feat(rocke): split-K forward implicit-GEMM convolution on gfx1250",
+// "Review follow-ups": split-K rejects it; "Auto-deduced degree": such specs
+// resolve to 1).
 conv_status make_plan(const conv_problem* prob, conv_dir dir, int32_t request, bool with_bias,
-                      int32_t sm_count, Plan* plan) {
+                      int32_t sm_count, Plan* plan, bool epilogue = false) {
   if (dir != CONV_DIR_FWD && dir != CONV_DIR_WGRAD && dir != CONV_DIR_DGRAD) return CONV_ERR_INVALID_ARG;
   Plan p;
   conv_status st = validate(prob, &p.sh);
@@ -164,8 +169,14 @@ conv_status make_plan(const conv_problem* prob, conv_dir dir, int32_t request, b
   if (request < -1) return CONV_ERR_INVALID_ARG;
   p.dir = dir;
   p.with_bias = with_bias && dir == CONV_DIR_WGRAD;
+  p.epilogue = epilogue;
+  if (epilogue) {
+    if (dir != CONV_DIR_FWD || request > 1) return CONV_ERR_INVALID_ARG;
+    request = 1;
+  }
   st = choose_kernel(p.sh, dir, &p.kernel, &p.geo);
   if (st != CONV_OK) return st;
+  if (epilogue && p.kernel == CONV_KERNEL_FWD_TC_CLUSTER) return CONV_ERR_UNSUPPORTED;
   // The cluster form takes at most 16 slices (one cluster per tile).
   if (p.kernel == CONV_KERNEL_FWD_TC_CLUSTER && request > p.geo.max_split && request <= p.geo.blocks)
     return CONV_ERR_UNSUPPORTED;
@@ -192,9 +203,14 @@ bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u
 // Which stages a call enqueues.
 enum Stages { kStage1 = 1, kStage2 = 2, kBoth = 3 };
 
+// A fused epilogue that changes nothing (no bias, bounds -inf / +inf).
+bool identity_epilogue(const conv_epilogue* ep) {
+  return !ep || (!ep->bias && std::isinf(ep->lo) && ep->lo < 0 && std::isinf(ep->hi) && ep->hi > 0);
+}
+
 conv_status run(const conv_problem* prob, conv_dir dir, const void* x, const void* b, void* out,
                 void* db, void* ws, uint64_t ws_bytes, int32_t split_k, void* stream, bool with_bias,
-                int stages) {
+                int stages, const conv_epilogue* ep = nullptr) {
   Shape sh;
   conv_status st = validate(prob, &sh);
   if (st != CONV_OK) return st;
@@ -210,12 +226,18 @@ conv_status run(const conv_problem* prob, conv_dir dir, const void* x, const voi
   if ((needs_inputs && x_elems > 0 && !x) || (needs_inputs && b_elems > 0 && !b) ||
       (out_elems > 0 && !out) || (with_bias && !db))
     return CONV_ERR_INVALID_ARG;
+  const bool epilogue = !identity_epilogue(ep);
+  if (epilogue) {
+    if (std::isnan(ep->lo) || std::isnan(ep->hi) || ep->lo > ep->hi) return CONV_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(ep->bias) % (uintptr_t)esize(sh.out_dt) != 0) return CONV_ERR_ALIGNMENT;
+    if (dir != CONV_DIR_FWD || split_k > 1) return CONV_ERR_INVALID_ARG;  // never split (make_plan too)
+  }
   if (!aligned16(x) || !aligned16(b) || !aligned16(out) || !aligned16(db) || !aligned16(ws))
     return CONV_ERR_ALIGNMENT;
   const int sms = current_sm_count();
   if (sms < 1) return CONV_ERR_CUDA;
   Plan plan;
-  st = make_plan(prob, dir, split_k, with_bias, sms, &plan);
+  st = make_plan(prob, dir, split_k, with_bias, sms, &plan, epilogue);
   if (st != CONV_OK) return st;
   if (plan.ws_bytes() > 0 && (!ws || ws_bytes < plan.ws_bytes())) return CONV_ERR_WORKSPACE_TOO_SMALL;
   if (out_elems == 0) return CONV_OK;  // an empty forward batch: nothing to write
@@ -230,6 +252,12 @@ conv_status run(const conv_problem* prob, conv_dir dir, const void* x, const voi
                   ? reinterpret_cast<float*>(static_cast<char*>(ws) + plan.aux_bytes + plan.slab_bytes)
                   : nullptr;
   a.stream = static_cast<cudaStream_t>(stream);
+  if (epilogue) {
+    a.ep = true;
+    a.ep_bias = ep->bias;
+    a.ep_lo = ep->lo;
+    a.ep_hi = ep->hi;
+  }
   cudaError_t err = cudaSuccess;
   if (stages & kStage1) {
     switch (plan.kernel) {
@@ -354,6 +382,11 @@ conv_status conv_describe_plan(const conv_problem* p, conv_dir dir, int32_t spli
 conv_status conv_fwd(const conv_problem* p, const void* x, const void* w, void* y, void* ws,
                      uint64_t ws_bytes, int32_t split_k, void* stream) {
   return run(p, CONV_DIR_FWD, x, w, y, nullptr, ws, ws_bytes, split_k, stream, false, kBoth);
+}
+
+conv_status conv_fwd_epilogue(const conv_problem* p, const void* x, const void* w, const conv_epilogue* ep,
+                              void* y, void* ws, uint64_t ws_bytes, int32_t split_k, void* stream) {
+  return run(p, CONV_DIR_FWD, x, w, y, nullptr, ws, ws_bytes, split_k, stream, false, kBoth, ep);
 }
 
 conv_status conv_dgrad(const conv_problem* p, const void* dy, const void* w, void* dx, void* ws,

@@ -46,6 +46,7 @@ struct Plan {
   uint64_t slab_bytes;       // S*E*4 rounded to 256 (0 when S == 1)
   uint64_t bias_slab_bytes;  // S*K*4 rounded to 256 (0 when S == 1 or no bias)
   bool fold;                 // stage 2 runs (S > 1 and the slices do not fold in-launch)
+  bool epilogue;             // a non-identity fused forward epilogue (then S == 1)
   uint64_t aux_bytes;        // kernel-private bytes at the start of ws (the data gradient's filter)
   uint64_t ws_bytes() const { return aux_bytes + slab_bytes + bias_slab_bytes; }
 };
@@ -58,6 +59,10 @@ struct Args {
   void* db;        // bias gradient or nullptr
   float* ws;       // slabs [S][E] (nullptr when S == 1)
   float* ws_bias;  // bias slabs [S][K] (nullptr when S == 1 or no bias)
+  // Fused forward epilogue (S == 1 only): out = min(max(acc + ep_bias[k], ep_lo), ep_hi).
+  const void* ep_bias = nullptr;  // [K] in the output type, or nullptr
+  float ep_lo = 0.f, ep_hi = 0.f;
+  bool ep = false;
   cudaStream_t stream;
 };
 

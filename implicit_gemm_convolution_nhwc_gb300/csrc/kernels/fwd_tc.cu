@@ -57,6 +57,7 @@ struct Tile {
   static constexpr int kLD = BN + 4;                // staged partial tile row stride, floats (conflict-free float4s)
   static_assert(BN == 128 || BN == 256, "tile width");
   static_assert(kBM * kLD * 4 <= kStages * kStage, "staged partial tile must fit in the ring");
+  static_assert(2 * kBM * 128 + BN * 4 <= kStages * kStage, "epilogue staging and bias must fit in the ring");
 };
 
 struct FwdParams {
@@ -70,6 +71,10 @@ struct FwdParams {
   int32_t TR;                   // output rows per M tile
   int32_t ph, pw, dh, dw;
   int32_t split;
+  // fused epilogue (unsplit only): y = min(max(acc + bias[k], ep_lo), ep_hi)
+  const void* ep_bias;
+  float ep_lo, ep_hi;
+  int32_t ep;
 };
 
 // 16 bytes of TE from 4 (fp32) or 8 (16-bit) values, rounded to nearest even.
@@ -109,7 +114,8 @@ __device__ __forceinline__ uint4 pack16<__half>(const float* v) {
 template <typename TE, int BN>
 __device__ __forceinline__ void store_tile_tma(uint32_t trow, uint8_t* stage, const CUtensorMap* tm, int32_t kx0,
                                                int32_t kx_end, int32_t py, int32_t pz, int m, bool have_acc,
-                                               bool leader, bool do_store) {
+                                               bool leader, bool do_store, const float* ep_bias = nullptr,
+                                               float ep_lo = 0.f, float ep_hi = 0.f, bool ep = false) {
   constexpr int CW = 128 / (int)sizeof(TE);  // channels per 128-byte chunk
   constexpr int VPU = 16 / (int)sizeof(TE);  // values per 16-byte unit
   // Only chunks that start below K: each one then commits exactly one bulk
@@ -130,6 +136,17 @@ __device__ __forceinline__ void store_tile_tma(uint32_t trow, uint8_t* stage, co
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[32 * h + i] = 0.f;
+      }
+    }
+    if (ep) {  // bias (staged in shared memory, fp32) + clamp on the accumulator, before the rounding
+      const float4* b4 = reinterpret_cast<const float4*>(ep_bias + c * CW);
+#pragma unroll
+      for (int i = 0; i < CW; i += 4) {
+        const float4 b = b4[i / 4];
+        v[i] = fminf(fmaxf(v[i] + b.x, ep_lo), ep_hi);
+        v[i + 1] = fminf(fmaxf(v[i + 1] + b.y, ep_lo), ep_hi);
+        v[i + 2] = fminf(fmaxf(v[i + 2] + b.z, ep_lo), ep_hi);
+        v[i + 3] = fminf(fmaxf(v[i + 3] + b.w, ep_lo), ep_hi);
       }
     }
     uint8_t* row = buf + m * 128;
@@ -314,9 +331,19 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
       if (ws)
         store_tile_tma<float, BN>(trow, stage, &tm_y, (int32_t)k0, (int32_t)fp.K, py, (int32_t)(sigma * fp.N + img),
                                   m, nblk > 0, threadIdx.x == 128, ok);
-      else
+      else {
+        // The epilogue's bias for the tile's BN channels, as fp32 in shared memory
+        // past the two staging buffers (0 beyond K or without a bias).
+        float* sbias = reinterpret_cast<float*>(smem + 2 * kBM * 128);
+        if (fp.ep) {
+          const TO* bias = static_cast<const TO*>(fp.ep_bias);
+          for (int i = threadIdx.x - 128; i < BN; i += 128)
+            sbias[i] = bias && k0 + i < fp.K ? to_f32(bias[k0 + i]) : 0.f;
+          named_bar_sync(1, 128);
+        }
         store_tile_tma<TO, BN>(trow, stage, &tm_y, (int32_t)k0, (int32_t)fp.K, py, (int32_t)img, m, nblk > 0,
-                               threadIdx.x == 128, ok);
+                               threadIdx.x == 128, ok, sbias, fp.ep_lo, fp.ep_hi, fp.ep != 0);
+      }
     }
   }
 
@@ -402,6 +429,11 @@ template <typename TO, uint32_t FMT, bool CL, int BN>
 cudaError_t launch_typed(const Plan& p, const Args& a, CUtensorMapDataType dt) {
   const Shape& s = p.sh;
   FwdParams fp = make_params(p, BN);
+  fp.ep_bias = a.ep_bias;
+  fp.ep_lo = a.ep_lo;
+  fp.ep_hi = a.ep_hi;
+  fp.ep = a.ep ? 1 : 0;
+  if (a.ep && (CL || a.ws)) return cudaErrorInvalidValue;  // the epilogue runs unsplit only
   constexpr size_t smem = Tile<BN>::kSmem;
   CUtensorMap tm_x, tm_w;
   const uint64_t x_dims[4] = {(uint64_t)s.c, (uint64_t)s.w, (uint64_t)s.h, (uint64_t)s.n};

@@ -75,11 +75,14 @@ __global__ void __launch_bounds__(kThreads) generic_bias_kernel(Shape sh, const 
   store_result(db, ws_bias, sh.k, sigma, k, acc);
 }
 
-// Y[n,ho,wo,k] over the reduction depth (r, s, c) of slice sigma.
+// Y[n,ho,wo,k] over the reduction depth (r, s, c) of slice sigma; unsplit,
+// with the fused epilogue min(max(acc + bias[k], lo), hi) when ep is set.
 template <typename TI, typename TO>
 __global__ void __launch_bounds__(kThreads) generic_fwd_kernel(Shape sh, const TI* __restrict__ x,
                                                                const TI* __restrict__ wt, TO* out, float* ws,
-                                                               int32_t S, int64_t tiles, int64_t blocks) {
+                                                               int32_t S, int64_t tiles, int64_t blocks,
+                                                               const TO* ep_bias, float ep_lo, float ep_hi,
+                                                               bool ep) {
   const int64_t tile = blockIdx.x % tiles;
   const int32_t sigma = (int32_t)(blockIdx.x / tiles);
   const int64_t E = sh.y_elems();
@@ -115,6 +118,7 @@ __global__ void __launch_bounds__(kThreads) generic_fwd_kernel(Shape sh, const T
       }
     }
   }
+  if (ep) acc = fminf(fmaxf(acc + (ep_bias ? to_f32(ep_bias[k]) : 0.f), ep_lo), ep_hi);
   store_result(out, ws, E, sigma, e, acc);
 }
 
@@ -181,8 +185,9 @@ cudaError_t launch_typed(const Plan& p, const Args& a) {
                                                                              p.geo.tiles, p.geo.blocks);
     return cudaGetLastError();
   }
-  generic_fwd_kernel<TI, TO><<<(unsigned)ctas, kThreads, 0, a.stream>>>(p.sh, x, b, out, a.ws, p.split,
-                                                                         p.geo.tiles, p.geo.blocks);
+  generic_fwd_kernel<TI, TO><<<(unsigned)ctas, kThreads, 0, a.stream>>>(
+      p.sh, x, b, out, a.ws, p.split, p.geo.tiles, p.geo.blocks, static_cast<const TO*>(a.ep_bias), a.ep_lo, a.ep_hi,
+      a.ep);
   return cudaGetLastError();
 }
 

@@ -176,6 +176,25 @@ conv_status conv_fwd(const conv_problem* p, const void* x, const void* w, void* 
 conv_status conv_wgrad(const conv_problem* p, const void* x, const void* dy, void* dw, void* ws,
                        uint64_t ws_bytes, int32_t split_k, void* stream);
 
+/* A fused forward epilogue: y = min(max(conv(x, w) + bias[k], lo), hi),
+ * applied to the fp32 accumulator before the one rounding into out_dtype
+ * [P2 "Review follow-ups": bias / ReLU / clamp are the non-identity
+ * epilogues]. bias is [k] in out_dtype, or NULL for none; ReLU is
+ * {lo = 0, hi = +inf}; {-inf, +inf} with no bias is the identity. lo <= hi,
+ * neither NaN. */
+typedef struct conv_epilogue {
+  const void* bias;
+  float lo, hi;
+} conv_epilogue;
+
+/* Forward with a fused epilogue. A non-identity epilogue cannot be applied
+ * per slice, so it runs unsplit [P2 "Review follow-ups": split-K rejects
+ * it; "Auto-deduced degree": such specs resolve to 1]: split_k -1, 0 or 1
+ * gives one slice, any other degree is CONV_ERR_INVALID_ARG; no workspace is
+ * needed. An identity epilogue (or ep == NULL) is exactly conv_fwd. */
+conv_status conv_fwd_epilogue(const conv_problem* p, const void* x, const void* w, const conv_epilogue* ep,
+                              void* y, void* ws, uint64_t ws_bytes, int32_t split_k, void* stream);
+
 /* Data gradient: dx[n,h,w,c] = sum over k, r, s of dy[n,ho,wo,k] * w[k,r,s,c]
  * for the (ho, wo) with ho*sh + r*dh - ph = h and wo*sw + s*dw - pw = w (the
  * forward's taps read backwards). dy and w in in_dtype, dx [n,h,w,c] in

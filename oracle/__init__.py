@@ -119,6 +119,16 @@ class Oracle:
                                   nthreads or _threads())
         return y
 
+    def fwd_epilogue(self, p: Problem, x, w, bias=None, lo: float = -np.inf, hi: float = np.inf,
+                     nthreads: int | None = None) -> np.ndarray:
+        """min(max(Y + bias[k], lo), hi) in float64: the fused bias / ReLU / clamp epilogue
+        ("feat(rocke): split-K forward implicit-GEMM convolution on gfx1250", "Review follow-ups"),
+        applied to the forward's exact sum."""
+        y = self.fwd(p, x, w, nthreads)
+        if bias is not None:
+            y = y + _f32(bias).astype(np.float64).reshape(1, 1, 1, p.k)
+        return np.minimum(np.maximum(y, lo), hi)
+
     def dgrad(self, p: Problem, dy, w, nthreads: int | None = None) -> np.ndarray:
         """dX [n, h, w, c] in float64: the gradient of the forward with respect to X."""
         ho, wo = self.out_hw(p)

@@ -19,7 +19,7 @@ _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "libsynth.so")
 _lib = None
 
-X_ID, W_ID, DY_ID = 0, 1, 2
+X_ID, W_ID, DY_ID, BIAS_ID = 0, 1, 2, 3
 DISTS = {"uniform": 0, "normal": 1, "integer": 2}
 
 

@@ -6,8 +6,9 @@ import pytest
 import torch
 
 import oracle
+import synth
 import implicit_gemm_convolution_nhwc_gb300 as cig
-from gpu_util import inputs, oproblem, relerr, run_dgrad, run_fwd, run_wgrad, tol
+from gpu_util import TORCH_DT, Guarded, inputs, oproblem, relerr, run_dgrad, run_fwd, run_wgrad, tol
 
 pytestmark = pytest.mark.gpu
 
@@ -228,6 +229,58 @@ def test_forward_tc_ragged(shape, dt):
     p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
     check_fwd(p, 6, ["fwd_tc", "fwd_tc_cluster", "generic"], [-1, 1, 3])
     check_fwd(p, 6, ["fwd_tc", "fwd_tc_cluster"], ["max"])
+    assert cig.device_errors() == 0
+
+
+# ------------------------------------------------------- fused forward epilogue
+
+INF = float("inf")
+
+
+def run_fwd_ep(p, x, w, bias, lo, hi, split_k=-1):
+    ho, wo = p.out_hw
+    y = Guarded(p.n * ho * wo * p.k, TORCH_DT[p.out_dtype])
+    cig.conv_fwd_epilogue(p, x.cuda(), w.cuda(), y.view, None if bias is None else bias.cuda(), lo, hi,
+                          None, split_k)
+    torch.cuda.synchronize()
+    assert y.intact(), "a write left its buffer"
+    return y.view.cpu().reshape(p.n, ho, wo, p.k)
+
+
+@pytest.mark.parametrize("shape", [
+    dict(n=2, h=10, w=12, c=128, k=136, r=3, s=3, pad_h=1, pad_w=1),          # tensor cores, K tail
+    dict(n=1, h=14, w=14, c=256, k=256, r=3, s=3, pad_h=1, pad_w=1),          # 128 x 256 tiles; conv_fwd would split
+    dict(n=2, h=9, w=11, c=12, k=8, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1),  # generic
+])
+@pytest.mark.parametrize("dt", [(BF16, BF16), (F16, F32), (F32, F32)], ids=lambda d: f"{d[0]}{d[1]}")
+def test_forward_fused_epilogue(shape, dt):
+    """Bias / ReLU / clamp fused into the unsplit forward ("feat(rocke): split-K forward
+    implicit-GEMM convolution on gfx1250", "Review follow-ups"), against the oracle."""
+    p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
+    x, w = inputs(p, 21, "normal", 0.0, 0.05, cig.DIR_FWD)
+    bias = synth.tensor((p.k,), TORCH_DT[p.out_dtype], "normal", 0.0, 0.1, 21, synth.BIAS_ID)
+    orc = oracle.get()
+    for use_bias, lo, hi in [(True, 0.0, INF), (True, -INF, INF), (False, 0.0, INF), (True, -0.05, 0.03)]:
+        b = bias if use_bias else None
+        ref = orc.fwd_epilogue(oproblem(p), x, w, b, lo, hi)
+        # bias and clamp are exact; the error is the sum's, so it is measured against the
+        # magnitude of the sum before the clamp
+        scale = np.abs(orc.fwd_epilogue(oproblem(p), x, w, b)).max()
+        for sk in (-1, 1):
+            got = run_fwd_ep(p, x, w, b, lo, hi, sk).double().numpy()
+            e = np.abs(got - ref).max() / scale
+            assert e <= tol(p), f"bias {use_bias} [{lo}, {hi}] split {sk}: err {e:.3e}"
+    # the identity epilogue is conv_fwd itself, bit for bit (same degree, same kernels)
+    ho, wo = p.out_hw
+    ident = Guarded(p.n * ho * wo * p.k, TORCH_DT[p.out_dtype])
+    ws = cig.workspace(p, cig.DIR_FWD, -1, False)
+    cig.conv_fwd_epilogue(p, x.cuda(), w.cuda(), ident.view, None, -INF, INF, ws, -1)
+    torch.cuda.synchronize()
+    plain = run_fwd(p, x, w, -1)
+    assert torch.equal(ident.view.cpu().view(torch.uint8), plain.reshape(-1).view(torch.uint8))
+    with pytest.raises(cig.ConvError) as err:
+        run_fwd_ep(p, x, w, bias, 0.0, INF, 2)
+    assert err.value.status == 1
     assert cig.device_errors() == 0
 
 

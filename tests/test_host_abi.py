@@ -242,3 +242,22 @@ def test_calls_validate_before_touching_the_device():
     assert lib.conv_wgrad_bias(p, 16, 16, 16, None, None, 0, -1, None) == 1
     assert lib.conv_fwd(p, 18, 32, 32, None, 0, -1, None) == 5
     assert lib.conv_wgrad(p, 16, 16, 16, None, 0, -3, None) == 1
+
+
+def test_fused_epilogue_validation_without_a_device():
+    """conv_fwd_epilogue: bounds and bias alignment are checked before anything else runs;
+    a non-identity epilogue is never split ("feat(rocke): split-K forward implicit-GEMM
+    convolution on gfx1250", "Review follow-ups")."""
+    lib = cig.load()
+    p = cig._cp(CONFIG3)
+    inf = float("inf")
+    ep = cig._CEpilogue(None, 1.0, 0.0)          # lo > hi
+    assert lib.conv_fwd_epilogue(p, 16, 16, ctypes.byref(ep), 16, None, 0, -1, None) == 1
+    ep = cig._CEpilogue(None, float("nan"), inf)  # NaN bound
+    assert lib.conv_fwd_epilogue(p, 16, 16, ctypes.byref(ep), 16, None, 0, -1, None) == 1
+    ep = cig._CEpilogue(17, 0.0, inf)            # bf16 bias at an odd address
+    assert lib.conv_fwd_epilogue(p, 16, 16, ctypes.byref(ep), 16, None, 0, -1, None) == 5
+    ep = cig._CEpilogue(None, 0.0, inf)          # ReLU with a pinned split: rejected
+    assert lib.conv_fwd_epilogue(p, 16, 16, ctypes.byref(ep), 16, None, 0, 4, None) == 1
+    ep = cig._CEpilogue(None, 0.0, inf)          # ReLU with NULL tensors
+    assert lib.conv_fwd_epilogue(p, None, None, ctypes.byref(ep), None, None, 0, -1, None) == 1

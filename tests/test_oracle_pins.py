@@ -183,8 +183,25 @@ def pin_1x1_dgrad_gemm(orc: Oracle):
     return relerr(orc.dgrad(p, dy, w).reshape(-1, 12), ref) <= 1e-12
 
 
+def pin_torch_fwd_bias_relu(orc: Oracle):
+    """The fused epilogue against torch's float64 conv2d with its own bias, then relu / clamp."""
+    for p in SHAPES:
+        x, w, _ = _inputs(p, orc)
+        b = rand((p.k,), 9, synth.W_ID + 7)
+        xt = torch.from_numpy(np.asarray(x, np.float64)).permute(0, 3, 1, 2)
+        wt = torch.from_numpy(np.asarray(w, np.float64)).permute(0, 3, 1, 2)
+        y = torch.nn.functional.conv2d(xt, wt, torch.from_numpy(b.astype(np.float64)),
+                                       stride=(p.stride_h, p.stride_w), padding=(p.pad_h, p.pad_w),
+                                       dilation=(p.dil_h, p.dil_w), groups=p.groups).permute(0, 2, 3, 1)
+        if relerr(orc.fwd_epilogue(p, x, w, b, 0.0), torch.relu(y).numpy()) > 1e-12:
+            return False
+        if relerr(orc.fwd_epilogue(p, x, w, b, -0.25, 0.5), torch.clamp(y, -0.25, 0.5).numpy()) > 1e-12:
+            return False
+    return True
+
+
 PINS = [pin_1x1_gemm, pin_bias_sum, pin_torch_fwd, pin_torch_wgrad, pin_all_ones, pin_adjoint,
-        pin_torch_dgrad, pin_adjoint_dgrad, pin_1x1_dgrad_gemm]
+        pin_torch_dgrad, pin_adjoint_dgrad, pin_1x1_dgrad_gemm, pin_torch_fwd_bias_relu]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
