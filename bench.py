@@ -45,6 +45,9 @@ WORKLOADS = {
     "fwd3x3_bf16_n64_c256": (dict(n=64, h=56, w=56, c=256, k=256, r=3, s=3, pad_h=1, pad_w=1, in_dtype=1,
                                   out_dtype=1), "fwd", "normal", (0.0, 0.02), 5,
                              "3x3 fwd bf16 NHWC N=64 H=W=56 C=K=256 pad 1 (compute-bound supplement)"),
+    "fwd3x3s2_bf16_n64": (dict(n=64, h=56, w=56, c=128, k=256, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1,
+                               in_dtype=1, out_dtype=1), "fwd", "normal", (0.0, 0.02), 6,
+                          "3x3 stride-2 fwd bf16 NHWC N=64 H=W=56 C=128 K=256 pad 1 (a downsampling layer)"),
     "dgrad3x3_bf16_n1": (dict(n=1, h=14, w=14, c=2048, k=512, r=3, s=3, pad_h=1, pad_w=1, in_dtype=1, out_dtype=1),
                          "dgrad", "normal", (0.0, 0.02), 2,
                          "3x3 dgrad bf16 NHWC N=1 H=W=14 C=2048 K=512 pad 1 (the small-M layer backwards), split-K"),

@@ -6,11 +6,13 @@
 //   A[m][(r,s,c)] = X[n, ho + r*dh - ph, wo + s*dw - pw, c],  B[k][(r,s,c)] = W[k,r,s,c].
 // Both are K-major in NHWC / channels-last memory, as the bf16/fp16 MMA wants.
 // An M tile is TR whole output rows (TR*Wo <= 128 pixels). For a reduction
-// block (r, s, 64 channels) its A tile is ONE 4-D TMA box {64 ch, Wo, TR, 1}
-// of X starting at (c0, s*dw - pw, ho0 + r*dh - ph, n): coordinates outside
-// the image read zeros, which is exactly the zero padding, and the box lands
-// as TR*Wo rows of 128 bytes in the 128B-swizzled K-major layout the MMA
-// reads. B is a 2-D box {64, 128} of W viewed as [K][R*S*C].
+// block (r, s, 64 channels) its A tile is ONE 4-D TMA box {64 ch, Wo*sw,
+// TR*sh, 1} of X starting at (c0, s*dw - pw, ho0*sh + r*dh - ph, n), read
+// with traversal strides (1, sw, sh, 1) so it holds exactly the Wo x TR
+// input positions the tile's outputs read through tap (r, s): coordinates
+// outside the image read zeros, which is exactly the zero padding, and the
+// box lands as TR*Wo rows of 128 bytes in the 128B-swizzled K-major layout
+// the MMA reads. B is a 2-D box {64, BN} of W viewed as [K][R*S*C].
 //
 // Split-K ("feat(rocke): split-K forward implicit-GEMM convolution on
 // gfx1250", "Two-stage split-K"): CTA (tile, sigma) reduces the blocks of
@@ -70,6 +72,7 @@ struct FwdParams {
   int64_t blocks;               // R * S * cblocks
   int32_t TR;                   // output rows per M tile
   int32_t ph, pw, dh, dw;
+  int32_t sh;                   // stride along H (along W it is the X map's traversal stride)
   int32_t split;
   // fused epilogue (unsplit only): y = min(max(acc + bias[k], ep_lo), ep_hi)
   const void* ep_bias;
@@ -222,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
   auto issue = [&]() {
     uint8_t* st = smem + (size_t)ps * kStage;
     mbar_arrive_expect_tx(&full[ps], tx);
-    tma_load_4d(st, &tm_x, cb * kBK, sx * fp.dw - fp.pw, (int32_t)ho0 + r * fp.dh - fp.ph, (int32_t)img,
+    tma_load_4d(st, &tm_x, cb * kBK, sx * fp.dw - fp.pw, (int32_t)ho0 * fp.sh + r * fp.dh - fp.ph, (int32_t)img,
                 &full[ps]);
     tma_load_2d(st + kA, &tm_w, rs * cg + cb * kBK, (int32_t)k0, &full[ps]);
     if (++cb == cblocks) {
@@ -388,12 +391,15 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
 }
 
 bool fwd_tc_admissible(const Shape& s) {
-  if (s.in_dt == CONV_F32 || s.groups != 1 || s.sh != 1 || s.sw != 1) return false;
+  if (s.in_dt == CONV_F32 || s.groups != 1) return false;
+  if (s.sh > 8 || s.sw > 8) return false;  // the TMA traversal stride takes 1..8
   if (s.cg % kBK != 0 || s.k % 8 != 0 || s.k < 128) return false;
-  if (s.wo > kBM || s.wo > s.w) return false;    // one TMA box spans a whole output row
+  // One TMA box spans a whole output row: Wo*sw input columns, no wider than the image.
+  if (s.wo > kBM || s.wo * s.sw > 256 || s.wo * s.sw > s.w) return false;
   if (s.n < 1 || s.n > 0x7fffffffLL || s.h > 0x7fffffffLL || s.w > 0x7fffffffLL) return false;
   const int64_t tr = kBM / s.wo;
-  if ((tr < s.ho ? tr : s.ho) > s.h) return false;  // no box taller than the image
+  const int64_t rows = (tr < s.ho ? tr : s.ho) * s.sh;  // input rows a box spans
+  if (rows > s.h || rows > 256) return false;           // no box taller than the image
   if (s.r * s.s * s.cg > 0x7fffffffLL) return false;
   return true;
 }
@@ -421,6 +427,7 @@ FwdParams make_params(const Plan& p, int bn) {
   fp.pw = (int32_t)s.pw;
   fp.dh = (int32_t)s.dh;
   fp.dw = (int32_t)s.dw;
+  fp.sh = (int32_t)s.sh;
   fp.split = p.split;
   return fp;
 }
@@ -438,11 +445,15 @@ cudaError_t launch_typed(const Plan& p, const Args& a, CUtensorMapDataType dt) {
   CUtensorMap tm_x, tm_w;
   const uint64_t x_dims[4] = {(uint64_t)s.c, (uint64_t)s.w, (uint64_t)s.h, (uint64_t)s.n};
   const uint64_t x_strides[3] = {(uint64_t)s.c * 2u, (uint64_t)(s.w * s.c) * 2u, (uint64_t)(s.h * s.w * s.c) * 2u};
-  const uint32_t x_box[4] = {(uint32_t)kBK, (uint32_t)s.wo, (uint32_t)fp.TR, 1u};
+  // Strided problems: the box spans Wo*sw columns and TR*sh rows and the map
+  // traverses them with strides (sw, sh), so the TR*Wo rows of 128 bytes land
+  // in shared memory exactly as for stride 1.
+  const uint32_t x_box[4] = {(uint32_t)kBK, (uint32_t)(s.wo * s.sw), (uint32_t)(fp.TR * s.sh), 1u};
+  const uint32_t x_estr[4] = {1u, (uint32_t)s.sw, (uint32_t)s.sh, 1u};
   const uint64_t w_dims[2] = {(uint64_t)(s.r * s.s * s.cg), (uint64_t)s.k};
   const uint64_t w_strides[1] = {(uint64_t)(s.r * s.s * s.cg) * 2u};
   const uint32_t w_box[2] = {(uint32_t)kBK, (uint32_t)BN};
-  if (!encode_tmap(&tm_x, dt, 4, a.x, x_dims, x_strides, x_box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  if (!encode_tmap(&tm_x, dt, 4, a.x, x_dims, x_strides, x_box, CU_TENSOR_MAP_SWIZZLE_128B, x_estr) ||
       !encode_tmap(&tm_w, dt, 2, a.b, w_dims, w_strides, w_box, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   // Output map of the two-stage form's epilogue: the slabs (fp32) under

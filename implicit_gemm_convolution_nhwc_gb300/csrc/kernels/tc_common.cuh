@@ -286,8 +286,12 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t caddr) {
 
 // Host: encode a tiled tensor map (through the driver entry point, no -lcuda).
 // dims/strides innermost first; strides are bytes for dims 1..rank-1.
+// element_strides (null: all 1) is the traversal stride per dimension: a
+// box of extent b along a dimension of stride e loads ceil(b / e) elements,
+// every e-th one.
 bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,
-                 const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle);
+                 const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle,
+                 const uint32_t* element_strides = nullptr);
 
 // Host: the device error word of the current device (a module-scope
 // __device__ variable, no allocation), or null.

@@ -32,7 +32,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,
-                 const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle) {
+                 const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle,
+                 const uint32_t* element_strides) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t d[5], st[4];
@@ -40,7 +41,7 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
   for (int i = 0; i < rank; ++i) {
     d[i] = dims[i];
     b[i] = box[i];
-    es[i] = 1;
+    es[i] = element_strides ? element_strides[i] : 1;
     if (i + 1 < rank) st[i] = strides_bytes[i];
   }
   CUresult r = fn(map, dtype, (cuuint32_t)rank, const_cast<void*>(base), d, st, b, es,

@@ -232,6 +232,22 @@ def test_forward_tc_ragged(shape, dt):
     assert cig.device_errors() == 0
 
 
+@pytest.mark.parametrize("shape", [
+    dict(n=2, h=16, w=16, c=128, k=128, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1),   # 3x3 downsample
+    dict(n=2, h=14, w=14, c=64, k=256, r=1, s=1, stride_h=2, stride_w=2),                       # 1x1 projection
+    dict(n=1, h=21, w=24, c=128, k=136, r=3, s=3, stride_h=3, stride_w=2, pad_h=1, pad_w=1),   # unequal strides, K tail
+    dict(n=1, h=16, w=16, c=64, k=128, r=3, s=3, stride_h=2, stride_w=2, pad_h=2, pad_w=2, dil_h=2, dil_w=2),
+])
+@pytest.mark.parametrize("dt", [(BF16, BF16), (F16, F32)], ids=lambda d: f"{d[0]}{d[1]}")
+def test_forward_tc_strided(shape, dt):
+    """Strided forwards on the tensor cores: the X box is read with TMA traversal strides."""
+    p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
+    assert cig.describe_plan(p, cig.DIR_FWD, -1)["kernel_name"] == "fwd_tc"
+    check_fwd(p, 7, ["fwd_tc", "generic"], [-1, 1, 3])
+    check_fwd(p, 7, ["fwd_tc_cluster"], [2])
+    assert cig.device_errors() == 0
+
+
 # ------------------------------------------------------- fused forward epilogue
 
 INF = float("inf")
