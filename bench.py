@@ -57,6 +57,12 @@ WORKLOADS = {
     "dw7x7_wgrad_bf16": (dict(n=32, h=56, w=56, c=384, k=384, r=7, s=7, pad_h=3, pad_w=3, groups=384,
                               in_dtype=1, out_dtype=1), "wgrad", "normal", (0.0, 1.0), 3,
                          "depthwise 7x7 wgrad bf16 NHWC N=32 H=W=56 C=K=384 pad 3"),
+    "dw7x7_fwd_bf16": (dict(n=32, h=56, w=56, c=384, k=384, r=7, s=7, pad_h=3, pad_w=3, groups=384,
+                            in_dtype=1, out_dtype=1), "fwd", "normal", (0.0, 1.0), 3,
+                       "depthwise 7x7 fwd bf16 NHWC N=32 H=W=56 C=K=384 pad 3"),
+    "grp3x3_fwd_f16_g64": (dict(n=64, h=28, w=28, c=512, k=512, r=3, s=3, pad_h=1, pad_w=1, groups=64,
+                                in_dtype=2, out_dtype=2), "fwd", "normal", (0.0, 1.0), 4,
+                           "grouped 3x3 fwd fp16 NHWC N=64 H=W=28 C=K=512 groups=64 (8 ch/group)"),
     "grp3x3_wgrad_f16_g64": (dict(n=64, h=28, w=28, c=512, k=512, r=3, s=3, pad_h=1, pad_w=1, groups=64,
                                   in_dtype=2, out_dtype=2), "wgrad", "normal", (0.0, 1.0), 4,
                              "grouped 3x3 wgrad fp16 NHWC N=64 H=W=28 C=K=512 groups=64 (8 ch/group)"),

@@ -45,19 +45,24 @@ constexpr int kA = kBM * 128;               // A tile bytes (128 rows x 128 B)
 
 // Tile of BN output channels (128, or 256 when K >= 256: an SM then loads
 // 48 KB per 2 M multiply-adds instead of 32 KB per 1 M, and its L2 -> shared
-// bandwidth, not the tensor pipe, is what bounds a block). Ring: 3 stages for
-// BN = 128 (2 CTAs per SM), 4 for BN = 256 (1 CTA per SM). (A deeper ring for
+// bandwidth, not the tensor pipe, is what bounds a block) and MS M sub-tiles
+// of TR output rows each: with MS = 2 two A tiles share the B tile (64 KB per
+// 4 M multiply-adds), which is taken when the grid has tiles to spare. Ring:
+// 3 stages for BN = 128 (2 CTAs per SM), 4 for BN = 256 (1 CTA per SM), 3 for
+// BN = 256 with MS = 2 (64 KB stages). (A deeper ring for
 // the cluster form would hold one CTA per SM, and then only 7 clusters of 16
 // fit on the GPU at once, fewer than the 8 tiles of the 3x3 small-M layer.)
-template <int BN>
+template <int BN, int MS>
 struct Tile {
   static constexpr int kB = BN * 128;              // B tile bytes (BN rows x 128 B)
-  static constexpr int kStage = kA + kB;
-  static constexpr int kStages = BN == 256 ? 4 : 3;
+  static constexpr int kStage = MS * kA + kB;      // MS A tiles (M sub-tiles) share one B tile
+  static constexpr int kStages = (BN == 256 && MS == 1) ? 4 : 3;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + 256;
-  static constexpr uint32_t kTmemCols = BN;
+  static constexpr uint32_t kTmemCols = BN * MS;   // one fp32 accumulator per M sub-tile
   static constexpr int kLD = BN + 4;                // staged partial tile row stride, floats (conflict-free float4s)
   static_assert(BN == 128 || BN == 256, "tile width");
+  static_assert(MS == 1 || MS == 2, "M sub-tiles");
+  static_assert(kTmemCols <= 512, "TMEM columns");
   static_assert(kBM * kLD * 4 <= kStages * kStage, "staged partial tile must fit in the ring");
   static_assert(2 * kBM * 128 + BN * 4 <= kStages * kStage, "epilogue staging and bias must fit in the ring");
 };
@@ -166,6 +171,7 @@ __device__ __forceinline__ void store_tile_tma(uint32_t trow, uint8_t* stage, co
     }
   }
   if (leader) bulk_wait<0>();
+  named_bar_sync(1, 128);  // the staging buffers are free again for a next call
 }
 
 template <typename TO>
@@ -185,11 +191,11 @@ __device__ __forceinline__ void store4<__half>(__half* dst, float4 v) {
   *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<uint2*>(h);
 }
 
-template <typename TO, uint32_t FMT, bool CL, int BN>
+template <typename TO, uint32_t FMT, bool CL, int BN, int MS>
 __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                   const __grid_constant__ CUtensorMap tm_y, TO* out, float* ws, FwdParams fp, unsigned* err) {
-  using T = Tile<BN>;
+  using T = Tile<BN, MS>;
   constexpr int kStages = T::kStages, kStage = T::kStage, kB = T::kB, kLD = T::kLD;
   constexpr uint32_t kTmemCols = T::kTmemCols;
   extern __shared__ uint8_t smem_raw[];
@@ -209,11 +215,11 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
   const int64_t tn = tile % fp.tiles_n;
   const int64_t tm = tile / fp.tiles_n;
   const int64_t img = tm / fp.tiles_m_per_img;
-  const int64_t ho0 = (tm % fp.tiles_m_per_img) * fp.TR;
+  const int64_t ho0 = (tm % fp.tiles_m_per_img) * fp.TR * MS;  // sub-tile h starts at row ho0 + h * TR
   const int64_t k0 = tn * BN;
   const int64_t b0 = slice_begin(fp.blocks, fp.split, sigma);
   const int64_t nblk = slice_begin(fp.blocks, fp.split, sigma + 1) - b0;
-  const uint32_t tx = (uint32_t)(fp.TR * fp.Wo * 128 + kB);
+  const uint32_t tx = (uint32_t)(MS * fp.TR * fp.Wo * 128 + kB);
 
   // Producer state (thread 0): the ring stage and its round's parity, and
   // the next block's (r, s, c-block), all advanced by increments.
@@ -225,9 +231,11 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
   auto issue = [&]() {
     uint8_t* st = smem + (size_t)ps * kStage;
     mbar_arrive_expect_tx(&full[ps], tx);
-    tma_load_4d(st, &tm_x, cb * kBK, sx * fp.dw - fp.pw, (int32_t)ho0 * fp.sh + r * fp.dh - fp.ph, (int32_t)img,
-                &full[ps]);
-    tma_load_2d(st + kA, &tm_w, rs * cg + cb * kBK, (int32_t)k0, &full[ps]);
+#pragma unroll
+    for (int h = 0; h < MS; ++h)  // a sub-tile past the image reads zeros (and is not stored)
+      tma_load_4d(st + h * kA, &tm_x, cb * kBK, sx * fp.dw - fp.pw,
+                  (int32_t)(ho0 + h * fp.TR) * fp.sh + r * fp.dh - fp.ph, (int32_t)img, &full[ps]);
+    tma_load_2d(st + MS * kA, &tm_w, rs * cg + cb * kBK, (int32_t)k0, &full[ps]);
     if (++cb == cblocks) {
       cb = 0;
       ++rs;
@@ -286,13 +294,16 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
       for (int64_t j = 0; j < nblk; ++j) {
         if (!mbar_wait(&full[s], ph, abort_flag, err)) break;
         tc_fence_after();
-        const uint32_t a = base + (uint32_t)(s * kStage), b = a + kA;
+        const uint32_t a = base + (uint32_t)(s * kStage), b = a + MS * kA;
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
           // K-major SW128: 8-row groups 1024 B apart; a K step of 16 elements is
           // a 32-byte advance inside the swizzled 128-byte row.
-          mma_f16(tmem, smem_desc_sw128(a + 32u * kk, 16, 1024), smem_desc_sw128(b + 32u * kk, 16, 1024), IDESC,
-                  (j > 0 || kk > 0) ? 1u : 0u);
+          const uint64_t bd = smem_desc_sw128(b + 32u * kk, 16, 1024);
+#pragma unroll
+          for (int h = 0; h < MS; ++h)
+            mma_f16(tmem + (uint32_t)(h * BN), smem_desc_sw128(a + (uint32_t)(h * kA) + 32u * kk, 16, 1024), bd,
+                    IDESC, (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&empty[s]);
         if (++s == kStages) {
@@ -327,25 +338,31 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
           *reinterpret_cast<float4*>(part + 32 * j + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
       }
     } else {
-      // Y (or slab sigma of the workspace, fp32) as [N (x S)][Ho*Wo][K].
+      // Y (or slab sigma of the workspace, fp32) as [N (x S)][Ho*Wo][K], one
+      // M sub-tile (accumulator columns h * BN ..) after the other.
       const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
       uint8_t* stage = smem;  // the ring is idle: every copy landed, every MMA completed
-      const int32_t py = (int32_t)(ho0 * fp.Wo);
-      if (ws)
-        store_tile_tma<float, BN>(trow, stage, &tm_y, (int32_t)k0, (int32_t)fp.K, py, (int32_t)(sigma * fp.N + img),
-                                  m, nblk > 0, threadIdx.x == 128, ok);
-      else {
-        // The epilogue's bias for the tile's BN channels, as fp32 in shared memory
-        // past the two staging buffers (0 beyond K or without a bias).
-        float* sbias = reinterpret_cast<float*>(smem + 2 * kBM * 128);
-        if (fp.ep) {
-          const TO* bias = static_cast<const TO*>(fp.ep_bias);
-          for (int i = threadIdx.x - 128; i < BN; i += 128)
-            sbias[i] = bias && k0 + i < fp.K ? to_f32(bias[k0 + i]) : 0.f;
-          named_bar_sync(1, 128);
-        }
-        store_tile_tma<TO, BN>(trow, stage, &tm_y, (int32_t)k0, (int32_t)fp.K, py, (int32_t)img, m, nblk > 0,
-                               threadIdx.x == 128, ok, sbias, fp.ep_lo, fp.ep_hi, fp.ep != 0);
+      // The epilogue's bias for the tile's BN channels, as fp32 in shared memory
+      // past the two staging buffers (0 beyond K or without a bias).
+      float* sbias = reinterpret_cast<float*>(smem + 2 * kBM * 128);
+      if (!ws && fp.ep) {
+        const TO* bias = static_cast<const TO*>(fp.ep_bias);
+        for (int i = threadIdx.x - 128; i < BN; i += 128)
+          sbias[i] = bias && k0 + i < fp.K ? to_f32(bias[k0 + i]) : 0.f;
+        named_bar_sync(1, 128);
+      }
+#pragma unroll 1
+      for (int h = 0; h < MS; ++h) {
+        const int64_t hrow = ho0 + h * fp.TR;
+        if (hrow >= fp.Ho) break;  // a sub-tile past the image (uniform over the 128 threads)
+        const int32_t py = (int32_t)(hrow * fp.Wo);
+        if (ws)
+          store_tile_tma<float, BN>(trow + (uint32_t)(h * BN), stage, &tm_y, (int32_t)k0, (int32_t)fp.K, py,
+                                    (int32_t)(sigma * fp.N + img), m, nblk > 0, threadIdx.x == 128, ok);
+        else
+          store_tile_tma<TO, BN>(trow + (uint32_t)(h * BN), stage, &tm_y, (int32_t)k0, (int32_t)fp.K, py,
+                                 (int32_t)img, m, nblk > 0, threadIdx.x == 128, ok, sbias, fp.ep_lo, fp.ep_hi,
+                                 fp.ep != 0);
       }
     }
   }
@@ -407,7 +424,22 @@ bool fwd_tc_admissible(const Shape& s) {
 // Tile width: 256 output channels when K >= 256 (the two-stage form), else 128.
 int tile_bn(const Shape& s, bool cluster) { return !cluster && s.k >= 256 ? 256 : 128; }
 
-FwdParams make_params(const Plan& p, int bn) {
+// Output rows of an M sub-tile.
+int64_t tile_rows(const Shape& s) { return kBM / s.wo < s.ho ? kBM / s.wo : s.ho; }
+
+// M sub-tiles per CTA: 2 for 256-wide tiles when the grid still has at least
+// 512 such double tiles (over three waves of one CTA per SM here), else 1:
+// the small-M layers keep their many split-K CTAs, and mid-sized grids keep
+// finer waves (a 3x3 stride-2 layer with 256 double tiles measured slower
+// than with 512 single ones).
+int tile_ms(const Shape& s, bool cluster) {
+  if (cluster || tile_bn(s, false) != 256) return 1;
+  const int64_t tr = tile_rows(s);
+  const int64_t pairs = s.n * ((s.ho + 2 * tr - 1) / (2 * tr)) * ((s.k + 255) / 256);
+  return pairs >= 512 ? 2 : 1;
+}
+
+FwdParams make_params(const Plan& p, int bn, int ms) {
   const Shape& s = p.sh;
   FwdParams fp;
   fp.N = s.n;
@@ -418,8 +450,8 @@ FwdParams make_params(const Plan& p, int bn) {
   fp.Cg = s.cg;
   fp.S_f = s.s;
   fp.cblocks = s.cg / kBK;
-  fp.TR = (int32_t)(kBM / s.wo < s.ho ? kBM / s.wo : s.ho);
-  fp.tiles_m_per_img = (s.ho + fp.TR - 1) / fp.TR;
+  fp.TR = (int32_t)tile_rows(s);
+  fp.tiles_m_per_img = (s.ho + (int64_t)ms * fp.TR - 1) / ((int64_t)ms * fp.TR);
   fp.tiles_n = (s.k + bn - 1) / bn;
   fp.tiles = s.n * fp.tiles_m_per_img * fp.tiles_n;
   fp.blocks = s.r * s.s * fp.cblocks;
@@ -432,16 +464,16 @@ FwdParams make_params(const Plan& p, int bn) {
   return fp;
 }
 
-template <typename TO, uint32_t FMT, bool CL, int BN>
+template <typename TO, uint32_t FMT, bool CL, int BN, int MS>
 cudaError_t launch_typed(const Plan& p, const Args& a, CUtensorMapDataType dt) {
   const Shape& s = p.sh;
-  FwdParams fp = make_params(p, BN);
+  FwdParams fp = make_params(p, BN, MS);
   fp.ep_bias = a.ep_bias;
   fp.ep_lo = a.ep_lo;
   fp.ep_hi = a.ep_hi;
   fp.ep = a.ep ? 1 : 0;
   if (a.ep && (CL || a.ws)) return cudaErrorInvalidValue;  // the epilogue runs unsplit only
-  constexpr size_t smem = Tile<BN>::kSmem;
+  constexpr size_t smem = Tile<BN, MS>::kSmem;
   CUtensorMap tm_x, tm_w;
   const uint64_t x_dims[4] = {(uint64_t)s.c, (uint64_t)s.w, (uint64_t)s.h, (uint64_t)s.n};
   const uint64_t x_strides[3] = {(uint64_t)s.c * 2u, (uint64_t)(s.w * s.c) * 2u, (uint64_t)(s.h * s.w * s.c) * 2u};
@@ -476,7 +508,7 @@ cudaError_t launch_typed(const Plan& p, const Args& a, CUtensorMapDataType dt) {
   const int64_t ctas = fp.tiles * p.split;
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (!CL) {
-    auto kern = fwd_tc_kernel<TO, FMT, false, BN>;
+    auto kern = fwd_tc_kernel<TO, FMT, false, BN, MS>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     // Slab sigma starts at ws + sigma * E; the kernel indexes pixels within it.
@@ -485,7 +517,7 @@ cudaError_t launch_typed(const Plan& p, const Args& a, CUtensorMapDataType dt) {
     return cudaGetLastError();
   }
   if (p.split < 1 || p.split > kMaxClusterSplit) return cudaErrorInvalidConfiguration;
-  auto kern = fwd_tc_kernel<TO, FMT, true, BN>;
+  auto kern = fwd_tc_kernel<TO, FMT, true, BN, MS>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   if (p.split > 8) {  // above the portable cluster size
@@ -519,11 +551,11 @@ namespace {
 Geometry geometry_of(const Shape& s, bool cluster) {
   Geometry g;
   if (!fwd_tc_admissible(s)) return g;
-  const int64_t tr = kBM / s.wo < s.ho ? kBM / s.wo : s.ho;
+  const int64_t rows = tile_rows(s) * tile_ms(s, cluster);  // output rows of a CTA's tile
   const int bn = tile_bn(s, cluster);
   g.ok = true;
   g.ctas_per_sm = bn == 256 ? 1 : 2;
-  g.tiles = s.n * ((s.ho + tr - 1) / tr) * ((s.k + bn - 1) / bn);
+  g.tiles = s.n * ((s.ho + rows - 1) / rows) * ((s.k + bn - 1) / bn);
   g.blocks = s.r * s.s * (s.cg / kBK);
   if (cluster) g.max_split = kMaxClusterSplit;
   return g;
@@ -534,20 +566,21 @@ Geometry geometry_fwd_tc(const Shape& s) { return geometry_of(s, false); }
 Geometry geometry_fwd_tc_cluster(const Shape& s) { return geometry_of(s, true); }
 
 namespace {
-template <bool CL, int BN>
+template <bool CL, int BN, int MS>
 cudaError_t launch_bn(const Plan& p, const Args& a) {
   if (p.sh.in_dt == CONV_BF16) {
-    if (p.sh.out_dt == CONV_F32) return launch_typed<float, 1u, CL, BN>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
-    return launch_typed<__nv_bfloat16, 1u, CL, BN>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+    if (p.sh.out_dt == CONV_F32) return launch_typed<float, 1u, CL, BN, MS>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+    return launch_typed<__nv_bfloat16, 1u, CL, BN, MS>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
   }
-  if (p.sh.out_dt == CONV_F32) return launch_typed<float, 0u, CL, BN>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
-  return launch_typed<__half, 0u, CL, BN>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+  if (p.sh.out_dt == CONV_F32) return launch_typed<float, 0u, CL, BN, MS>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+  return launch_typed<__half, 0u, CL, BN, MS>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
 }
 }  // namespace
 
 cudaError_t launch_fwd_tc(const Plan& p, const Args& a) {
-  return tile_bn(p.sh, false) == 256 ? launch_bn<false, 256>(p, a) : launch_bn<false, 128>(p, a);
+  if (tile_bn(p.sh, false) == 128) return launch_bn<false, 128, 1>(p, a);
+  return tile_ms(p.sh, false) == 2 ? launch_bn<false, 256, 2>(p, a) : launch_bn<false, 256, 1>(p, a);
 }
-cudaError_t launch_fwd_tc_cluster(const Plan& p, const Args& a) { return launch_bn<true, 128>(p, a); }
+cudaError_t launch_fwd_tc_cluster(const Plan& p, const Args& a) { return launch_bn<true, 128, 1>(p, a); }
 
 }  // namespace cig

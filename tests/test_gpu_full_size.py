@@ -142,3 +142,34 @@ def test_dgrad3x3_compute_bound_supplement_sampled_images():
         e = relerr(dxc[i:i + 1], ref)
         assert e <= 1e-2, f"image {i}: err {e:.3e}"
     assert cig.device_errors() == 0
+
+
+@pytest.mark.parametrize("direction", ["fwd", "dgrad"])
+def test_two_m_subtiles_with_a_partial_second(direction):
+    """512 images of 14x14 (K = C = 256, 3x3, pad 1, bf16): enough tiles for CTAs with two M
+    sub-tiles of 9 output rows sharing the weight tile, the second one cut at row 14.
+    Images 0, 1 and 511 against the oracle as N=1 problems."""
+    n, hw, c, k = 512, 14, 256, 256
+    p = cig.Problem(n=n, h=hw, w=hw, c=c, k=k, r=3, s=3, pad_h=1, pad_w=1, in_dtype=cig.BF16, out_dtype=cig.BF16)
+    p1 = cig.Problem(n=1, h=hw, w=hw, c=c, k=k, r=3, s=3, pad_h=1, pad_w=1, in_dtype=cig.BF16, out_dtype=cig.BF16)
+    w = synth.tensor((k, 3, 3, c), torch.bfloat16, "normal", 0.0, 0.05, 8, synth.W_ID)
+    orc = oracle.get()
+    if direction == "fwd":
+        info = cig.describe_plan(p, cig.DIR_FWD, -1)
+        assert info["kernel_name"] == "fwd_tc" and info["tiles"] == n  # one double tile per image
+        a = synth.tensor((n, hw, hw, c), torch.bfloat16, "normal", 0.0, 0.05, 8, synth.X_ID)
+        out = torch.empty((n, hw, hw, k), dtype=torch.bfloat16, device="cuda")
+        cig.conv_fwd(p, a.cuda(), w.cuda(), out, cig.workspace(p, cig.DIR_FWD, -1, False), -1)
+    else:
+        info = cig.describe_plan(p, cig.DIR_DGRAD, -1)
+        assert info["kernel_name"] == "dgrad_tc" and info["tiles"] == n
+        a = synth.tensor((n, hw, hw, k), torch.bfloat16, "normal", 0.0, 0.05, 8, synth.DY_ID)
+        out = torch.empty((n, hw, hw, c), dtype=torch.bfloat16, device="cuda")
+        cig.conv_dgrad(p, a.cuda(), w.cuda(), out, cig.workspace(p, cig.DIR_DGRAD, -1, False), -1)
+    torch.cuda.synchronize()
+    got = out.cpu()
+    for i in (0, 1, 511):
+        ref = orc.fwd(oproblem(p1), a[i:i + 1], w) if direction == "fwd" else orc.dgrad(oproblem(p1), a[i:i + 1], w)
+        e = relerr(got[i:i + 1], ref)
+        assert e <= 1e-2, f"{direction} image {i}: err {e:.3e}"
+    assert cig.device_errors() == 0
