@@ -79,6 +79,7 @@ Geometry geometry_wgrad1x1_tf32x3(const Shape& s);
 Geometry geometry_fwd_tc(const Shape& s);
 Geometry geometry_fwd_tc_cluster(const Shape& s);
 Geometry geometry_dgrad_tc(const Shape& s);
+Geometry geometry_fwd_depthwise(const Shape& s);
 // The forward problem a stride-1, ungrouped data gradient equals (dY as the
 // input, the transformed filter, padding dil * (f - 1) - pad).
 Shape dgrad_as_forward(const Shape& s);
@@ -92,6 +93,7 @@ cudaError_t launch_wgrad1x1_tf32x3(const Plan& p, const Args& a);
 cudaError_t launch_fwd_tc(const Plan& p, const Args& a);
 cudaError_t launch_fwd_tc_cluster(const Plan& p, const Args& a);
 cudaError_t launch_dgrad_tc(const Plan& p, const Args& a);
+cudaError_t launch_fwd_depthwise(const Plan& p, const Args& a);
 cudaError_t launch_wgrad_depthwise(const Plan& p, const Args& a);
 cudaError_t launch_wgrad_grouped(const Plan& p, const Args& a);
 // Stage 2: out = cast(sum of slabs) (and the bias slabs into db).

@@ -105,10 +105,12 @@ typedef enum conv_kernel {
                                         thread-block cluster folding through distributed
                                         shared memory [P2 "Changes": single-launch split-K]:
                                         no workspace, no stage 2 */
-  CONV_KERNEL_DGRAD_TC = 8           /* 16-bit, stride-1, ungrouped data gradient: the filter
+  CONV_KERNEL_DGRAD_TC = 8,          /* 16-bit, stride-1, ungrouped data gradient: the filter
                                         rotated 180 degrees with k and c swapped (written into
                                         the workspace), then the forward tensor-core kernel
                                         over dY */
+  CONV_KERNEL_FWD_DEPTHWISE = 9      /* depthwise forward (C = K = groups, C even, filter
+                                        width 3/5/7, W stride 1/2), CUDA cores, unsplit */
 } conv_kernel;
 
 /* What a call with these arguments would run. */

@@ -173,3 +173,25 @@ def test_two_m_subtiles_with_a_partial_second(direction):
         e = relerr(got[i:i + 1], ref)
         assert e <= 1e-2, f"{direction} image {i}: err {e:.3e}"
     assert cig.device_errors() == 0
+
+
+def test_depthwise_7x7_forward_full_sampled_images():
+    """Depthwise 7x7 forward bf16, N=32, 56x56, C=K=384, pad 3 (the depthwise configuration's
+    forward twin), auto: images 0, 17 and 31 against the oracle as N=1 problems."""
+    n, hw, c = 32, 56, 384
+    p = cig.Problem(n=n, h=hw, w=hw, c=c, k=c, r=7, s=7, pad_h=3, pad_w=3, groups=c,
+                    in_dtype=cig.BF16, out_dtype=cig.BF16)
+    assert cig.describe_plan(p, cig.DIR_FWD, -1)["kernel_name"] == "fwd_depthwise"
+    x = synth.tensor((n, hw, hw, c), torch.bfloat16, "normal", 0.0, 1.0, 3, synth.X_ID)
+    w = synth.tensor((c, 7, 7, 1), torch.bfloat16, "normal", 0.0, 1.0, 3, synth.W_ID)
+    y = torch.empty((n, hw, hw, c), dtype=torch.bfloat16, device="cuda")
+    cig.conv_fwd(p, x.cuda(), w.cuda(), y, None, -1)
+    torch.cuda.synchronize()
+    yc = y.cpu()
+    orc = oracle.get()
+    p1 = cig.Problem(n=1, h=hw, w=hw, c=c, k=c, r=7, s=7, pad_h=3, pad_w=3, groups=c,
+                     in_dtype=cig.BF16, out_dtype=cig.BF16)
+    for i in (0, 17, 31):
+        e = relerr(yc[i:i + 1], orc.fwd(oproblem(p1), x[i:i + 1], w))
+        assert e <= 1e-2, f"image {i}: err {e:.3e}"
+    assert cig.device_errors() == 0

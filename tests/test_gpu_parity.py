@@ -248,6 +248,22 @@ def test_forward_tc_strided(shape, dt):
     assert cig.device_errors() == 0
 
 
+@pytest.mark.parametrize("shape", [
+    dict(n=2, h=13, w=17, c=128, k=128, groups=128, r=7, s=7, pad_h=3, pad_w=3),   # 7x7, ragged W chunks
+    dict(n=3, h=9, w=10, c=96, k=96, groups=96, r=3, s=3, pad_h=1, pad_w=1),       # a half channel block
+    dict(n=2, h=14, w=15, c=64, k=64, groups=64, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1),
+    dict(n=1, h=12, w=20, c=64, k=64, groups=64, r=5, s=5, pad_h=4, pad_w=2, dil_h=2),  # H dilation
+    dict(n=2, h=10, w=12, c=32, k=32, groups=32, r=7, s=7),                         # no padding
+    dict(n=1, h=9, w=23, c=64, k=64, groups=64, r=3, s=7, stride_h=3, stride_w=2, pad_h=0, pad_w=3),
+])
+@pytest.mark.parametrize("dt", [(BF16, BF16), (F16, F32), (F32, F32)], ids=lambda d: f"{d[0]}{d[1]}")
+def test_forward_depthwise(shape, dt):
+    p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
+    assert cig.describe_plan(p, cig.DIR_FWD, -1)["kernel_name"] == "fwd_depthwise"
+    check_fwd(p, 13, ["auto", "generic"], [-1, 1])
+    assert cig.device_errors() == 0
+
+
 # ------------------------------------------------------- fused forward epilogue
 
 INF = float("inf")
@@ -267,6 +283,7 @@ def run_fwd_ep(p, x, w, bias, lo, hi, split_k=-1):
     dict(n=2, h=10, w=12, c=128, k=136, r=3, s=3, pad_h=1, pad_w=1),          # tensor cores, K tail
     dict(n=1, h=14, w=14, c=256, k=256, r=3, s=3, pad_h=1, pad_w=1),          # 128 x 256 tiles; conv_fwd would split
     dict(n=2, h=9, w=11, c=12, k=8, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1),  # generic
+    dict(n=2, h=13, w=17, c=96, k=96, groups=96, r=7, s=7, pad_h=3, pad_w=3),             # depthwise kernel
 ])
 @pytest.mark.parametrize("dt", [(BF16, BF16), (F16, F32), (F32, F32)], ids=lambda d: f"{d[0]}{d[1]}")
 def test_forward_fused_epilogue(shape, dt):
