@@ -78,6 +78,8 @@ struct FwdParams {
   int32_t TR;                   // output rows per M tile
   int32_t ph, pw, dh, dw;
   int32_t sh;                   // stride along H (along W it is the X map's traversal stride)
+  int32_t a_coff;               // 1: the X channel coordinate starts at the tile's first output channel
+                                // (block-diagonal grouped problems), 0: at 0
   int32_t split;
   // fused epilogue (unsplit only): y = min(max(acc + bias[k], ep_lo), ep_hi)
   const void* ep_bias;
@@ -233,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
     mbar_arrive_expect_tx(&full[ps], tx);
 #pragma unroll
     for (int h = 0; h < MS; ++h)  // a sub-tile past the image reads zeros (and is not stored)
-      tma_load_4d(st + h * kA, &tm_x, cb * kBK, sx * fp.dw - fp.pw,
+      tma_load_4d(st + h * kA, &tm_x, (fp.a_coff ? (int32_t)k0 : 0) + cb * kBK, sx * fp.dw - fp.pw,
                   (int32_t)(ho0 + h * fp.TR) * fp.sh + r * fp.dh - fp.ph, (int32_t)img, &full[ps]);
     tma_load_2d(st + MS * kA, &tm_w, rs * cg + cb * kBK, (int32_t)k0, &full[ps]);
     if (++cb == cblocks) {
@@ -460,14 +462,16 @@ FwdParams make_params(const Plan& p, int bn, int ms) {
   fp.dh = (int32_t)s.dh;
   fp.dw = (int32_t)s.dw;
   fp.sh = (int32_t)s.sh;
+  fp.a_coff = 0;
   fp.split = p.split;
   return fp;
 }
 
 template <typename TO, uint32_t FMT, bool CL, int BN, int MS>
-cudaError_t launch_typed(const Plan& p, const Args& a, CUtensorMapDataType dt) {
+cudaError_t launch_typed(const Plan& p, const Args& a, CUtensorMapDataType dt, bool block = false) {
   const Shape& s = p.sh;
   FwdParams fp = make_params(p, BN, MS);
+  fp.a_coff = block ? 1 : 0;
   fp.ep_bias = a.ep_bias;
   fp.ep_lo = a.ep_lo;
   fp.ep_hi = a.ep_hi;
@@ -565,15 +569,24 @@ Geometry geometry_of(const Shape& s, bool cluster) {
 Geometry geometry_fwd_tc(const Shape& s) { return geometry_of(s, false); }
 Geometry geometry_fwd_tc_cluster(const Shape& s) { return geometry_of(s, true); }
 
+// A channel-block problem (see launch_fwd_tc_block): 128-wide tiles, one M
+// sub-tile, 2 CTAs per SM; the cluster form's tiling without its split cap.
+Geometry geometry_fwd_tc_block(const Shape& b) {
+  Geometry g = geometry_of(b, true);
+  g.max_split = 0;
+  return g;
+}
+
 namespace {
 template <bool CL, int BN, int MS>
-cudaError_t launch_bn(const Plan& p, const Args& a) {
+cudaError_t launch_bn(const Plan& p, const Args& a, bool block = false) {
   if (p.sh.in_dt == CONV_BF16) {
-    if (p.sh.out_dt == CONV_F32) return launch_typed<float, 1u, CL, BN, MS>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
-    return launch_typed<__nv_bfloat16, 1u, CL, BN, MS>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+    if (p.sh.out_dt == CONV_F32)
+      return launch_typed<float, 1u, CL, BN, MS>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, block);
+    return launch_typed<__nv_bfloat16, 1u, CL, BN, MS>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, block);
   }
-  if (p.sh.out_dt == CONV_F32) return launch_typed<float, 0u, CL, BN, MS>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
-  return launch_typed<__half, 0u, CL, BN, MS>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+  if (p.sh.out_dt == CONV_F32) return launch_typed<float, 0u, CL, BN, MS>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, block);
+  return launch_typed<__half, 0u, CL, BN, MS>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, block);
 }
 }  // namespace
 
@@ -582,5 +595,6 @@ cudaError_t launch_fwd_tc(const Plan& p, const Args& a) {
   return tile_ms(p.sh, false) == 2 ? launch_bn<false, 256, 2>(p, a) : launch_bn<false, 256, 1>(p, a);
 }
 cudaError_t launch_fwd_tc_cluster(const Plan& p, const Args& a) { return launch_bn<true, 128, 1>(p, a); }
+cudaError_t launch_fwd_tc_block(const Plan& p, const Args& a) { return launch_bn<false, 128, 1>(p, a, true); }
 
 }  // namespace cig

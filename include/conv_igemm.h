@@ -109,8 +109,11 @@ typedef enum conv_kernel {
                                         rotated 180 degrees with k and c swapped (written into
                                         the workspace), then the forward tensor-core kernel
                                         over dY */
-  CONV_KERNEL_FWD_DEPTHWISE = 9      /* depthwise forward (C = K = groups, C even, filter
+  CONV_KERNEL_FWD_DEPTHWISE = 9,     /* depthwise forward (C = K = groups, C even, filter
                                         width 3/5/7, W stride 1/2), CUDA cores, unsplit */
+  CONV_KERNEL_FWD_GROUPED_TC = 10    /* 16-bit grouped forward (Cg = Kg dividing 128, C % 128 = 0):
+                                        each 128-channel block as a dense tensor-core forward with
+                                        a block-diagonal filter written into the workspace */
 } conv_kernel;
 
 /* What a call with these arguments would run. */
@@ -158,7 +161,8 @@ conv_status resolve_split_k(const conv_problem* p, conv_dir dir, int32_t request
  * plus S x k x 4 (rounded up to 256) when with_bias and dir is the weight
  * gradient; the data gradient's tensor-core path adds the transformed filter
  * (k x r x s x c elements of in_dtype, rounded up to 256) in front, at every
- * degree. */
+ * degree, and the grouped forward's tensor-core path its block-diagonal
+ * filter (k x r x s x 128 elements of in_dtype, rounded up to 256). */
 conv_status conv_workspace_bytes_for(const conv_problem* p, conv_dir dir, int32_t split_k,
                                      int32_t with_bias, int32_t sm_count, uint64_t* bytes);
 conv_status conv_workspace_bytes(const conv_problem* p, conv_dir dir, int32_t split_k,
@@ -192,8 +196,10 @@ typedef struct conv_epilogue {
 /* Forward with a fused epilogue. A non-identity epilogue cannot be applied
  * per slice, so it runs unsplit [P2 "Review follow-ups": split-K rejects
  * it; "Auto-deduced degree": such specs resolve to 1]: split_k -1, 0 or 1
- * gives one slice, any other degree is CONV_ERR_INVALID_ARG; no workspace is
- * needed. An identity epilogue (or ep == NULL) is exactly conv_fwd. */
+ * gives one slice, any other degree is CONV_ERR_INVALID_ARG; the workspace
+ * is what conv_workspace_bytes reports at degree 1 (0 except for a kernel's
+ * transformed filter). An identity epilogue (or ep == NULL) is exactly
+ * conv_fwd. */
 conv_status conv_fwd_epilogue(const conv_problem* p, const void* x, const void* w, const conv_epilogue* ep,
                               void* y, void* ws, uint64_t ws_bytes, int32_t split_k, void* stream);
 

@@ -195,3 +195,26 @@ def test_depthwise_7x7_forward_full_sampled_images():
         e = relerr(yc[i:i + 1], orc.fwd(oproblem(p1), x[i:i + 1], w))
         assert e <= 1e-2, f"image {i}: err {e:.3e}"
     assert cig.device_errors() == 0
+
+
+@pytest.mark.parametrize("groups", [64, 128], ids=["cpg8", "cpg4"])
+def test_grouped_3x3_forward_full_sampled_images(groups):
+    """Grouped 3x3 forward fp16, N=64, 28x28, C=K=512 (the grouped configuration's forward
+    twin), auto (block-diagonal tensor-core blocks): images 0 and 63 against the oracle."""
+    n, hw, c = 64, 28, 512
+    p = cig.Problem(n=n, h=hw, w=hw, c=c, k=c, r=3, s=3, pad_h=1, pad_w=1, groups=groups,
+                    in_dtype=cig.F16, out_dtype=cig.F16)
+    assert cig.describe_plan(p, cig.DIR_FWD, -1)["kernel_name"] == "fwd_grouped_tc"
+    x = synth.tensor((n, hw, hw, c), torch.float16, "normal", 0.0, 1.0, 4, synth.X_ID)
+    w = synth.tensor((c, 3, 3, c // groups), torch.float16, "normal", 0.0, 1.0, 4, synth.W_ID)
+    y = torch.empty((n, hw, hw, c), dtype=torch.float16, device="cuda")
+    cig.conv_fwd(p, x.cuda(), w.cuda(), y, cig.workspace(p, cig.DIR_FWD, -1, False), -1)
+    torch.cuda.synchronize()
+    yc = y.cpu()
+    orc = oracle.get()
+    p1 = cig.Problem(n=1, h=hw, w=hw, c=c, k=c, r=3, s=3, pad_h=1, pad_w=1, groups=groups,
+                     in_dtype=cig.F16, out_dtype=cig.F16)
+    for i in (0, 63):
+        e = relerr(yc[i:i + 1], orc.fwd(oproblem(p1), x[i:i + 1], w))
+        assert e <= 1e-2, f"image {i}: err {e:.3e}"
+    assert cig.device_errors() == 0

@@ -264,6 +264,23 @@ def test_forward_depthwise(shape, dt):
     assert cig.device_errors() == 0
 
 
+@pytest.mark.parametrize("shape", [
+    dict(n=2, h=10, w=12, c=128, k=128, groups=16, r=3, s=3, pad_h=1, pad_w=1),     # cpg 8
+    dict(n=3, h=9, w=9, c=256, k=256, groups=64, r=3, s=3, pad_h=1, pad_w=1),       # cpg 4, two blocks
+    dict(n=1, h=14, w=13, c=128, k=128, groups=64, r=5, s=5, pad_h=2, pad_w=2),     # cpg 2
+    dict(n=2, h=16, w=16, c=384, k=384, groups=24, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1),  # cpg 16
+    dict(n=2, h=7, w=9, c=128, k=128, groups=32, r=1, s=1),                          # pointwise cpg 4
+])
+@pytest.mark.parametrize("dt", [(BF16, BF16), (F16, F32), (F16, F16)], ids=lambda d: f"{d[0]}{d[1]}")
+def test_forward_grouped_tc(shape, dt):
+    """Grouped forwards as block-diagonal dense 128-channel blocks on the tensor cores."""
+    p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
+    assert cig.describe_plan(p, cig.DIR_FWD, -1)["kernel_name"] == "fwd_grouped_tc"
+    check_fwd(p, 14, ["fwd_grouped_tc", "generic"], [-1, 1, 3])
+    check_fwd(p, 14, ["fwd_grouped_tc"], ["max"])
+    assert cig.device_errors() == 0
+
+
 # ------------------------------------------------------- fused forward epilogue
 
 INF = float("inf")
@@ -272,8 +289,9 @@ INF = float("inf")
 def run_fwd_ep(p, x, w, bias, lo, hi, split_k=-1):
     ho, wo = p.out_hw
     y = Guarded(p.n * ho * wo * p.k, TORCH_DT[p.out_dtype])
+    ws = cig.workspace(p, cig.DIR_FWD, 1, False)  # unsplit: a kernel's transformed filter at most
     cig.conv_fwd_epilogue(p, x.cuda(), w.cuda(), y.view, None if bias is None else bias.cuda(), lo, hi,
-                          None, split_k)
+                          ws, split_k)
     torch.cuda.synchronize()
     assert y.intact(), "a write left its buffer"
     return y.view.cpu().reshape(p.n, ho, wo, p.k)
@@ -284,6 +302,7 @@ def run_fwd_ep(p, x, w, bias, lo, hi, split_k=-1):
     dict(n=1, h=14, w=14, c=256, k=256, r=3, s=3, pad_h=1, pad_w=1),          # 128 x 256 tiles; conv_fwd would split
     dict(n=2, h=9, w=11, c=12, k=8, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1),  # generic
     dict(n=2, h=13, w=17, c=96, k=96, groups=96, r=7, s=7, pad_h=3, pad_w=3),             # depthwise kernel
+    dict(n=2, h=10, w=12, c=128, k=128, groups=16, r=3, s=3, pad_h=1, pad_w=1),           # grouped, tensor cores
 ])
 @pytest.mark.parametrize("dt", [(BF16, BF16), (F16, F32), (F32, F32)], ids=lambda d: f"{d[0]}{d[1]}")
 def test_forward_fused_epilogue(shape, dt):
