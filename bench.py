@@ -449,7 +449,7 @@ def run_ours(a, rank, world, local_rank):
         # past the ridge point (flop per byte of the measured peaks) the tensor
         # pipe bounds it, else HBM
         bound = "tensor" if flops / in_bytes > pk["bf16"] * 1e12 / (pk["hbm"] * 1e9) else "hbm"
-    elif kname == "fwd_grouped_tc":
+    elif kname in ("fwd_grouped_tc", "wgrad_grouped_tc"):
         bound = "tensor_blockdiag"
     elif kname in ("wgrad_depthwise", "wgrad_grouped", "fwd_depthwise") or kname == "generic":
         bound = "alu"

@@ -111,9 +111,13 @@ typedef enum conv_kernel {
                                         over dY */
   CONV_KERNEL_FWD_DEPTHWISE = 9,     /* depthwise forward (C = K = groups, C even, filter
                                         width 3/5/7, W stride 1/2), CUDA cores, unsplit */
-  CONV_KERNEL_FWD_GROUPED_TC = 10    /* 16-bit grouped forward (Cg = Kg dividing 128, C % 128 = 0):
+  CONV_KERNEL_FWD_GROUPED_TC = 10,   /* 16-bit grouped forward (Cg = Kg dividing 128, C % 128 = 0):
                                         each 128-channel block as a dense tensor-core forward with
                                         a block-diagonal filter written into the workspace */
+  CONV_KERNEL_WGRAD_GROUPED_TC = 11  /* 16-bit grouped weight gradient (Cg = Kg in 2..32, C % 128 = 0,
+                                        filter width <= 4): per 128-channel block and tap, the dense
+                                        product on the tensor cores with MN-major operands, of which
+                                        the diagonal group blocks are kept */
 } conv_kernel;
 
 /* What a call with these arguments would run. */

@@ -429,8 +429,9 @@ def test_config5_grouped_full(groups):
     """Grouped 3x3 wgrad fp16, N=64, 28x28, C=K=512, groups 64 / 128, pad 1, N(0,1) seed 4."""
     p = cig.Problem(n=64, h=28, w=28, c=512, k=512, r=3, s=3, pad_h=1, pad_w=1, groups=groups,
                     in_dtype=F16, out_dtype=F16)
-    assert cig.describe_plan(p, cig.DIR_WGRAD, -1)["kernel_name"] == "wgrad_grouped"
-    check_wgrad(p, 4, ["auto"], [-1, 1, 9], bias=False)
+    assert cig.describe_plan(p, cig.DIR_WGRAD, -1)["kernel_name"] == "wgrad_grouped_tc"
+    check_wgrad(p, 4, ["auto", "wgrad_grouped"], [-1, 1, 9], bias=False)
+    check_wgrad(p, 4, ["auto"], [-1], bias=True)
     assert cig.device_errors() == 0
 
 
@@ -445,4 +446,23 @@ def test_config5_grouped_full(groups):
 def test_grouped_ragged(shape, dt):
     p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
     check_wgrad(p, 9, ["wgrad_grouped", "generic"], [-1, 1, 3], bias=True)
+    assert cig.device_errors() == 0
+
+
+@pytest.mark.parametrize("shape", [
+    dict(n=3, h=11, w=13, c=128, k=128, groups=16, r=3, s=3, pad_h=1, pad_w=1),    # cpg 8
+    dict(n=2, h=9, w=30, c=256, k=256, groups=64, r=3, s=3, pad_h=1, pad_w=1),     # cpg 4, two blocks
+    dict(n=2, h=7, w=9, c=128, k=128, groups=32, r=3, s=1),                         # cpg 4, 3x1, no padding
+    dict(n=1, h=12, w=12, c=128, k=128, groups=8, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1),  # cpg 16
+    dict(n=2, h=6, w=5, c=128, k=128, groups=4, r=3, s=3, pad_h=1, pad_w=1),       # cpg 32
+    dict(n=2, h=8, w=8, c=128, k=128, groups=64, r=3, s=3, pad_h=1, pad_w=1),      # cpg 2
+])
+@pytest.mark.parametrize("dt", [(F16, F16), (BF16, F32)], ids=lambda d: f"{d[0]}{d[1]}")
+def test_wgrad_grouped_tc(shape, dt):
+    """Grouped weight gradients as block-diagonal dense blocks on the tensor cores (MN-major
+    operands), with the bias gradient summed from the dY tiles."""
+    p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
+    assert cig.describe_plan(p, cig.DIR_WGRAD, -1)["kernel_name"] == "wgrad_grouped_tc"
+    check_wgrad(p, 15, ["wgrad_grouped_tc", "generic"], [-1, 1, 3], bias=True)
+    check_wgrad(p, 15, ["wgrad_grouped_tc"], ["max"], bias=True)
     assert cig.device_errors() == 0
