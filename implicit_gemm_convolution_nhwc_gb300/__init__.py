@@ -26,7 +26,8 @@ STATUS = ["CONV_OK", "CONV_ERR_INVALID_ARG", "CONV_ERR_UNSUPPORTED", "CONV_ERR_W
 EXPORTS = ["conv_status_string", "conv_output_dims", "resolve_split_k_for", "resolve_split_k",
            "conv_workspace_bytes_for", "conv_workspace_bytes", "conv_describe_plan", "conv_fwd",
            "conv_fwd_epilogue", "conv_dgrad", "conv_wgrad", "conv_wgrad_bias", "conv_stage1", "conv_stage2", "conv_batch_split_count",
-           "conv_wgrad_bias_static_ws", "conv_device_errors", "conv_set_kernel_override"]
+           "conv_wgrad_bias_static_ws", "conv_device_errors", "conv_selftest_wait_timeout",
+           "conv_set_kernel_override"]
 
 
 class ConvError(RuntimeError):
@@ -126,6 +127,7 @@ def load(build_if_missing: bool = True):
         "conv_set_kernel_override": ([I32], ctypes.c_int),
         "conv_device_errors": ([ctypes.POINTER(ctypes.c_uint32), I32], ctypes.c_int),
         "conv_wgrad_bias_static_ws": ([P, V, V, V, V, I32, V], ctypes.c_int),
+        "conv_selftest_wait_timeout": ([U64, ctypes.POINTER(ctypes.c_uint32), V], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -305,6 +307,15 @@ def conv_stage2(p: Problem, direction: int, out, db=None, ws=None, split_k: int 
     st = load().conv_stage2(_cp(p), direction, _ptr(out), _ptr(db), _ptr(ws), 0 if ws is None else ws.numel(),
                             split_k, _stream(stream))
     _check(st, "conv_stage2")
+
+
+def selftest_wait_timeout(limit_ns: int = 1_000_000, stream=None) -> bool:
+    """Runs a kernel whose pipeline wait can never complete, bounded by limit_ns: True when
+    the wait gave up as designed (the device error word then has bit 0 set)."""
+    out = ctypes.c_uint32()
+    _check(load().conv_selftest_wait_timeout(limit_ns, ctypes.byref(out), _stream(stream)),
+           "conv_selftest_wait_timeout")
+    return bool(out.value)
 
 
 def device_errors(clear: bool = True) -> int:

@@ -272,6 +272,13 @@ conv_status conv_wgrad_bias_static_ws(const conv_problem* p, const void* x, cons
  * the kernel ends early instead of hanging. clear != 0 resets the word. */
 conv_status conv_device_errors(uint32_t* flags, int32_t clear);
 
+/* Testing aid for the bounded waits: one CTA waits on a pipeline barrier that
+ * nothing ever completes, giving up after limit_ns (1 .. 1e9 ns) of global
+ * time. The kernel returns (no fault, no hang), bit 0 of the device error
+ * word is set (see conv_device_errors) and *gave_up = 1 when the wait gave up
+ * and raised its abort word. Synchronises the stream. */
+conv_status conv_selftest_wait_timeout(uint64_t limit_ns, uint32_t* gave_up, void* stream);
+
 /* Testing aid: force stage 1 to one kernel (CONV_KERNEL_AUTO restores the
  * normal choice). A forced kernel that cannot take a problem makes the call
  * fail with CONV_ERR_UNSUPPORTED. Process-wide, not thread-safe. */

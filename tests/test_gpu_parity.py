@@ -466,3 +466,17 @@ def test_wgrad_grouped_tc(shape, dt):
     check_wgrad(p, 15, ["wgrad_grouped_tc", "generic"], [-1, 1, 3], bias=True)
     check_wgrad(p, 15, ["wgrad_grouped_tc"], ["max"], bias=True)
     assert cig.device_errors() == 0
+
+
+def test_bounded_wait_gives_up_and_the_context_survives():
+    """A pipeline wait that can never complete gives up after its limit (here 1 ms), records
+    the timeout in the device error word and lets the kernel return; the context stays usable
+    (no device fault is involved: the wait simply ends)."""
+    cig.device_errors(clear=True)
+    assert cig.selftest_wait_timeout(1_000_000)
+    assert cig.device_errors(clear=True) & 1
+    assert cig.device_errors(clear=True) == 0
+    # a convolution right after it is correct
+    p = cig.Problem(n=4, h=16, w=16, c=8, k=16)
+    check_wgrad(p, 0, ["auto"], [-1], "uniform", -1.0, 1.0)
+    assert cig.device_errors() == 0

@@ -261,3 +261,11 @@ def test_fused_epilogue_validation_without_a_device():
     assert lib.conv_fwd_epilogue(p, 16, 16, ctypes.byref(ep), 16, None, 0, 4, None) == 1
     ep = cig._CEpilogue(None, 0.0, inf)          # ReLU with NULL tensors
     assert lib.conv_fwd_epilogue(p, None, None, ctypes.byref(ep), None, None, 0, -1, None) == 1
+
+
+def test_selftest_arguments_checked_without_a_device():
+    lib = cig.load()
+    out = ctypes.c_uint32()
+    assert lib.conv_selftest_wait_timeout(0, ctypes.byref(out), None) == 1           # no limit
+    assert lib.conv_selftest_wait_timeout(2_000_000_000, ctypes.byref(out), None) == 1  # over 1 s
+    assert lib.conv_selftest_wait_timeout(1000, None, None) == 1
