@@ -98,27 +98,25 @@ __device__ __forceinline__ void row_pass(const uint8_t* xrow, const uint8_t* dyr
 #pragma unroll
   for (int j = 0; j < S; ++j) load_x(wo_a + j, win[j]);
   int wo = wo_a;
-  {
-    for (; wo + S <= wo_b; wo += S) {
+  for (; wo + S <= wo_b; wo += S) {
 #pragma unroll
-      for (int t = 0; t < S; ++t) {
-        const float2 d = *reinterpret_cast<const float2*>(dp + (wo + t) * kPix);
-        if constexpr (CPG == 1) {
+    for (int t = 0; t < S; ++t) {
+      const float2 d = *reinterpret_cast<const float2*>(dp + (wo + t) * kPix);
+      if constexpr (CPG == 1) {
 #pragma unroll
-          for (int j = 0; j < S; ++j) acc.v[j][0][0] = fma2(d, win[(t + j) % S][0], acc.v[j][0][0]);
-        } else {
-          const float2 d0 = make_float2(d.x, d.x), d1 = make_float2(d.y, d.y);
+        for (int j = 0; j < S; ++j) acc.v[j][0][0] = fma2(d, win[(t + j) % S][0], acc.v[j][0][0]);
+      } else {
+        const float2 d0 = make_float2(d.x, d.x), d1 = make_float2(d.y, d.y);
 #pragma unroll
-          for (int j = 0; j < S; ++j)
+        for (int j = 0; j < S; ++j)
 #pragma unroll
-            for (int c = 0; c < CP; ++c) {
-              acc.v[j][0][c] = fma2(d0, win[(t + j) % S][c], acc.v[j][0][c]);
-              acc.v[j][1][c] = fma2(d1, win[(t + j) % S][c], acc.v[j][1][c]);
-            }
-        }
-        if (BIAS) bsum = __fadd2_rn(bsum, d);
-        if (t + 1 < S || wo + S < wo_b) load_x(wo + t + S, win[t]);
+          for (int c = 0; c < CP; ++c) {
+            acc.v[j][0][c] = fma2(d0, win[(t + j) % S][c], acc.v[j][0][c]);
+            acc.v[j][1][c] = fma2(d1, win[(t + j) % S][c], acc.v[j][1][c]);
+          }
       }
+      if (BIAS) bsum = __fadd2_rn(bsum, d);
+      if (t + 1 < S || wo + S < wo_b) load_x(wo + t + S, win[t]);
     }
   }
   for (; wo < wo_b; ++wo) {  // the last (wo_b - wo_a) % S pixels

@@ -42,7 +42,6 @@ struct GwParams {
   int64_t tiles_per_img;  // ceil(Ho / TR)
   int64_t blocks;         // N * tiles_per_img (the split-K reduction blocks)
   int64_t kblocks;        // K / 128
-  int32_t rows_per_tap_group;  // 1: a CTA owns the S taps of one filter row
   int32_t split;
   int64_t E;              // dW elements (one slab)
 };
@@ -266,7 +265,6 @@ cudaError_t launch_typed(const Plan& p, const Args& a, CUtensorMapDataType dt) {
   gp.tiles_per_img = (s.ho + gp.TR - 1) / gp.TR;
   gp.blocks = s.n * gp.tiles_per_img;
   gp.kblocks = s.k / kCB;
-  gp.rows_per_tap_group = 1;
   gp.split = p.split;
   gp.E = s.w_elems();
   CUtensorMap tm_dy, tm_x;

@@ -480,3 +480,25 @@ def test_bounded_wait_gives_up_and_the_context_survives():
     p = cig.Problem(n=4, h=16, w=16, c=8, k=16)
     check_wgrad(p, 0, ["auto"], [-1], "uniform", -1.0, 1.0)
     assert cig.device_errors() == 0
+
+
+@pytest.mark.parametrize("shape", [
+    dict(h=9, w=11, c=128, k=128, groups=16, r=3, s=3, pad_h=1, pad_w=1, in_dtype=F16, out_dtype=F16),   # grouped
+    dict(h=9, w=11, c=64, k=64, groups=64, r=7, s=7, pad_h=3, pad_w=3, in_dtype=BF16, out_dtype=BF16),   # depthwise
+    dict(h=14, w=14, c=128, k=256, r=3, s=3, pad_h=1, pad_w=1, in_dtype=BF16, out_dtype=F32),            # dense 16-bit
+])
+def test_empty_batch_every_direction(shape):
+    """N = 0: the weight and bias gradients are exactly zero, the forward, the fused forward
+    and the data gradient write nothing and fail nothing."""
+    p = cig.Problem(n=0, **shape)
+    x, dy = inputs(p, 3)
+    dw, db = run_wgrad(p, x, dy, -1, True)
+    assert torch.count_nonzero(dw.float()) == 0 and torch.count_nonzero(db.float()) == 0
+    xw = inputs(p, 3, direction=cig.DIR_FWD)
+    assert run_fwd(p, xw[0], xw[1], -1).numel() == 0
+    assert run_dgrad(p, dy, xw[1], -1).numel() == 0
+    ho, wo = p.out_hw
+    y = torch.empty(0, dtype=TORCH_DT[p.out_dtype], device="cuda")
+    cig.conv_fwd_epilogue(p, xw[0].cuda(), xw[1].cuda(), y, None, 0.0, INF, None, -1)
+    torch.cuda.synchronize()
+    assert cig.device_errors() == 0
