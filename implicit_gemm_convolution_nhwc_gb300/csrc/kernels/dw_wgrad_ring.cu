@@ -1,0 +1,540 @@
+// 16-bit depthwise weight gradient (+ bias gradient) for square F x F filters
+// (3, 5, 7), unit stride and dilation, with the filter taps in registers and
+// the input rows streamed by TMA:
+//
+//   dW[c, r, s] = sum over (n, ho, wo) of dY[n, ho, wo, c] * X[n, ho + r - ph, wo + s - pw, c]
+//   db[c]       = sum over (n, ho, wo) of dY[n, ho, wo, c]
+//
+// ("perf(rocke): depthwise 7x7 and grouped cpg4/8 wgrad on batched mfma
+// 4x4x4", "Technical Details".)
+//
+// A CTA owns 64 channels and a split-K slice [q_b, q_e) of the (n, ho) output
+// rows, and walks it TR output rows (one step) at a time. Output row (n, ho)
+// reads input rows ho - ph .. ho - ph + F - 1 of image n; consecutive rows of
+// one image share F - 1 of them, so the slice's input rows form one sequence
+// (a new image starts F fresh rows) streamed through a ring of shared-memory
+// row buffers, each the box {64 channels, W columns} of one row (TMA fills
+// rows outside the image, and channels past C, with zeros). A step's dY rows
+// sit in its step slot, each padded with zero columns on both sides so that
+// the inner loop reads dY column j in [-(F - 1), pw + W) unguarded. A step
+// slot has one full mbarrier, on which the step's dY rows and the input rows
+// it is the first to read all land, and one empty mbarrier, on which every
+// warp arrives when done with the step. The loads of step S + ahead are
+// issued at step S by lane 0 of warp S mod 16, so the issuing work rotates
+// over the warps; every wait is bounded. The rings hold `slack` steps more
+// than the loads in flight need, so an issue at step S only reuses slots that
+// steps before S - slack used: the warps may drift apart by that many steps
+// before an issuing warp waits for the slowest one.
+//
+// The 16 warps are 8 column groups x 2 tap halves: a warp takes a range of
+// input columns and half of the F*F taps (in row-major tap order) of its lane's
+// two adjacent channels, as packed fp32 pairs. Walking its input columns wi
+// left to right, column wi meets output pixel wo = wi + pw - s through tap
+// column s, so the lane keeps the last F dY pairs in a register window and
+// does one packed FMA (__ffma2_rn) per tap it holds per column, from
+// four-byte shared-memory loads. At the end the column groups' sums are added
+// in group order, one filter row at a time (deterministic), and the tile goes
+// out as contiguous fp32 to slab sigma of the workspace or, unsplit, rounded
+// into dW / db.
+#include "tc_common.cuh"
+
+namespace cig {
+namespace {
+
+constexpr int kThreads = 512;  // 16 warps, 128 registers a thread
+constexpr int kWarps = kThreads / 32;
+constexpr int kGroups = kWarps / 2;  // column groups
+constexpr int kCB = 64;              // channels per CTA (2 per lane)
+constexpr int kMaxDepth = 5;         // ahead + slack, at most
+constexpr size_t kSmemLimit = 227 * 1024;
+
+struct RingParams {
+  int64_t C, Ho;
+  int64_t rows;     // N * Ho: the reduction blocks
+  int64_t cblocks;  // ceil(C / 64): the tiles
+  int32_t W, Wo, ph, pw;
+  int32_t CW;       // input columns of a column group
+  int32_t RX, RS;   // ring slots: input rows, steps
+  int32_t TR;       // output rows a step
+  int32_t ahead;    // steps between a load's issue and its use
+  int32_t split;
+};
+
+// Static shared memory of the F form (the group-order reduction).
+constexpr size_t static_smem(int F) {
+  return (size_t)kGroups * F * 2 * 32 * 4 + (size_t)kCB * F * F * 4 + kCB * 4;
+}
+
+// Columns of a dY ring slot: F - 1 zero columns, then dY columns 0 .. Wo - 1,
+// then zero columns up to column pw + W - 1.
+int64_t dy_slot_cols(int64_t W, int64_t pw, int64_t F) { return F - 1 + pw + W; }
+
+// Ring depth d = ahead + slack (in steps of TR rows): d + 1 step slots. The
+// steps from S - slack to S + ahead cover m = (d + 1) TR - 1 row advances,
+// each +1 input row or +F at an image start (at most ceil(m / Ho) of those);
+// the input-row ring holds what they read, so that loading step S + ahead
+// only reuses rows that steps before S - slack read.
+int64_t ring_rows(int64_t F, int64_t Ho, int64_t d, int64_t tr) {
+  const int64_t m = (d + 1) * tr - 1;
+  return m + F + (F - 1) * ((m + Ho - 1) / Ho);
+}
+int ahead_of_depth(int d) { return d >= 3 ? 2 : 1; }
+
+size_t ring_smem(const Shape& s, int d, int tr) {
+  const int64_t rx = ring_rows(s.s, s.ho, d, tr), rs = 1 + d;
+  return (size_t)(rx * s.w * 128 + rs * tr * dy_slot_cols(s.w, s.pw, s.s) * 128 + 2 * rs * 8 + rs * 4 + 16);
+}
+
+struct RingShape {
+  int d = 0, tr = 0;
+};
+
+// Two rows a step and the deepest ring that fits (up to kMaxDepth), else one
+// row a step ({0, 0}: none fits).
+RingShape ring_shape(const Shape& s) {
+  for (int tr = 2; tr >= 1; --tr)
+    for (int d = kMaxDepth; d >= 2; --d)
+      if (ring_smem(s, d, tr) + static_smem((int)s.s) <= kSmemLimit) return RingShape{d, tr};
+  if (ring_smem(s, 1, 1) + static_smem((int)s.s) <= kSmemLimit) return RingShape{1, 1};
+  return RingShape{};
+}
+
+// A 16-bit pair from shared memory (32-bit shared address), widened to fp32.
+template <typename T>
+__device__ __forceinline__ float2 lds2(uint32_t a);
+template <>
+__device__ __forceinline__ float2 lds2<__nv_bfloat16>(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+  return make_float2(__uint_as_float(__byte_perm(v, 0u, 0x1044u)), __uint_as_float(v & 0xffff0000u));
+}
+template <>
+__device__ __forceinline__ float2 lds2<__half>(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+  __half2 h;
+  memcpy(&h, &v, sizeof(h));
+  return __half22float2(h);
+}
+
+// An output row's place: the ring slot of the first input row it reads, and
+// its (image, output row). Advanced one row at a time, so the loop does no
+// 64-bit division.
+struct RowPos {
+  int32_t xs;
+  int32_t ho, n;
+  bool first;  // the slice's first row: all F input rows are new
+  __device__ __forceinline__ int fresh(int F) const { return first || ho == 0 ? F : 1; }
+  __device__ __forceinline__ int32_t slot(int r, const RingParams& p) const {
+    return xs + r >= p.RX ? xs + r - p.RX : xs + r;
+  }
+  __device__ __forceinline__ void advance(int F, const RingParams& p) {
+    const bool cross = ++ho == p.Ho;
+    if (cross) {
+      ho = 0;
+      ++n;
+    }
+    xs += cross ? F : 1;
+    if (xs >= p.RX) xs -= p.RX;
+    first = false;
+  }
+};
+
+// A step's slot in the step ring and its wrap count (the slot's mbarrier
+// phase parity is the wrap count & 1).
+struct StepPos {
+  int32_t ss;
+  uint32_t sw;
+  __device__ __forceinline__ void advance(const RingParams& p) {
+    if (++ss == p.RS) {
+      ss = 0;
+      ++sw;
+    }
+  }
+};
+
+struct Ring {
+  const CUtensorMap* tm_x;
+  const CUtensorMap* tm_dy;
+  uint8_t* xring;
+  uint8_t* dring;
+  uint64_t* full;
+  uint64_t* empty;
+  int32_t* siss;  // wrap count of the last step loaded into each step slot (-1: none)
+  volatile uint32_t* abort_flag;
+  unsigned* err;
+  uint32_t rowX, rowD, txD;
+  int32_t c0;
+};
+
+// Loads a step: the dY rows of its `rows` output rows (the first at row
+// position a) and the input rows they are the first to read, all landing on
+// the step slot's full mbarrier, once every warp is done with the slot's
+// previous step. False: the wait gave up.
+template <int F>
+__device__ bool issue_step(const Ring& g, const RingParams& p, RowPos a, StepPos st, int32_t rows) {
+  if (st.sw > 0 && !mbar_wait(&g.empty[st.ss], (st.sw - 1u) & 1u, g.abort_flag, g.err)) return false;
+  uint32_t bytes = 0;
+  {
+    RowPos b = a;
+    for (int32_t j = 0; j < rows; ++j, b.advance(F, p)) bytes += g.txD + (uint32_t)b.fresh(F) * g.rowX;
+  }
+  uint64_t* bar = &g.full[st.ss];
+  mbar_arrive_expect_tx(bar, bytes);
+  for (int32_t j = 0; j < rows; ++j, a.advance(F, p)) {
+    tma_load_4d(g.dring + ((size_t)st.ss * p.TR + j) * g.rowD + (size_t)(F - 1) * 128, g.tm_dy, g.c0, 0, a.ho, a.n,
+                bar);
+    for (int r = F - a.fresh(F); r < F; ++r)
+      tma_load_4d(g.xring + (size_t)a.slot(r, p) * g.rowX, g.tm_x, g.c0, 0, a.ho - p.ph + r, a.n, bar);
+  }
+  g.siss[st.ss] = (int32_t)st.sw;
+  return true;
+}
+
+// The taps a half holds: T0 .. T0 + NT - 1 in row-major order, in filter rows
+// R0 .. R0 + NR - 1.
+template <int F, int HALF>
+struct Taps {
+  static constexpr int NA = (F * F + 1) / 2;
+  static constexpr int T0 = HALF ? NA : 0;
+  static constexpr int NT = HALF ? F * F - NA : NA;
+  static constexpr int R0 = T0 / F;
+  static constexpr int NR = (T0 + NT - 1) / F - R0 + 1;
+};
+
+// One column sweep of a warp over NROWS output rows of one image (NROWS = 2:
+// rows ho and ho + 1, which share all but one of their input rows): dY row j
+// at dy0[j] (column c at dy0[j] + c * 128), input row R0 + i of the first row
+// at xs[i]. For each input column u in [u_beg, u_end) the lane loads the dY
+// pair of every row and the input pair of every row in reach (32-bit shared
+// addresses), then adds tap
+// (r, s) of row j as x[r + j][u] * dY_j[u + pw - s], in a fixed order.
+template <typename TI, int F, int HALF, int NROWS>
+__device__ __forceinline__ void sweep(float2 (&acc)[Taps<F, HALF>::NT], float2& bsum,
+                                      const uint32_t (&dy0)[NROWS],
+                                      const uint32_t (&xs)[Taps<F, HALF>::NR + NROWS - 1], int32_t u_beg,
+                                      int32_t u_end, int32_t pw, bool group0) {
+  using TP = Taps<F, HALF>;
+  constexpr int NX = TP::NR + NROWS - 1;
+  const float2 zero = make_float2(0.f, 0.f);
+  // Window slot ((u - u_beg) mod F) of row j holds its dY column pw + u;
+  // before u = u_beg it holds columns pw + u_beg - F + 1 .. pw + u_beg - 1.
+  // Column group 0's window covers the columns below pw, which no group's
+  // columns reach, so it adds those to the bias sum.
+  float2 dwin[NROWS][F];
+#pragma unroll
+  for (int j = 0; j < NROWS; ++j) {
+    dwin[j][0] = zero;
+#pragma unroll
+    for (int k = 1; k < F; ++k) {
+      dwin[j][F - k] = lds2<TI>(dy0[j] + (uint32_t)((pw + u_beg - k) * 128));
+      if (HALF == 0 && group0) bsum = __fadd2_rn(bsum, dwin[j][F - k]);
+    }
+  }
+  // F columns from u0 (cnt < F: only the first cnt, at the end of the range)
+  auto columns = [&](int32_t u0, int32_t cnt) {
+#pragma unroll
+    for (int t = 0; t < F; ++t) {
+      if (t < cnt) {
+        const int32_t u = u0 + t;  // input column wi
+#pragma unroll
+        for (int j = 0; j < NROWS; ++j) {
+          dwin[j][t] = lds2<TI>(dy0[j] + (uint32_t)((pw + u) * 128));
+          if (HALF == 0) bsum = __fadd2_rn(bsum, dwin[j][t]);
+        }
+        float2 xv[NX];
+#pragma unroll
+        for (int i = 0; i < NX; ++i) xv[i] = lds2<TI>(xs[i] + (uint32_t)(u * 128));
+#pragma unroll
+        for (int j = 0; j < NROWS; ++j)
+#pragma unroll
+          for (int i = 0; i < TP::NT; ++i) {
+            const int tau = TP::T0 + i, r = tau / F, s = tau % F;
+            acc[i] = __ffma2_rn(xv[r - TP::R0 + j], dwin[j][(t - s + F) % F], acc[i]);
+          }
+      }
+    }
+  };
+  int32_t u0 = u_beg;
+#pragma unroll 1
+  for (; u0 + F <= u_end; u0 += F) columns(u0, F);
+  if (u0 < u_end) columns(u0, u_end - u0);
+}
+
+template <typename TI, int F, int HALF>
+__device__ __forceinline__ void run_half(const Ring& g, const RingParams& p, int64_t q_b, int64_t q_e,
+                                         float (*red)[F][2][32], float* res, float* resb) {
+  using TP = Taps<F, HALF>;
+  constexpr int FF = F * F;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, grp = warp >> 1;
+  const float2 zero = make_float2(0.f, 0.f);
+  float2 acc[TP::NT];
+#pragma unroll
+  for (int i = 0; i < TP::NT; ++i) acc[i] = zero;
+  float2 bsum = zero;
+  const int32_t u_beg = grp * p.CW;
+  const int32_t u_end = u_beg + p.CW < p.W ? u_beg + p.CW : p.W;
+
+  RowPos cur{0, (int32_t)(q_b % p.Ho), (int32_t)(q_b / p.Ho), true};
+  StepPos sc{0, 0u};
+  RowPos la = cur;  // first row of the step loaded for at step S: S + ahead
+  StepPos sl{0, 0u};
+  for (int i = 0; i < p.ahead * p.TR && q_b + i < q_e; ++i) la.advance(F, p);
+  for (int i = 0; i < p.ahead; ++i) sl.advance(p);
+  int32_t issuer = 0;  // warp that loads at step S: S mod 16
+  int64_t qa = q_b + (int64_t)p.ahead * p.TR;  // first row of step S + ahead
+
+  for (int64_t q = q_b; q < q_e; q += p.TR) {
+    const int32_t rows = q_e - q < p.TR ? (int32_t)(q_e - q) : p.TR;
+    if (warp == issuer && lane == 0 && qa < q_e)
+      issue_step<F>(g, p, la, sl, q_e - qa < p.TR ? (int32_t)(q_e - qa) : p.TR);
+    // Lanes that spin on an mbarrier can hold up a divergent lane of the same
+    // warp; reconverge before any of them waits.
+    __syncwarp();
+    for (int32_t j = 0; j < p.TR && qa < q_e; ++j, ++qa) la.advance(F, p);
+    sl.advance(p);
+    issuer = (issuer + 1) & (kWarps - 1);
+
+    if (!__all_sync(0xffffffffu, mbar_wait(&g.full[sc.ss], sc.sw & 1u, g.abort_flag, g.err))) break;
+
+    // dY row j of the step: column c at dy_row(j) + c * 128 (zero for c < 0 and c >= Wo)
+    auto dy_row = [&](int32_t j) {
+      return smem_u32(g.dring + ((size_t)sc.ss * p.TR + j) * g.rowD + (size_t)(F - 1) * 128 + lane * 4);
+    };
+    auto x_row = [&](int r) { return smem_u32(g.xring + (size_t)cur.slot(r, p) * g.rowX + lane * 4); };
+    if (rows == 2 && cur.ho + 1 < p.Ho) {  // two rows of one image: one sweep
+      if (u_beg < u_end) {
+        const uint32_t dy0[2] = {dy_row(0), dy_row(1)};
+        uint32_t xs[TP::NR + 1];
+#pragma unroll
+        for (int i = 0; i <= TP::NR; ++i) xs[i] = x_row(TP::R0 + i);
+        sweep<TI, F, HALF, 2>(acc, bsum, dy0, xs, u_beg, u_end, p.pw, grp == 0);
+      }
+      cur.advance(F, p);
+      cur.advance(F, p);
+    } else {
+#pragma unroll 1
+      for (int32_t j = 0; j < rows; ++j, cur.advance(F, p)) {
+        if (u_beg >= u_end) continue;
+        const uint32_t dy0[1] = {dy_row(j)};
+        uint32_t xs[TP::NR];
+#pragma unroll
+        for (int i = 0; i < TP::NR; ++i) xs[i] = x_row(TP::R0 + i);
+        sweep<TI, F, HALF, 1>(acc, bsum, dy0, xs, u_beg, u_end, p.pw, grp == 0);
+      }
+    }
+
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&g.empty[sc.ss]);
+    __syncwarp();
+    sc.advance(p);
+  }
+  signal_dependents();
+
+  // Group-order sums, one filter row at a time: in round r every warp puts
+  // the taps (r, s) it holds into red[group][s], then thread i adds value
+  // (s, component, lane) = (i / 64, (i / 32) % 2, i % 32) over groups 0..7.
+#pragma unroll
+  for (int r = 0; r < F; ++r) {
+#pragma unroll
+    for (int s = 0; s < F; ++s) {
+      const int tau = r * F + s;
+      if (tau >= TP::T0 && tau < TP::T0 + TP::NT) {
+        red[grp][s][0][lane] = acc[tau - TP::T0].x;
+        red[grp][s][1][lane] = acc[tau - TP::T0].y;
+      }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < F * 64; i += kThreads) {
+      const int s = i >> 6, comp = (i >> 5) & 1, l = i & 31;
+      float sum = red[0][s][comp][l];
+#pragma unroll
+      for (int gg = 1; gg < kGroups; ++gg) sum += red[gg][s][comp][l];
+      res[(2 * l + comp) * FF + r * F + s] = sum;
+    }
+    __syncthreads();
+  }
+  if (HALF == 0) {
+    red[grp][0][0][lane] = bsum.x;
+    red[grp][0][1][lane] = bsum.y;
+  }
+  __syncthreads();
+  if (threadIdx.x < 64) {
+    const int comp = threadIdx.x >> 5, l = threadIdx.x & 31;
+    float sum = red[0][0][comp][l];
+#pragma unroll
+    for (int gg = 1; gg < kGroups; ++gg) sum += red[gg][0][comp][l];
+    resb[2 * l + comp] = sum;
+  }
+}
+
+template <typename TI, typename TO, int F>
+__global__ void __launch_bounds__(kThreads, 1)
+    dw_wgrad_ring_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
+                         TO* out, float* ws, TO* db, float* ws_bias, RingParams p, unsigned* err) {
+  constexpr int FF = F * F;
+  __shared__ float red[kGroups][F][2][32];  // one filter row of every column group's sums, lane-minor
+  __shared__ float res[kCB * FF];           // the tile [64 channels][F][F]
+  __shared__ float resb[kCB];
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int32_t dcols = F - 1 + p.pw + p.W;  // columns of a dY slot
+
+  Ring g;
+  g.tm_x = &tm_x;
+  g.tm_dy = &tm_dy;
+  g.rowX = (uint32_t)p.W * 128u;
+  g.rowD = (uint32_t)dcols * 128u;
+  g.txD = (uint32_t)p.Wo * 128u;
+  g.xring = smem;
+  g.dring = smem + (size_t)p.RX * g.rowX;
+  g.full = reinterpret_cast<uint64_t*>(g.dring + (size_t)p.RS * p.TR * g.rowD);
+  g.empty = g.full + p.RS;
+  g.siss = reinterpret_cast<int32_t*>(g.empty + p.RS);
+  g.abort_flag = reinterpret_cast<volatile uint32_t*>(g.siss + p.RS);
+  g.err = err;
+
+  const int64_t cb = blockIdx.x % p.cblocks;
+  const int32_t sigma = (int32_t)(blockIdx.x / p.cblocks);
+  g.c0 = (int32_t)(cb * kCB);
+  const int64_t q_b = slice_begin(p.rows, p.split, sigma), q_e = slice_begin(p.rows, p.split, sigma + 1);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < p.RS; ++i) {
+      mbar_init(&g.full[i], 1);
+      mbar_init(&g.empty[i], kWarps);
+      g.siss[i] = -1;
+    }
+    *g.abort_flag = 0u;
+    mbar_fence_init();
+    tma_prefetch(&tm_x);
+    tma_prefetch(&tm_dy);
+    // The first `ahead` steps load into fresh slots.
+    RowPos a{0, (int32_t)(q_b % p.Ho), (int32_t)(q_b / p.Ho), true};
+    StepPos st{0, 0u};
+    for (int64_t q = q_b; q < q_e && st.ss < p.ahead; st.advance(p)) {
+      const int32_t rows = q_e - q < p.TR ? (int32_t)(q_e - q) : p.TR;
+      issue_step<F>(g, p, a, st, rows);
+      for (int32_t j = 0; j < rows; ++j, ++q) a.advance(F, p);
+    }
+  }
+  {  // the zero columns of the dY rows (TMA writes only columns F - 1 .. F - 2 + Wo)
+    const int32_t pads = dcols - p.Wo, words = p.RS * p.TR * pads * 32;
+    for (int32_t i = threadIdx.x; i < words; i += kThreads) {
+      const int32_t slot = i / (pads * 32), col = (i / 32) % pads, word = i % 32;
+      const int32_t pos = col < F - 1 ? col : col + p.Wo;
+      reinterpret_cast<uint32_t*>(g.dring + (size_t)slot * g.rowD + (size_t)pos * 128)[word] = 0u;
+    }
+  }
+  __syncthreads();
+
+  if ((threadIdx.x >> 5) & 1)
+    run_half<TI, F, 1>(g, p, q_b, q_e, red, res, resb);
+  else
+    run_half<TI, F, 0>(g, p, q_b, q_e, red, res, resb);
+
+  // No copy may still be landing in shared memory when the CTA exits: wait
+  // for the last step loaded into each step slot (bounded, no early exit).
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < p.RS; ++i)
+      if (g.siss[i] >= 0) mbar_wait(&g.full[i], (uint32_t)g.siss[i] & 1u, nullptr, err);
+  }
+
+  const int64_t nc = p.C - cb * kCB < kCB ? p.C - cb * kCB : kCB;
+  const int64_t E = p.C * FF, base = cb * kCB * FF;  // dW [C][F][F][1]: the tile is contiguous
+  for (int64_t i = threadIdx.x; i < nc * FF; i += kThreads) {
+    if (ws) ws[(int64_t)sigma * E + base + i] = res[i];
+    else store_out(out + base + i, res[i]);
+  }
+  if (db) {
+    for (int64_t i = threadIdx.x; i < nc; i += kThreads) {
+      if (ws_bias) ws_bias[(int64_t)sigma * p.C + cb * kCB + i] = resb[i];
+      else store_out(db + cb * kCB + i, resb[i]);
+    }
+  }
+}
+
+template <typename TI, typename TO, int F>
+cudaError_t launch_f(const Plan& pl, const Args& a, const RingParams& p, CUtensorMapDataType dt) {
+  const Shape& s = pl.sh;
+  CUtensorMap tm_x, tm_dy;
+  const uint64_t x_dims[4] = {(uint64_t)s.c, (uint64_t)s.w, (uint64_t)s.h, (uint64_t)s.n};
+  const uint64_t x_strides[3] = {(uint64_t)s.c * 2u, (uint64_t)(s.w * s.c) * 2u, (uint64_t)(s.h * s.w * s.c) * 2u};
+  const uint32_t x_box[4] = {(uint32_t)kCB, (uint32_t)s.w, 1u, 1u};
+  const uint64_t y_dims[4] = {(uint64_t)s.c, (uint64_t)s.wo, (uint64_t)s.ho, (uint64_t)s.n};
+  const uint64_t y_strides[3] = {(uint64_t)s.c * 2u, (uint64_t)(s.wo * s.c) * 2u, (uint64_t)(s.ho * s.wo * s.c) * 2u};
+  const uint32_t y_box[4] = {(uint32_t)kCB, (uint32_t)s.wo, 1u, 1u};
+  if (!encode_tmap(&tm_x, dt, 4, a.x, x_dims, x_strides, x_box, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_tmap(&tm_dy, dt, 4, a.b, y_dims, y_strides, y_box, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  const size_t smem = ring_smem(s, p.RS - 1, p.TR);
+  auto kern = dw_wgrad_ring_kernel<TI, TO, F>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  const int64_t ctas = pl.geo.tiles * pl.split;
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kern<<<(unsigned)ctas, kThreads, smem, a.stream>>>(tm_x, tm_dy, static_cast<TO*>(a.out), a.ws,
+                                                     pl.with_bias ? static_cast<TO*>(a.db) : nullptr, a.ws_bias, p,
+                                                     device_error_word());
+  return cudaGetLastError();
+}
+
+template <typename TI, typename TO>
+cudaError_t launch_typed(const Plan& pl, const Args& a, CUtensorMapDataType dt) {
+  const Shape& s = pl.sh;
+  RingParams p;
+  p.C = s.c;
+  p.Ho = s.ho;
+  p.rows = s.n * s.ho;
+  p.cblocks = (s.c + kCB - 1) / kCB;
+  p.W = (int32_t)s.w;
+  p.Wo = (int32_t)s.wo;
+  p.ph = (int32_t)s.ph;
+  p.pw = (int32_t)s.pw;
+  p.CW = (int32_t)((s.w + kGroups - 1) / kGroups);
+  const RingShape rs = ring_shape(s);
+  if (rs.d < 1) return cudaErrorInvalidValue;
+  p.ahead = ahead_of_depth(rs.d);
+  p.TR = rs.tr;
+  p.RX = (int32_t)ring_rows(s.s, s.ho, rs.d, rs.tr);
+  p.RS = 1 + rs.d;
+  p.split = pl.split;
+  switch (s.s) {
+    case 3: return launch_f<TI, TO, 3>(pl, a, p, dt);
+    case 5: return launch_f<TI, TO, 5>(pl, a, p, dt);
+    case 7: return launch_f<TI, TO, 7>(pl, a, p, dt);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+Geometry geometry_wgrad_depthwise_ring(const Shape& s) {
+  Geometry g;
+  const bool depthwise = s.groups == s.c && s.groups == s.k;
+  if (!depthwise || s.in_dt == CONV_F32 || s.n < 1) return g;
+  if (s.r != s.s || !(s.s == 3 || s.s == 5 || s.s == 7)) return g;
+  if (s.sh != 1 || s.sw != 1 || s.dh != 1 || s.dw != 1) return g;
+  if (s.pw > s.s - 1 || s.ph > s.r - 1) return g;
+  // TMA: 16-byte row strides, a 64-channel box inside the channel extent,
+  // whole rows of at most 256 columns; coordinates in 32 bits.
+  if (s.c % 8 != 0 || s.c < kCB || s.w > 256 || s.wo > 256) return g;
+  if (s.n > 0x7fffffffLL || s.h + s.r > 0x7fffffffLL) return g;
+  if (ring_shape(s).d < 1) return g;
+  g.ok = true;
+  g.ctas_per_sm = 1;
+  g.tiles = (s.c + kCB - 1) / kCB;
+  g.blocks = s.n * s.ho;
+  return g;
+}
+
+cudaError_t launch_wgrad_depthwise_ring(const Plan& p, const Args& a) {
+  const int in = p.sh.in_dt, out = p.sh.out_dt;
+  if (in == CONV_BF16)
+    return out == CONV_F32 ? launch_typed<__nv_bfloat16, float>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16)
+                           : launch_typed<__nv_bfloat16, __nv_bfloat16>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+  return out == CONV_F32 ? launch_typed<__half, float>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)
+                         : launch_typed<__half, __half>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+}
+
+}  // namespace cig

@@ -426,7 +426,14 @@ Geometry direct_geometry(const Shape& s) {
 
 }  // namespace
 
+// The TMA-ring, register-tap form (dw_wgrad_ring.cu) the depthwise kernel
+// takes for square 3/5/7 filters.
+Geometry geometry_wgrad_depthwise_ring(const Shape& s);
+cudaError_t launch_wgrad_depthwise_ring(const Plan& p, const Args& a);
+
 Geometry geometry_wgrad_depthwise(const Shape& s) {
+  const Geometry reg = geometry_wgrad_depthwise_ring(s);  // square 3/5/7 filters: TMA row rings, taps in registers
+  if (reg.ok) return reg;
   const bool depthwise = s.groups == s.c && s.groups == s.k;
   if (!depthwise || !common_ok(s, 1)) return Geometry{};
   if (!(s.s == 3 || s.s == 5 || s.s == 7 || s.s == 9 || s.s == 11)) return Geometry{};
@@ -440,6 +447,7 @@ Geometry geometry_wgrad_grouped(const Shape& s) {
 }
 
 cudaError_t launch_wgrad_depthwise(const Plan& p, const Args& a) {
+  if (geometry_wgrad_depthwise_ring(p.sh).ok) return launch_wgrad_depthwise_ring(p, a);
   const int in = p.sh.in_dt, out = p.sh.out_dt;
   if (in == CONV_BF16)
     return out == CONV_F32 ? launch_depthwise_t<__nv_bfloat16, float>(p, a)

@@ -416,6 +416,11 @@ def test_config4_depthwise_full():
     dict(n=1, h=12, w=20, c=64, k=64, groups=64, r=3, s=11, pad_h=1, pad_w=5),
     dict(n=2, h=10, w=12, c=64, k=64, groups=64, r=7, s=7),                  # no padding: Wo = W - 6
     dict(n=3, h=5, w=9, c=192, k=192, groups=192, r=7, s=7, pad_h=3, pad_w=3),  # fewer rows than taps
+    dict(n=2, h=11, w=13, c=96, k=96, groups=96, r=7, s=7, pad_h=6, pad_w=6),   # pad F-1, C % 64 != 0
+    dict(n=1, h=4, w=5, c=72, k=72, groups=72, r=3, s=3, pad_h=2, pad_w=0),     # 8 channels in the last tile
+    dict(n=2, h=6, w=70, c=136, k=136, groups=136, r=5, s=5, pad_h=1, pad_w=4),
+    dict(n=2, h=9, w=10, c=64, k=64, groups=64, r=3, s=3, pad_h=1, pad_w=3),    # pad_w = F: shared-memory form
+    dict(n=1, h=3, w=90, c=64, k=64, groups=64, r=7, s=7, pad_h=3, pad_w=3),    # rings one row ahead
 ])
 @pytest.mark.parametrize("dt", [(BF16, BF16), (BF16, F32), (F16, F16)], ids=lambda d: f"{d[0]}{d[1]}")
 def test_depthwise_ragged(shape, dt):
