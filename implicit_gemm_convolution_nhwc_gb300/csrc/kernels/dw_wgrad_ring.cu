@@ -20,30 +20,29 @@
 // slot has one full mbarrier, on which the step's dY rows and the input rows
 // it is the first to read all land, and one empty mbarrier, on which every
 // warp arrives when done with the step. The loads of step S + ahead are
-// issued at step S by lane 0 of warp S mod 16, so the issuing work rotates
+// issued at step S by lane 0 of warp S mod 8, so the issuing work rotates
 // over the warps; every wait is bounded. The rings hold `slack` steps more
 // than the loads in flight need, so an issue at step S only reuses slots that
 // steps before S - slack used: the warps may drift apart by that many steps
 // before an issuing warp waits for the slowest one.
 //
-// The 16 warps are 8 column groups x 2 tap halves: a warp takes a range of
-// input columns and half of the F*F taps (in row-major tap order) of its lane's
-// two adjacent channels, as packed fp32 pairs. Walking its input columns wi
-// left to right, column wi meets output pixel wo = wi + pw - s through tap
-// column s, so the lane keeps the last F dY pairs in a register window and
-// does one packed FMA (__ffma2_rn) per tap it holds per column, from
-// four-byte shared-memory loads. At the end the column groups' sums are added
-// in group order, one filter row at a time (deterministic), and the tile goes
-// out as contiguous fp32 to slab sigma of the workspace or, unsplit, rounded
-// into dW / db.
+// Each of the 8 warps takes a range of input columns, and a lane all F*F
+// taps of its two adjacent channels as packed fp32 pairs. Walking its input
+// columns wi left to right, column wi meets output pixel wo = wi + pw - s
+// through tap column s, so the lane keeps the last F dY pairs of each output
+// row in a register window and does F*F packed FMAs (__ffma2_rn) per row per
+// column, from four-byte shared-memory loads widened to fp32; the two rows of
+// a step within one image share one sweep (and all but one input row). At
+// the end the warps' sums are added in warp order, one filter row at a time
+// (deterministic), and the tile goes out as contiguous fp32 to slab sigma of
+// the workspace or, unsplit, rounded into dW / db.
 #include "tc_common.cuh"
 
 namespace cig {
 namespace {
 
-constexpr int kThreads = 512;  // 16 warps, 128 registers a thread
+constexpr int kThreads = 256;  // 8 warps, up to 255 registers a thread
 constexpr int kWarps = kThreads / 32;
-constexpr int kGroups = kWarps / 2;  // column groups
 constexpr int kCB = 64;              // channels per CTA (2 per lane)
 constexpr int kMaxDepth = 5;         // ahead + slack, at most
 constexpr size_t kSmemLimit = 227 * 1024;
@@ -53,16 +52,16 @@ struct RingParams {
   int64_t rows;     // N * Ho: the reduction blocks
   int64_t cblocks;  // ceil(C / 64): the tiles
   int32_t W, Wo, ph, pw;
-  int32_t CW;       // input columns of a column group
+  int32_t CW;       // input columns of a warp
   int32_t RX, RS;   // ring slots: input rows, steps
   int32_t TR;       // output rows a step
   int32_t ahead;    // steps between a load's issue and its use
   int32_t split;
 };
 
-// Static shared memory of the F form (the group-order reduction).
+// Static shared memory of the F form (the warp-order reduction).
 constexpr size_t static_smem(int F) {
-  return (size_t)kGroups * F * 2 * 32 * 4 + (size_t)kCB * F * F * 4 + kCB * 4;
+  return (size_t)kWarps * F * 2 * 32 * 4 + (size_t)kCB * F * F * 4 + kCB * 4;
 }
 
 // Columns of a dY ring slot: F - 1 zero columns, then dY columns 0 .. Wo - 1,
@@ -191,36 +190,23 @@ __device__ bool issue_step(const Ring& g, const RingParams& p, RowPos a, StepPos
   return true;
 }
 
-// The taps a half holds: T0 .. T0 + NT - 1 in row-major order, in filter rows
-// R0 .. R0 + NR - 1.
-template <int F, int HALF>
-struct Taps {
-  static constexpr int NA = (F * F + 1) / 2;
-  static constexpr int T0 = HALF ? NA : 0;
-  static constexpr int NT = HALF ? F * F - NA : NA;
-  static constexpr int R0 = T0 / F;
-  static constexpr int NR = (T0 + NT - 1) / F - R0 + 1;
-};
-
 // One column sweep of a warp over NROWS output rows of one image (NROWS = 2:
 // rows ho and ho + 1, which share all but one of their input rows): dY row j
-// at dy0[j] (column c at dy0[j] + c * 128), input row R0 + i of the first row
-// at xs[i]. For each input column u in [u_beg, u_end) the lane loads the dY
-// pair of every row and the input pair of every row in reach (32-bit shared
-// addresses), then adds tap
-// (r, s) of row j as x[r + j][u] * dY_j[u + pw - s], in a fixed order.
-template <typename TI, int F, int HALF, int NROWS>
-__device__ __forceinline__ void sweep(float2 (&acc)[Taps<F, HALF>::NT], float2& bsum,
-                                      const uint32_t (&dy0)[NROWS],
-                                      const uint32_t (&xs)[Taps<F, HALF>::NR + NROWS - 1], int32_t u_beg,
-                                      int32_t u_end, int32_t pw, bool group0) {
-  using TP = Taps<F, HALF>;
-  constexpr int NX = TP::NR + NROWS - 1;
+// at dy0[j] (column c at dy0[j] + c * 128), input row i of the first row at
+// xs[i] (32-bit shared addresses). For each input column u in [u_beg, u_end)
+// the lane loads the dY pair of every row and the input pair of every row in
+// reach, then adds tap (r, s) of row j as x[r + j][u] * dY_j[u + pw - s], in a
+// fixed order.
+template <typename TI, int F, int NROWS>
+__device__ __forceinline__ void sweep(float2 (&acc)[F * F], float2& bsum, const uint32_t (&dy0)[NROWS],
+                                      const uint32_t (&xs)[F + NROWS - 1], int32_t u_beg, int32_t u_end, int32_t pw,
+                                      bool warp0) {
+  constexpr int NX = F + NROWS - 1;
   const float2 zero = make_float2(0.f, 0.f);
   // Window slot ((u - u_beg) mod F) of row j holds its dY column pw + u;
   // before u = u_beg it holds columns pw + u_beg - F + 1 .. pw + u_beg - 1.
-  // Column group 0's window covers the columns below pw, which no group's
-  // columns reach, so it adds those to the bias sum.
+  // Warp 0's window covers the columns below pw, which no warp's columns
+  // reach, so it adds those to the bias sum.
   float2 dwin[NROWS][F];
 #pragma unroll
   for (int j = 0; j < NROWS; ++j) {
@@ -228,7 +214,7 @@ __device__ __forceinline__ void sweep(float2 (&acc)[Taps<F, HALF>::NT], float2& 
 #pragma unroll
     for (int k = 1; k < F; ++k) {
       dwin[j][F - k] = lds2<TI>(dy0[j] + (uint32_t)((pw + u_beg - k) * 128));
-      if (HALF == 0 && group0) bsum = __fadd2_rn(bsum, dwin[j][F - k]);
+      if (warp0) bsum = __fadd2_rn(bsum, dwin[j][F - k]);
     }
   }
   // F columns from u0 (cnt < F: only the first cnt, at the end of the range)
@@ -240,7 +226,7 @@ __device__ __forceinline__ void sweep(float2 (&acc)[Taps<F, HALF>::NT], float2& 
 #pragma unroll
         for (int j = 0; j < NROWS; ++j) {
           dwin[j][t] = lds2<TI>(dy0[j] + (uint32_t)((pw + u) * 128));
-          if (HALF == 0) bsum = __fadd2_rn(bsum, dwin[j][t]);
+          bsum = __fadd2_rn(bsum, dwin[j][t]);
         }
         float2 xv[NX];
 #pragma unroll
@@ -248,9 +234,9 @@ __device__ __forceinline__ void sweep(float2 (&acc)[Taps<F, HALF>::NT], float2& 
 #pragma unroll
         for (int j = 0; j < NROWS; ++j)
 #pragma unroll
-          for (int i = 0; i < TP::NT; ++i) {
-            const int tau = TP::T0 + i, r = tau / F, s = tau % F;
-            acc[i] = __ffma2_rn(xv[r - TP::R0 + j], dwin[j][(t - s + F) % F], acc[i]);
+          for (int i = 0; i < F * F; ++i) {
+            const int r = i / F, s = i % F;
+            acc[i] = __ffma2_rn(xv[r + j], dwin[j][(t - s + F) % F], acc[i]);
           }
       }
     }
@@ -261,18 +247,19 @@ __device__ __forceinline__ void sweep(float2 (&acc)[Taps<F, HALF>::NT], float2& 
   if (u0 < u_end) columns(u0, u_end - u0);
 }
 
-template <typename TI, int F, int HALF>
-__device__ __forceinline__ void run_half(const Ring& g, const RingParams& p, int64_t q_b, int64_t q_e,
+// A warp's part of the kernel: the step loop, then its share of the
+// warp-order reduction into res / resb.
+template <typename TI, int F>
+__device__ __forceinline__ void run_warp(const Ring& g, const RingParams& p, int64_t q_b, int64_t q_e,
                                          float (*red)[F][2][32], float* res, float* resb) {
-  using TP = Taps<F, HALF>;
   constexpr int FF = F * F;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, grp = warp >> 1;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float2 zero = make_float2(0.f, 0.f);
-  float2 acc[TP::NT];
+  float2 acc[FF];
 #pragma unroll
-  for (int i = 0; i < TP::NT; ++i) acc[i] = zero;
+  for (int i = 0; i < FF; ++i) acc[i] = zero;
   float2 bsum = zero;
-  const int32_t u_beg = grp * p.CW;
+  const int32_t u_beg = warp * p.CW;
   const int32_t u_end = u_beg + p.CW < p.W ? u_beg + p.CW : p.W;
 
   RowPos cur{0, (int32_t)(q_b % p.Ho), (int32_t)(q_b / p.Ho), true};
@@ -281,7 +268,7 @@ __device__ __forceinline__ void run_half(const Ring& g, const RingParams& p, int
   StepPos sl{0, 0u};
   for (int i = 0; i < p.ahead * p.TR && q_b + i < q_e; ++i) la.advance(F, p);
   for (int i = 0; i < p.ahead; ++i) sl.advance(p);
-  int32_t issuer = 0;  // warp that loads at step S: S mod 16
+  int32_t issuer = 0;  // warp that loads at step S: S mod 8
   int64_t qa = q_b + (int64_t)p.ahead * p.TR;  // first row of step S + ahead
 
   for (int64_t q = q_b; q < q_e; q += p.TR) {
@@ -305,10 +292,10 @@ __device__ __forceinline__ void run_half(const Ring& g, const RingParams& p, int
     if (rows == 2 && cur.ho + 1 < p.Ho) {  // two rows of one image: one sweep
       if (u_beg < u_end) {
         const uint32_t dy0[2] = {dy_row(0), dy_row(1)};
-        uint32_t xs[TP::NR + 1];
+        uint32_t xs[F + 1];
 #pragma unroll
-        for (int i = 0; i <= TP::NR; ++i) xs[i] = x_row(TP::R0 + i);
-        sweep<TI, F, HALF, 2>(acc, bsum, dy0, xs, u_beg, u_end, p.pw, grp == 0);
+        for (int i = 0; i <= F; ++i) xs[i] = x_row(i);
+        sweep<TI, F, 2>(acc, bsum, dy0, xs, u_beg, u_end, p.pw, warp == 0);
       }
       cur.advance(F, p);
       cur.advance(F, p);
@@ -317,10 +304,10 @@ __device__ __forceinline__ void run_half(const Ring& g, const RingParams& p, int
       for (int32_t j = 0; j < rows; ++j, cur.advance(F, p)) {
         if (u_beg >= u_end) continue;
         const uint32_t dy0[1] = {dy_row(j)};
-        uint32_t xs[TP::NR];
+        uint32_t xs[F];
 #pragma unroll
-        for (int i = 0; i < TP::NR; ++i) xs[i] = x_row(TP::R0 + i);
-        sweep<TI, F, HALF, 1>(acc, bsum, dy0, xs, u_beg, u_end, p.pw, grp == 0);
+        for (int i = 0; i < F; ++i) xs[i] = x_row(i);
+        sweep<TI, F, 1>(acc, bsum, dy0, xs, u_beg, u_end, p.pw, warp == 0);
       }
     }
 
@@ -331,39 +318,34 @@ __device__ __forceinline__ void run_half(const Ring& g, const RingParams& p, int
   }
   signal_dependents();
 
-  // Group-order sums, one filter row at a time: in round r every warp puts
-  // the taps (r, s) it holds into red[group][s], then thread i adds value
-  // (s, component, lane) = (i / 64, (i / 32) % 2, i % 32) over groups 0..7.
+  // Warp-order sums, one filter row at a time: in round r every warp puts
+  // its taps (r, s) into red[warp][s], then thread i adds value
+  // (s, component, lane) = (i / 64, (i / 32) % 2, i % 32) over warps 0..7.
 #pragma unroll
   for (int r = 0; r < F; ++r) {
 #pragma unroll
     for (int s = 0; s < F; ++s) {
-      const int tau = r * F + s;
-      if (tau >= TP::T0 && tau < TP::T0 + TP::NT) {
-        red[grp][s][0][lane] = acc[tau - TP::T0].x;
-        red[grp][s][1][lane] = acc[tau - TP::T0].y;
-      }
+      red[warp][s][0][lane] = acc[r * F + s].x;
+      red[warp][s][1][lane] = acc[r * F + s].y;
     }
     __syncthreads();
     for (int i = threadIdx.x; i < F * 64; i += kThreads) {
       const int s = i >> 6, comp = (i >> 5) & 1, l = i & 31;
       float sum = red[0][s][comp][l];
 #pragma unroll
-      for (int gg = 1; gg < kGroups; ++gg) sum += red[gg][s][comp][l];
+      for (int w = 1; w < kWarps; ++w) sum += red[w][s][comp][l];
       res[(2 * l + comp) * FF + r * F + s] = sum;
     }
     __syncthreads();
   }
-  if (HALF == 0) {
-    red[grp][0][0][lane] = bsum.x;
-    red[grp][0][1][lane] = bsum.y;
-  }
+  red[warp][0][0][lane] = bsum.x;
+  red[warp][0][1][lane] = bsum.y;
   __syncthreads();
   if (threadIdx.x < 64) {
     const int comp = threadIdx.x >> 5, l = threadIdx.x & 31;
     float sum = red[0][0][comp][l];
 #pragma unroll
-    for (int gg = 1; gg < kGroups; ++gg) sum += red[gg][0][comp][l];
+    for (int w = 1; w < kWarps; ++w) sum += red[w][0][comp][l];
     resb[2 * l + comp] = sum;
   }
 }
@@ -373,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     dw_wgrad_ring_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
                          TO* out, float* ws, TO* db, float* ws_bias, RingParams p, unsigned* err) {
   constexpr int FF = F * F;
-  __shared__ float red[kGroups][F][2][32];  // one filter row of every column group's sums, lane-minor
+  __shared__ float red[kWarps][F][2][32];  // one filter row of every warp's sums, lane-minor
   __shared__ float res[kCB * FF];           // the tile [64 channels][F][F]
   __shared__ float resb[kCB];
   extern __shared__ __align__(128) uint8_t smem[];
@@ -427,10 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  if ((threadIdx.x >> 5) & 1)
-    run_half<TI, F, 1>(g, p, q_b, q_e, red, res, resb);
-  else
-    run_half<TI, F, 0>(g, p, q_b, q_e, red, res, resb);
+  run_warp<TI, F>(g, p, q_b, q_e, red, res, resb);
 
   // No copy may still be landing in shared memory when the CTA exits: wait
   // for the last step loaded into each step slot (bounded, no early exit).
@@ -491,7 +470,7 @@ cudaError_t launch_typed(const Plan& pl, const Args& a, CUtensorMapDataType dt) 
   p.Wo = (int32_t)s.wo;
   p.ph = (int32_t)s.ph;
   p.pw = (int32_t)s.pw;
-  p.CW = (int32_t)((s.w + kGroups - 1) / kGroups);
+  p.CW = (int32_t)((s.w + kWarps - 1) / kWarps);
   const RingShape rs = ring_shape(s);
   if (rs.d < 1) return cudaErrorInvalidValue;
   p.ahead = ahead_of_depth(rs.d);
