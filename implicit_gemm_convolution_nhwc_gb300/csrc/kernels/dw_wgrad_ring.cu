@@ -36,10 +36,15 @@
 // the end the warps' sums are added in warp order, one filter row at a time
 // (deterministic), and the tile goes out as contiguous fp32 to slab sigma of
 // the workspace or, unsplit, rounded into dW / db.
-#include "tc_common.cuh"
+#include "dw_ring.cuh"
 
 namespace cig {
 namespace {
+
+using dwring::lds2;
+using dwring::ring_rows;
+using dwring::RowPos;
+using dwring::StepPos;
 
 constexpr int kThreads = 256;  // 8 warps, up to 255 registers a thread
 constexpr int kWarps = kThreads / 32;
@@ -68,15 +73,7 @@ constexpr size_t static_smem(int F) {
 // then zero columns up to column pw + W - 1.
 int64_t dy_slot_cols(int64_t W, int64_t pw, int64_t F) { return F - 1 + pw + W; }
 
-// Ring depth d = ahead + slack (in steps of TR rows): d + 1 step slots. The
-// steps from S - slack to S + ahead cover m = (d + 1) TR - 1 row advances,
-// each +1 input row or +F at an image start (at most ceil(m / Ho) of those);
-// the input-row ring holds what they read, so that loading step S + ahead
-// only reuses rows that steps before S - slack read.
-int64_t ring_rows(int64_t F, int64_t Ho, int64_t d, int64_t tr) {
-  const int64_t m = (d + 1) * tr - 1;
-  return m + F + (F - 1) * ((m + Ho - 1) / Ho);
-}
+// Ring depth d = ahead + slack (in steps of TR rows): d + 1 step slots.
 int ahead_of_depth(int d) { return d >= 3 ? 2 : 1; }
 
 size_t ring_smem(const Shape& s, int d, int tr) {
@@ -97,60 +94,6 @@ RingShape ring_shape(const Shape& s) {
   if (ring_smem(s, 1, 1) + static_smem((int)s.s) <= kSmemLimit) return RingShape{1, 1};
   return RingShape{};
 }
-
-// A 16-bit pair from shared memory (32-bit shared address), widened to fp32.
-template <typename T>
-__device__ __forceinline__ float2 lds2(uint32_t a);
-template <>
-__device__ __forceinline__ float2 lds2<__nv_bfloat16>(uint32_t a) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
-  return make_float2(__uint_as_float(__byte_perm(v, 0u, 0x1044u)), __uint_as_float(v & 0xffff0000u));
-}
-template <>
-__device__ __forceinline__ float2 lds2<__half>(uint32_t a) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
-  __half2 h;
-  memcpy(&h, &v, sizeof(h));
-  return __half22float2(h);
-}
-
-// An output row's place: the ring slot of the first input row it reads, and
-// its (image, output row). Advanced one row at a time, so the loop does no
-// 64-bit division.
-struct RowPos {
-  int32_t xs;
-  int32_t ho, n;
-  bool first;  // the slice's first row: all F input rows are new
-  __device__ __forceinline__ int fresh(int F) const { return first || ho == 0 ? F : 1; }
-  __device__ __forceinline__ int32_t slot(int r, const RingParams& p) const {
-    return xs + r >= p.RX ? xs + r - p.RX : xs + r;
-  }
-  __device__ __forceinline__ void advance(int F, const RingParams& p) {
-    const bool cross = ++ho == p.Ho;
-    if (cross) {
-      ho = 0;
-      ++n;
-    }
-    xs += cross ? F : 1;
-    if (xs >= p.RX) xs -= p.RX;
-    first = false;
-  }
-};
-
-// A step's slot in the step ring and its wrap count (the slot's mbarrier
-// phase parity is the wrap count & 1).
-struct StepPos {
-  int32_t ss;
-  uint32_t sw;
-  __device__ __forceinline__ void advance(const RingParams& p) {
-    if (++ss == p.RS) {
-      ss = 0;
-      ++sw;
-    }
-  }
-};
 
 struct Ring {
   const CUtensorMap* tm_x;

@@ -251,7 +251,14 @@ cudaError_t launch_typed(const Plan& pl, const Args& a) {
 
 }  // namespace
 
+// The TMA-ring, register-tap form (dw_fwd_ring.cu) the depthwise forward
+// takes for 16-bit square 3/5/7 filters at unit stride.
+Geometry geometry_fwd_depthwise_ring(const Shape& s);
+cudaError_t launch_fwd_depthwise_ring(const Plan& p, const Args& a);
+
 Geometry geometry_fwd_depthwise(const Shape& s) {
+  const Geometry ring = geometry_fwd_depthwise_ring(s);
+  if (ring.ok) return ring;
   Geometry g;
   const bool depthwise = s.groups == s.c && s.groups == s.k;
   if (!depthwise || s.c % 2 != 0) return g;
@@ -268,6 +275,7 @@ Geometry geometry_fwd_depthwise(const Shape& s) {
 
 cudaError_t launch_fwd_depthwise(const Plan& p, const Args& a) {
   if (p.split != 1 || a.ws) return cudaErrorInvalidValue;
+  if (geometry_fwd_depthwise_ring(p.sh).ok) return launch_fwd_depthwise_ring(p, a);
   const int in = p.sh.in_dt, out = p.sh.out_dt;
   if (in == CONV_F32) return launch_typed<float, float>(p, a);
   if (in == CONV_BF16)

@@ -255,6 +255,9 @@ def test_forward_tc_strided(shape, dt):
     dict(n=1, h=12, w=20, c=64, k=64, groups=64, r=5, s=5, pad_h=4, pad_w=2, dil_h=2),  # H dilation
     dict(n=2, h=10, w=12, c=32, k=32, groups=32, r=7, s=7),                         # no padding
     dict(n=1, h=9, w=23, c=64, k=64, groups=64, r=3, s=7, stride_h=3, stride_w=2, pad_h=0, pad_w=3),
+    dict(n=3, h=5, w=9, c=72, k=72, groups=72, r=5, s=5, pad_h=4, pad_w=4),        # pad F-1, 8-channel tile, steps across images
+    dict(n=4, h=3, w=30, c=64, k=64, groups=64, r=3, s=3, pad_h=0, pad_w=2),       # one output row an image
+    dict(n=1, h=40, w=60, c=64, k=64, groups=64, r=7, s=7, pad_h=3, pad_w=3),      # a wide row ring
 ])
 @pytest.mark.parametrize("dt", [(BF16, BF16), (F16, F32), (F32, F32)], ids=lambda d: f"{d[0]}{d[1]}")
 def test_forward_depthwise(shape, dt):
