@@ -549,7 +549,7 @@ def run_ours(a, rank, world, local_rank):
         "roofline": roof, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
         "gpu_launches": a.steps * (1 + (1 if plan["needs_fold"] else 0) +
                                    (1 if kname == "generic" and bias else 0) +
-                                   (1 if kname in ("dgrad_tc", "fwd_grouped_tc") else 0)),  # their filter transforms
+                                   (1 if kname == "fwd_grouped_tc" else 0)),  # its filter expansion
         "timing": "value: the timed steps through conv_wgrad_bias / conv_fwd / conv_dgrad; stage_ms: a second loop of "
                   "conv_stage1 + conv_stage2 with an event between them",
         "stage_ms": {"stage1_mean": round(stage1_ms, 5), "stage1_min": round(min(s1), 5),

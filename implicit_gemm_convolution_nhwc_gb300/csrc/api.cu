@@ -189,12 +189,9 @@ conv_status make_plan(const conv_problem* prob, conv_dir dir, int32_t request, b
   p.fold = p.split > 1 && p.kernel != CONV_KERNEL_FWD_TC_CLUSTER;
   p.out_elems = dir == CONV_DIR_FWD ? p.sh.y_elems() : dir == CONV_DIR_WGRAD ? p.sh.w_elems() : p.sh.x_elems();
   p.slab_bytes = p.bias_slab_bytes = 0;
-  // The data gradient's tensor-core path writes the transformed filter (as
-  // many in_dtype elements as W) at the start of the workspace.
-  // The grouped forward's block-diagonal filter ([K][R][S][128]) likewise.
+  // The grouped forward's tensor-core path writes its block-diagonal filter
+  // ([K][R][S][128] in_dtype elements) at the start of the workspace.
   p.aux_bytes = 0;
-  if (p.kernel == CONV_KERNEL_DGRAD_TC)
-    p.aux_bytes = round256((uint64_t)p.sh.w_elems() * (uint64_t)esize(p.sh.in_dt));
   if (p.kernel == CONV_KERNEL_FWD_GROUPED_TC)
     p.aux_bytes = round256((uint64_t)(p.sh.k * p.sh.r * p.sh.s) * 128u * (uint64_t)esize(p.sh.in_dt));
   if (p.fold) {

@@ -80,6 +80,8 @@ struct FwdParams {
   int32_t sh;                   // stride along H (along W it is the X map's traversal stride)
   int32_t a_coff;               // 1: the X channel coordinate starts at the tile's first output channel
                                 // (block-diagonal grouped problems), 0: at 0
+  int32_t taps;                 // R * S (read by the MN-major B form: tap rs of the problem is tap
+                                // taps - 1 - rs of the filter it reads)
   int32_t split;
   // fused epilogue (unsplit only): y = min(max(acc + bias[k], ep_lo), ep_hi)
   const void* ep_bias;
@@ -193,7 +195,12 @@ __device__ __forceinline__ void store4<__half>(__half* dst, float4 v) {
   *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<uint2*>(h);
 }
 
-template <typename TO, uint32_t FMT, bool CL, int BN, int MS>
+// BMN: B is read MN-major from a filter laid out [C'][R][S][K'] (the
+// reduction channel outermost, output channels contiguous) with the taps
+// reversed: the data gradient's own filter, which as a forward problem is
+// W'[c][r'][s'][k] = W[k][R-1-r'][S-1-s'][c]. Each stage then holds BN / 64
+// atoms of 64 output channels x 64 reduction rows (128B-swizzled, 8 KB apart).
+template <typename TO, uint32_t FMT, bool CL, int BN, int MS, bool BMN = false>
 __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                   const __grid_constant__ CUtensorMap tm_y, TO* out, float* ws, FwdParams fp, unsigned* err) {
@@ -207,7 +214,8 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
   uint64_t* tmem_full = empty + kStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_full + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
-  constexpr uint32_t IDESC = mma_idesc(FMT, 0u, 0u, (uint32_t)BN, (uint32_t)kBM);
+  constexpr uint32_t IDESC = mma_idesc(FMT, 0u, BMN ? 1u : 0u, (uint32_t)BN, (uint32_t)kBM);
+  constexpr uint32_t kAtom = 64u * 128u;  // one MN-major B atom: 64 reduction rows of 128 bytes
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // Two-stage form: CTA = sigma * tiles + tile. Cluster form: the S CTAs of
@@ -237,7 +245,13 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
     for (int h = 0; h < MS; ++h)  // a sub-tile past the image reads zeros (and is not stored)
       tma_load_4d(st + h * kA, &tm_x, (fp.a_coff ? (int32_t)k0 : 0) + cb * kBK, sx * fp.dw - fp.pw,
                   (int32_t)(ho0 + h * fp.TR) * fp.sh + r * fp.dh - fp.ph, (int32_t)img, &full[ps]);
-    tma_load_2d(st + MS * kA, &tm_w, rs * cg + cb * kBK, (int32_t)k0, &full[ps]);
+    if (BMN) {
+#pragma unroll
+      for (int j = 0; j < BN / 64; ++j)
+        tma_load_3d(st + MS * kA + j * kAtom, &tm_w, (int32_t)k0 + 64 * j, fp.taps - 1 - rs, cb * kBK, &full[ps]);
+    } else {
+      tma_load_2d(st + MS * kA, &tm_w, rs * cg + cb * kBK, (int32_t)k0, &full[ps]);
+    }
     if (++cb == cblocks) {
       cb = 0;
       ++rs;
@@ -300,8 +314,11 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
           // K-major SW128: 8-row groups 1024 B apart; a K step of 16 elements is
-          // a 32-byte advance inside the swizzled 128-byte row.
-          const uint64_t bd = smem_desc_sw128(b + 32u * kk, 16, 1024);
+          // a 32-byte advance inside the swizzled 128-byte row. MN-major SW128
+          // (BMN): atoms kAtom apart, 8-row groups 1024 B apart; a K step of 16
+          // rows is 2048 B.
+          const uint64_t bd =
+              BMN ? smem_desc_sw128(b + 2048u * kk, kAtom, 1024) : smem_desc_sw128(b + 32u * kk, 16, 1024);
 #pragma unroll
           for (int h = 0; h < MS; ++h)
             mma_f16(tmem + (uint32_t)(h * BN), smem_desc_sw128(a + (uint32_t)(h * kA) + 32u * kk, 16, 1024), bd,
@@ -463,11 +480,12 @@ FwdParams make_params(const Plan& p, int bn, int ms) {
   fp.dw = (int32_t)s.dw;
   fp.sh = (int32_t)s.sh;
   fp.a_coff = 0;
+  fp.taps = (int32_t)(s.r * s.s);
   fp.split = p.split;
   return fp;
 }
 
-template <typename TO, uint32_t FMT, bool CL, int BN, int MS>
+template <typename TO, uint32_t FMT, bool CL, int BN, int MS, bool BMN = false>
 cudaError_t launch_typed(const Plan& p, const Args& a, CUtensorMapDataType dt, bool block = false) {
   const Shape& s = p.sh;
   FwdParams fp = make_params(p, BN, MS);
@@ -486,12 +504,21 @@ cudaError_t launch_typed(const Plan& p, const Args& a, CUtensorMapDataType dt, b
   // in shared memory exactly as for stride 1.
   const uint32_t x_box[4] = {(uint32_t)kBK, (uint32_t)(s.wo * s.sw), (uint32_t)(fp.TR * s.sh), 1u};
   const uint32_t x_estr[4] = {1u, (uint32_t)s.sw, (uint32_t)s.sh, 1u};
-  const uint64_t w_dims[2] = {(uint64_t)(s.r * s.s * s.cg), (uint64_t)s.k};
-  const uint64_t w_strides[1] = {(uint64_t)(s.r * s.s * s.cg) * 2u};
-  const uint32_t w_box[2] = {(uint32_t)kBK, (uint32_t)BN};
-  if (!encode_tmap(&tm_x, dt, 4, a.x, x_dims, x_strides, x_box, CU_TENSOR_MAP_SWIZZLE_128B, x_estr) ||
-      !encode_tmap(&tm_w, dt, 2, a.b, w_dims, w_strides, w_box, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!encode_tmap(&tm_x, dt, 4, a.x, x_dims, x_strides, x_box, CU_TENSOR_MAP_SWIZZLE_128B, x_estr))
     return cudaErrorInvalidValue;
+  if (BMN) {  // the filter [C'][R*S][K']: boxes of 64 output channels x 1 tap x 64 reduction channels
+    const uint64_t w_dims[3] = {(uint64_t)s.k, (uint64_t)(s.r * s.s), (uint64_t)s.cg};
+    const uint64_t w_strides[2] = {(uint64_t)s.k * 2u, (uint64_t)(s.r * s.s * s.k) * 2u};
+    const uint32_t w_box[3] = {64u, 1u, (uint32_t)kBK};
+    if (!encode_tmap(&tm_w, dt, 3, a.b, w_dims, w_strides, w_box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  } else {  // W [K][R*S*Cg]: boxes of 64 reduction elements x BN output channels
+    const uint64_t w_dims[2] = {(uint64_t)(s.r * s.s * s.cg), (uint64_t)s.k};
+    const uint64_t w_strides[1] = {(uint64_t)(s.r * s.s * s.cg) * 2u};
+    const uint32_t w_box[2] = {(uint32_t)kBK, (uint32_t)BN};
+    if (!encode_tmap(&tm_w, dt, 2, a.b, w_dims, w_strides, w_box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   // Output map of the two-stage form's epilogue: the slabs (fp32) under
   // split-K, else Y, as [N (x S)][Ho*Wo][K], boxes of 128 bytes x TR*Wo pixels.
   CUtensorMap tm_y;
@@ -512,7 +539,7 @@ cudaError_t launch_typed(const Plan& p, const Args& a, CUtensorMapDataType dt, b
   const int64_t ctas = fp.tiles * p.split;
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (!CL) {
-    auto kern = fwd_tc_kernel<TO, FMT, false, BN, MS>;
+    auto kern = fwd_tc_kernel<TO, FMT, false, BN, MS, BMN>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     // Slab sigma starts at ws + sigma * E; the kernel indexes pixels within it.
@@ -578,15 +605,16 @@ Geometry geometry_fwd_tc_block(const Shape& b) {
 }
 
 namespace {
-template <bool CL, int BN, int MS>
+template <bool CL, int BN, int MS, bool BMN = false>
 cudaError_t launch_bn(const Plan& p, const Args& a, bool block = false) {
   if (p.sh.in_dt == CONV_BF16) {
     if (p.sh.out_dt == CONV_F32)
-      return launch_typed<float, 1u, CL, BN, MS>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, block);
-    return launch_typed<__nv_bfloat16, 1u, CL, BN, MS>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, block);
+      return launch_typed<float, 1u, CL, BN, MS, BMN>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, block);
+    return launch_typed<__nv_bfloat16, 1u, CL, BN, MS, BMN>(p, a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, block);
   }
-  if (p.sh.out_dt == CONV_F32) return launch_typed<float, 0u, CL, BN, MS>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, block);
-  return launch_typed<__half, 0u, CL, BN, MS>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, block);
+  if (p.sh.out_dt == CONV_F32)
+    return launch_typed<float, 0u, CL, BN, MS, BMN>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, block);
+  return launch_typed<__half, 0u, CL, BN, MS, BMN>(p, a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, block);
 }
 }  // namespace
 
@@ -596,5 +624,11 @@ cudaError_t launch_fwd_tc(const Plan& p, const Args& a) {
 }
 cudaError_t launch_fwd_tc_cluster(const Plan& p, const Args& a) { return launch_bn<true, 128, 1>(p, a); }
 cudaError_t launch_fwd_tc_block(const Plan& p, const Args& a) { return launch_bn<false, 128, 1>(p, a, true); }
+// The forward form of a data gradient with B read MN-major from the data
+// gradient's own filter (see fwd_tc_kernel's BMN).
+cudaError_t launch_fwd_tc_filter_mn(const Plan& p, const Args& a) {
+  if (tile_bn(p.sh, false) == 128) return launch_bn<false, 128, 1, true>(p, a);
+  return tile_ms(p.sh, false) == 2 ? launch_bn<false, 256, 2, true>(p, a) : launch_bn<false, 256, 1, true>(p, a);
+}
 
 }  // namespace cig

@@ -129,8 +129,8 @@ typedef struct conv_plan_info {
   int64_t tiles;             /* output tiles of stage 1 */
   int64_t reduction_blocks;  /* reduction blocks; a pinned degree may not exceed it */
   int64_t ctas;              /* stage-1 CTAs = tiles * S */
-  uint64_t workspace_bytes;  /* bytes the call needs (0 without stage 2, except the data
-                                gradient's transformed filter) */
+  uint64_t workspace_bytes;  /* bytes the call needs (0 without stage 2, except the grouped
+                                forward's block-diagonal filter) */
   int32_t max_split;         /* largest degree a pinned request may ask of this kernel */
 } conv_plan_info;
 
@@ -163,10 +163,9 @@ conv_status resolve_split_k(const conv_problem* p, conv_dir dir, int32_t request
 /* Workspace bytes a call with this degree request needs: 0 when the degree
  * resolves to 1, else S x E x 4 rounded up to 256 bytes (E = output elements),
  * plus S x k x 4 (rounded up to 256) when with_bias and dir is the weight
- * gradient; the data gradient's tensor-core path adds the transformed filter
- * (k x r x s x c elements of in_dtype, rounded up to 256) in front, at every
- * degree, and the grouped forward's tensor-core path its block-diagonal
- * filter (k x r x s x 128 elements of in_dtype, rounded up to 256). */
+ * gradient; the grouped forward's tensor-core path adds its block-diagonal
+ * filter (k x r x s x 128 elements of in_dtype, rounded up to 256) in front,
+ * at every degree. */
 conv_status conv_workspace_bytes_for(const conv_problem* p, conv_dir dir, int32_t split_k,
                                      int32_t with_bias, int32_t sm_count, uint64_t* bytes);
 conv_status conv_workspace_bytes(const conv_problem* p, conv_dir dir, int32_t split_k,
@@ -210,9 +209,8 @@ conv_status conv_fwd_epilogue(const conv_problem* p, const void* x, const void* 
 /* Data gradient: dx[n,h,w,c] = sum over k, r, s of dy[n,ho,wo,k] * w[k,r,s,c]
  * for the (ho, wo) with ho*sh + r*dh - ph = h and wo*sw + s*dw - pw = w (the
  * forward's taps read backwards). dy and w in in_dtype, dx [n,h,w,c] in
- * out_dtype. The reduction (r, s, k) splits like the forward's. The
- * tensor-core path keeps the transformed filter at the start of ws, so it
- * needs a workspace even at degree 1 (conv_workspace_bytes says how much). */
+ * out_dtype. The reduction (r, s, k) splits like the forward's; the
+ * workspace is the slabs only (none at degree 1). */
 conv_status conv_dgrad(const conv_problem* p, const void* dy, const void* w, void* dx, void* ws,
                        uint64_t ws_bytes, int32_t split_k, void* stream);
 
