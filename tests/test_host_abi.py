@@ -268,3 +268,45 @@ def test_selftest_arguments_checked_without_a_device():
     assert lib.conv_selftest_wait_timeout(0, ctypes.byref(out), None) == 1           # no limit
     assert lib.conv_selftest_wait_timeout(2_000_000_000, ctypes.byref(out), None) == 1  # over 1 s
     assert lib.conv_selftest_wait_timeout(1000, None, None) == 1
+
+
+def dw(**kw):
+    """A 16-bit depthwise problem (C = K = groups)."""
+    base = dict(n=2, h=12, w=14, c=64, r=7, s=7, pad_h=3, pad_w=3, in_dtype=BF16, out_dtype=BF16)
+    base.update(kw)
+    return Problem(k=base["c"], groups=base["c"], **base)
+
+
+def test_depthwise_ring_selection():
+    """Which depthwise shapes the row-ring kernels take (16-bit, square 3/5/7 filters, unit stride and
+    dilation, pad_w <= F-1, C % 8 == 0 and C >= 64, rows of at most 256 columns that fit the ring),
+    told apart by what the plan reports: the weight gradient's shared-memory form needs C % 64 == 0
+    and 16-bit inputs; the forward's shared-weight form runs 4 CTAs per SM, the ring form 1."""
+    wg = lambda p: cig.describe_plan(p, DIR_WGRAD, -1, sm_count=SMS)  # noqa: E731
+    fw = lambda p: cig.describe_plan(p, DIR_FWD, -1, sm_count=SMS)  # noqa: E731
+    # C = 72: only the ring takes the weight gradient (two 64-channel tiles, the last 8 wide)
+    info = wg(dw(c=72))
+    assert info["kernel_name"] == "wgrad_depthwise" and info["tiles"] == 2 and info["ctas_per_sm"] == 1
+    assert fw(dw(c=72))["kernel_name"] == "fwd_depthwise" and fw(dw(c=72))["ctas_per_sm"] == 1
+    # C % 8 != 0 or C < 64: neither TMA ring; the weight gradient falls to the generic kernel, the
+    # forward to its shared-weight form
+    for c in (34, 32):
+        assert wg(dw(c=c))["kernel_name"] == "generic"
+        assert fw(dw(c=c))["kernel_name"] == "fwd_depthwise" and fw(dw(c=c))["ctas_per_sm"] == 4
+    # fp32 inputs: no ring (and no shared-memory weight-gradient form)
+    assert wg(dw(in_dtype=F32, out_dtype=F32))["kernel_name"] == "generic"
+    assert fw(dw(in_dtype=F32, out_dtype=F32))["ctas_per_sm"] == 4
+    # pad_w = F: past the ring's padding; C % 64 == 0 keeps the shared-memory weight-gradient form
+    p = dw(r=3, s=3, pad_h=1, pad_w=3)
+    assert wg(p)["kernel_name"] == "wgrad_depthwise" and fw(p)["ctas_per_sm"] == 4
+    # non-square and strided filters: the forward's shared-weight form
+    assert fw(dw(r=3, s=7, pad_h=1))["ctas_per_sm"] == 4
+    assert fw(dw(r=3, s=3, pad_h=1, pad_w=1, stride_w=2))["ctas_per_sm"] == 4
+    # a row too wide for the forward's ring (28 rows of 64 channels x W columns) but not for the
+    # weight gradient's (whose ring is shallower)
+    wide = dw(h=20, w=80)
+    assert fw(wide)["ctas_per_sm"] == 4 and wg(wide)["ctas_per_sm"] == 1
+    # the ring grids: the forward spreads (n, ho) rows over about one CTA per SM
+    info = fw(CONFIG4)
+    assert info["ctas_per_sm"] == 1 and info["ctas"] == 150 and info["split_k"] == 1
+    assert cig.workspace_bytes(CONFIG4, DIR_FWD, -1, sm_count=SMS) == 0
