@@ -61,11 +61,13 @@ struct RingParams {
   int32_t RX, RS;   // ring slots: input rows, steps
   int32_t TR;       // output rows a step
   int32_t ahead;    // steps between a load's issue and its use
+  int32_t red_off;  // byte offset of the reduction's buffers in shared memory
   int32_t split;
 };
 
-// Static shared memory of the F form (the warp-order reduction).
-constexpr size_t static_smem(int F) {
+// Shared memory of the warp-order reduction (red, res, resb), which reuses
+// the rings' bytes once every load has landed.
+constexpr size_t reduce_smem(int F) {
   return (size_t)kWarps * F * 2 * 32 * 4 + (size_t)kCB * F * F * 4 + kCB * 4;
 }
 
@@ -85,13 +87,29 @@ struct RingShape {
   int d = 0, tr = 0;
 };
 
-// Two rows a step and the deepest ring that fits (up to kMaxDepth), else one
-// row a step ({0, 0}: none fits).
+// Where the reduction goes: over the ring rows and dY rows when they are large
+// enough (the mbarriers after them are never overwritten), else after
+// everything.
+size_t ring_data_bytes(const Shape& s, const RingShape& rs) {
+  return (size_t)(ring_rows(s.s, s.ho, rs.d, rs.tr) * s.w * 128 +
+                  (1 + rs.d) * rs.tr * dy_slot_cols(s.w, s.pw, s.s) * 128);
+}
+size_t reduce_offset(const Shape& s, const RingShape& rs) {
+  return ring_data_bytes(s, rs) >= reduce_smem((int)s.s) ? 0 : (ring_smem(s, rs.d, rs.tr) + 127) / 128 * 128;
+}
+size_t kernel_smem(const Shape& s, const RingShape& rs) {
+  const size_t off = reduce_offset(s, rs);
+  return off == 0 ? ring_smem(s, rs.d, rs.tr) : off + reduce_smem((int)s.s);
+}
+
+// Three, else two rows a step with the deepest ring that fits (up to
+// kMaxDepth, at least one step of slack), else one row a step ({0, 0}: none
+// fits).
 RingShape ring_shape(const Shape& s) {
-  for (int tr = 2; tr >= 1; --tr)
+  for (int tr = 3; tr >= 1; --tr)
     for (int d = kMaxDepth; d >= 2; --d)
-      if (ring_smem(s, d, tr) + static_smem((int)s.s) <= kSmemLimit) return RingShape{d, tr};
-  if (ring_smem(s, 1, 1) + static_smem((int)s.s) <= kSmemLimit) return RingShape{1, 1};
+      if (kernel_smem(s, RingShape{d, tr}) <= kSmemLimit) return RingShape{d, tr};
+  if (kernel_smem(s, RingShape{1, 1}) <= kSmemLimit) return RingShape{1, 1};
   return RingShape{};
 }
 
@@ -232,25 +250,45 @@ __device__ __forceinline__ void run_warp(const Ring& g, const RingParams& p, int
       return smem_u32(g.dring + ((size_t)sc.ss * p.TR + j) * g.rowD + (size_t)(F - 1) * 128 + lane * 4);
     };
     auto x_row = [&](int r) { return smem_u32(g.xring + (size_t)cur.slot(r, p) * g.rowX + lane * 4); };
-    if (rows == 2 && cur.ho + 1 < p.Ho) {  // two rows of one image: one sweep
-      if (u_beg < u_end) {
-        const uint32_t dy0[2] = {dy_row(0), dy_row(1)};
-        uint32_t xs[F + 1];
-#pragma unroll
-        for (int i = 0; i <= F; ++i) xs[i] = x_row(i);
-        sweep<TI, F, 2>(acc, bsum, dy0, xs, u_beg, u_end, p.pw, warp == 0);
-      }
-      cur.advance(F, p);
-      cur.advance(F, p);
-    } else {
+    // The step's rows in runs within one image; a run of L rows shares one
+    // sweep (and all but L - 1 of its input rows).
 #pragma unroll 1
-      for (int32_t j = 0; j < rows; ++j, cur.advance(F, p)) {
-        if (u_beg >= u_end) continue;
-        const uint32_t dy0[1] = {dy_row(j)};
-        uint32_t xs[F];
+    for (int32_t j = 0; j < rows;) {
+      const int32_t left = p.Ho - cur.ho;  // rows of this image from cur on
+      const int32_t run = rows - j < left ? rows - j : left;
+      if (run >= 3) {
+        if (u_beg < u_end) {
+          const uint32_t dy0[3] = {dy_row(j), dy_row(j + 1), dy_row(j + 2)};
+          uint32_t xs[F + 2];
 #pragma unroll
-        for (int i = 0; i < F; ++i) xs[i] = x_row(i);
-        sweep<TI, F, 1>(acc, bsum, dy0, xs, u_beg, u_end, p.pw, warp == 0);
+          for (int i = 0; i < F + 2; ++i) xs[i] = x_row(i);
+          sweep<TI, F, 3>(acc, bsum, dy0, xs, u_beg, u_end, p.pw, warp == 0);
+        }
+        j += 3;
+        cur.advance(F, p);
+        cur.advance(F, p);
+        cur.advance(F, p);
+      } else if (run == 2) {
+        if (u_beg < u_end) {
+          const uint32_t dy0[2] = {dy_row(j), dy_row(j + 1)};
+          uint32_t xs[F + 1];
+#pragma unroll
+          for (int i = 0; i <= F; ++i) xs[i] = x_row(i);
+          sweep<TI, F, 2>(acc, bsum, dy0, xs, u_beg, u_end, p.pw, warp == 0);
+        }
+        j += 2;
+        cur.advance(F, p);
+        cur.advance(F, p);
+      } else {
+        if (u_beg < u_end) {
+          const uint32_t dy0[1] = {dy_row(j)};
+          uint32_t xs[F];
+#pragma unroll
+          for (int i = 0; i < F; ++i) xs[i] = x_row(i);
+          sweep<TI, F, 1>(acc, bsum, dy0, xs, u_beg, u_end, p.pw, warp == 0);
+        }
+        j += 1;
+        cur.advance(F, p);
       }
     }
 
@@ -260,6 +298,16 @@ __device__ __forceinline__ void run_warp(const Ring& g, const RingParams& p, int
     sc.advance(p);
   }
   signal_dependents();
+
+  // The reduction below reuses the rings' shared memory: first every load
+  // must have landed (wait for the last step loaded into each step slot;
+  // bounded, no early exit).
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < p.RS; ++i)
+      if (g.siss[i] >= 0) mbar_wait(&g.full[i], (uint32_t)g.siss[i] & 1u, nullptr, g.err);
+  }
+  __syncthreads();
 
   // Warp-order sums, one filter row at a time: in round r every warp puts
   // its taps (r, s) into red[warp][s], then thread i adds value
@@ -298,10 +346,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     dw_wgrad_ring_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
                          TO* out, float* ws, TO* db, float* ws_bias, RingParams p, unsigned* err) {
   constexpr int FF = F * F;
-  __shared__ float red[kWarps][F][2][32];  // one filter row of every warp's sums, lane-minor
-  __shared__ float res[kCB * FF];           // the tile [64 channels][F][F]
-  __shared__ float resb[kCB];
   extern __shared__ __align__(128) uint8_t smem[];
+  // After the step loop: one filter row of every warp's sums (lane-minor), the
+  // tile [64 channels][F][F] and the bias sums, over the rings' bytes.
+  auto red = reinterpret_cast<float (*)[F][2][32]>(smem + p.red_off);
+  float* res = reinterpret_cast<float*>(smem + p.red_off + (size_t)kWarps * F * 2 * 32 * 4);
+  float* resb = res + kCB * FF;
   const int32_t dcols = F - 1 + p.pw + p.W;  // columns of a dY slot
 
   Ring g;
@@ -353,14 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
 
   run_warp<TI, F>(g, p, q_b, q_e, red, res, resb);
-
-  // No copy may still be landing in shared memory when the CTA exits: wait
-  // for the last step loaded into each step slot (bounded, no early exit).
   __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < p.RS; ++i)
-      if (g.siss[i] >= 0) mbar_wait(&g.full[i], (uint32_t)g.siss[i] & 1u, nullptr, err);
-  }
 
   const int64_t nc = p.C - cb * kCB < kCB ? p.C - cb * kCB : kCB;
   const int64_t E = p.C * FF, base = cb * kCB * FF;  // dW [C][F][F][1]: the tile is contiguous
@@ -389,7 +432,7 @@ cudaError_t launch_f(const Plan& pl, const Args& a, const RingParams& p, CUtenso
   if (!encode_tmap(&tm_x, dt, 4, a.x, x_dims, x_strides, x_box, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !encode_tmap(&tm_dy, dt, 4, a.b, y_dims, y_strides, y_box, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  const size_t smem = ring_smem(s, p.RS - 1, p.TR);
+  const size_t smem = kernel_smem(s, RingShape{p.RS - 1, p.TR});
   auto kern = dw_wgrad_ring_kernel<TI, TO, F>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
@@ -420,6 +463,7 @@ cudaError_t launch_typed(const Plan& pl, const Args& a, CUtensorMapDataType dt) 
   p.TR = rs.tr;
   p.RX = (int32_t)ring_rows(s.s, s.ho, rs.d, rs.tr);
   p.RS = 1 + rs.d;
+  p.red_off = (int32_t)reduce_offset(s, rs);
   p.split = pl.split;
   switch (s.s) {
     case 3: return launch_f<TI, TO, 3>(pl, a, p, dt);
