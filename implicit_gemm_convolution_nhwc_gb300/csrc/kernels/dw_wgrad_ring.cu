@@ -31,11 +31,12 @@
 // columns wi left to right, column wi meets output pixel wo = wi + pw - s
 // through tap column s, so the lane keeps the last F dY pairs of each output
 // row in a register window and does F*F packed FMAs (__ffma2_rn) per row per
-// column, from four-byte shared-memory loads widened to fp32; the two rows of
-// a step within one image share one sweep (and all but one input row). At
-// the end the warps' sums are added in warp order, one filter row at a time
-// (deterministic), and the tile goes out as contiguous fp32 to slab sigma of
-// the workspace or, unsplit, rounded into dW / db.
+// column, from four-byte shared-memory loads widened to fp32; the rows of a
+// step within one image share one sweep (each adds one input row). At the end,
+// once every load has landed, the warps' sums are added in warp order, one
+// filter row at a time (deterministic), in shared memory over the rings'
+// bytes, and the tile goes out as contiguous fp32 to slab sigma of the
+// workspace or, unsplit, rounded into dW / db.
 #include "dw_ring.cuh"
 
 namespace cig {
