@@ -81,7 +81,8 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("split_k", ctypes.c_int32), ("needs_fold", ctypes.c_int32),
                 ("ctas_per_sm", ctypes.c_int32), ("tiles", ctypes.c_int64),
                 ("reduction_blocks", ctypes.c_int64), ("ctas", ctypes.c_int64),
-                ("workspace_bytes", ctypes.c_uint64), ("max_split", ctypes.c_int32)]
+                ("workspace_bytes", ctypes.c_uint64), ("max_split", ctypes.c_int32),
+                ("fold_width", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         d = {f[0]: getattr(self, f[0]) for f in self._fields_}

@@ -87,6 +87,38 @@ Geometry geometry_of(conv_kernel k, const Shape& s, conv_dir dir) {
   }
 }
 
+// Width fold ("feat(rocke): split-K forward implicit-GEMM convolution on
+// gfx1250", the fold_width commit): when f divides the filter width, the W
+// stride, the input width and the W padding (unit W dilation, one group), the
+// problem equals one with W/f positions of f*C channels, filter width S/f and
+// W stride sw/f, on the same memory: X [N][H][W][C] is [N][H][W/f][f*C], W
+// [K][R][S][C] is [K][R][S/f][f*C] (tap s = f*s' + j, channel j*C + c), and
+// Y is unchanged. f is the largest such factor (1: no fold).
+int64_t gcd64(int64_t a, int64_t b) {
+  while (b != 0) {
+    const int64_t t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+int64_t fold_width_of(const Shape& s) {
+  if (s.groups != 1 || s.dw != 1) return 1;
+  return gcd64(gcd64(gcd64(s.s, s.sw), s.w), s.pw);
+}
+
+Shape fold_width(const Shape& s, int64_t f) {
+  Shape t = s;
+  t.w = s.w / f;
+  t.s = s.s / f;
+  t.sw = s.sw / f;
+  t.pw = s.pw / f;
+  t.c = s.c * f;
+  t.cg = t.c;
+  return t;
+}
+
 // The kernel a call runs: the override if set, else the first fast kernel
 // that takes the problem, else the generic one.
 conv_status choose_kernel(const Shape& s, conv_dir dir, conv_kernel* kernel, Geometry* geo) {
@@ -164,8 +196,28 @@ conv_status resolve_degree(const Shape& s, conv_dir dir, const Geometry& g, int3
 // ("feat(rocke): split-K forward implicit-GEMM convolution on gfx1250",
 // "Review follow-ups": split-K rejects it; "Auto-deduced degree": such specs
 // resolve to 1).
+// The kernel for a problem, folding its width when only the folded problem
+// has a kernel faster than the generic one (then *s becomes the folded shape
+// and *fold its factor).
+conv_status choose_kernel_folded(Shape* s, conv_dir dir, conv_kernel* kernel, Geometry* geo, int64_t* fold) {
+  *fold = 1;
+  conv_status st = choose_kernel(*s, dir, kernel, geo);
+  if (st == CONV_OK && *kernel != CONV_KERNEL_GENERIC) return st;
+  const int64_t f = fold_width_of(*s);
+  if (f < 2) return st;
+  const Shape t = fold_width(*s, f);
+  conv_kernel kt;
+  Geometry gt;
+  if (choose_kernel(t, dir, &kt, &gt) != CONV_OK || kt == CONV_KERNEL_GENERIC) return st;
+  *s = t;
+  *kernel = kt;
+  *geo = gt;
+  *fold = f;
+  return CONV_OK;
+}
+
 conv_status make_plan(const conv_problem* prob, conv_dir dir, int32_t request, bool with_bias,
-                      int32_t sm_count, Plan* plan, bool epilogue = false) {
+                      int32_t sm_count, Plan* plan, bool epilogue = false, int64_t* fold_out = nullptr) {
   if (dir != CONV_DIR_FWD && dir != CONV_DIR_WGRAD && dir != CONV_DIR_DGRAD) return CONV_ERR_INVALID_ARG;
   Plan p;
   conv_status st = validate(prob, &p.sh);
@@ -178,8 +230,10 @@ conv_status make_plan(const conv_problem* prob, conv_dir dir, int32_t request, b
     if (dir != CONV_DIR_FWD || request > 1) return CONV_ERR_INVALID_ARG;
     request = 1;
   }
-  st = choose_kernel(p.sh, dir, &p.kernel, &p.geo);
+  int64_t fold = 1;
+  st = choose_kernel_folded(&p.sh, dir, &p.kernel, &p.geo, &fold);
   if (st != CONV_OK) return st;
+  if (fold_out) *fold_out = fold;
   if (epilogue && p.kernel == CONV_KERNEL_FWD_TC_CLUSTER) return CONV_ERR_UNSUPPORTED;
   // The cluster form takes at most 16 slices (one cluster per tile).
   if (p.kernel == CONV_KERNEL_FWD_TC_CLUSTER && request > p.geo.max_split && request <= p.geo.blocks)
@@ -372,9 +426,11 @@ conv_status conv_describe_plan(const conv_problem* p, conv_dir dir, int32_t spli
                                int32_t with_bias, int32_t sm_count, conv_plan_info* info) {
   if (!info) return CONV_ERR_INVALID_ARG;
   Plan plan;
-  conv_status st = make_plan(p, dir, split_k, with_bias != 0, sm_count, &plan);
+  int64_t fold = 1;
+  conv_status st = make_plan(p, dir, split_k, with_bias != 0, sm_count, &plan, false, &fold);
   if (st != CONV_OK) return st;
   info->kernel = plan.kernel;
+  info->fold_width = (int32_t)fold;
   info->split_k = plan.split;
   info->needs_fold = plan.fold ? 1 : 0;
   info->ctas_per_sm = plan.geo.ctas_per_sm;

@@ -132,6 +132,10 @@ typedef struct conv_plan_info {
   uint64_t workspace_bytes;  /* bytes the call needs (0 without stage 2, except the grouped
                                 forward's block-diagonal filter) */
   int32_t max_split;         /* largest degree a pinned request may ask of this kernel */
+  int32_t fold_width;        /* f > 1: the call runs the width-folded problem (f adjacent W
+                                positions as f*C channels, filter width S/f, W stride sw/f, on
+                                the same memory), chosen when only it has a kernel faster than
+                                the generic one; 1: no fold */
 } conv_plan_info;
 
 /* Human-readable name of a status. Never NULL. */

@@ -510,3 +510,29 @@ def test_empty_batch_every_direction(shape):
     cig.conv_fwd_epilogue(p, xw[0].cuda(), xw[1].cuda(), y, None, 0.0, INF, None, -1)
     torch.cuda.synchronize()
     assert cig.device_errors() == 0
+
+
+# ------------------------------------------------------------- width fold
+
+
+@pytest.mark.parametrize("shape,direction,dt,kernel", [
+    (dict(n=2, h=16, w=16, c=32, k=128, r=2, s=2, stride_h=2, stride_w=2), cig.DIR_FWD, (BF16, BF16), "fwd_tc"),
+    (dict(n=3, h=20, w=24, c=16, k=256, r=4, s=4, stride_h=4, stride_w=4), cig.DIR_FWD, (F16, F32), "fwd_tc"),
+    (dict(n=2, h=9, w=16, c=32, k=136, r=3, s=2, stride_w=2, pad_h=1), cig.DIR_FWD, (BF16, BF16), "fwd_tc"),
+    (dict(n=2, h=8, w=16, c=64, k=64, r=1, s=2, stride_w=2), cig.DIR_WGRAD, (F32, F32), "wgrad_1x1_tf32x3"),
+    (dict(n=2, h=8, w=16, c=64, k=128, r=1, s=2, stride_w=2), cig.DIR_DGRAD, (BF16, BF16), "dgrad_tc"),
+], ids=["2x2s2", "4x4s4", "3x2ws2", "wgrad1x2", "dgrad1x2"])
+def test_width_fold(shape, direction, dt, kernel):
+    """Calls the planner width-folds ("feat(rocke): split-K forward implicit-GEMM convolution on gfx1250",
+    the fold_width commit) run the folded problem on the same tensors; checked against the oracle on the
+    original problem."""
+    p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
+    info = cig.describe_plan(p, direction, -1)
+    assert info["kernel_name"] == kernel and info["fold_width"] > 1
+    if direction == cig.DIR_FWD:
+        check_fwd(p, 21, ["auto", "generic"], [-1, 1, 2])
+    elif direction == cig.DIR_WGRAD:
+        check_wgrad(p, 21, ["auto"], [-1, 1, 2], bias=True)
+    else:
+        check_dgrad(p, 21, ["auto", "generic"], [-1, 1, 2])
+    assert cig.device_errors() == 0
