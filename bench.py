@@ -48,6 +48,9 @@ WORKLOADS = {
     "fwd3x3s2_bf16_n64": (dict(n=64, h=56, w=56, c=128, k=256, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1,
                                in_dtype=1, out_dtype=1), "fwd", "normal", (0.0, 0.02), 6,
                           "3x3 stride-2 fwd bf16 NHWC N=64 H=W=56 C=128 K=256 pad 1 (a downsampling layer)"),
+    "fwd2x2s2_bf16_n64_c32": (dict(n=64, h=112, w=112, c=32, k=128, r=2, s=2, stride_h=2, stride_w=2,
+                                   in_dtype=1, out_dtype=1), "fwd", "normal", (0.0, 0.02), 7,
+                              "2x2 stride-2 fwd bf16 NHWC N=64 H=W=112 C=32 K=128 (a downsampling layer; width-folded)"),
     "dgrad3x3_bf16_n1": (dict(n=1, h=14, w=14, c=2048, k=512, r=3, s=3, pad_h=1, pad_w=1, in_dtype=1, out_dtype=1),
                          "dgrad", "normal", (0.0, 0.02), 2,
                          "3x3 dgrad bf16 NHWC N=1 H=W=14 C=2048 K=512 pad 1 (the small-M layer backwards), split-K"),
@@ -540,7 +543,7 @@ def run_ours(a, rank, world, local_rank):
         "warmup": a.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": DT_NAME[p.in_dtype], "data": "synthetic (seeded counter-based generator)",
         "config": {"workload": desc + (" + fused bias/ReLU epilogue" if fused else ""), "name": a.workload,
-                   "kernel": kname, "split_k": plan["split_k"],
+                   "kernel": kname, "split_k": plan["split_k"], "fold_width": plan.get("fold_width", 1),
                    "split_k_request": a.split_k, "ctas": plan["ctas"], "workspace_bytes": plan["workspace_bytes"],
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                    "l2": "flushed between steps (2x L2 buffer written)" if flush is not None
