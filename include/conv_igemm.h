@@ -204,8 +204,8 @@ typedef struct conv_epilogue {
  * per slice, so it runs unsplit [P2 "Review follow-ups": split-K rejects
  * it; "Auto-deduced degree": such specs resolve to 1]: split_k -1, 0 or 1
  * gives one slice, any other degree is CONV_ERR_INVALID_ARG; the workspace
- * is what conv_workspace_bytes reports at degree 1 (0 except for a kernel's
- * transformed filter). An identity epilogue (or ep == NULL) is exactly
+ * is what conv_workspace_bytes reports at degree 1 (0 except for the grouped
+ * forward's block-diagonal filter). An identity epilogue (or ep == NULL) is exactly
  * conv_fwd. */
 conv_status conv_fwd_epilogue(const conv_problem* p, const void* x, const void* w, const conv_epilogue* ep,
                               void* y, void* ws, uint64_t ws_bytes, int32_t split_k, void* stream);
