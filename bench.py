@@ -63,6 +63,16 @@ WORKLOADS = {
     "dw7x7_fwd_bf16": (dict(n=32, h=56, w=56, c=384, k=384, r=7, s=7, pad_h=3, pad_w=3, groups=384,
                             in_dtype=1, out_dtype=1), "fwd", "normal", (0.0, 1.0), 3,
                        "depthwise 7x7 fwd bf16 NHWC N=32 H=W=56 C=K=384 pad 3"),
+    "dw7x7_dgrad_bf16": (dict(n=32, h=56, w=56, c=384, k=384, r=7, s=7, pad_h=3, pad_w=3, groups=384,
+                              in_dtype=1, out_dtype=1), "dgrad", "normal", (0.0, 1.0), 3,
+                         "depthwise 7x7 dgrad bf16 NHWC N=32 H=W=56 C=K=384 pad 3"),
+    "wgrad3x3_bf16_n64_c256": (dict(n=64, h=56, w=56, c=256, k=256, r=3, s=3, pad_h=1, pad_w=1, in_dtype=1,
+                                    out_dtype=1), "wgrad", "normal", (0.0, 0.02), 5,
+                               "3x3 wgrad+db bf16 NHWC N=64 H=W=56 C=K=256 pad 1 (compute-bound supplement, "
+                               "weight gradient)"),
+    "grp3x3_dgrad_f16_g64": (dict(n=64, h=28, w=28, c=512, k=512, r=3, s=3, pad_h=1, pad_w=1, groups=64,
+                                  in_dtype=2, out_dtype=2), "dgrad", "normal", (0.0, 1.0), 4,
+                             "grouped 3x3 dgrad fp16 NHWC N=64 H=W=28 C=K=512 groups=64 (8 ch/group)"),
     "grp3x3_fwd_f16_g64": (dict(n=64, h=28, w=28, c=512, k=512, r=3, s=3, pad_h=1, pad_w=1, groups=64,
                                 in_dtype=2, out_dtype=2), "fwd", "normal", (0.0, 1.0), 4,
                            "grouped 3x3 fwd fp16 NHWC N=64 H=W=28 C=K=512 groups=64 (8 ch/group)"),
@@ -330,6 +340,237 @@ def time_oracle(p, direction, dist, args, seed, target_s: float):
 
 # --------------------------------------------------------------- our arm
 
+# The configurations (and the compute-bound supplement) timed after the
+# headline and reported under "per_config", each at its own automatic plan.
+PER_CONFIG = ["wgrad1x1_f32_n4", "fwd3x3_bf16_n1", "dgrad3x3_bf16_n1", "dw7x7_wgrad_bf16", "dw7x7_dgrad_bf16",
+              "grp3x3_wgrad_f16_g64", "grp3x3_wgrad_f16_g128", "fwd3x3_bf16_n64_c256", "dgrad3x3_bf16_n64_c256",
+              "wgrad3x3_bf16_n64_c256"]
+# The split-K degrees swept on the small-M layer (auto first).
+SWEEP = {"fwd3x3_bf16_n1": [-1, 1, 2, 4, 8, 16, 32]}
+
+
+def roofline_for(kname, p, direction, flops, in_bytes, stage1_ms, pk, sms):
+    """The dominant kernel (stage 1) against the roofline that bounds it."""
+    alu_peak = sms * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12  # FP32 FMA lanes x 2 flop x max clock
+    if kname in ("wgrad_1x1_tf32x3", "wgrad_1x1_ffma") or direction == "wgrad" and kname == "generic" and p.r == 1:
+        bound = "hbm"
+    elif kname in ("fwd_tc", "fwd_tc_cluster", "dgrad_tc", "wgrad_tc"):
+        # past the ridge point (flop per byte of the measured peaks) the tensor
+        # pipe bounds it, else HBM
+        bound = "tensor" if flops / in_bytes > pk["bf16"] * 1e12 / (pk["hbm"] * 1e9) else "hbm"
+    elif kname in ("fwd_grouped_tc", "wgrad_grouped_tc", "dgrad_grouped_tc"):
+        bound = "tensor_blockdiag"
+    elif kname in ("wgrad_depthwise", "wgrad_grouped", "fwd_depthwise", "dgrad_depthwise") or kname == "generic":
+        bound = "alu"
+    else:
+        bound = "hbm"
+    tens_src = pk["source"] + " (dense bf16 GEMM, burst; fp16 runs at the same nominal rate)"
+    if bound == "tensor_blockdiag":
+        # Each 128-channel block runs as a dense MMA with a block-diagonal filter:
+        # the tensor pipe executes 128 / Cg times the useful multiply-adds.
+        waste = 128 // (p.c // p.groups)
+        achieved = flops * waste / (stage1_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": round(achieved / pk["bf16"], 4), "peak_source": tens_src,
+                "executed_per_useful": waste,
+                "useful_tflops": round(flops / (stage1_ms * 1e-3) / 1e12, 3),
+                "useful_frac_of_fp32_pipe": round(flops / (stage1_ms * 1e-3) / 1e12 / alu_peak, 4)}
+    elif bound == "tensor":
+        achieved = flops / (stage1_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": round(achieved / pk["bf16"], 4), "peak_source": tens_src}
+    elif bound == "hbm":
+        achieved = in_bytes / (stage1_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
+                "frac": round(achieved / pk["hbm"], 4), "peak_source": pk["source"] + " (HBM copy)"}
+    else:
+        achieved = flops / (stage1_ms * 1e-3) / 1e12
+        roof = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(alu_peak, 2), "unit": "TFLOP/s",
+                "frac": round(achieved / alu_peak, 4),
+                "peak_source": f"derived: {sms} SMs x 128 FP32 lanes x 2 flop x max SM clock"}
+    # HBM fraction beside any other bound (the bandwidth-bound kernels' targets are stated against HBM)
+    roof["hbm_frac"] = round(in_bytes / (stage1_ms * 1e-3) / 1e9 / pk["hbm"], 4)
+    return roof
+
+
+class Workload:
+    """One workload on the device: inputs, outputs, workspace and plan, and the
+    step (one call through the public API) and staged step (stage 1, then
+    stage 2, with an event between them)."""
+
+    def __init__(self, name, dev, sms, split_k=-1, fused=False, batch=0):
+        import torch
+        import implicit_gemm_convolution_nhwc_gb300 as cig
+        kw, direction, dist, args, seed, desc = WORKLOADS[name]
+        if batch:
+            kw = dict(kw, n=batch)
+            desc = f"{desc} [batch overridden to N={batch}]"
+        self.name, self.desc, self.direction = name, desc, direction
+        self.dist, self.args, self.seed = dist, args, seed
+        self.cig, self.torch = cig, torch
+        self.dev, self.sms = dev, sms
+        self.split_k, self.fused = split_k, fused
+        p = self.p = cig.Problem(**kw)
+        self.d = {"fwd": cig.DIR_FWD, "wgrad": cig.DIR_WGRAD, "dgrad": cig.DIR_DGRAD}[direction]
+        self.bias = direction == "wgrad"
+        self.x, self.b, _ = make_inputs_on_device(p, direction, dist, args, seed, dev)
+        ho, wo = p.out_hw
+        self.odt = odt = {0: torch.float32, 1: torch.bfloat16, 2: torch.float16}[p.out_dtype]
+        if direction == "fwd":
+            self.out, self.db = torch.empty((p.n, ho, wo, p.k), dtype=odt, device=dev), None
+        elif direction == "dgrad":
+            self.out, self.db = torch.empty((p.n, p.h, p.w, p.c), dtype=odt, device=dev), None
+        else:
+            self.out = torch.empty((p.k, p.r, p.s, p.c // p.groups), dtype=odt, device=dev)
+            self.db = torch.empty(p.k, dtype=odt, device=dev)
+        if fused and direction != "fwd":
+            raise SystemExit("--bias-relu applies to forward workloads only")
+        self.ep_bias = None
+        if fused:  # the fused bias + ReLU epilogue runs unsplit
+            import synth
+            self.ep_bias = synth.tensor((p.k,), odt, "normal", 0.0, 0.1, seed, synth.BIAS_ID).to(dev)
+            if split_k > 1:
+                raise SystemExit("--bias-relu runs unsplit: use --split-k -1, 0 or 1")
+        self.plan = cig.describe_plan(p, self.d, 1 if fused else split_k, self.bias, sm_count=sms)
+        self.ws = cig.workspace(p, self.d, 1 if fused else split_k, self.bias, dev)
+        self.in_bytes = problem_bytes(p, direction)
+        self.flush = None
+        if self.in_bytes < 4 * L2_BYTES:  # small inputs: flush L2 between steps
+            self.flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+
+    def call(self, x, b):
+        cig, p, s = self.cig, self.p, self.stream
+        if self.fused:
+            cig.conv_fwd_epilogue(p, x, b, self.out, self.ep_bias, 0.0, float("inf"), self.ws, self.split_k, s)
+        elif self.direction == "fwd":
+            cig.conv_fwd(p, x, b, self.out, self.ws, self.split_k, s)
+        elif self.direction == "dgrad":
+            cig.conv_dgrad(p, x, b, self.out, self.ws, self.split_k, s)
+        else:
+            cig.conv_wgrad_bias(p, x, b, self.out, self.db, self.ws, self.split_k, s)
+
+    def step(self, ev=None):
+        """One step through the user-facing call (stage 1 + fold)."""
+        if self.flush is not None:
+            self.flush.fill_(1.0)
+        if ev is not None:
+            ev[0].record(self.stream)
+        self.call(self.x, self.b)
+        if ev is not None:
+            ev[1].record(self.stream)
+
+    def staged(self, ev):
+        """The same step with an event between the stages (per-kernel times)."""
+        cig, p, s = self.cig, self.p, self.stream
+        if self.flush is not None:
+            self.flush.fill_(1.0)
+        ev[0].record(s)
+        if self.fused:  # one unsplit launch: all of it is stage 1
+            self.call(self.x, self.b)
+            ev[1].record(s)
+        else:
+            cig.conv_stage1(p, self.d, self.x, self.b, self.out, self.db, self.ws, self.split_k, s)
+            ev[1].record(s)
+            cig.conv_stage2(p, self.d, self.out, self.db, self.ws, self.split_k, s)
+        ev[2].record(s)
+
+    def launches_per_step(self):
+        kname = self.plan["kernel_name"]
+        return (1 + (1 if self.plan["needs_fold"] else 0) + (1 if kname == "generic" and self.bias else 0) +
+                (1 if kname in ("fwd_grouped_tc", "dgrad_grouped_tc") else 0))  # the filter expansion
+
+    def time(self, steps, warmup, world=1, sampler=None):
+        """(ms per step, stage-1 ms list, fold ms list). With an L2 flush between
+        steps only each step's call is timed; otherwise the whole back-to-back
+        region is."""
+        torch, dev, stream = self.torch, self.dev, self.stream
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            import torch.distributed as dist_
+            dist_.barrier()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        if sampler is not None:
+            sampler.mark(True)
+        start.record(stream)
+        for i in range(steps):
+            self.step(evs[i] if self.flush is not None else None)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        if sampler is not None:
+            sampler.mark(False)
+        total_ms = sum(e[0].elapsed_time(e[1]) for e in evs) if self.flush is not None else start.elapsed_time(end)
+        if world > 1:
+            total_ms = max_over_ranks(total_ms, dev)
+        sev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        for i in range(steps):
+            self.staged(sev[i])
+        torch.cuda.synchronize(dev)
+        s1 = [e[0].elapsed_time(e[1]) for e in sev]
+        s2 = [e[1].elapsed_time(e[2]) for e in sev]
+        return total_ms / steps, s1, s2
+
+    def free(self):
+        self.x = self.b = self.out = self.db = self.ws = self.flush = self.ep_bias = None
+
+
+def per_config(dev, sms, pk, steps, warmup):
+    """Every configuration (and the supplement) at its automatic plan, under one
+    clock sampler: kernel, degree, stage-1 and step times, and the roofline."""
+    import torch
+    out = {}
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    time.sleep(0.3)
+    t_begin = time.time()
+    for name in PER_CONFIG:
+        if name not in WORKLOADS:
+            continue
+        try:
+            wl = Workload(name, dev, sms)
+        except Exception as e:  # pragma: no cover - reported, not fatal
+            out[name] = {"error": str(e)[:200]}
+            continue
+        kname = wl.plan["kernel_name"]
+        if kname == "generic" and wl.p.flops() > 2e10:  # the direct kernel would take seconds per step
+            out[name] = {"kernel": kname, "skipped": "generic kernel on a large problem"}
+            wl.free()
+            continue
+        ms, s1, s2 = wl.time(steps, warmup)
+        st1 = statistics.mean(s1)
+        flops = wl.p.flops()
+        roof = roofline_for(kname, wl.p, wl.direction, flops, wl.in_bytes, st1, pk, sms)
+        entry = {"workload": wl.desc, "kernel": kname, "split_k": wl.plan["split_k"],
+                 "fold_width": wl.plan.get("fold_width", 1), "ctas": wl.plan["ctas"],
+                 "step_ms": round(ms, 5), "stage1_ms": round(st1, 5), "fold_ms": round(statistics.mean(s2), 5),
+                 "tflops": round(flops / (ms * 1e-3) / 1e12, 3), "launches_per_step": wl.launches_per_step(),
+                 "l2": "flushed" if wl.flush is not None else "inputs larger than L2",
+                 "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac", "hbm_frac")
+                              if k in roof}}
+        if "useful_frac_of_fp32_pipe" in roof:
+            entry["roofline"]["useful_frac_of_fp32_pipe"] = roof["useful_frac_of_fp32_pipe"]
+        wl.free()
+        for req in SWEEP.get(name, []):
+            sw = Workload(name, dev, sms, split_k=req)
+            ms_s, s1_s, _ = sw.time(steps, warmup)
+            entry.setdefault("split_sweep", []).append(
+                {"request": req, "split_k": sw.plan["split_k"], "step_ms": round(ms_s, 5),
+                 "stage1_ms": round(statistics.mean(s1_s), 5)})
+            sw.free()
+        out[name] = entry
+        torch.cuda.empty_cache()
+    out["clocks"] = sampler.stop()
+    out["seconds"] = round(time.time() - t_begin, 1)
+    out["timing"] = ("per workload: warm-up, then each step (one call through the public API) timed with CUDA "
+                     "events on its stream; L2 flushed between steps when the inputs are smaller than 4x L2")
+    return out
+
+
 def run_ours(a, rank, world, local_rank):
     import torch
     import implicit_gemm_convolution_nhwc_gb300 as cig
@@ -338,153 +579,21 @@ def run_ours(a, rank, world, local_rank):
     cig.load(build_if_missing=True)
     if a.kernel != "auto":
         cig.set_kernel_override(a.kernel)
-    kw, direction, dist, args, seed, desc = WORKLOADS[a.workload]
-    if a.batch:
-        kw = dict(kw, n=a.batch)
-        desc = f"{desc} [batch overridden to N={a.batch}]"
-    p = cig.Problem(**kw)
-    d = {"fwd": cig.DIR_FWD, "wgrad": cig.DIR_WGRAD, "dgrad": cig.DIR_DGRAD}[direction]
-    bias = direction == "wgrad"
-    x, b, _ = make_inputs_on_device(p, direction, dist, args, seed, dev)
-    ho, wo = p.out_hw
-    odt = {0: torch.float32, 1: torch.bfloat16, 2: torch.float16}[p.out_dtype]
-    if direction == "fwd":
-        out = torch.empty((p.n, ho, wo, p.k), dtype=odt, device=dev)
-        db = None
-    elif direction == "dgrad":
-        out = torch.empty((p.n, p.h, p.w, p.c), dtype=odt, device=dev)
-        db = None
-    else:
-        out = torch.empty((p.k, p.r, p.s, p.c // p.groups), dtype=odt, device=dev)
-        db = torch.empty(p.k, dtype=odt, device=dev)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    fused = bool(a.bias_relu)
-    if fused and direction != "fwd":
-        raise SystemExit("--bias-relu applies to forward workloads only")
-    ep_bias = None
-    if fused:  # the fused bias + ReLU epilogue runs unsplit
-        import synth
-        ep_bias = synth.tensor((p.k,), odt, "normal", 0.0, 0.1, seed, synth.BIAS_ID).to(dev)
-        if a.split_k > 1:
-            raise SystemExit("--bias-relu runs unsplit: use --split-k -1, 0 or 1")
-    plan = cig.describe_plan(p, d, 1 if fused else a.split_k, bias, sm_count=sms)
-    ws = cig.workspace(p, d, 1 if fused else a.split_k, bias, dev)
-    in_bytes = problem_bytes(p, direction)
-    flush = None
-    if in_bytes - 0 < 4 * L2_BYTES:  # small inputs: flush L2 between steps
-        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def step(ev=None):
-        """One step through the user-facing call (stage 1 + fold)."""
-        if flush is not None:
-            flush.fill_(1.0)
-        if ev is not None:
-            ev[0].record(stream)
-        if fused:
-            cig.conv_fwd_epilogue(p, x, b, out, ep_bias, 0.0, float("inf"), ws, a.split_k, stream)
-        elif direction == "fwd":
-            cig.conv_fwd(p, x, b, out, ws, a.split_k, stream)
-        elif direction == "dgrad":
-            cig.conv_dgrad(p, x, b, out, ws, a.split_k, stream)
-        else:
-            cig.conv_wgrad_bias(p, x, b, out, db, ws, a.split_k, stream)
-        if ev is not None:
-            ev[1].record(stream)
-
-    def staged(ev):
-        """The same step with an event between the stages (per-kernel times)."""
-        if flush is not None:
-            flush.fill_(1.0)
-        ev[0].record(stream)
-        if fused:  # one unsplit launch: all of it is stage 1
-            cig.conv_fwd_epilogue(p, x, b, out, ep_bias, 0.0, float("inf"), ws, a.split_k, stream)
-            ev[1].record(stream)
-        else:
-            cig.conv_stage1(p, d, x, b, out, db, ws, a.split_k, stream)
-            ev[1].record(stream)
-            cig.conv_stage2(p, d, out, db, ws, a.split_k, stream)
-        ev[2].record(stream)
-
-    for _ in range(a.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        import torch.distributed as dist_
-        dist_.barrier()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(a.steps)]
+    wl = Workload(a.workload, dev, sms, split_k=a.split_k, fused=bool(a.bias_relu), batch=a.batch)
+    p, direction, plan = wl.p, wl.direction, wl.plan
+    in_bytes, flush = wl.in_bytes, wl.flush
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(dev)
-    sampler.mark(True)
-    start.record(stream)
-    for i in range(a.steps):
-        step(evs[i] if flush is not None else None)
-    end.record(stream)
-    torch.cuda.synchronize(dev)
-    sampler.mark(False)
+    ms_step, s1, s2 = wl.time(a.steps, a.warmup, world, sampler)
     clocks = sampler.stop()
-    # With an L2 flush between steps, only each step's call is timed;
-    # otherwise the whole back-to-back region is.
-    total_ms = sum(e[0].elapsed_time(e[1]) for e in evs) if flush is not None else start.elapsed_time(end)
-    if world > 1:
-        total_ms = max_over_ranks(total_ms, dev)
-    # Per-kernel durations (stage 1 is the roofline's kernel), from a second
-    # loop with an event between the stages.
-    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.steps)]
-    for i in range(a.steps):
-        staged(sev[i])
-    torch.cuda.synchronize(dev)
-    s1 = [e[0].elapsed_time(e[1]) for e in sev]
-    s2 = [e[1].elapsed_time(e[2]) for e in sev]
-    ms_step = total_ms / a.steps
     flops = p.flops()
     value = flops * world / (ms_step * 1e-3) / 1e12
     pk = peaks()
     stage1_ms = statistics.mean(s1)
     kname = plan["kernel_name"]
-    if kname in ("wgrad_1x1_tf32x3", "wgrad_1x1_ffma") or direction == "wgrad" and kname == "generic" and p.r == 1:
-        bound = "hbm"
-    elif kname in ("fwd_tc", "fwd_tc_cluster", "dgrad_tc"):
-        # past the ridge point (flop per byte of the measured peaks) the tensor
-        # pipe bounds it, else HBM
-        bound = "tensor" if flops / in_bytes > pk["bf16"] * 1e12 / (pk["hbm"] * 1e9) else "hbm"
-    elif kname in ("fwd_grouped_tc", "wgrad_grouped_tc"):
-        bound = "tensor_blockdiag"
-    elif kname in ("wgrad_depthwise", "wgrad_grouped", "fwd_depthwise") or kname == "generic":
-        bound = "alu"
-    else:
-        bound = "hbm"
-    if bound == "tensor_blockdiag":
-        # Each 128-channel block runs as a dense MMA with a block-diagonal filter:
-        # the tensor pipe executes 128 / Cg times the useful multiply-adds.
-        waste = 128 // (p.c // p.groups)
-        achieved = flops * waste / (stage1_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
-                "frac": round(achieved / pk["bf16"], 4),
-                "peak_source": pk["source"] + " (dense bf16 GEMM, burst; fp16 runs at the same nominal rate)",
-                "executed_per_useful": waste,
-                "useful_tflops": round(flops / (stage1_ms * 1e-3) / 1e12, 3),
-                "useful_frac_of_fp32_pipe": round(flops / (stage1_ms * 1e-3) / 1e12 /
-                                                  (152 * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12), 4)}
-    elif bound == "tensor":
-        achieved = flops / (stage1_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
-                "frac": round(achieved / pk["bf16"], 4),
-                "peak_source": pk["source"] + " (dense bf16 GEMM, burst; fp16 runs at the same nominal rate)"}
-    elif bound == "hbm":
-        achieved = in_bytes / (stage1_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
-                "frac": round(achieved / pk["hbm"], 4), "peak_source": pk["source"] + " (HBM copy)"}
-    else:
-        alu_peak = 152 * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12  # FP32 FMA lanes x 2 flop x max clock
-        achieved = flops / (stage1_ms * 1e-3) / 1e12
-        roof = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(alu_peak, 2), "unit": "TFLOP/s",
-                "frac": round(achieved / alu_peak, 4),
-                "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop x max SM clock"}
+    roof = roofline_for(kname, p, direction, flops, in_bytes, stage1_ms, pk, sms)
     roof["kernel"] = kname
     roof["traffic"] = recorded_traffic(kname, a.workload)
     roof["kernel_ms"] = round(stage1_ms, 5)
@@ -493,25 +602,19 @@ def run_ours(a, rank, world, local_rank):
     # e2e: inputs from pinned host memory and the result back, every step
     e2e = None
     if not a.no_e2e:
-        del x, b
+        out, db = wl.out, wl.db
+        wl.x = wl.b = None
         torch.cuda.empty_cache()
-        xh_d, bh_d, hosts = make_inputs_on_device(p, direction, dist, args, seed, dev, pinned_copy=True)
-        out_h = torch.empty(out.shape, dtype=odt, pin_memory=True)
-        db_h = torch.empty(p.k, dtype=odt, pin_memory=True) if db is not None else None
+        xh_d, bh_d, hosts = make_inputs_on_device(p, direction, wl.dist, wl.args, wl.seed, dev, pinned_copy=True)
+        out_h = torch.empty(out.shape, dtype=wl.odt, pin_memory=True)
+        db_h = torch.empty(p.k, dtype=wl.odt, pin_memory=True) if db is not None else None
         h2d = hosts[0].numel() * hosts[0].element_size() + hosts[1].numel() * hosts[1].element_size()
         d2h = out.numel() * out.element_size() + (db.numel() * db.element_size() if db is not None else 0)
 
         def e2e_step():
             xh_d.copy_(hosts[0], non_blocking=True)
             bh_d.copy_(hosts[1], non_blocking=True)
-            if fused:
-                cig.conv_fwd_epilogue(p, xh_d, bh_d, out, ep_bias, 0.0, float("inf"), ws, a.split_k, stream)
-            elif direction == "fwd":
-                cig.conv_fwd(p, xh_d, bh_d, out, ws, a.split_k, stream)
-            elif direction == "dgrad":
-                cig.conv_dgrad(p, xh_d, bh_d, out, ws, a.split_k, stream)
-            else:
-                cig.conv_wgrad_bias(p, xh_d, bh_d, out, db, ws, a.split_k, stream)
+            wl.call(xh_d, bh_d)
             out_h.copy_(out, non_blocking=True)
             if db_h is not None:
                 db_h.copy_(db, non_blocking=True)
@@ -521,28 +624,36 @@ def run_ours(a, rank, world, local_rank):
         n_e2e = max(1, min(a.steps, 5))
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
+        t0.record(wl.stream)
         for _ in range(n_e2e):
             e2e_step()
-        t1.record(stream)
+        t1.record(wl.stream)
         torch.cuda.synchronize(dev)
         e2e_ms = t0.elapsed_time(t1) / n_e2e
         e2e = {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                "steps": n_e2e}
         del xh_d, bh_d, hosts
+    launches = wl.launches_per_step()
+    wl.free()
+    torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        fps, secs, n_s, used = time_oracle(p, direction, dist, args, seed, a.cpu_seconds)
+        fps, secs, n_s, used = time_oracle(p, direction, wl.dist, wl.args, wl.seed, a.cpu_seconds)
         cpu = {"value": round(fps / 1e12, 6), "unit": "TFLOP/s", "cores": used, "kind": "oracle",
                "sample": f"first {n_s} of {p.n} batch samples, every output, fp64 oracle ({secs:.1f} s)"}
+
+    configs = None
+    if world == 1 and not a.no_per_config and a.kernel == "auto" and not a.batch:
+        cig.set_kernel_override("auto")
+        configs = per_config(dev, sms, pk, a.per_config_steps, a.warmup)
 
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": DT_NAME[p.in_dtype], "data": "synthetic (seeded counter-based generator)",
-        "config": {"workload": desc + (" + fused bias/ReLU epilogue" if fused else ""), "name": a.workload,
+        "config": {"workload": wl.desc + (" + fused bias/ReLU epilogue" if wl.fused else ""), "name": a.workload,
                    "kernel": kname, "split_k": plan["split_k"], "fold_width": plan.get("fold_width", 1),
                    "split_k_request": a.split_k, "ctas": plan["ctas"], "workspace_bytes": plan["workspace_bytes"],
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
@@ -550,14 +661,14 @@ def run_ours(a, rank, world, local_rank):
                    else f"inputs larger than L2 ({in_bytes / 1e9:.2f} GB)",
                    "algorithmic_bytes": in_bytes, "flops_per_step": flops},
         "roofline": roof, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
-        "gpu_launches": a.steps * (1 + (1 if plan["needs_fold"] else 0) +
-                                   (1 if kname == "generic" and bias else 0) +
-                                   (1 if kname == "fwd_grouped_tc" else 0)),  # its filter expansion
+        "gpu_launches": a.steps * launches,
         "timing": "value: the timed steps through conv_wgrad_bias / conv_fwd / conv_dgrad; stage_ms: a second loop of "
                   "conv_stage1 + conv_stage2 with an event between them",
         "stage_ms": {"stage1_mean": round(stage1_ms, 5), "stage1_min": round(min(s1), 5),
                      "fold_mean": round(statistics.mean(s2), 5)},
     }
+    if configs is not None:
+        line["per_config"] = configs
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -626,6 +737,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--batch", type=int, default=0, help="override N (small cases for profiling)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-configuration block after the headline")
+    ap.add_argument("--per-config-steps", type=int, default=20)
     a = ap.parse_args()
     if a.warmup < 3:
         a.warmup = 3

@@ -199,9 +199,12 @@ conv_status resolve_degree(const Shape& s, conv_dir dir, const Geometry& g, int3
 // The kernel for a problem, folding its width when only the folded problem
 // has a kernel faster than the generic one (then *s becomes the folded shape
 // and *fold its factor).
+// A forced kernel (the testing override) applies to the problem as given:
+// no fold is tried, so a kernel that cannot take it fails the call.
 conv_status choose_kernel_folded(Shape* s, conv_dir dir, conv_kernel* kernel, Geometry* geo, int64_t* fold) {
   *fold = 1;
   conv_status st = choose_kernel(*s, dir, kernel, geo);
+  if (g_kernel_override != CONV_KERNEL_AUTO) return st;
   if (st == CONV_OK && *kernel != CONV_KERNEL_GENERIC) return st;
   const int64_t f = fold_width_of(*s);
   if (f < 2) return st;
@@ -501,22 +504,16 @@ namespace {
 constexpr uint64_t kStaticScratchBytes = 8ull << 20;  // 8 MiB on every device that loads the library
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-// The array's device address on the current device, looked up once per device
-// (the first call on a device does this set-up).
+// The array's device address in the current context, looked up on every call
+// (no cache: after a device reset the module reloads and the array may move).
+// The first lookup on a device loads the library's module there, which commits
+// the array's 8 MiB.
 void* static_scratch_address() {
-  static void* cached[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
-    cudaGetLastError();
-    return nullptr;
-  }
-  if (dev < 64 && cached[dev]) return cached[dev];
   void* ptr = nullptr;
   if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess) {
     cudaGetLastError();
     return nullptr;
   }
-  if (dev < 64) cached[dev] = ptr;
   return ptr;
 }
 
@@ -532,8 +529,10 @@ conv_status conv_wgrad_bias_static_ws(const conv_problem* p, const void* x, cons
   conv_status st = conv_workspace_bytes_for(p, CONV_DIR_WGRAD, split_k, 1, sms, &need);
   if (st != CONV_OK) return st;
   if (need > kStaticScratchBytes) return CONV_ERR_WORKSPACE_TOO_SMALL;
-  void* scratch = need > 0 ? static_scratch_address() : nullptr;
-  if (need > 0 && !scratch) return CONV_ERR_CUDA;
+  // Looked up even when this call needs no slabs, so an empty-batch call
+  // (n = 0) serves as the set-up call that loads the module.
+  void* scratch = static_scratch_address();
+  if (!scratch) return CONV_ERR_CUDA;
   return run(p, CONV_DIR_WGRAD, x, dy, dw, db, scratch, need > 0 ? kStaticScratchBytes : 0, split_k, stream, true,
              kBoth);
 }

@@ -52,17 +52,14 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
   return r == CUDA_SUCCESS;
 }
 
+// Looked up on every call, not cached: after a device reset the module reloads
+// in a new context and the word may live at another address.
 unsigned* device_error_word() {
-  static unsigned* cached[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
-  if (dev < 64 && cached[dev]) return cached[dev];
   void* p = nullptr;
   if (cudaGetSymbolAddress(&p, g_conv_device_errors) != cudaSuccess) {
     cudaGetLastError();
     return nullptr;
   }
-  if (dev < 64) cached[dev] = static_cast<unsigned*>(p);
   return static_cast<unsigned*>(p);
 }
 

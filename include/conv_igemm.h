@@ -31,8 +31,11 @@
  *    enqueues its kernels on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream). Pointers must be 16-byte aligned device pointers.
  *  - Errors are loud [P1 "Motivation"]: every argument is checked before the
- *    first launch, so a non-OK status means nothing was enqueued, except
- *    CONV_ERR_CUDA, which reports a failed launch.
+ *    first launch, so a status other than CONV_OK and CONV_ERR_CUDA means
+ *    nothing was enqueued. CONV_ERR_CUDA reports a failed CUDA call; when a
+ *    call enqueues two kernels (stage 1, then the fold or the bias sum) and
+ *    the second launch fails, the first is already enqueued on the stream, so
+ *    after CONV_ERR_CUDA the outputs (and the workspace) are undefined.
  *  - Split-K [P2 "Two-stage split-K"]: the reduction (N*Ho*Wo for the weight
  *    gradient, R*S*Cg for the forward) is cut into S slices. Stage 1 writes
  *    one fp32 partial slab per slice into the caller's workspace, each
@@ -105,10 +108,9 @@ typedef enum conv_kernel {
                                         thread-block cluster folding through distributed
                                         shared memory [P2 "Changes": single-launch split-K]:
                                         no workspace, no stage 2 */
-  CONV_KERNEL_DGRAD_TC = 8,          /* 16-bit, stride-1, ungrouped data gradient: the filter
-                                        rotated 180 degrees with k and c swapped (written into
-                                        the workspace), then the forward tensor-core kernel
-                                        over dY */
+  CONV_KERNEL_DGRAD_TC = 8,          /* 16-bit, stride-1, ungrouped data gradient: the forward
+                                        tensor-core kernel over dY with the filter rotated 180
+                                        degrees and k and c swapped, read in place (MN-major) */
   CONV_KERNEL_FWD_DEPTHWISE = 9,     /* depthwise forward (C = K = groups, C even, filter
                                         width 3/5/7, W stride 1/2), CUDA cores, unsplit */
   CONV_KERNEL_FWD_GROUPED_TC = 10,   /* 16-bit grouped forward (Cg = Kg dividing 128, C % 128 = 0):
@@ -259,8 +261,14 @@ int64_t conv_batch_split_count(int64_t n, int64_t max_n);
  *  - A degree whose slabs need more than 8 MiB (conv_workspace_bytes with
  *    with_bias = 1 above 8388608) is rejected with
  *    CONV_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
- *  - The first call on a device looks up the array's device address on that
- *    device (once); make that first call before any stream capture.
+ *  - Every call looks up the array's device address in the current context
+ *    (cudaGetSymbolAddress). The first call on a device loads the library's
+ *    module there, which commits the array's 8 MiB of device memory: that
+ *    first call is a one-time allocation by the CUDA runtime and can fail
+ *    with CONV_ERR_CUDA when the device memory is exhausted, so make it
+ *    during set-up and before any stream capture. A call with an empty batch
+ *    (p->n = 0, NULL tensors allowed where they hold no elements) does only
+ *    that set-up and writes dw = db = 0.
  *  - Every call shares the one array. Its contents between calls do not
  *    matter (every slab element is written before it is read), but two calls
  *    whose kernels overlap on the GPU (different streams, no ordering) race
@@ -282,8 +290,9 @@ conv_status conv_device_errors(uint32_t* flags, int32_t clear);
 conv_status conv_selftest_wait_timeout(uint64_t limit_ns, uint32_t* gave_up, void* stream);
 
 /* Testing aid: force stage 1 to one kernel (CONV_KERNEL_AUTO restores the
- * normal choice). A forced kernel that cannot take a problem makes the call
- * fail with CONV_ERR_UNSUPPORTED. Process-wide, not thread-safe. */
+ * normal choice). The forced kernel runs the problem as given (no width fold
+ * is tried); a forced kernel that cannot take it makes the call fail with
+ * CONV_ERR_UNSUPPORTED. Process-wide, not thread-safe. */
 conv_status conv_set_kernel_override(int32_t kernel);
 
 #ifdef __cplusplus

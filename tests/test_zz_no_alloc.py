@@ -6,7 +6,9 @@ plugin/enqueue path forbids allocation after set-up) and hold no workspace:
 its split-K slabs live in one fixed 8 MiB device array inside the library.
 These tests call it through the C ABI and compare it with conv_wgrad_bias on
 the same inputs, twice in a row (the array keeps the previous call's
-contents, which must not matter). This file is collected last on purpose.
+contents, which must not matter). Both calls run the same kernels at the same
+split-K degree, so the outputs must be bit-identical. This file is collected
+last on purpose.
 """
 import ctypes
 
@@ -27,14 +29,24 @@ def _regular(p, x, dy, split_k):
     return dw, db
 
 
-def _static(p, x, dy, split_k):
-    dw = torch.full((p.k, p.r, p.s, p.c // p.groups), float("nan"), dtype=x.dtype, device="cuda")
-    db = torch.full((p.k,), float("nan"), dtype=x.dtype, device="cuda")
+def _static_into(p, x, dy, dw, db, split_k):
     lib = cig.load()
     st = lib.conv_wgrad_bias_static_ws(cig._cp(p), x.data_ptr(), dy.data_ptr(), dw.data_ptr(), db.data_ptr(),
                                        split_k, torch.cuda.current_stream().cuda_stream)
     assert st == 0, cig.STATUS[st]
-    return dw, db
+
+
+def _setup_call():
+    """The documented set-up call: an empty batch loads the module and commits the array."""
+    p0 = cig.Problem(n=0, h=8, w=8, c=8, k=8)
+    dw = torch.empty((8, 1, 1, 8), device="cuda")
+    db = torch.empty(8, device="cuda")
+    lib = cig.load()
+    st = lib.conv_wgrad_bias_static_ws(cig._cp(p0), None, None, dw.data_ptr(), db.data_ptr(), -1,
+                                       torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert st == 0, cig.STATUS[st]
+    assert not dw.any() and not db.any()
 
 
 @pytest.mark.parametrize("shape, split_k", [
@@ -46,12 +58,22 @@ def test_static_workspace_matches_the_workspace_call(shape, split_k):
     x, dy = inputs(p, 11)
     x, dy = x.cuda(), dy.cuda()
     assert 0 < cig.workspace_bytes(p, cig.DIR_WGRAD, split_k, True) <= cig.STATIC_WS_BYTES
+    _setup_call()
     ref_w, ref_b = _regular(p, x, dy, split_k)
-    for _ in range(2):  # two calls in a row share (and overwrite) the array
-        dw, db = _static(p, x, dy, split_k)
+    torch.cuda.synchronize()
+    for i in range(2):  # two calls in a row share (and overwrite) the array
+        dw = torch.full((p.k, p.r, p.s, p.c // p.groups), float("nan"), dtype=x.dtype, device="cuda")
+        db = torch.full((p.k,), float("nan"), dtype=x.dtype, device="cuda")
         torch.cuda.synchronize()
+        before = (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0])
+        _static_into(p, x, dy, dw, db, split_k)
+        torch.cuda.synchronize()
+        after = (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0])
+        assert after == before, f"call {i}: device memory changed {before} -> {after}"
+        # same kernels, same degree: bit-identical to the workspace call
+        assert torch.equal(dw, ref_w), f"call {i}: dW differs"
+        assert torch.equal(db, ref_b), f"call {i}: db differs"
         assert relerr(dw.cpu(), ref_w.cpu().double().numpy()) <= tol(p)
-        assert relerr(db.cpu(), ref_b.cpu().double().numpy()) <= tol(p)
     assert cig.device_errors() == 0
 
 
