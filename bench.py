@@ -171,7 +171,7 @@ class ClockSampler:
                 continue
             rows.append((t, f))
         inside = [f for t, f in rows if self.t0 is not None and self.t0 - 0.1 <= t <= (self.t1 or t) + 0.1]
-        use = inside or rows
+        use = inside or [f for t, f in rows]
         if not use:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
 
@@ -528,6 +528,7 @@ def per_config(dev, sms, pk, steps, warmup):
     sampler.start()
     time.sleep(0.3)
     t_begin = time.time()
+    sampler.mark(True)
     for name in PER_CONFIG:
         if name not in WORKLOADS:
             continue
@@ -564,6 +565,7 @@ def per_config(dev, sms, pk, steps, warmup):
             sw.free()
         out[name] = entry
         torch.cuda.empty_cache()
+    sampler.mark(False)
     out["clocks"] = sampler.stop()
     out["seconds"] = round(time.time() - t_begin, 1)
     out["timing"] = ("per workload: warm-up, then each step (one call through the public API) timed with CUDA "

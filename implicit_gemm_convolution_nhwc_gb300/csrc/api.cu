@@ -81,6 +81,7 @@ Geometry geometry_of(conv_kernel k, const Shape& s, conv_dir dir) {
     case CONV_KERNEL_FWD_DEPTHWISE: return dir == CONV_DIR_FWD ? geometry_fwd_depthwise(s) : Geometry{};
     case CONV_KERNEL_FWD_GROUPED_TC: return dir == CONV_DIR_FWD ? geometry_fwd_grouped_tc(s) : Geometry{};
     case CONV_KERNEL_WGRAD_GROUPED_TC: return dir == CONV_DIR_WGRAD ? geometry_wgrad_grouped_tc(s) : Geometry{};
+    case CONV_KERNEL_WGRAD_TC: return dir == CONV_DIR_WGRAD ? geometry_wgrad_tc(s) : Geometry{};
     case CONV_KERNEL_WGRAD_DEPTHWISE: return dir == CONV_DIR_WGRAD ? geometry_wgrad_depthwise(s) : Geometry{};
     case CONV_KERNEL_WGRAD_GROUPED: return dir == CONV_DIR_WGRAD ? geometry_wgrad_grouped(s) : Geometry{};
     default: return Geometry{};
@@ -130,15 +131,16 @@ conv_status choose_kernel(const Shape& s, conv_dir dir, conv_kernel* kernel, Geo
     return CONV_OK;
   }
   static const conv_kernel wgrad_order[] = {CONV_KERNEL_WGRAD_1X1_TF32X3, CONV_KERNEL_WGRAD_1X1_FFMA,
-                                            CONV_KERNEL_WGRAD_DEPTHWISE, CONV_KERNEL_WGRAD_GROUPED_TC,
-                                            CONV_KERNEL_WGRAD_GROUPED, CONV_KERNEL_GENERIC};
+                                            CONV_KERNEL_WGRAD_DEPTHWISE,   CONV_KERNEL_WGRAD_GROUPED_TC,
+                                            CONV_KERNEL_WGRAD_TC,          CONV_KERNEL_WGRAD_GROUPED,
+                                            CONV_KERNEL_GENERIC};
   // The cluster form of the forward is reached only through the override:
   // on the 3x3 small-M layer it measured slower than the two-stage form.
   static const conv_kernel fwd_order[] = {CONV_KERNEL_FWD_TC, CONV_KERNEL_FWD_DEPTHWISE, CONV_KERNEL_FWD_GROUPED_TC,
                                           CONV_KERNEL_GENERIC};
   static const conv_kernel dgrad_order[] = {CONV_KERNEL_DGRAD_TC, CONV_KERNEL_GENERIC};
   const conv_kernel* order = dir == CONV_DIR_WGRAD ? wgrad_order : dir == CONV_DIR_FWD ? fwd_order : dgrad_order;
-  const int count = dir == CONV_DIR_WGRAD ? 6 : dir == CONV_DIR_FWD ? 4 : 2;
+  const int count = dir == CONV_DIR_WGRAD ? 7 : dir == CONV_DIR_FWD ? 4 : 2;
   for (int i = 0; i < count; ++i) {
     Geometry g = geometry_of(order[i], s, dir);
     if (g.ok) {
@@ -333,6 +335,7 @@ conv_status run(const conv_problem* prob, conv_dir dir, const void* x, const voi
       case CONV_KERNEL_FWD_DEPTHWISE: err = launch_fwd_depthwise(plan, a); break;
       case CONV_KERNEL_FWD_GROUPED_TC: err = launch_fwd_grouped_tc(plan, a); break;
       case CONV_KERNEL_WGRAD_GROUPED_TC: err = launch_wgrad_grouped_tc(plan, a); break;
+      case CONV_KERNEL_WGRAD_TC: err = launch_wgrad_tc(plan, a); break;
       case CONV_KERNEL_WGRAD_DEPTHWISE: err = launch_wgrad_depthwise(plan, a); break;
       case CONV_KERNEL_WGRAD_GROUPED: err = launch_wgrad_grouped(plan, a); break;
       default: return CONV_ERR_UNSUPPORTED;
@@ -539,7 +542,7 @@ conv_status conv_wgrad_bias_static_ws(const conv_problem* p, const void* x, cons
 
 
 conv_status conv_set_kernel_override(int32_t kernel) {
-  if (kernel < CONV_KERNEL_AUTO || kernel > CONV_KERNEL_WGRAD_GROUPED_TC) return CONV_ERR_INVALID_ARG;
+  if (kernel < CONV_KERNEL_AUTO || kernel > CONV_KERNEL_WGRAD_TC) return CONV_ERR_INVALID_ARG;
   g_kernel_override = kernel;
   return CONV_OK;
 }

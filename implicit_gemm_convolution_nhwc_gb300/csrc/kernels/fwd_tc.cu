@@ -33,7 +33,7 @@
 // its shared memory) alive until its peers have read it.
 //
 // Warp roles: 0 TMA producer, 1 MMA issuer, 2 TMEM owner, 4-7 epilogue.
-#include "tc_common.cuh"
+#include "tc_store.cuh"
 
 namespace cig {
 namespace {
@@ -88,95 +88,6 @@ struct FwdParams {
   float ep_lo, ep_hi;
   int32_t ep;
 };
-
-// 16 bytes of TE from 4 (fp32) or 8 (16-bit) values, rounded to nearest even.
-template <typename TE>
-__device__ __forceinline__ uint4 pack16(const float* v);
-template <>
-__device__ __forceinline__ uint4 pack16<float>(const float* v) {
-  return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
-}
-template <>
-__device__ __forceinline__ uint4 pack16<__nv_bfloat16>(const float* v) {
-  uint4 r;
-  __nv_bfloat162 h[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-  memcpy(&r, h, 16);
-  return r;
-}
-template <>
-__device__ __forceinline__ uint4 pack16<__half>(const float* v) {
-  uint4 r;
-  __half2 h[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
-  memcpy(&r, h, 16);
-  return r;
-}
-
-// Epilogue of the two-stage form: the tile's rows go through shared memory
-// and TMA tensor stores. For each 128-byte column chunk (32 fp32 or 64 16-bit
-// channels) the thread of row m writes its 128 bytes into a 128B-swizzled
-// staging buffer (8 conflict-free 16-byte stores; two 16 KB buffers in the
-// idle ring, alternating), and one thread stores the box {chunk, TR*Wo
-// pixels, 1}; the tensor map clips it at K and at the image's Ho*Wo pixels.
-// Few instructions per thread: the four epilogue warps issue every one of
-// them, one CTA per SM.
-template <typename TE, int BN>
-__device__ __forceinline__ void store_tile_tma(uint32_t trow, uint8_t* stage, const CUtensorMap* tm, int32_t kx0,
-                                               int32_t kx_end, int32_t py, int32_t pz, int m, bool have_acc,
-                                               bool leader, bool do_store, const float* ep_bias = nullptr,
-                                               float ep_lo = 0.f, float ep_hi = 0.f, bool ep = false) {
-  constexpr int CW = 128 / (int)sizeof(TE);  // channels per 128-byte chunk
-  constexpr int VPU = 16 / (int)sizeof(TE);  // values per 16-byte unit
-  // Only chunks that start below K: each one then commits exactly one bulk
-  // group, which the buffer-reuse wait below counts on.
-  const int nch = min(BN / CW, (kx_end - kx0 + CW - 1) / CW);
-#pragma unroll 1
-  for (int c = 0; c < nch; ++c) {
-    uint8_t* buf = stage + (c & 1) * (kBM * 128);
-    if (c >= 2) {  // the store that last read this buffer (chunk c - 2) must be done reading
-      if (leader) bulk_wait_read<1>();
-      named_bar_sync(1, 128);
-    }
-    float v[CW];
-#pragma unroll
-    for (int h = 0; h < CW / 32; ++h) {
-      if (have_acc) {
-        tmem_ld32(trow + (uint32_t)(c * CW + 32 * h), v + 32 * h);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[32 * h + i] = 0.f;
-      }
-    }
-    if (ep) {  // bias (staged in shared memory, fp32) + clamp on the accumulator, before the rounding
-      const float4* b4 = reinterpret_cast<const float4*>(ep_bias + c * CW);
-#pragma unroll
-      for (int i = 0; i < CW; i += 4) {
-        const float4 b = b4[i / 4];
-        v[i] = fminf(fmaxf(v[i] + b.x, ep_lo), ep_hi);
-        v[i + 1] = fminf(fmaxf(v[i + 1] + b.y, ep_lo), ep_hi);
-        v[i + 2] = fminf(fmaxf(v[i + 2] + b.z, ep_lo), ep_hi);
-        v[i + 3] = fminf(fmaxf(v[i + 3] + b.w, ep_lo), ep_hi);
-      }
-    }
-    uint8_t* row = buf + m * 128;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const uint4 pk = pack16<TE>(v + u * VPU);
-      st_shared_v4(row + ((u ^ (m & 7)) << 4), pk.x, pk.y, pk.z, pk.w);
-    }
-    fence_proxy_async_smem();
-    named_bar_sync(1, 128);
-    if (leader && do_store) {
-      tma_store_3d(tm, buf, kx0 + c * CW, py, pz);
-      bulk_commit();
-    }
-  }
-  if (leader) bulk_wait<0>();
-  named_bar_sync(1, 128);  // the staging buffers are free again for a next call
-}
 
 template <typename TO>
 __device__ __forceinline__ void store4(TO* dst, float4 v);
@@ -375,13 +286,15 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
         const int64_t hrow = ho0 + h * fp.TR;
         if (hrow >= fp.Ho) break;  // a sub-tile past the image (uniform over the 128 threads)
         const int32_t py = (int32_t)(hrow * fp.Wo);
+        // the box {chunk, TR*Wo pixels, 1} at (channel, first pixel, image), clipped at K and Ho*Wo
+        const int32_t pz = ws ? (int32_t)(sigma * fp.N + img) : (int32_t)img;
+        auto store = [&](const void* buf, int32_t x) { tma_store_3d(&tm_y, buf, x, py, pz); };
         if (ws)
-          store_tile_tma<float, BN>(trow + (uint32_t)(h * BN), stage, &tm_y, (int32_t)k0, (int32_t)fp.K, py,
-                                    (int32_t)(sigma * fp.N + img), m, nblk > 0, threadIdx.x == 128, ok);
+          store_rows_tma<float>(trow + (uint32_t)(h * BN), stage, BN, (int32_t)k0, (int32_t)fp.K, m, nblk > 0,
+                                threadIdx.x == 128, ok, store);
         else
-          store_tile_tma<TO, BN>(trow + (uint32_t)(h * BN), stage, &tm_y, (int32_t)k0, (int32_t)fp.K, py,
-                                 (int32_t)img, m, nblk > 0, threadIdx.x == 128, ok, sbias, fp.ep_lo, fp.ep_hi,
-                                 fp.ep != 0);
+          store_rows_tma<TO>(trow + (uint32_t)(h * BN), stage, BN, (int32_t)k0, (int32_t)fp.K, m, nblk > 0,
+                             threadIdx.x == 128, ok, store, sbias, fp.ep_lo, fp.ep_hi, fp.ep != 0);
       }
     }
   }

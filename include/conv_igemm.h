@@ -116,10 +116,14 @@ typedef enum conv_kernel {
   CONV_KERNEL_FWD_GROUPED_TC = 10,   /* 16-bit grouped forward (Cg = Kg dividing 128, C % 128 = 0):
                                         each 128-channel block as a dense tensor-core forward with
                                         a block-diagonal filter written into the workspace */
-  CONV_KERNEL_WGRAD_GROUPED_TC = 11  /* 16-bit grouped weight gradient (Cg = Kg in 2..32, C % 128 = 0,
+  CONV_KERNEL_WGRAD_GROUPED_TC = 11, /* 16-bit grouped weight gradient (Cg = Kg in 2..32, C % 128 = 0,
                                         filter width <= 4): per 128-channel block and tap, the dense
                                         product on the tensor cores with MN-major operands, of which
                                         the diagonal group blocks are kept */
+  CONV_KERNEL_WGRAD_TC = 12          /* 16-bit dense weight gradient (one group, or Cg % 64 = 0 and
+                                        Kg % 128 = 0; C, K >= 64 and multiples of 8): per filter tap
+                                        the product dY^T X over the output pixels on the tensor
+                                        cores, both operands MN-major straight from TMA boxes */
 } conv_kernel;
 
 /* What a call with these arguments would run. */

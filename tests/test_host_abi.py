@@ -310,3 +310,40 @@ def test_depthwise_ring_selection():
     info = fw(CONFIG4)
     assert info["ctas_per_sm"] == 1 and info["ctas"] == 150 and info["split_k"] == 1
     assert cig.workspace_bytes(CONFIG4, DIR_FWD, -1, sm_count=SMS) == 0
+
+
+SUPPLEMENT = Problem(n=64, h=56, w=56, c=256, k=256, r=3, s=3, pad_h=1, pad_w=1, in_dtype=BF16, out_dtype=BF16)
+
+
+def test_dense_wgrad_tensor_core_selection():
+    """Which weight gradients the dense tensor-core kernel takes (16-bit, one group or Cg % 64 == 0 with
+    Kg % 128 == 0, C and K >= 64 and multiples of 8), and its tiling: 256 output channels x up to 256
+    input channels x one tap per CTA, split-K over pixel blocks to fill the SMs once."""
+    r256 = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    wg = lambda p, req=-1, bias=True: cig.describe_plan(p, DIR_WGRAD, req, with_bias=bias, sm_count=SMS)  # noqa
+    info = wg(SUPPLEMENT)
+    # 9 taps x one 256 x 256 tile; 56x56 images in 8x8 pixel blocks (no padded row): 64 * 49 blocks
+    assert (info["kernel_name"], info["tiles"], info["reduction_blocks"]) == ("wgrad_tc", 9, 64 * 49)
+    assert info["split_k"] == SMS // 9 and info["ctas"] == 9 * (SMS // 9) and info["ctas_per_sm"] == 1
+    E = 256 * 9 * 256
+    assert info["workspace_bytes"] == r256(info["split_k"] * E * 4) + r256(info["split_k"] * 256 * 4)
+    assert wg(SUPPLEMENT, bias=False)["workspace_bytes"] == r256(info["split_k"] * E * 4)
+    assert wg(SUPPLEMENT, 1)["workspace_bytes"] == 0 and wg(SUPPLEMENT, 1)["needs_fold"] == 0
+    # the small-M layer's weight gradient: 2 x 8 x 9 = 144 tiles fill the GPU unsplit
+    info = wg(CONFIG3)
+    assert (info["kernel_name"], info["tiles"], info["split_k"]) == ("wgrad_tc", 144, 1)
+    # 1x1 16-bit, groups with Kg % 128 == 0, fp16
+    assert wg(Problem(n=4, h=16, w=16, c=128, k=256, in_dtype=F16, out_dtype=F32))["kernel_name"] == "wgrad_tc"
+    g2 = Problem(n=2, h=12, w=12, c=128, k=256, r=3, s=3, pad_h=1, pad_w=1, groups=2, in_dtype=BF16,
+                 out_dtype=BF16)
+    info = wg(g2)
+    assert info["kernel_name"] == "wgrad_tc" and info["tiles"] == 2 * 9
+    # not taken: fp32, fewer than 64 channels, channels not a multiple of 8, groups with Kg = 64
+    assert wg(Problem(n=4, h=16, w=16, c=128, k=256, r=3, s=3, pad_h=1, pad_w=1))["kernel_name"] == "generic"
+    for c, k in ((32, 128), (128, 32), (100, 128)):
+        p = Problem(n=2, h=8, w=8, c=c, k=k, r=3, s=3, pad_h=1, pad_w=1, in_dtype=BF16, out_dtype=BF16)
+        assert wg(p)["kernel_name"] == "generic", (c, k)
+    g8 = Problem(n=2, h=8, w=8, c=512, k=512, r=3, s=3, pad_h=1, pad_w=1, groups=8, in_dtype=BF16, out_dtype=BF16)
+    assert wg(g8)["kernel_name"] == "generic"
+    # the grouped configurations keep their block-diagonal kernel
+    assert wg(CONFIG5A)["kernel_name"] == "wgrad_grouped_tc" and wg(CONFIG5B)["kernel_name"] == "wgrad_grouped_tc"
