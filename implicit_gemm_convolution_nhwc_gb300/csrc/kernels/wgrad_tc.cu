@@ -24,7 +24,8 @@
 // The CTAs of one slice are consecutive, so the tiles that read the same
 // pixels run together and share them through L2. The bias gradient (db = sum
 // of dY) is summed from the dY tiles in shared memory by the epilogue warps,
-// idle during the main loop, on the CTAs of tap 0 and input-channel tile 0.
+// idle during the main loop, each output channel's sum in one of the CTAs that
+// read its dY (spread over the taps and input-channel tiles).
 //
 // Warp roles: 0 TMA producer, 1 MMA issuer, 2 TMEM owner, 4-7 bias sums and
 // epilogue (TMA-store through shared memory).
@@ -39,6 +40,20 @@ constexpr int kThreads = 256;
 constexpr int kMaxStages = 8;
 constexpr int kStageBudget = 64 * 1024;  // bytes of one ring stage at most
 constexpr size_t kSmemMax = 232448;      // dynamic shared memory a CTA may use (227 KB)
+
+// A pair of 16-bit values (one 32-bit word, the lower one first) widened to fp32.
+template <typename T>
+__device__ __forceinline__ float2 widen2(uint32_t v);
+template <>
+__device__ __forceinline__ float2 widen2<__nv_bfloat16>(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+template <>
+__device__ __forceinline__ float2 widen2<__half>(uint32_t v) {
+  __half2 h;
+  memcpy(&h, &v, sizeof(h));
+  return __half22float2(h);
+}
 
 struct WtParams {
   int64_t K, Ho, Wo;        // output channels (all groups), output extent
@@ -88,7 +103,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t xc0 = (int32_t)(grp * wp.Cg) + c0;                // ... as a channel of X
   const int64_t b0 = slice_begin(wp.blocks, wp.split, sigma);
   const int64_t nblk = slice_begin(wp.blocks, wp.split, sigma + 1) - b0;
-  const bool do_bias = (db != nullptr || ws_bias != nullptr) && tap == 0 && ct == 0;
+  // The bias gradient of the tile's output channels is shared out over the CTAs of the same
+  // channel tile and slice (every input-channel tile and tap reads the same dY): CTA w of them sums
+  // the 16-byte chunks [q0, q1) (8 channels each) of the dY atoms, each chunk in exactly one CTA.
+  const int nchunk = 8 * 2 * wp.MS;
+  const int64_t workers = wp.ctiles * taps, widx = ct * taps + tap;
+  const int q0 = (int)(nchunk * widx / workers), q1 = (int)(nchunk * (widx + 1) / workers);
+  const bool do_bias = (db != nullptr || ws_bias != nullptr) && q1 > q0;
   const int rows = wp.TR * wp.BW;  // rows TMA writes per atom; [rows, BP) stay zero
   const uint32_t tx = (uint32_t)((MA + NA) * rows * 128);
 
@@ -190,21 +211,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 4) {
     const int q = warp - 4;
     const int m = 32 * q + lane;  // row m of each M sub-tile (TMEM lane m)
-    // ---------------------------------------------------- bias sums (tap 0, channel tile 0)
-    float bsum[2] = {0.f, 0.f};
+    // ---------------------------------------------------- bias sums (this CTA's chunks)
+    // Thread t sums chunk q0 + t % cc over the rows p = ph, ph + nph, ... of every block
+    // (ph = t / cc, nph = 128 / cc phases); the phases are added in order at the end.
+    const int t = threadIdx.x - 128;
+    const int cc = q1 - q0 > 0 ? q1 - q0 : 1, nph = 128 / cc, ph0 = t / cc, qc = q0 + t % cc;
+    float2 bacc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     if (do_bias) {
-      const int unit = (m % 64) / 8, el = (m % 8) * 2;
+      const int catom = qc / 8, cu = qc % 8;  // the chunk's dY atom and 16-byte unit
       int s = 0;
       uint32_t ph = 0;
       for (int64_t j = 0; j < nblk; ++j) {
         if (!mbar_wait(&full[s], ph, abort_flag, err)) break;
-        const uint8_t* st = smem + (size_t)s * stage_bytes;
-        for (int h = 0; h < wp.MS; ++h) {
-          const uint8_t* at = st + (size_t)(2 * h + m / 64) * AS;
-          float part = 0.f;
-          for (int p = 0; p < rows; ++p)
-            part += to_f32(*reinterpret_cast<const TI*>(at + p * 128 + ((unit ^ (p & 7)) << 4) + el));
-          bsum[h] += part;
+        if (ph0 < nph) {
+          const uint8_t* at = smem + (size_t)s * stage_bytes + (size_t)catom * AS;
+          for (int p = ph0; p < rows; p += nph) {
+            const uint4 v = *reinterpret_cast<const uint4*>(at + p * 128 + ((cu ^ (p & 7)) << 4));
+            bacc[0] = __fadd2_rn(bacc[0], widen2<TI>(v.x));
+            bacc[1] = __fadd2_rn(bacc[1], widen2<TI>(v.y));
+            bacc[2] = __fadd2_rn(bacc[2], widen2<TI>(v.z));
+            bacc[3] = __fadd2_rn(bacc[3], widen2<TI>(v.w));
+          }
         }
         mbar_arrive(&empty[s]);
         if (++s == stages) {
@@ -212,6 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ph ^= 1u;
         }
       }
+      // The epilogue below reuses the ring as staging: every bias warp must be done reading it
+      // (the last MMA can complete before a slower warp has summed the last stages).
+      named_bar_sync(1, 128);
     }
     // ---------------------------------------------------- epilogue
     const bool ok = mbar_wait(tmem_full, 0u, nullptr, err) && *abort_flag == 0u;
@@ -233,12 +263,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         store_rows_tma<TO>(trow + (uint32_t)(h * wp.BN), stage, wp.BN, c0, wp.Cg, m, nblk > 0, threadIdx.x == 128,
                            ok, store);
     }
-    if (do_bias && ok) {
-      for (int h = 0; h < wp.MS; ++h) {
-        const int64_t k = (int64_t)k0 + 128 * h + m;
+    if (do_bias) {
+      // The partial sums [phase][chunk][8] after the staging buffers (the ring is idle), then
+      // channel j of this CTA's 8 cc channels adds its nph phases in order (deterministic).
+      float* red = reinterpret_cast<float*>(smem + 2 * 128 * 128);
+      if (ph0 < nph) {
+        float* mine = red + (ph0 * cc + t % cc) * 8;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          mine[2 * i] = bacc[i].x;
+          mine[2 * i + 1] = bacc[i].y;
+        }
+      }
+      named_bar_sync(1, 128);
+      for (int j = t; j < 8 * cc && ok; j += 128) {
+        const int64_t k = (int64_t)k0 + 8 * q0 + j;
         if (k >= kend) continue;
-        if (ws_bias) ws_bias[(int64_t)sigma * wp.K + k] = bsum[h];
-        else store_out(db + k, bsum[h]);
+        float sum = 0.f;
+        for (int q2 = 0; q2 < nph; ++q2) sum += red[(q2 * cc + j / 8) * 8 + j % 8];
+        if (ws_bias) ws_bias[(int64_t)sigma * wp.K + k] = sum;
+        else store_out(db + k, sum);
       }
     }
   }
