@@ -343,8 +343,8 @@ def time_oracle(p, direction, dist, args, seed, target_s: float):
 # The configurations (and the compute-bound supplement) timed after the
 # headline and reported under "per_config", each at its own automatic plan.
 PER_CONFIG = ["wgrad1x1_f32_n4", "fwd3x3_bf16_n1", "dgrad3x3_bf16_n1", "dw7x7_wgrad_bf16", "dw7x7_dgrad_bf16",
-              "grp3x3_wgrad_f16_g64", "grp3x3_wgrad_f16_g128", "fwd3x3_bf16_n64_c256", "dgrad3x3_bf16_n64_c256",
-              "wgrad3x3_bf16_n64_c256"]
+              "grp3x3_wgrad_f16_g64", "grp3x3_wgrad_f16_g128", "grp3x3_dgrad_f16_g64", "fwd3x3_bf16_n64_c256",
+              "dgrad3x3_bf16_n64_c256", "wgrad3x3_bf16_n64_c256"]
 # The split-K degrees swept on the small-M layer (auto first).
 SWEEP = {"fwd3x3_bf16_n1": [-1, 1, 2, 4, 8, 16, 32]}
 

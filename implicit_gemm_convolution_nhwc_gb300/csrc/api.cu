@@ -82,6 +82,8 @@ Geometry geometry_of(conv_kernel k, const Shape& s, conv_dir dir) {
     case CONV_KERNEL_FWD_GROUPED_TC: return dir == CONV_DIR_FWD ? geometry_fwd_grouped_tc(s) : Geometry{};
     case CONV_KERNEL_WGRAD_GROUPED_TC: return dir == CONV_DIR_WGRAD ? geometry_wgrad_grouped_tc(s) : Geometry{};
     case CONV_KERNEL_WGRAD_TC: return dir == CONV_DIR_WGRAD ? geometry_wgrad_tc(s) : Geometry{};
+    case CONV_KERNEL_DGRAD_DEPTHWISE: return dir == CONV_DIR_DGRAD ? geometry_dgrad_depthwise(s) : Geometry{};
+    case CONV_KERNEL_DGRAD_GROUPED_TC: return dir == CONV_DIR_DGRAD ? geometry_dgrad_grouped_tc(s) : Geometry{};
     case CONV_KERNEL_WGRAD_DEPTHWISE: return dir == CONV_DIR_WGRAD ? geometry_wgrad_depthwise(s) : Geometry{};
     case CONV_KERNEL_WGRAD_GROUPED: return dir == CONV_DIR_WGRAD ? geometry_wgrad_grouped(s) : Geometry{};
     default: return Geometry{};
@@ -138,9 +140,10 @@ conv_status choose_kernel(const Shape& s, conv_dir dir, conv_kernel* kernel, Geo
   // on the 3x3 small-M layer it measured slower than the two-stage form.
   static const conv_kernel fwd_order[] = {CONV_KERNEL_FWD_TC, CONV_KERNEL_FWD_DEPTHWISE, CONV_KERNEL_FWD_GROUPED_TC,
                                           CONV_KERNEL_GENERIC};
-  static const conv_kernel dgrad_order[] = {CONV_KERNEL_DGRAD_TC, CONV_KERNEL_GENERIC};
+  static const conv_kernel dgrad_order[] = {CONV_KERNEL_DGRAD_TC, CONV_KERNEL_DGRAD_DEPTHWISE,
+                                            CONV_KERNEL_DGRAD_GROUPED_TC, CONV_KERNEL_GENERIC};
   const conv_kernel* order = dir == CONV_DIR_WGRAD ? wgrad_order : dir == CONV_DIR_FWD ? fwd_order : dgrad_order;
-  const int count = dir == CONV_DIR_WGRAD ? 7 : dir == CONV_DIR_FWD ? 4 : 2;
+  const int count = dir == CONV_DIR_WGRAD ? 7 : dir == CONV_DIR_FWD ? 4 : 4;
   for (int i = 0; i < count; ++i) {
     Geometry g = geometry_of(order[i], s, dir);
     if (g.ok) {
@@ -249,10 +252,13 @@ conv_status make_plan(const conv_problem* prob, conv_dir dir, int32_t request, b
   p.out_elems = dir == CONV_DIR_FWD ? p.sh.y_elems() : dir == CONV_DIR_WGRAD ? p.sh.w_elems() : p.sh.x_elems();
   p.slab_bytes = p.bias_slab_bytes = 0;
   // The grouped forward's tensor-core path writes its block-diagonal filter
-  // ([K][R][S][128] in_dtype elements) at the start of the workspace.
+  // ([K][R][S][128] in_dtype elements) at the start of the workspace; the
+  // grouped data gradient its turned one ([C][R][S][128]).
   p.aux_bytes = 0;
   if (p.kernel == CONV_KERNEL_FWD_GROUPED_TC)
     p.aux_bytes = round256((uint64_t)(p.sh.k * p.sh.r * p.sh.s) * 128u * (uint64_t)esize(p.sh.in_dt));
+  if (p.kernel == CONV_KERNEL_DGRAD_GROUPED_TC)
+    p.aux_bytes = round256((uint64_t)(p.sh.c * p.sh.r * p.sh.s) * 128u * (uint64_t)esize(p.sh.in_dt));
   if (p.fold) {
     int64_t b;
     if (!mul_ok(p.out_elems, 4, &b) || !mul_ok(b, p.split, &b)) return CONV_ERR_OVERFLOW;
@@ -336,6 +342,8 @@ conv_status run(const conv_problem* prob, conv_dir dir, const void* x, const voi
       case CONV_KERNEL_FWD_GROUPED_TC: err = launch_fwd_grouped_tc(plan, a); break;
       case CONV_KERNEL_WGRAD_GROUPED_TC: err = launch_wgrad_grouped_tc(plan, a); break;
       case CONV_KERNEL_WGRAD_TC: err = launch_wgrad_tc(plan, a); break;
+      case CONV_KERNEL_DGRAD_DEPTHWISE: err = launch_dgrad_depthwise(plan, a); break;
+      case CONV_KERNEL_DGRAD_GROUPED_TC: err = launch_dgrad_grouped_tc(plan, a); break;
       case CONV_KERNEL_WGRAD_DEPTHWISE: err = launch_wgrad_depthwise(plan, a); break;
       case CONV_KERNEL_WGRAD_GROUPED: err = launch_wgrad_grouped(plan, a); break;
       default: return CONV_ERR_UNSUPPORTED;
@@ -542,7 +550,7 @@ conv_status conv_wgrad_bias_static_ws(const conv_problem* p, const void* x, cons
 
 
 conv_status conv_set_kernel_override(int32_t kernel) {
-  if (kernel < CONV_KERNEL_AUTO || kernel > CONV_KERNEL_WGRAD_TC) return CONV_ERR_INVALID_ARG;
+  if (kernel < CONV_KERNEL_AUTO || kernel > CONV_KERNEL_DGRAD_GROUPED_TC) return CONV_ERR_INVALID_ARG;
   g_kernel_override = kernel;
   return CONV_OK;
 }

@@ -63,6 +63,9 @@ struct Args {
   const void* ep_bias = nullptr;  // [K] in the output type, or nullptr
   float ep_lo = 0.f, ep_hi = 0.f;
   bool ep = false;
+  // Depthwise forward kernels: read filter tap R*S - 1 - t for tap t (the
+  // filter turned by 180 degrees; the data gradient as a forward).
+  bool rev_taps = false;
   cudaStream_t stream;
 };
 
@@ -91,6 +94,11 @@ cudaError_t launch_fwd_tc_block(const Plan& p, const Args& a);
 // The forward problem a stride-1, ungrouped data gradient equals (dY as the
 // input, the transformed filter, padding dil * (f - 1) - pad).
 Shape dgrad_as_forward(const Shape& s);
+// The forward problem a stride-1 data gradient equals with its groups kept
+// (dY as the input, C and K swapped, padding dil * (f - 1) - pad).
+Shape dgrad_as_forward_grouped(const Shape& s);
+Geometry geometry_dgrad_depthwise(const Shape& s);
+Geometry geometry_dgrad_grouped_tc(const Shape& s);
 Geometry geometry_wgrad_depthwise(const Shape& s);
 Geometry geometry_wgrad_grouped(const Shape& s);
 
@@ -105,6 +113,8 @@ cudaError_t launch_fwd_depthwise(const Plan& p, const Args& a);
 cudaError_t launch_fwd_grouped_tc(const Plan& p, const Args& a);
 cudaError_t launch_wgrad_grouped_tc(const Plan& p, const Args& a);
 cudaError_t launch_wgrad_tc(const Plan& p, const Args& a);
+cudaError_t launch_dgrad_depthwise(const Plan& p, const Args& a);
+cudaError_t launch_dgrad_grouped_tc(const Plan& p, const Args& a);
 cudaError_t launch_wgrad_depthwise(const Plan& p, const Args& a);
 cudaError_t launch_wgrad_grouped(const Plan& p, const Args& a);
 // Stage 2: out = cast(sum of slabs) (and the bias slabs into db).

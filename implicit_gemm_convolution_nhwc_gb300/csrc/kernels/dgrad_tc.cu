@@ -11,6 +11,9 @@
 // from W: for a tap, W is a [k][c] matrix with c contiguous, which is W'
 // read MN-major (output channels c contiguous), at tap R*S - 1 - (r'*S + s').
 // The fold is the forward's.
+//
+// Grouped and depthwise data gradients at stride 1 take the same identity
+// with the groups kept (below, and the grouped one in grouped_tc.cu).
 #include "common.cuh"
 
 namespace cig {
@@ -40,6 +43,42 @@ Geometry geometry_dgrad_tc(const Shape& s) {
   if (s.in_dt == CONV_F32 || s.groups != 1 || s.sh != 1 || s.sw != 1) return Geometry{};
   if (s.ph > s.dh * (s.r - 1) || s.pw > s.dw * (s.s - 1)) return Geometry{};  // ph' and pw' >= 0
   return geometry_fwd_tc(dgrad_as_forward(s));
+}
+
+// The same identity with the groups kept: output channel c of the forward
+// problem (group g) reads dY channels g*Kg .. g*Kg + Kg - 1 through
+// W'[c, r', s', kk] = W[g*Kg + kk, R-1-r', S-1-s', c - g*Cg].
+Shape dgrad_as_forward_grouped(const Shape& s) {
+  Shape t = dgrad_as_forward(s);
+  t.groups = s.groups;
+  t.cg = s.kg;
+  t.kg = s.cg;
+  return t;
+}
+
+// Depthwise data gradient ("feat(rocke): split-K forward implicit-GEMM
+// convolution on gfx1250", the depthwise data gradient pasted into it: at
+// stride 1 it is the depthwise forward with the filter turned by 180 degrees
+// and padding F - 1 - pad): for groups = C = K the turned filter W'[c, r', s']
+// = W[c, R-1-r', S-1-s'] is W itself with its taps read backwards, so the
+// depthwise forward kernels run on dY with reversed taps and the padding
+// dil * (f - 1) - pad. Unsplit (the reduction is R*S taps).
+Geometry geometry_dgrad_depthwise(const Shape& s) {
+  const bool depthwise = s.groups == s.c && s.groups == s.k;
+  if (!depthwise || s.sh != 1 || s.sw != 1) return Geometry{};
+  if (s.ph > s.dh * (s.r - 1) || s.pw > s.dw * (s.s - 1)) return Geometry{};
+  return geometry_fwd_depthwise(dgrad_as_forward_grouped(s));
+}
+
+cudaError_t launch_dgrad_depthwise(const Plan& p, const Args& a) {
+  Plan fp = p;
+  fp.sh = dgrad_as_forward_grouped(p.sh);
+  fp.dir = CONV_DIR_FWD;
+  fp.kernel = CONV_KERNEL_FWD_DEPTHWISE;
+  fp.geo = geometry_fwd_depthwise(fp.sh);
+  Args fa = a;
+  fa.rev_taps = true;
+  return launch_fwd_depthwise(fp, fa);
 }
 
 cudaError_t launch_dgrad_tc(const Plan& p, const Args& a) {

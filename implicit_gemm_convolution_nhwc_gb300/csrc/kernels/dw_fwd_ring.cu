@@ -55,6 +55,7 @@ struct FwdRingParams {
   const void* ep_bias;  // fused epilogue, when ep
   float ep_lo, ep_hi;
   int32_t ep;
+  int32_t rev;          // 1: tap t reads filter tap F*F - 1 - t (the data gradient's turned filter)
 };
 
 // The ring is one step deep plus the step in use (ahead 1, no slack).
@@ -229,7 +230,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   float2 tap[FF];
 #pragma unroll
   for (int i = 0; i < FF; ++i)
-    tap[i] = cok ? make_float2(ldf<TI>(w + c * FF + i), ldf<TI>(w + (c + 1) * FF + i)) : make_float2(0.f, 0.f);
+    tap[i] = cok ? make_float2(ldf<TI>(w + c * FF + (p.rev ? FF - 1 - i : i)),
+                               ldf<TI>(w + (c + 1) * FF + (p.rev ? FF - 1 - i : i)))
+                 : make_float2(0.f, 0.f);
   float2 bias = make_float2(0.f, 0.f);
   if (p.ep && p.ep_bias && cok) {
     const TO* b = static_cast<const TO*>(p.ep_bias);
@@ -322,6 +325,7 @@ cudaError_t launch_typed(const Plan& pl, const Args& a, CUtensorMapDataType dt) 
   p.ep_lo = a.ep_lo;
   p.ep_hi = a.ep_hi;
   p.ep = a.ep ? 1 : 0;
+  p.rev = a.rev_taps ? 1 : 0;
   switch (s.s) {
     case 3: return launch_f<TI, TO, 3>(pl, a, p, dt);
     case 5: return launch_f<TI, TO, 5>(pl, a, p, dt);

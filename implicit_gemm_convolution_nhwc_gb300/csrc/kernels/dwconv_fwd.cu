@@ -69,6 +69,7 @@ struct DwParams {
   const void* ep_bias;
   float ep_lo, ep_hi;
   int32_t ep;
+  int32_t rev;  // 1: tap t reads filter tap R*S - 1 - t (the data gradient's turned filter)
 };
 
 // Stores the kQ outputs of a chunk (ragged tail), with the fused epilogue.
@@ -116,7 +117,8 @@ __global__ void __launch_bounds__(kThreads, 2) dwconv_fwd_kernel(const TI* __res
     const int tap = i >> 5;
     const int64_t cc = cb * kCB + 2 * (i & 31);
     float2 v = make_float2(0.f, 0.f);
-    if (cc < p.C) v = make_float2(to_f32(w[cc * taps + tap]), to_f32(w[(cc + 1) * taps + tap]));
+    const int wt = p.rev ? taps - 1 - tap : tap;
+    if (cc < p.C) v = make_float2(to_f32(w[cc * taps + wt]), to_f32(w[(cc + 1) * taps + wt]));
     swt[i] = v;
   }
   __syncthreads();  // the last barrier: warps may leave below
@@ -229,6 +231,7 @@ cudaError_t launch_typed(const Plan& pl, const Args& a) {
   p.ep_lo = a.ep_lo;
   p.ep_hi = a.ep_hi;
   p.ep = a.ep ? 1 : 0;
+  p.rev = a.rev_taps ? 1 : 0;
   const int key = (int)s.s * 10 + (int)s.sw;
   if (pair) {
     switch (key) {

@@ -120,10 +120,16 @@ typedef enum conv_kernel {
                                         filter width <= 4): per 128-channel block and tap, the dense
                                         product on the tensor cores with MN-major operands, of which
                                         the diagonal group blocks are kept */
-  CONV_KERNEL_WGRAD_TC = 12          /* 16-bit dense weight gradient (one group, or Cg % 64 = 0 and
+  CONV_KERNEL_WGRAD_TC = 12,         /* 16-bit dense weight gradient (one group, or Cg % 64 = 0 and
                                         Kg % 128 = 0; C, K >= 64 and multiples of 8): per filter tap
                                         the product dY^T X over the output pixels on the tensor
                                         cores, both operands MN-major straight from TMA boxes */
+  CONV_KERNEL_DGRAD_DEPTHWISE = 13,  /* stride-1 depthwise data gradient: the depthwise forward
+                                        kernels over dY with the filter's taps read backwards
+                                        (turned 180 degrees), padding dil*(f-1)-pad; unsplit */
+  CONV_KERNEL_DGRAD_GROUPED_TC = 14  /* stride-1 16-bit grouped data gradient (Cg = Kg dividing 128,
+                                        C % 128 = 0): the block-diagonal grouped forward over dY
+                                        with the turned filter written into the workspace */
 } conv_kernel;
 
 /* What a call with these arguments would run. */
@@ -173,9 +179,10 @@ conv_status resolve_split_k(const conv_problem* p, conv_dir dir, int32_t request
 /* Workspace bytes a call with this degree request needs: 0 when the degree
  * resolves to 1, else S x E x 4 rounded up to 256 bytes (E = output elements),
  * plus S x k x 4 (rounded up to 256) when with_bias and dir is the weight
- * gradient; the grouped forward's tensor-core path adds its block-diagonal
- * filter (k x r x s x 128 elements of in_dtype, rounded up to 256) in front,
- * at every degree. */
+ * gradient; the grouped forward's and grouped data gradient's tensor-core
+ * paths add their block-diagonal filter (k x r x s x 128 elements of
+ * in_dtype, rounded up to 256; c x r x s x 128 for the data gradient) in
+ * front, at every degree. */
 conv_status conv_workspace_bytes_for(const conv_problem* p, conv_dir dir, int32_t split_k,
                                      int32_t with_bias, int32_t sm_count, uint64_t* bytes);
 conv_status conv_workspace_bytes(const conv_problem* p, conv_dir dir, int32_t split_k,
@@ -218,9 +225,11 @@ conv_status conv_fwd_epilogue(const conv_problem* p, const void* x, const void* 
 
 /* Data gradient: dx[n,h,w,c] = sum over k, r, s of dy[n,ho,wo,k] * w[k,r,s,c]
  * for the (ho, wo) with ho*sh + r*dh - ph = h and wo*sw + s*dw - pw = w (the
- * forward's taps read backwards). dy and w in in_dtype, dx [n,h,w,c] in
- * out_dtype. The reduction (r, s, k) splits like the forward's; the
- * workspace is the slabs only (none at degree 1). */
+ * forward's taps read backwards), k running over the output channels of c's
+ * group. dy and w in in_dtype, dx [n,h,w,c] in out_dtype. The reduction
+ * (r, s, k) splits like the forward's; the workspace is the slabs (none at
+ * degree 1), after the turned block-diagonal filter of the grouped
+ * tensor-core path (see conv_workspace_bytes). */
 conv_status conv_dgrad(const conv_problem* p, const void* dy, const void* w, void* dx, void* ws,
                        uint64_t ws_bytes, int32_t split_k, void* stream);
 

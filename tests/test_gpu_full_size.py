@@ -217,3 +217,38 @@ def test_grouped_3x3_forward_full_sampled_images(groups):
         e = relerr(yc[i:i + 1], orc.fwd(oproblem(p1), x[i:i + 1], w))
         assert e <= 1e-2, f"image {i}: err {e:.3e}"
     assert cig.device_errors() == 0
+
+
+def test_depthwise_7x7_dgrad_full():
+    """Depthwise 7x7 data gradient bf16, N=32, 56x56, C=K=384, pad 3 (the depthwise configuration's layer
+    backwards; dY ~ N(0, 1) seed 3, W as in the forward), auto: every element against the oracle."""
+    n, hw, c = 32, 56, 384
+    p = cig.Problem(n=n, h=hw, w=hw, c=c, k=c, r=7, s=7, pad_h=3, pad_w=3, groups=c,
+                    in_dtype=cig.BF16, out_dtype=cig.BF16)
+    assert cig.describe_plan(p, cig.DIR_DGRAD, -1)["kernel_name"] == "dgrad_depthwise"
+    dy = synth.tensor((n, hw, hw, c), torch.bfloat16, "normal", 0.0, 1.0, 3, synth.DY_ID)
+    w = synth.tensor((c, 7, 7, 1), torch.bfloat16, "normal", 0.0, 1.0, 3, synth.W_ID)
+    dx = torch.empty((n, hw, hw, c), dtype=torch.bfloat16, device="cuda")
+    cig.conv_dgrad(p, dy.cuda(), w.cuda(), dx, None, -1)
+    torch.cuda.synchronize()
+    e = relerr(dx.cpu(), oracle.get().dgrad(oproblem(p), dy, w))
+    assert e <= 1e-2, f"err {e:.3e}"
+    assert cig.device_errors() == 0
+
+
+@pytest.mark.parametrize("groups", [64, 128], ids=["cpg8", "cpg4"])
+def test_grouped_3x3_dgrad_full(groups):
+    """Grouped 3x3 data gradient fp16, N=64, 28x28, C=K=512 (the grouped configuration's layer backwards;
+    dY ~ N(0, 1) seed 4), auto: every element against the oracle."""
+    n, hw, c = 64, 28, 512
+    p = cig.Problem(n=n, h=hw, w=hw, c=c, k=c, r=3, s=3, pad_h=1, pad_w=1, groups=groups,
+                    in_dtype=cig.F16, out_dtype=cig.F16)
+    assert cig.describe_plan(p, cig.DIR_DGRAD, -1)["kernel_name"] == "dgrad_grouped_tc"
+    dy = synth.tensor((n, hw, hw, c), torch.float16, "normal", 0.0, 1.0, 4, synth.DY_ID)
+    w = synth.tensor((c, 3, 3, c // groups), torch.float16, "normal", 0.0, 1.0, 4, synth.W_ID)
+    dx = torch.empty((n, hw, hw, c), dtype=torch.float16, device="cuda")
+    cig.conv_dgrad(p, dy.cuda(), w.cuda(), dx, cig.workspace(p, cig.DIR_DGRAD, -1, False), -1)
+    torch.cuda.synchronize()
+    e = relerr(dx.cpu(), oracle.get().dgrad(oproblem(p), dy, w))
+    assert e <= 1e-2, f"err {e:.3e}"
+    assert cig.device_errors() == 0

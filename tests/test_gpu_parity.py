@@ -401,6 +401,46 @@ def test_dgrad_config3_layer():
     assert cig.device_errors() == 0
 
 
+@pytest.mark.parametrize("shape, ring", [
+    (dict(n=3, h=13, w=17, c=72, r=7, s=7, pad_h=3, pad_w=3), True),     # channel tail, the ring form
+    (dict(n=2, h=11, w=9, c=64, r=5, s=5, pad_h=1, pad_w=2), True),      # turned padding 3 / 2
+    (dict(n=2, h=6, w=30, c=128, r=3, s=3), True),                       # no padding: turned padding 2
+    (dict(n=2, h=12, w=10, c=34, r=3, s=5, pad_h=1, pad_w=2), False),    # non-square, C < 64: shared form
+    (dict(n=1, h=15, w=11, c=40, r=3, s=3, pad_h=2, pad_w=1, dil_h=2), False),  # H dilation
+])
+@pytest.mark.parametrize("dt", [(BF16, BF16), (F16, F32), (F32, F32)], ids=lambda d: f"{d[0]}{d[1]}")
+def test_dgrad_depthwise(shape, ring, dt):
+    """Depthwise data gradient at stride 1 as the depthwise forward over dY with the filter's taps read
+    backwards (the turned-filter identity of the depthwise data gradient pasted into "feat(rocke):
+    split-K forward implicit-GEMM convolution on gfx1250")."""
+    c = shape["c"]
+    p = cig.Problem(**shape, k=c, groups=c, in_dtype=dt[0], out_dtype=dt[1])
+    info = cig.describe_plan(p, cig.DIR_DGRAD, -1)
+    assert info["kernel_name"] == "dgrad_depthwise" and info["split_k"] == 1
+    assert (info["ctas_per_sm"] == 1) == (ring and dt[0] != F32)
+    check_dgrad(p, 13, ["auto", "generic"], [-1, 1])
+    assert cig.device_errors() == 0
+
+
+@pytest.mark.parametrize("shape", [
+    dict(n=2, h=10, w=12, c=256, k=256, r=3, s=3, pad_h=1, pad_w=1, groups=32),    # 8 per group
+    dict(n=1, h=9, w=11, c=128, k=128, r=3, s=3, pad_h=1, pad_w=1, groups=32),     # 4 per group
+    dict(n=2, h=8, w=8, c=128, k=128, r=5, s=5, pad_h=2, pad_w=2, groups=64),      # 2 per group
+    dict(n=1, h=12, w=12, c=256, k=256, r=3, s=3, pad_h=2, pad_w=2, dil_h=2, dil_w=2, groups=8),  # 32
+    dict(n=2, h=7, w=13, c=128, k=128, r=1, s=1, groups=8),                         # pointwise, 16
+])
+@pytest.mark.parametrize("dt", [(F16, F16), (BF16, F32)], ids=lambda d: f"{d[0]}{d[1]}")
+def test_dgrad_grouped_tc(shape, dt):
+    """Grouped data gradient at stride 1 as the block-diagonal grouped forward over dY with the turned
+    filter in the group blocks."""
+    p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
+    info = cig.describe_plan(p, cig.DIR_DGRAD, -1)
+    assert info["kernel_name"] == "dgrad_grouped_tc" and info["workspace_bytes"] > 0
+    check_dgrad(p, 14, ["auto"], [-1, 1, 2, "max"])
+    check_dgrad(p, 14, ["generic"], [1])
+    assert cig.device_errors() == 0
+
+
 # ------------------------------------------------------- depthwise / grouped
 
 

@@ -175,8 +175,9 @@ def test_forward_cluster_form_selection():
 
 def test_dgrad_plans():
     """Data gradient: the tensor-core path (16-bit, stride 1, one group) reads
-    the filter in place, so its workspace is the slabs alone; strided or
-    grouped problems take the generic kernel."""
+    the filter in place, so its workspace is the slabs alone; grouped and
+    depthwise stride-1 problems take the turned-filter forwards; strided ones
+    take the generic kernel."""
     r256 = lambda v: (v + 255) // 256 * 256  # noqa: E731
     p = CONFIG3
     E = p.n * p.h * p.w * p.c
@@ -192,7 +193,15 @@ def test_dgrad_plans():
                       in_dtype=BF16, out_dtype=BF16)
     info = cig.describe_plan(strided, cig.DIR_DGRAD, 1, sm_count=SMS)
     assert info["kernel_name"] == "generic" and info["workspace_bytes"] == 0
-    assert cig.describe_plan(CONFIG5A, cig.DIR_DGRAD, -1, sm_count=SMS)["kernel_name"] == "generic"
+    # grouped (Cg = Kg dividing 128) and depthwise data gradients at stride 1 take the turned-filter forwards
+    info = cig.describe_plan(CONFIG5A, cig.DIR_DGRAD, -1, sm_count=SMS)
+    assert info["kernel_name"] == "dgrad_grouped_tc"
+    assert info["workspace_bytes"] == r256(CONFIG5A.c * 9 * 128 * 2)  # the turned block-diagonal filter
+    info = cig.describe_plan(CONFIG4, cig.DIR_DGRAD, -1, sm_count=SMS)
+    assert (info["kernel_name"], info["split_k"], info["workspace_bytes"]) == ("dgrad_depthwise", 1, 0)
+    strided_dw = Problem(n=2, h=9, w=9, c=64, k=64, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1,
+                         groups=64, in_dtype=BF16, out_dtype=BF16)
+    assert cig.describe_plan(strided_dw, cig.DIR_DGRAD, -1, sm_count=SMS)["kernel_name"] == "generic"
     # the planner ignores with_bias outside the weight gradient
     assert cig.describe_plan(p, cig.DIR_DGRAD, -1, with_bias=True, sm_count=SMS) == auto
     with pytest.raises(cig.ConvError) as e:
