@@ -6,10 +6,11 @@
 // in the same launch.
 //
 // Bandwidth- and latency-bound: the slabs were just written by stage 1 and
-// usually sit in L2. Each thread owns 1 or 4 consecutive elements and issues
-// the loads of a batch of slabs (32 or 16) before it adds any of them, so a
-// warp keeps a batch of independent 4- or 16-byte loads in flight; the adds
-// still happen strictly in slice order.
+// usually sit in L2. Each thread owns 4 consecutive elements (1 when E is
+// small or not a multiple of 4) and issues the loads of a batch of B slabs
+// (B sized to S, so a small S keeps few registers and a high occupancy)
+// before it adds any of them, so every warp keeps a batch of independent
+// loads in flight; the adds still happen strictly in slice order.
 #include "common.cuh"
 
 namespace cig {
@@ -22,14 +23,12 @@ struct Vec;
 template <>
 struct Vec<1> {
   using T = float;
-  static constexpr int kBatch = 32;  // slabs whose loads are in flight together
   static __device__ __forceinline__ T load(const float* p) { return __ldcs(p); }
   static __device__ __forceinline__ void add(T& a, const T& b) { a += b; }
 };
 template <>
 struct Vec<4> {
   using T = float4;
-  static constexpr int kBatch = 16;
   static __device__ __forceinline__ T load(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
   static __device__ __forceinline__ void add(T& a, const T& b) {
     a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
@@ -37,12 +36,11 @@ struct Vec<4> {
 };
 
 // Sum of S slabs (stride E floats) at element e, in slice order. Each batch
-// issues all of its (predicated) loads before its first add, the last,
-// partial batch included, so no slab load waits on the previous add.
-template <int V>
+// of B slabs issues all of its (predicated) loads before its first add, the
+// last, partial batch included, so no slab load waits on the previous add.
+template <int V, int B>
 __device__ __forceinline__ typename Vec<V>::T fold_at(const float* ws, int64_t E, int32_t S, int64_t e) {
   using T = typename Vec<V>::T;
-  constexpr int B = Vec<V>::kBatch;
   T acc = Vec<V>::load(ws + e);
   for (int32_t s = 1; s < S; s += B) {
     T v[B];
@@ -58,19 +56,20 @@ __device__ __forceinline__ typename Vec<V>::T fold_at(const float* ws, int64_t E
 
 template <typename TO>
 __device__ __forceinline__ void store_vec(TO* out, int64_t e, float v) { store_out(out + e, v); }
-template <typename TO>
-__device__ __forceinline__ void store_vec(TO* out, int64_t e, float4 v) {
-  store_out(out + e + 0, v.x);
-  store_out(out + e + 1, v.y);
-  store_out(out + e + 2, v.z);
-  store_out(out + e + 3, v.w);
-}
 __device__ __forceinline__ void store_vec(float* out, int64_t e, float4 v) {
   *reinterpret_cast<float4*>(out + e) = v;
 }
+__device__ __forceinline__ void store_vec(__nv_bfloat16* out, int64_t e, float4 v) {
+  __nv_bfloat162 h[2] = {__floats2bfloat162_rn(v.x, v.y), __floats2bfloat162_rn(v.z, v.w)};
+  *reinterpret_cast<uint2*>(out + e) = *reinterpret_cast<uint2*>(h);
+}
+__device__ __forceinline__ void store_vec(__half* out, int64_t e, float4 v) {
+  __half2 h[2] = {__floats2half2_rn(v.x, v.y), __floats2half2_rn(v.z, v.w)};
+  *reinterpret_cast<uint2*>(out + e) = *reinterpret_cast<uint2*>(h);
+}
 
 // Units [0, E / V) cover the main slabs, then [0, K) the bias slabs (if any).
-template <typename TO, int V>
+template <typename TO, int V, int B>
 __global__ void __launch_bounds__(kThreads) fold_kernel(const float* __restrict__ ws, TO* out, int64_t E,
                                                         const float* __restrict__ wsb, TO* db, int64_t K,
                                                         int32_t S) {
@@ -82,26 +81,45 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const float* __restrict_
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   for (int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x; u < units; u += stride) {
     if (u < main_units) {
-      store_vec(out, u * V, fold_at<V>(ws, E, S, u * V));
+      store_vec(out, u * V, fold_at<V, B>(ws, E, S, u * V));
     } else {
       const int64_t k = u - main_units;
-      store_out(db + k, fold_at<1>(wsb, K, S, k));
+      store_out(db + k, fold_at<1, B>(wsb, K, S, k));
     }
   }
+}
+
+// The batch: just above S - 1 (the first slab loads alone) up to 8 (16-byte
+// units) or 32 (single floats) slabs, which keeps the registers of a batch
+// of float4 loads near 64.
+template <typename TO>
+cudaError_t launch_b4(const cudaLaunchConfig_t& cfg, const float* ws, TO* out, int64_t E, const float* wsb, TO* db,
+                      int64_t K, int32_t S) {
+  if (S <= 5) return cudaLaunchKernelEx(&cfg, fold_kernel<TO, 4, 4>, ws, out, E, wsb, db, K, S);
+  return cudaLaunchKernelEx(&cfg, fold_kernel<TO, 4, 8>, ws, out, E, wsb, db, K, S);
+}
+template <typename TO>
+cudaError_t launch_b1(const cudaLaunchConfig_t& cfg, const float* ws, TO* out, int64_t E, const float* wsb, TO* db,
+                      int64_t K, int32_t S) {
+  if (S <= 5) return cudaLaunchKernelEx(&cfg, fold_kernel<TO, 1, 4>, ws, out, E, wsb, db, K, S);
+  if (S <= 9) return cudaLaunchKernelEx(&cfg, fold_kernel<TO, 1, 8>, ws, out, E, wsb, db, K, S);
+  if (S <= 17) return cudaLaunchKernelEx(&cfg, fold_kernel<TO, 1, 16>, ws, out, E, wsb, db, K, S);
+  return cudaLaunchKernelEx(&cfg, fold_kernel<TO, 1, 32>, ws, out, E, wsb, db, K, S);
 }
 
 template <typename TO>
 cudaError_t launch_typed(const Plan& p, const Args& a) {
   const int64_t E = p.out_elems;
-  const int sms = current_sm_count();
-  const int cap = (sms > 0 ? sms : 148) * 16;
+  const int sms = current_sm_count() > 0 ? current_sm_count() : 148;
   TO* out = static_cast<TO*>(a.out);
   TO* db = p.with_bias ? static_cast<TO*>(a.db) : nullptr;
   const int64_t bias_units = p.with_bias ? p.sh.k : 0;
-  // 16-byte units when they still give every SM several CTAs; else one float
-  // per thread for more loads in flight.
-  const bool vec4 = (E % 4) == 0 && (E / 4) >= (int64_t)(sms > 0 ? sms : 148) * kThreads * 4;
-  const int grid = launch_grid_cap((vec4 ? E / 4 : E) + bias_units, kThreads, cap / 8 > 0 ? cap / 8 : 1, 8);
+  // 16-byte units (4 elements) when E allows and still gives every SM two
+  // CTAs of them, else single floats (more threads, more loads in flight);
+  // one thread per unit, up to 8 CTAs per SM resident, a grid-stride loop
+  // beyond that.
+  const bool vec4 = (E % 4) == 0 && E / 4 >= (int64_t)sms * 2 * kThreads;
+  const int grid = launch_grid_cap((vec4 ? E / 4 : E) + bias_units, kThreads, sms, 8);
   // Programmatic dependent launch: the fold may be scheduled as soon as the
   // stage-1 CTAs signal (griddepcontrol.launch_dependents) and then waits in
   // griddepcontrol.wait for stage 1 to finish, hiding its launch latency.
@@ -115,12 +133,8 @@ cudaError_t launch_typed(const Plan& p, const Args& a) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const float* ws = a.ws;
-  const float* wsb = a.ws_bias;
-  const int64_t K = p.sh.k;
-  const int32_t S = p.split;
-  if (vec4) return cudaLaunchKernelEx(&cfg, fold_kernel<TO, 4>, ws, out, E, wsb, db, K, S);
-  return cudaLaunchKernelEx(&cfg, fold_kernel<TO, 1>, ws, out, E, wsb, db, K, S);
+  if (vec4) return launch_b4<TO>(cfg, a.ws, out, E, a.ws_bias, db, p.sh.k, p.split);
+  return launch_b1<TO>(cfg, a.ws, out, E, a.ws_bias, db, p.sh.k, p.split);
 }
 
 }  // namespace
