@@ -127,9 +127,14 @@ typedef enum conv_kernel {
   CONV_KERNEL_DGRAD_DEPTHWISE = 13,  /* stride-1 depthwise data gradient: the depthwise forward
                                         kernels over dY with the filter's taps read backwards
                                         (turned 180 degrees), padding dil*(f-1)-pad; unsplit */
-  CONV_KERNEL_DGRAD_GROUPED_TC = 14  /* stride-1 16-bit grouped data gradient (Cg = Kg dividing 128,
+  CONV_KERNEL_DGRAD_GROUPED_TC = 14, /* stride-1 16-bit grouped data gradient (Cg = Kg dividing 128,
                                         C % 128 = 0): the block-diagonal grouped forward over dY
                                         with the turned filter written into the workspace */
+  CONV_KERNEL_WGRAD_GROUPED_MMA = 15 /* 16-bit grouped weight gradient (Cg = Kg in 2..32, C % 64 = 0,
+                                        unit stride and dilation, 1x1, 3 x (1..4) or 5 x (1..6)
+                                        filters): warp-level m16n8k16 MMAs over input columns with
+                                        the filter column applied as a shift of dY, so every product
+                                        is a gradient element (8 or more channels per group) */
 } conv_kernel;
 
 /* What a call with these arguments would run. */

@@ -477,9 +477,12 @@ def test_config5_grouped_full(groups):
     """Grouped 3x3 wgrad fp16, N=64, 28x28, C=K=512, groups 64 / 128, pad 1, N(0,1) seed 4."""
     p = cig.Problem(n=64, h=28, w=28, c=512, k=512, r=3, s=3, pad_h=1, pad_w=1, groups=groups,
                     in_dtype=F16, out_dtype=F16)
-    assert cig.describe_plan(p, cig.DIR_WGRAD, -1)["kernel_name"] == "wgrad_grouped_tc"
-    check_wgrad(p, 4, ["auto", "wgrad_grouped"], [-1, 1, 9], bias=False)
+    assert cig.describe_plan(p, cig.DIR_WGRAD, -1)["kernel_name"] == "wgrad_grouped_mma"
+    check_wgrad(p, 4, ["auto", "wgrad_grouped_tc"], [-1, 1, 9], bias=False)
     check_wgrad(p, 4, ["auto"], [-1], bias=True)
+    x, dy = inputs(p, 4)
+    a, b = run_wgrad(p, x, dy, -1, True), run_wgrad(p, x, dy, -1, True)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
     assert cig.device_errors() == 0
 
 
@@ -508,11 +511,41 @@ def test_grouped_ragged(shape, dt):
 @pytest.mark.parametrize("dt", [(F16, F16), (BF16, F32)], ids=lambda d: f"{d[0]}{d[1]}")
 def test_wgrad_grouped_tc(shape, dt):
     """Grouped weight gradients as block-diagonal dense blocks on the tensor cores (MN-major
-    operands), with the bias gradient summed from the dY tiles."""
+    operands), with the bias gradient summed from the dY tiles (the automatic choice for the strided
+    problem, through the override for the others)."""
     p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
-    assert cig.describe_plan(p, cig.DIR_WGRAD, -1)["kernel_name"] == "wgrad_grouped_tc"
+    assert cig.describe_plan(p, cig.DIR_WGRAD, -1)["kernel_name"] in ("wgrad_grouped_tc", "wgrad_grouped_mma")
     check_wgrad(p, 15, ["wgrad_grouped_tc", "generic"], [-1, 1, 3], bias=True)
     check_wgrad(p, 15, ["wgrad_grouped_tc"], ["max"], bias=True)
+    assert cig.device_errors() == 0
+
+
+@pytest.mark.parametrize("shape", [
+    dict(n=3, h=11, w=13, c=128, k=128, groups=16, r=3, s=3, pad_h=1, pad_w=1),    # cpg 8, 3 columns past W
+    dict(n=2, h=9, w=30, c=256, k=256, groups=64, r=3, s=3, pad_h=1, pad_w=1),     # cpg 4, two 16-column steps
+    dict(n=2, h=7, w=9, c=128, k=128, groups=32, r=3, s=1),                         # cpg 4, 3x1, no padding
+    dict(n=2, h=6, w=5, c=128, k=128, groups=4, r=3, s=3, pad_h=1, pad_w=1),       # cpg 32: 4 pairs a warp
+    dict(n=2, h=8, w=8, c=128, k=128, groups=64, r=3, s=3, pad_h=1, pad_w=1),      # cpg 2
+    dict(n=2, h=10, w=17, c=128, k=128, groups=8, r=3, s=2, pad_h=1, pad_w=1),     # cpg 16, 3x2
+    dict(n=2, h=7, w=9, c=64, k=64, groups=16, r=5, s=5, pad_h=2, pad_w=2),        # cpg 4, 5x5
+    dict(n=4, h=6, w=6, c=192, k=192, groups=24, r=1, s=1),                         # cpg 8, pointwise
+    dict(n=1, h=4, w=5, c=64, k=64, groups=8, r=3, s=3),                            # no padding, Wo = 3
+    dict(n=2, h=9, w=40, c=64, k=64, groups=8, r=3, s=4, pad_h=1, pad_w=2),        # even filter width
+    dict(n=1, h=5, w=100, c=64, k=64, groups=8, r=3, s=3, pad_h=1, pad_w=1),       # 7 column steps
+])
+@pytest.mark.parametrize("dt", [(F16, F16), (BF16, F32)], ids=lambda d: f"{d[0]}{d[1]}")
+def test_wgrad_grouped_mma(shape, dt):
+    """Grouped weight gradients on warp-level MMAs with the filter column applied as a shift of dY
+    ("perf(rocke): depthwise 7x7 and grouped cpg4/8 wgrad on batched mfma 4x4x4", "Technical
+    Details"), with and without the bias gradient; reruns bit-identical."""
+    p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
+    info = cig.describe_plan(p, cig.DIR_WGRAD, -1, True)
+    assert info["kernel_name"] == "wgrad_grouped_mma"
+    check_wgrad(p, 16, ["auto"], [-1, 1, 3, "max"], bias=True)
+    check_wgrad(p, 16, ["auto"], [-1, 2], bias=False)
+    x, dy = inputs(p, 16)
+    a, b = run_wgrad(p, x, dy, 3, True), run_wgrad(p, x, dy, 3, True)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
     assert cig.device_errors() == 0
 
 

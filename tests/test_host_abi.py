@@ -354,5 +354,12 @@ def test_dense_wgrad_tensor_core_selection():
         assert wg(p)["kernel_name"] == "generic", (c, k)
     g8 = Problem(n=2, h=8, w=8, c=512, k=512, r=3, s=3, pad_h=1, pad_w=1, groups=8, in_dtype=BF16, out_dtype=BF16)
     assert wg(g8)["kernel_name"] == "generic"
-    # the grouped configurations keep their block-diagonal kernel
-    assert wg(CONFIG5A)["kernel_name"] == "wgrad_grouped_tc" and wg(CONFIG5B)["kernel_name"] == "wgrad_grouped_tc"
+    # the grouped configurations take the warp-level MMA kernel: 8 channel blocks of 64, split over the SMs
+    for cfg in (CONFIG5A, CONFIG5B):
+        info = wg(cfg)
+        assert (info["kernel_name"], info["tiles"], info["reduction_blocks"]) == ("wgrad_grouped_mma", 8, 64 * 28)
+        assert info["split_k"] == SMS // 8 and info["ctas_per_sm"] == 1
+    # strided grouped problems keep the block-diagonal tensor-core kernel
+    strided = Problem(n=1, h=12, w=12, c=128, k=128, groups=8, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1,
+                      in_dtype=F16, out_dtype=F16)
+    assert wg(strided)["kernel_name"] == "wgrad_grouped_tc"

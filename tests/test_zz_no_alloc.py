@@ -51,7 +51,7 @@ def _setup_call():
 
 @pytest.mark.parametrize("shape, split_k", [
     (dict(n=8, h=64, w=64, c=96, k=64), -1),                 # tensor-core 1x1 path, auto degree
-    (dict(n=2, h=14, w=14, c=64, k=64, r=3, s=3, pad_h=1, pad_w=1, groups=8), 5),  # generic path, pinned
+    (dict(n=2, h=14, w=14, c=64, k=64, r=3, s=3, pad_h=1, pad_w=1, groups=8), 5),  # grouped path, pinned
 ])
 def test_static_workspace_matches_the_workspace_call(shape, split_k):
     p = cig.Problem(**shape)
