@@ -39,8 +39,6 @@ using dwring::ring_rows;
 using dwring::RowPos;
 using dwring::StepPos;
 
-constexpr int kThreads = 256;  // 8 warps
-constexpr int kWarps = kThreads / 32;
 constexpr int kCB = 64;        // channels per CTA: 8 chunks of 8
 constexpr int kMaxDepth = 6;   // ahead + slack, at most
 constexpr size_t kSmemLimit = 227 * 1024;
@@ -178,11 +176,23 @@ __device__ __forceinline__ void pair_of(int q, int cg, int& kch, int& cch) {
   cch = grp * g8 + q % g8;
 }
 
-// SP = ceil(S / 2) pairs of filter columns; CPW chunk pairs a warp.
-template <typename TI, typename TO, int R, int SP, int CPW>
-__global__ void __launch_bounds__(kThreads, 1)
+// The fragments of one 16-column step: A for each pair of filter columns, B
+// for each filter row.
+template <int R, int SP>
+struct Frags {
+  uint32_t a[SP][4];
+  uint32_t b[R][2];
+};
+
+// SP = ceil(S / 2) pairs of filter columns; CPW chunk pairs a warp; NG warp
+// groups of 8 (a group takes every NG-th row of a step; their sums are added
+// in group order at the end).
+template <typename TI, typename TO, int R, int SP, int CPW, int NG>
+__global__ void __launch_bounds__(256 * NG, 1)
     wgrad_grouped_mma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
                              TO* out, float* ws, TO* db, float* ws_bias, GmParams p, unsigned* err) {
+  constexpr int kT = 256 * NG;          // threads
+  constexpr int kW = kT / 32;           // warps
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   Ring g;
@@ -201,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   g.err = err;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int wl = warp & 7, grp = warp >> 3;  // warp within its group, group
   const int64_t cb = blockIdx.x % p.cblocks;
   const int32_t sigma = (int32_t)(blockIdx.x / p.cblocks);
   g.c0 = (int32_t)(cb * kCB);
@@ -209,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.RS; ++i) {
       mbar_init(&g.full[i], 1);
-      mbar_init(&g.empty[i], kWarps);
+      mbar_init(&g.empty[i], kW);
       g.siss[i] = -1;
     }
     *g.abort_flag = 0u;
@@ -231,10 +242,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   // mi = lane / 8 holds filter column s0 (mi even) or s1 (mi odd) and input
   // columns u0 + 8 (mi / 2) + lane % 8; for B (x2) lanes 0..15 give input
   // columns u0 + lane (lanes 16..31 repeat them; their addresses are unused).
+  // u0 is a multiple of 16, so the swizzled offset of a lane's row within a
+  // slot is u0 * 128 plus a per-lane constant.
   int kch[CPW], cch[CPW];
 #pragma unroll
-  for (int i = 0; i < CPW; ++i) pair_of(warp + kWarps * i, p.Cg, kch[i], cch[i]);
+  for (int i = 0; i < CPW; ++i) pair_of(wl + 8 * i, p.Cg, kch[i], cch[i]);
   const int mi = lane >> 3, arow = (mi >> 1) * 8 + (lane & 7), brow = lane & 15;
+  uint32_t aoff[CPW][SP], boff[CPW];
+#pragma unroll
+  for (int i = 0; i < CPW; ++i) {
+#pragma unroll
+    for (int sp = 0; sp < SP; ++sp) {
+      const int s = 2 * sp + (mi & 1);
+      const int pix = arow + p.S - 1 - (s < p.S ? s : p.S - 1);  // dY slot pixel = input column + S - 1 - s
+      aoff[i][sp] = chunk_addr(0u, pix, kch[i]);
+    }
+    boff[i] = chunk_addr(0u, brow, cch[i]);
+  }
   float acc[CPW][R][SP][4];
 #pragma unroll
   for (int i = 0; i < CPW; ++i)
@@ -245,14 +269,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[i][r][sp][e] = 0.f;
   float2 bacc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-  // The lane's filter column per pair: s0 = 2 sp, s1 = 2 sp + 1 (the last one
-  // repeated for odd S; those rows are not stored).
-  int32_t ashift[SP];
-#pragma unroll
-  for (int sp = 0; sp < SP; ++sp) {
-    const int s = 2 * sp + (mi & 1);
-    ashift[sp] = p.S - 1 - (s < p.S ? s : p.S - 1);  // dY slot pixel = input column + S - 1 - s
-  }
 
   RowPos cur{0, (int32_t)(q_b % p.Ho), (int32_t)(q_b / p.Ho), true};
   StepPos sc{0, 0u};
@@ -260,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   StepPos sl{0, 0u};
   for (int i = 0; i < p.ahead * p.TR && q_b + i < q_e; ++i) la.advance(R, p);
   for (int i = 0; i < p.ahead; ++i) sl.advance(p);
-  int32_t issuer = 0;  // warp that loads at step S: S mod 8
+  int32_t issuer = 0;  // warp that loads at step S: S mod kW
   int64_t qa = q_b + (int64_t)p.ahead * p.TR;  // first row of step S + ahead
 
   for (int64_t q = q_b; q < q_e; q += p.TR) {
@@ -272,43 +288,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     for (int32_t j = 0; j < p.TR && qa < q_e; ++j, ++qa) la.advance(R, p);
     sl.advance(p);
-    issuer = (issuer + 1) & (kWarps - 1);
+    issuer = issuer + 1 == kW ? 0 : issuer + 1;
 
     if (!__all_sync(0xffffffffu, mbar_wait(&g.full[sc.ss], sc.sw & 1u, g.abort_flag, g.err))) break;
 
 #pragma unroll 1
     for (int32_t j = 0; j < rows; ++j) {
-      const uint32_t dslot = smem_u32(g.dring + ((size_t)sc.ss * p.TR + j) * g.rowD);
-      uint32_t xslot[R];
+      if (j % NG == grp) {
+        const uint32_t dslot = smem_u32(g.dring + ((size_t)sc.ss * p.TR + j) * g.rowD);
+        uint32_t xslot[R];
 #pragma unroll
-      for (int r = 0; r < R; ++r) xslot[r] = smem_u32(g.xring + (size_t)cur.slot(r, p) * g.rowX);
-#pragma unroll 1
-      for (int32_t us = 0; us < p.US; ++us) {
-        const int32_t u0 = us * 16;
+        for (int r = 0; r < R; ++r) xslot[r] = smem_u32(g.xring + (size_t)cur.slot(r, p) * g.rowX);
 #pragma unroll
         for (int i = 0; i < CPW; ++i) {
-          uint32_t a[SP][4], b[R][2];
+          // one 16-column step ahead: its fragments load while the MMAs of the current one run
+          auto load = [&](int32_t us, Frags<R, SP>& f) {
+            const uint32_t u = (uint32_t)us * 2048u;
 #pragma unroll
-          for (int sp = 0; sp < SP; ++sp) ldsm_x4_t(chunk_addr(dslot, u0 + arow + ashift[sp], kch[i]), a[sp]);
+            for (int sp = 0; sp < SP; ++sp) ldsm_x4_t(dslot + u + aoff[i][sp], f.a[sp]);
 #pragma unroll
-          for (int r = 0; r < R; ++r) ldsm_x2_t(chunk_addr(xslot[r], u0 + brow, cch[i]), b[r]);
+            for (int r = 0; r < R; ++r) ldsm_x2_t(xslot[r] + u + boff[i], f.b[r]);
+          };
+          Frags<R, SP> fc;
+          load(0, fc);
+#pragma unroll 1
+          for (int32_t us = 0; us < p.US; ++us) {
+            Frags<R, SP> fn;
+            if (us + 1 < p.US) load(us + 1, fn);
 #pragma unroll
-          for (int r = 0; r < R; ++r)
+            for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int sp = 0; sp < SP; ++sp) mma16816<TI>(acc[i][r][sp], a[sp], b[r]);
+              for (int sp = 0; sp < SP; ++sp) mma16816<TI>(acc[i][r][sp], fc.a[sp], fc.b[r]);
+            fc = fn;
+          }
         }
-      }
-      // bias: chunk `warp` of the dY row, dY columns lane, lane + 32, ...
-      for (int32_t wo = lane; wo < p.Wo; wo += 32) {
-        const int32_t pix = wo - p.pw + p.S - 1;
-        uint4 v;
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                     : "r"(chunk_addr(dslot, pix, warp)));
-        bacc[0] = __fadd2_rn(bacc[0], widen<TI>(v.x));
-        bacc[1] = __fadd2_rn(bacc[1], widen<TI>(v.y));
-        bacc[2] = __fadd2_rn(bacc[2], widen<TI>(v.z));
-        bacc[3] = __fadd2_rn(bacc[3], widen<TI>(v.w));
+        // bias: chunk `wl` of the dY row, dY columns lane, lane + 32, ...
+        for (int32_t wo = lane; wo < p.Wo; wo += 32) {
+          uint4 v;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                       : "r"(chunk_addr(dslot, wo - p.pw + p.S - 1, wl)));
+          bacc[0] = __fadd2_rn(bacc[0], widen<TI>(v.x));
+          bacc[1] = __fadd2_rn(bacc[1], widen<TI>(v.y));
+          bacc[2] = __fadd2_rn(bacc[2], widen<TI>(v.z));
+          bacc[3] = __fadd2_rn(bacc[3], widen<TI>(v.w));
+        }
       }
       cur.advance(R, p);
     }
@@ -320,21 +344,75 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   signal_dependents();
 
-  // No copy may still be landing in shared memory when the CTA exits (wait
-  // for the last step loaded into each step slot; bounded, no early exit).
+  // No copy may still be landing in shared memory when the CTA exits, nor
+  // when the groups' sums reuse it below (wait for the last step loaded into
+  // each step slot; bounded, no early exit).
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.RS; ++i)
       if (g.siss[i] >= 0) mbar_wait(&g.full[i], (uint32_t)g.siss[i] & 1u, nullptr, err);
   }
+  __syncthreads();
   const bool ok = *g.abort_flag == 0u;
+
+  // lanes' bias partial sums of chunk `wl`, added by a tree of fixed shape
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      bacc[i].x += __shfl_down_sync(0xffffffffu, bacc[i].x, off);
+      bacc[i].y += __shfl_down_sync(0xffffffffu, bacc[i].y, off);
+    }
+  if (NG > 1) {
+    // groups 1.. hand their sums to group 0 through shared memory (over the
+    // ring), which adds them in group order
+    constexpr int NV = CPW * R * SP * 4;
+    float* red = reinterpret_cast<float*>(smem);  // [group - 1][8 warps][NV + 8][32 lanes]
+    if (grp > 0) {
+      float* mine = red + (((size_t)(grp - 1) * 8 + wl) * (NV + 8)) * 32 + lane;
+      int v = 0;
+#pragma unroll
+      for (int i = 0; i < CPW; ++i)
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int sp = 0; sp < SP; ++sp)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mine[(v++) * 32] = acc[i][r][sp][e];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        mine[(NV + 2 * i) * 32] = bacc[i].x;
+        mine[(NV + 2 * i + 1) * 32] = bacc[i].y;
+      }
+    }
+    __syncthreads();
+    if (grp > 0) return;
+#pragma unroll 1
+    for (int gg = 1; gg < NG; ++gg) {
+      const float* theirs = red + (((size_t)(gg - 1) * 8 + wl) * (NV + 8)) * 32 + lane;
+      int v = 0;
+#pragma unroll
+      for (int i = 0; i < CPW; ++i)
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int sp = 0; sp < SP; ++sp)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[i][r][sp][e] += theirs[(v++) * 32];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        bacc[i].x += theirs[(NV + 2 * i) * 32];
+        bacc[i].y += theirs[(NV + 2 * i + 1) * 32];
+      }
+    }
+  }
 
   // The results: fragment element e of pair i, filter row r and column pair
   // sp is row m = lane / 4 + 8 (e / 2) (filter column 2 sp + m / 8, output
   // channel m % 8 of the k chunk) and column n = 2 (lane % 4) + e % 2 (input
   // channel n of the c chunk).
-  const int64_t Cg = p.Cg, RS_ = (int64_t)R * p.S;
-  const int64_t E = p.C * RS_ * Cg;  // dW elements (C = K)
+  const int64_t Cg = p.Cg;
+  const int64_t E = p.C * R * p.S * Cg;  // dW elements (C = K)
 #pragma unroll
   for (int i = 0; i < CPW; ++i)
 #pragma unroll
@@ -352,23 +430,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ws) ws[(int64_t)sigma * E + dst] = acc[i][r][sp][e];
           else store_out(out + dst, acc[i][r][sp][e]);
         }
-  if (db || ws_bias) {
-    // lanes' partial sums of chunk `warp`, added in lane order by a tree of
-    // fixed shape (deterministic)
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        bacc[i].x += __shfl_down_sync(0xffffffffu, bacc[i].x, off);
-        bacc[i].y += __shfl_down_sync(0xffffffffu, bacc[i].y, off);
-      }
-    if (lane == 0 && ok) {
-      const float v8[8] = {bacc[0].x, bacc[0].y, bacc[1].x, bacc[1].y, bacc[2].x, bacc[2].y, bacc[3].x, bacc[3].y};
-      for (int t = 0; t < 8; ++t) {
-        const int64_t k = cb * kCB + warp * 8 + t;
-        if (ws_bias) ws_bias[(int64_t)sigma * p.C + k] = v8[t];
-        else store_out(db + k, v8[t]);
-      }
+  if ((db || ws_bias) && lane == 0 && ok) {
+    const float v8[8] = {bacc[0].x, bacc[0].y, bacc[1].x, bacc[1].y, bacc[2].x, bacc[2].y, bacc[3].x, bacc[3].y};
+    for (int t = 0; t < 8; ++t) {
+      const int64_t k = cb * kCB + wl * 8 + t;
+      if (ws_bias) ws_bias[(int64_t)sigma * p.C + k] = v8[t];
+      else store_out(db + k, v8[t]);
     }
   }
 }
@@ -376,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Chunk pairs a warp: 8 pairs a CTA for Cg <= 8, Cg for more.
 int pairs_per_warp(const Shape& s) { return s.cg <= 8 ? 1 : (int)(s.cg / 8); }
 
-template <typename TI, typename TO, int R, int SP, int CPW>
+template <typename TI, typename TO, int R, int SP, int CPW, int NG>
 cudaError_t launch_k(const Plan& pl, const Args& a, const GmParams& p, CUtensorMapDataType dt, size_t smem) {
   const Shape& s = pl.sh;
   CUtensorMap tm_x, tm_dy;
@@ -389,26 +456,33 @@ cudaError_t launch_k(const Plan& pl, const Args& a, const GmParams& p, CUtensorM
   if (!encode_tmap(&tm_x, dt, 4, a.x, x_dims, x_strides, x_box, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tmap(&tm_dy, dt, 4, a.b, y_dims, y_strides, y_box, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  auto kern = wgrad_grouped_mma_kernel<TI, TO, R, SP, CPW>;
+  auto kern = wgrad_grouped_mma_kernel<TI, TO, R, SP, CPW, NG>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const int64_t ctas = pl.geo.tiles * pl.split;
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<(unsigned)ctas, kThreads, smem, a.stream>>>(tm_x, tm_dy, static_cast<TO*>(a.out), a.ws,
+  kern<<<(unsigned)ctas, 256 * NG, smem, a.stream>>>(tm_x, tm_dy, static_cast<TO*>(a.out), a.ws,
                                                      pl.with_bias ? static_cast<TO*>(a.db) : nullptr,
                                                      pl.with_bias ? a.ws_bias : nullptr, p, device_error_word());
   return cudaGetLastError();
 }
 
+// Warp groups: 2 (512 threads) when a warp's accumulator tiles (R x SP x pairs) are at most 12, so its
+// registers stay within the 128 a thread that 512 threads allow; else 1.
+constexpr int groups_of(int tiles) { return tiles <= 12 ? 2 : 1; }
+
 // Chunk pairs a warp: 1, 2 or 4, as many as keep R x SP x pairs <= 24 accumulator tiles.
 template <typename TI, typename TO, int R, int SP>
 cudaError_t launch_rs(const Plan& pl, const Args& a, const GmParams& p, CUtensorMapDataType dt, size_t smem) {
+  // two groups of 8 warps (16 warps an SM) while the accumulators stay small enough
   switch (pairs_per_warp(pl.sh)) {
-    case 1: return launch_k<TI, TO, R, SP, 1>(pl, a, p, dt, smem);
-    case 2: return R * SP * 2 <= 24 ? launch_k<TI, TO, R, SP, (R * SP * 2 <= 24 ? 2 : 1)>(pl, a, p, dt, smem)
-                                    : cudaErrorInvalidValue;
-    case 4: return R * SP * 4 <= 24 ? launch_k<TI, TO, R, SP, (R * SP * 4 <= 24 ? 4 : 1)>(pl, a, p, dt, smem)
-                                    : cudaErrorInvalidValue;
+    case 1: return launch_k<TI, TO, R, SP, 1, groups_of(R * SP)>(pl, a, p, dt, smem);
+    case 2: return R * SP * 2 <= 24
+                       ? launch_k<TI, TO, R, SP, (R * SP * 2 <= 24 ? 2 : 1), groups_of(R * SP * 2)>(pl, a, p, dt, smem)
+                       : cudaErrorInvalidValue;
+    case 4: return R * SP * 4 <= 24
+                       ? launch_k<TI, TO, R, SP, (R * SP * 4 <= 24 ? 4 : 1), groups_of(R * SP * 4)>(pl, a, p, dt, smem)
+                       : cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }
@@ -465,7 +539,12 @@ Geometry geometry_wgrad_grouped_mma(const Shape& s) {
   // TMA: rows of at most 256 columns (the dY box adds S - 1), 32-bit coordinates
   if ((s.w + 15) / 16 * 16 + s.s - 1 > 256 || s.wo > s.w + 2 * s.pw) return g;
   if (s.n > 0x7fffffffLL || s.h + s.r > 0x7fffffffLL) return g;
-  if (ring_shape(s).d < 1) return g;
+  const RingShape rs = ring_shape(s);
+  if (rs.d < 1) return g;
+  // two warp groups add their sums through shared memory over the ring's rows
+  const int64_t tiles = s.r * spk * pairs_per_warp(s);
+  const size_t ring_bytes = ring_smem(s, rs.d, rs.tr) - 1024;
+  if (tiles <= 12 && (size_t)(tiles * 4 + 8) * 8 * 32 * 4 > ring_bytes) return g;
   g.ok = true;
   g.ctas_per_sm = 1;
   g.tiles = s.c / kCB;
