@@ -71,10 +71,11 @@ struct RingShape {
   int d = 0, tr = 0;
 };
 
-// Four, else fewer rows a step with the deepest ring that fits (at least one
-// step of slack).
+// The most rows a step (up to 8: the per-step bookkeeping is paid once per
+// step) with the deepest ring that fits, at least one step ahead and one of
+// slack.
 RingShape ring_shape(const Shape& s) {
-  for (int tr = 4; tr >= 1; --tr)
+  for (int tr = 8; tr >= 1; --tr)
     for (int d = kMaxDepth; d >= 2; --d)
       if (ring_smem(s, d, tr) <= kSmemLimit) return RingShape{d, tr};
   return RingShape{};
@@ -162,26 +163,22 @@ __device__ __forceinline__ float2 widen<__half>(uint32_t v) {
   return __half22float2(h);
 }
 
-// The (k chunk, c chunk) pair q of a CTA's 8 channel chunks: for Cg >= 8 the
-// group q / G^2 (G = Cg / 8 chunks a group) and its chunks ((q / G) % G,
-// q % G); for Cg < 8 chunk q with itself.
-__device__ __forceinline__ void pair_of(int q, int cg, int& kch, int& cch) {
-  if (cg < 8) {
-    kch = cch = q;
-    return;
-  }
+// The c chunk of pair i of the warp that owns k chunk w (every pair of a warp
+// shares its k chunk, so the A fragments are loaded once for all of them):
+// for Cg >= 8 the i-th of the Cg / 8 chunks of w's group, for Cg < 8 chunk w
+// itself (which holds several whole groups).
+__device__ __forceinline__ int c_chunk_of(int w, int i, int cg) {
+  if (cg < 8) return w;
   const int g8 = cg / 8;
-  const int grp = q / (g8 * g8);
-  kch = grp * g8 + (q / g8) % g8;
-  cch = grp * g8 + q % g8;
+  return (w / g8) * g8 + i;
 }
 
 // The fragments of one 16-column step: A for each pair of filter columns, B
 // for each filter row.
-template <int R, int SP>
+template <int R, int SP, int CPW>
 struct Frags {
   uint32_t a[SP][4];
-  uint32_t b[R][2];
+  uint32_t b[CPW][R][2];
 };
 
 // SP = ceil(S / 2) pairs of filter columns; CPW chunk pairs a warp; NG warp
@@ -244,21 +241,25 @@ __global__ void __launch_bounds__(256 * NG, 1)
   // columns u0 + lane (lanes 16..31 repeat them; their addresses are unused).
   // u0 is a multiple of 16, so the swizzled offset of a lane's row within a
   // slot is u0 * 128 plus a per-lane constant.
-  int kch[CPW], cch[CPW];
+  const int kch = wl;
+  int cch[CPW];
 #pragma unroll
-  for (int i = 0; i < CPW; ++i) pair_of(wl + 8 * i, p.Cg, kch[i], cch[i]);
+  for (int i = 0; i < CPW; ++i) cch[i] = c_chunk_of(wl, i, p.Cg);
   const int mi = lane >> 3, arow = (mi >> 1) * 8 + (lane & 7), brow = lane & 15;
-  uint32_t aoff[CPW][SP], boff[CPW];
+  uint32_t aoff[SP], boff[CPW];
 #pragma unroll
-  for (int i = 0; i < CPW; ++i) {
-#pragma unroll
-    for (int sp = 0; sp < SP; ++sp) {
-      const int s = 2 * sp + (mi & 1);
-      const int pix = arow + p.S - 1 - (s < p.S ? s : p.S - 1);  // dY slot pixel = input column + S - 1 - s
-      aoff[i][sp] = chunk_addr(0u, pix, kch[i]);
-    }
-    boff[i] = chunk_addr(0u, brow, cch[i]);
+  for (int sp = 0; sp < SP; ++sp) {
+    const int s = 2 * sp + (mi & 1);
+    const int pix = arow + p.S - 1 - (s < p.S ? s : p.S - 1);  // dY slot pixel = input column + S - 1 - s
+    aoff[sp] = chunk_addr(0u, pix, kch);
   }
+#pragma unroll
+  for (int i = 0; i < CPW; ++i) boff[i] = chunk_addr(0u, brow, cch[i]);
+  // The bias of chunk wl comes from the A fragments of filter column pw (a
+  // real tap): its window is dY columns 0 .. 16 US - 1, each once, zero past
+  // Wo. Thread (g = lane / 4, t = lane % 4) holds output channel g at pixels
+  // 2t, 2t + 1 (register bh) and 2t + 8, 2t + 9 (register 2 + bh) of each step.
+  const int bsp = p.pw / 2, bh = p.pw % 2;
   float acc[CPW][R][SP][4];
 #pragma unroll
   for (int i = 0; i < CPW; ++i)
@@ -268,7 +269,8 @@ __global__ void __launch_bounds__(256 * NG, 1)
       for (int sp = 0; sp < SP; ++sp)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[i][r][sp][e] = 0.f;
-  float2 bacc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  float2 bacc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  const uint32_t dring_u32 = smem_u32(g.dring), xring_u32 = smem_u32(g.xring);
 
   RowPos cur{0, (int32_t)(q_b % p.Ho), (int32_t)(q_b / p.Ho), true};
   StepPos sc{0, 0u};
@@ -292,49 +294,61 @@ __global__ void __launch_bounds__(256 * NG, 1)
 
     if (!__all_sync(0xffffffffu, mbar_wait(&g.full[sc.ss], sc.sw & 1u, g.abort_flag, g.err))) break;
 
+    {
+      RowPos rp = cur;  // this group's rows of the step: grp, grp + NG, ...
+      for (int i = 0; i < grp; ++i) rp.advance(R, p);
 #pragma unroll 1
-    for (int32_t j = 0; j < rows; ++j) {
-      if (j % NG == grp) {
-        const uint32_t dslot = smem_u32(g.dring + ((size_t)sc.ss * p.TR + j) * g.rowD);
-        uint32_t xslot[R];
+      for (int32_t j = grp; j < rows; j += NG) {
+        const uint32_t dslot = dring_u32 + (uint32_t)((sc.ss * p.TR + j) * g.rowD);
+        uint32_t ab[SP], bb[CPW][R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) xslot[r] = smem_u32(g.xring + (size_t)cur.slot(r, p) * g.rowX);
+        for (int sp = 0; sp < SP; ++sp) ab[sp] = dslot + aoff[sp];
 #pragma unroll
-        for (int i = 0; i < CPW; ++i) {
-          // one 16-column step ahead: its fragments load while the MMAs of the current one run
-          auto load = [&](int32_t us, Frags<R, SP>& f) {
-            const uint32_t u = (uint32_t)us * 2048u;
+        for (int r = 0; r < R; ++r) {
+          const uint32_t xslot = xring_u32 + (uint32_t)rp.slot(r, p) * g.rowX;
 #pragma unroll
-            for (int sp = 0; sp < SP; ++sp) ldsm_x4_t(dslot + u + aoff[i][sp], f.a[sp]);
-#pragma unroll
-            for (int r = 0; r < R; ++r) ldsm_x2_t(xslot[r] + u + boff[i], f.b[r]);
-          };
-          Frags<R, SP> fc;
-          load(0, fc);
+          for (int i = 0; i < CPW; ++i) bb[i][r] = xslot + boff[i];
+        }
+        // blocks of up to four 16-column steps, unrolled (offsets are immediates)
 #pragma unroll 1
-          for (int32_t us = 0; us < p.US; ++us) {
-            Frags<R, SP> fn;
-            if (us + 1 < p.US) load(us + 1, fn);
+        for (int32_t u0 = 0; u0 < p.US; u0 += 4) {
 #pragma unroll
-            for (int r = 0; r < R; ++r)
+          for (int t = 0; t < 4; ++t) {
+            if (u0 + t < p.US) {
+              Frags<R, SP, CPW> f;
 #pragma unroll
-              for (int sp = 0; sp < SP; ++sp) mma16816<TI>(acc[i][r][sp], fc.a[sp], fc.b[r]);
-            fc = fn;
+              for (int sp = 0; sp < SP; ++sp) ldsm_x4_t(ab[sp] + t * 2048, f.a[sp]);
+#pragma unroll
+              for (int i = 0; i < CPW; ++i)
+#pragma unroll
+                for (int r = 0; r < R; ++r) ldsm_x2_t(bb[i][r] + t * 2048, f.b[i][r]);
+#pragma unroll
+              for (int i = 0; i < CPW; ++i)
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                  for (int sp = 0; sp < SP; ++sp) mma16816<TI>(acc[i][r][sp], f.a[sp], f.b[i][r]);
+              uint32_t lo = 0u, hi = 0u;  // the bias column's registers, chosen by selects (no local memory)
+#pragma unroll
+              for (int sp = 0; sp < SP; ++sp)
+                if (sp == bsp) {
+                  lo = bh ? f.a[sp][1] : f.a[sp][0];
+                  hi = bh ? f.a[sp][3] : f.a[sp][2];
+                }
+              bacc[0] = __fadd2_rn(bacc[0], widen<TI>(lo));
+              bacc[1] = __fadd2_rn(bacc[1], widen<TI>(hi));
+            }
           }
+#pragma unroll
+          for (int sp = 0; sp < SP; ++sp) ab[sp] += 4 * 2048;
+#pragma unroll
+          for (int i = 0; i < CPW; ++i)
+#pragma unroll
+            for (int r = 0; r < R; ++r) bb[i][r] += 4 * 2048;
         }
-        // bias: chunk `wl` of the dY row, dY columns lane, lane + 32, ...
-        for (int32_t wo = lane; wo < p.Wo; wo += 32) {
-          uint4 v;
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                       : "r"(chunk_addr(dslot, wo - p.pw + p.S - 1, wl)));
-          bacc[0] = __fadd2_rn(bacc[0], widen<TI>(v.x));
-          bacc[1] = __fadd2_rn(bacc[1], widen<TI>(v.y));
-          bacc[2] = __fadd2_rn(bacc[2], widen<TI>(v.z));
-          bacc[3] = __fadd2_rn(bacc[3], widen<TI>(v.w));
-        }
+        for (int i = 0; i < NG; ++i) rp.advance(R, p);
       }
-      cur.advance(R, p);
+      for (int32_t j = 0; j < rows; ++j) cur.advance(R, p);
     }
 
     __syncwarp();
@@ -355,21 +369,18 @@ __global__ void __launch_bounds__(256 * NG, 1)
   __syncthreads();
   const bool ok = *g.abort_flag == 0u;
 
-  // lanes' bias partial sums of chunk `wl`, added by a tree of fixed shape
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      bacc[i].x += __shfl_down_sync(0xffffffffu, bacc[i].x, off);
-      bacc[i].y += __shfl_down_sync(0xffffffffu, bacc[i].y, off);
-    }
+  // the bias partial sums of output channel lane / 4 of chunk wl: the lane's four pixels a step, then
+  // the four lanes of the channel, in a fixed order
+  float bsum = (bacc[0].x + bacc[0].y) + (bacc[1].x + bacc[1].y);
+  bsum += __shfl_xor_sync(0xffffffffu, bsum, 1);
+  bsum += __shfl_xor_sync(0xffffffffu, bsum, 2);
   if (NG > 1) {
     // groups 1.. hand their sums to group 0 through shared memory (over the
     // ring), which adds them in group order
     constexpr int NV = CPW * R * SP * 4;
-    float* red = reinterpret_cast<float*>(smem);  // [group - 1][8 warps][NV + 8][32 lanes]
+    float* red = reinterpret_cast<float*>(smem);  // [group - 1][8 warps][NV + 1][32 lanes]
     if (grp > 0) {
-      float* mine = red + (((size_t)(grp - 1) * 8 + wl) * (NV + 8)) * 32 + lane;
+      float* mine = red + (((size_t)(grp - 1) * 8 + wl) * (NV + 1)) * 32 + lane;
       int v = 0;
 #pragma unroll
       for (int i = 0; i < CPW; ++i)
@@ -379,17 +390,13 @@ __global__ void __launch_bounds__(256 * NG, 1)
           for (int sp = 0; sp < SP; ++sp)
 #pragma unroll
             for (int e = 0; e < 4; ++e) mine[(v++) * 32] = acc[i][r][sp][e];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        mine[(NV + 2 * i) * 32] = bacc[i].x;
-        mine[(NV + 2 * i + 1) * 32] = bacc[i].y;
-      }
+      mine[NV * 32] = bsum;
     }
     __syncthreads();
     if (grp > 0) return;
 #pragma unroll 1
     for (int gg = 1; gg < NG; ++gg) {
-      const float* theirs = red + (((size_t)(gg - 1) * 8 + wl) * (NV + 8)) * 32 + lane;
+      const float* theirs = red + (((size_t)(gg - 1) * 8 + wl) * (NV + 1)) * 32 + lane;
       int v = 0;
 #pragma unroll
       for (int i = 0; i < CPW; ++i)
@@ -399,11 +406,7 @@ __global__ void __launch_bounds__(256 * NG, 1)
           for (int sp = 0; sp < SP; ++sp)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[i][r][sp][e] += theirs[(v++) * 32];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        bacc[i].x += theirs[(NV + 2 * i) * 32];
-        bacc[i].y += theirs[(NV + 2 * i + 1) * 32];
-      }
+      bsum += theirs[NV * 32];
     }
   }
 
@@ -423,20 +426,17 @@ __global__ void __launch_bounds__(256 * NG, 1)
         for (int e = 0; e < 4; ++e) {
           const int m = (lane >> 2) + 8 * (e >> 1), n = 2 * (lane & 3) + (e & 1);
           const int s = 2 * sp + (m >> 3);
-          const int64_t k = cb * kCB + kch[i] * 8 + (m & 7);
+          const int64_t k = cb * kCB + kch * 8 + (m & 7);
           const int64_t c = cb * kCB + cch[i] * 8 + n;
           if (!ok || s >= p.S || k / Cg != c / Cg) continue;
           const int64_t dst = ((k * R + r) * p.S + s) * Cg + (c % Cg);
           if (ws) ws[(int64_t)sigma * E + dst] = acc[i][r][sp][e];
           else store_out(out + dst, acc[i][r][sp][e]);
         }
-  if ((db || ws_bias) && lane == 0 && ok) {
-    const float v8[8] = {bacc[0].x, bacc[0].y, bacc[1].x, bacc[1].y, bacc[2].x, bacc[2].y, bacc[3].x, bacc[3].y};
-    for (int t = 0; t < 8; ++t) {
-      const int64_t k = cb * kCB + wl * 8 + t;
-      if (ws_bias) ws_bias[(int64_t)sigma * p.C + k] = v8[t];
-      else store_out(db + k, v8[t]);
-    }
+  if ((db || ws_bias) && (lane & 3) == 0 && ok) {
+    const int64_t k = cb * kCB + wl * 8 + (lane >> 2);
+    if (ws_bias) ws_bias[(int64_t)sigma * p.C + k] = bsum;
+    else store_out(db + k, bsum);
   }
 }
 
@@ -544,7 +544,7 @@ Geometry geometry_wgrad_grouped_mma(const Shape& s) {
   // two warp groups add their sums through shared memory over the ring's rows
   const int64_t tiles = s.r * spk * pairs_per_warp(s);
   const size_t ring_bytes = ring_smem(s, rs.d, rs.tr) - 1024;
-  if (tiles <= 12 && (size_t)(tiles * 4 + 8) * 8 * 32 * 4 > ring_bytes) return g;
+  if (tiles <= 12 && (size_t)(tiles * 4 + 1) * 8 * 32 * 4 > ring_bytes) return g;
   g.ok = true;
   g.ctas_per_sm = 1;
   g.tiles = s.c / kCB;
