@@ -41,6 +41,7 @@ using dwring::StepPos;
 
 constexpr int kCB = 64;        // channels per CTA: 8 chunks of 8
 constexpr int kMaxDepth = 6;   // ahead + slack, at most
+constexpr int kMaxTR = 8;      // output rows a step, at most
 constexpr size_t kSmemLimit = 227 * 1024;
 
 struct GmParams {
@@ -64,7 +65,8 @@ int64_t dy_slot_pixels(const Shape& s) { return ((s.w + 15) / 16 * 16 + s.s - 1 
 
 size_t ring_smem(const Shape& s, int d, int tr) {
   const int64_t rx = ring_rows(s.r, s.ho, d, tr), rs = 1 + d;
-  return 1024 + (size_t)(rx * x_slot_pixels(s) * 128 + rs * tr * dy_slot_pixels(s) * 128) + 2 * rs * 8 + rs * 4 + 16;
+  return 1024 + (size_t)(rx * x_slot_pixels(s) * 128 + rs * tr * dy_slot_pixels(s) * 128) + 2 * rs * 8 + rs * 4 + 16 +
+         (size_t)rs * tr * 4;
 }
 
 struct RingShape {
@@ -75,7 +77,7 @@ struct RingShape {
 // step) with the deepest ring that fits, at least one step ahead and one of
 // slack.
 RingShape ring_shape(const Shape& s) {
-  for (int tr = 8; tr >= 1; --tr)
+  for (int tr = kMaxTR; tr >= 1; --tr)
     for (int d = kMaxDepth; d >= 2; --d)
       if (ring_smem(s, d, tr) <= kSmemLimit) return RingShape{d, tr};
   return RingShape{};
@@ -92,6 +94,9 @@ struct Ring {
   uint64_t* empty;
   int32_t* siss;  // wrap count of the last step loaded into each step slot (-1: none)
   volatile uint32_t* abort_flag;
+  // per step slot and row: the input-ring slot of the row's first input row, + 65536 when the row
+  // starts a new input-row sequence (the run's first row or an image's first row)
+  int32_t* rowinfo;
   unsigned* err;
   uint32_t rowX, rowD, txX, txD;
   int32_t c0;
@@ -108,6 +113,11 @@ __device__ bool issue_step(const Ring& g, const GmParams& p, RowPos a, StepPos s
   {
     RowPos b = a;
     for (int32_t j = 0; j < rows; ++j, b.advance(R, p)) bytes += g.txD + (uint32_t)b.fresh(R) * g.txX;
+  }
+  {  // the rows' input slots, published by the arrive below (release) to the warps that wait on it
+    RowPos b = a;
+    for (int32_t j = 0; j < rows; ++j, b.advance(R, p))
+      g.rowinfo[st.ss * p.TR + j] = b.xs + (b.fresh(R) == R ? 65536 : 0);
   }
   uint64_t* bar = &g.full[st.ss];
   mbar_arrive_expect_tx(bar, bytes);
@@ -205,6 +215,7 @@ __global__ void __launch_bounds__(256 * NG, 1)
   g.empty = g.full + p.RS;
   g.siss = reinterpret_cast<int32_t*>(g.empty + p.RS);
   g.abort_flag = reinterpret_cast<volatile uint32_t*>(g.siss + p.RS);
+  g.rowinfo = reinterpret_cast<int32_t*>(g.siss + p.RS + 4);
   g.err = err;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -246,12 +257,15 @@ __global__ void __launch_bounds__(256 * NG, 1)
 #pragma unroll
   for (int i = 0; i < CPW; ++i) cch[i] = c_chunk_of(wl, i, p.Cg);
   const int mi = lane >> 3, arow = (mi >> 1) * 8 + (lane & 7), brow = lane & 15;
-  uint32_t aoff[SP], boff[CPW];
+  // aoff: the x4 load of a pair; aoff1: the x2 load of a single (last, odd-S) filter column, lanes
+  // 0..15 giving its input columns 0..15
+  uint32_t aoff[SP], aoff1[SP], boff[CPW];
 #pragma unroll
   for (int sp = 0; sp < SP; ++sp) {
     const int s = 2 * sp + (mi & 1);
     const int pix = arow + p.S - 1 - (s < p.S ? s : p.S - 1);  // dY slot pixel = input column + S - 1 - s
     aoff[sp] = chunk_addr(0u, pix, kch);
+    aoff1[sp] = chunk_addr(0u, brow + p.S - 1 - (2 * sp < p.S ? 2 * sp : p.S - 1), kch);
   }
 #pragma unroll
   for (int i = 0; i < CPW; ++i) boff[i] = chunk_addr(0u, brow, cch[i]);
@@ -272,9 +286,8 @@ __global__ void __launch_bounds__(256 * NG, 1)
   float2 bacc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
   const uint32_t dring_u32 = smem_u32(g.dring), xring_u32 = smem_u32(g.xring);
 
-  RowPos cur{0, (int32_t)(q_b % p.Ho), (int32_t)(q_b / p.Ho), true};
   StepPos sc{0, 0u};
-  RowPos la = cur;  // first row of the step loaded at step S: S + ahead
+  RowPos la{0, (int32_t)(q_b % p.Ho), (int32_t)(q_b / p.Ho), true};  // first row of the step loaded at step S: S + ahead
   StepPos sl{0, 0u};
   for (int i = 0; i < p.ahead * p.TR && q_b + i < q_e; ++i) la.advance(R, p);
   for (int i = 0; i < p.ahead; ++i) sl.advance(p);
@@ -295,60 +308,75 @@ __global__ void __launch_bounds__(256 * NG, 1)
     if (!__all_sync(0xffffffffu, mbar_wait(&g.full[sc.ss], sc.sw & 1u, g.abort_flag, g.err))) break;
 
     {
-      RowPos rp = cur;  // this group's rows of the step: grp, grp + NG, ...
-      for (int i = 0; i < grp; ++i) rp.advance(R, p);
+      // This group's rows of the step: a contiguous run [j0, j1), walked for
+      // each 16-column step with the B fragments of the R input rows in a
+      // window that slides by one row within an image (one new input row a row).
+      const int32_t j0 = (rows * grp) / NG, j1 = (rows * (grp + 1)) / NG;
+      int32_t info[kMaxTR];
+#pragma unroll
+      for (int32_t j = 0; j < kMaxTR; ++j) info[j] = j0 + j < j1 ? g.rowinfo[sc.ss * p.TR + j0 + j] : 0;
 #pragma unroll 1
-      for (int32_t j = grp; j < rows; j += NG) {
-        const uint32_t dslot = dring_u32 + (uint32_t)((sc.ss * p.TR + j) * g.rowD);
-        uint32_t ab[SP], bb[CPW][R];
+      for (int32_t us = 0; us < p.US; ++us) {
+        const uint32_t uo = (uint32_t)us * 2048u;
+        uint32_t bw[CPW][R][2];
 #pragma unroll
-        for (int sp = 0; sp < SP; ++sp) ab[sp] = dslot + aoff[sp];
+        for (int32_t jj = 0; jj < kMaxTR; ++jj) {
+          if (j0 + jj >= j1) break;
+          const int32_t j = j0 + jj;
+          const int32_t xs = info[jj] & 0xffff;
+          auto xslot = [&](int r) {
+            const int32_t sl = xs + r >= p.RX ? xs + r - p.RX : xs + r;
+            return xring_u32 + (uint32_t)sl * g.rowX + uo;
+          };
+          if (jj == 0 || (info[jj] >> 16) != 0) {  // a fresh window
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const uint32_t xslot = xring_u32 + (uint32_t)rp.slot(r, p) * g.rowX;
+            for (int r = 0; r < R; ++r) {
+              const uint32_t xa = xslot(r);
 #pragma unroll
-          for (int i = 0; i < CPW; ++i) bb[i][r] = xslot + boff[i];
-        }
-        // blocks of up to four 16-column steps, unrolled (offsets are immediates)
-#pragma unroll 1
-        for (int32_t u0 = 0; u0 < p.US; u0 += 4) {
+              for (int i = 0; i < CPW; ++i) ldsm_x2_t(xa + boff[i], bw[i][r]);
+            }
+          } else {  // slide by one input row
+            const uint32_t xa = xslot(R - 1);
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            if (u0 + t < p.US) {
-              Frags<R, SP, CPW> f;
+            for (int i = 0; i < CPW; ++i) {
 #pragma unroll
-              for (int sp = 0; sp < SP; ++sp) ldsm_x4_t(ab[sp] + t * 2048, f.a[sp]);
+              for (int r = 0; r + 1 < R; ++r) {
+                bw[i][r][0] = bw[i][r + 1][0];
+                bw[i][r][1] = bw[i][r + 1][1];
+              }
+              ldsm_x2_t(xa + boff[i], bw[i][R - 1]);
+            }
+          }
+          const uint32_t dslot = dring_u32 + (uint32_t)((sc.ss * p.TR + j) * g.rowD) + uo;
+          uint32_t af[SP][4];
 #pragma unroll
-              for (int i = 0; i < CPW; ++i)
-#pragma unroll
-                for (int r = 0; r < R; ++r) ldsm_x2_t(bb[i][r] + t * 2048, f.b[i][r]);
-#pragma unroll
-              for (int i = 0; i < CPW; ++i)
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-#pragma unroll
-                  for (int sp = 0; sp < SP; ++sp) mma16816<TI>(acc[i][r][sp], f.a[sp], f.b[i][r]);
-              uint32_t lo = 0u, hi = 0u;  // the bias column's registers, chosen by selects (no local memory)
-#pragma unroll
-              for (int sp = 0; sp < SP; ++sp)
-                if (sp == bsp) {
-                  lo = bh ? f.a[sp][1] : f.a[sp][0];
-                  hi = bh ? f.a[sp][3] : f.a[sp][2];
-                }
-              bacc[0] = __fadd2_rn(bacc[0], widen<TI>(lo));
-              bacc[1] = __fadd2_rn(bacc[1], widen<TI>(hi));
+          for (int sp = 0; sp < SP; ++sp) {
+            if (2 * sp + 1 < p.S) {
+              ldsm_x4_t(dslot + aoff[sp], af[sp]);
+            } else {  // a single filter column: rows 8..15 repeat rows 0..7 (not stored)
+              uint32_t h2[2];
+              ldsm_x2_t(dslot + aoff1[sp], h2);
+              af[sp][0] = af[sp][1] = h2[0];
+              af[sp][2] = af[sp][3] = h2[1];
             }
           }
 #pragma unroll
-          for (int sp = 0; sp < SP; ++sp) ab[sp] += 4 * 2048;
-#pragma unroll
           for (int i = 0; i < CPW; ++i)
 #pragma unroll
-            for (int r = 0; r < R; ++r) bb[i][r] += 4 * 2048;
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+              for (int sp = 0; sp < SP; ++sp) mma16816<TI>(acc[i][r][sp], af[sp], bw[i][r]);
+          uint32_t lo = 0u, hi = 0u;  // the bias column's registers, chosen by selects (no local memory)
+#pragma unroll
+          for (int sp = 0; sp < SP; ++sp)
+            if (sp == bsp) {
+              lo = bh ? af[sp][1] : af[sp][0];
+              hi = bh ? af[sp][3] : af[sp][2];
+            }
+          bacc[0] = __fadd2_rn(bacc[0], widen<TI>(lo));
+          bacc[1] = __fadd2_rn(bacc[1], widen<TI>(hi));
         }
-        for (int i = 0; i < NG; ++i) rp.advance(R, p);
       }
-      for (int32_t j = 0; j < rows; ++j) cur.advance(R, p);
     }
 
     __syncwarp();
@@ -467,9 +495,9 @@ cudaError_t launch_k(const Plan& pl, const Args& a, const GmParams& p, CUtensorM
   return cudaGetLastError();
 }
 
-// Warp groups: 2 (512 threads) when a warp's accumulator tiles (R x SP x pairs) are at most 12, so its
+// Warp groups: 2 (512 threads) when a warp's accumulator tiles (R x SP x pairs) are at most 8, so its
 // registers stay within the 128 a thread that 512 threads allow; else 1.
-constexpr int groups_of(int tiles) { return tiles <= 12 ? 2 : 1; }
+constexpr int groups_of(int tiles) { return tiles <= 8 ? 2 : 1; }
 
 // Chunk pairs a warp: 1, 2 or 4, as many as keep R x SP x pairs <= 24 accumulator tiles.
 template <typename TI, typename TO, int R, int SP>
@@ -544,7 +572,7 @@ Geometry geometry_wgrad_grouped_mma(const Shape& s) {
   // two warp groups add their sums through shared memory over the ring's rows
   const int64_t tiles = s.r * spk * pairs_per_warp(s);
   const size_t ring_bytes = ring_smem(s, rs.d, rs.tr) - 1024;
-  if (tiles <= 12 && (size_t)(tiles * 4 + 1) * 8 * 32 * 4 > ring_bytes) return g;
+  if (tiles <= 8 && (size_t)(tiles * 4 + 1) * 8 * 32 * 4 > ring_bytes) return g;
   g.ok = true;
   g.ctas_per_sm = 1;
   g.tiles = s.c / kCB;
