@@ -287,21 +287,29 @@ __global__ void __launch_bounds__(256 * NG, 1)
   const uint32_t dring_u32 = smem_u32(g.dring), xring_u32 = smem_u32(g.xring);
 
   StepPos sc{0, 0u};
-  RowPos la{0, (int32_t)(q_b % p.Ho), (int32_t)(q_b / p.Ho), true};  // first row of the step loaded at step S: S + ahead
-  StepPos sl{0, 0u};
-  for (int i = 0; i < p.ahead * p.TR && q_b + i < q_e; ++i) la.advance(R, p);
+  StepPos sl{0, 0u};  // the step slot of step S + ahead
   for (int i = 0; i < p.ahead; ++i) sl.advance(p);
   int32_t issuer = 0;  // warp that loads at step S: S mod kW
   int64_t qa = q_b + (int64_t)p.ahead * p.TR;  // first row of step S + ahead
+  // The issuing lane places row qa in closed form (only it pays the divisions):
+  // its image and row, and its first input row's index in the slice's input-row
+  // sequence (R rows for the slice's first row and for each image start, one
+  // more for every other row), which modulo RX is its ring slot.
+  const int32_t n_b = (int32_t)(q_b / p.Ho);
+  auto row_pos = [&](int64_t qq) {
+    const int32_t n = (int32_t)(qq / p.Ho), ho = (int32_t)(qq - (int64_t)n * p.Ho);
+    const int64_t seq = (qq - q_b) + (int64_t)(R - 1) * (n - n_b);
+    return RowPos{(int32_t)(seq % p.RX), ho, n, qq == q_b};
+  };
 
   for (int64_t q = q_b; q < q_e; q += p.TR) {
     const int32_t rows = q_e - q < p.TR ? (int32_t)(q_e - q) : p.TR;
     if (warp == issuer && lane == 0 && qa < q_e)
-      issue_step<R>(g, p, la, sl, q_e - qa < p.TR ? (int32_t)(q_e - qa) : p.TR);
+      issue_step<R>(g, p, row_pos(qa), sl, q_e - qa < p.TR ? (int32_t)(q_e - qa) : p.TR);
     // Lanes that spin on an mbarrier can hold up a divergent lane of the same
     // warp; reconverge before any of them waits.
     __syncwarp();
-    for (int32_t j = 0; j < p.TR && qa < q_e; ++j, ++qa) la.advance(R, p);
+    qa += p.TR;
     sl.advance(p);
     issuer = issuer + 1 == kW ? 0 : issuer + 1;
 
@@ -312,9 +320,7 @@ __global__ void __launch_bounds__(256 * NG, 1)
       // each 16-column step with the B fragments of the R input rows in a
       // window that slides by one row within an image (one new input row a row).
       const int32_t j0 = (rows * grp) / NG, j1 = (rows * (grp + 1)) / NG;
-      int32_t info[kMaxTR];
-#pragma unroll
-      for (int32_t j = 0; j < kMaxTR; ++j) info[j] = j0 + j < j1 ? g.rowinfo[sc.ss * p.TR + j0 + j] : 0;
+      const int32_t* info = g.rowinfo + sc.ss * p.TR + j0;
 #pragma unroll 1
       for (int32_t us = 0; us < p.US; ++us) {
         const uint32_t uo = (uint32_t)us * 2048u;
@@ -323,12 +329,13 @@ __global__ void __launch_bounds__(256 * NG, 1)
         for (int32_t jj = 0; jj < kMaxTR; ++jj) {
           if (j0 + jj >= j1) break;
           const int32_t j = j0 + jj;
-          const int32_t xs = info[jj] & 0xffff;
+          const int32_t inf = info[jj];
+          const int32_t xs = inf & 0xffff;
           auto xslot = [&](int r) {
             const int32_t sl = xs + r >= p.RX ? xs + r - p.RX : xs + r;
             return xring_u32 + (uint32_t)sl * g.rowX + uo;
           };
-          if (jj == 0 || (info[jj] >> 16) != 0) {  // a fresh window
+          if (jj == 0 || (inf >> 16) != 0) {  // a fresh window
 #pragma unroll
             for (int r = 0; r < R; ++r) {
               const uint32_t xa = xslot(r);
@@ -471,6 +478,13 @@ __global__ void __launch_bounds__(256 * NG, 1)
 // Chunk pairs a warp: 8 pairs a CTA for Cg <= 8, Cg for more.
 int pairs_per_warp(const Shape& s) { return s.cg <= 8 ? 1 : (int)(s.cg / 8); }
 
+// Warp groups: 2 (512 threads) when a warp's accumulator tiles (R x SP x pairs) are at most 8, so its
+// registers stay within the 128 a thread that 512 threads allow; else 1.
+constexpr int groups_of(int tiles) { return tiles <= 8 ? 2 : 1; }
+// The filter columns' pairs the kernel is instantiated with for R filter rows.
+int sp_of(int64_t r) { return r == 1 ? 1 : r == 3 ? 2 : 3; }
+int warp_groups(const Shape& s) { return groups_of((int)(s.r * sp_of(s.r) * pairs_per_warp(s))); }
+
 template <typename TI, typename TO, int R, int SP, int CPW, int NG>
 cudaError_t launch_k(const Plan& pl, const Args& a, const GmParams& p, CUtensorMapDataType dt, size_t smem) {
   const Shape& s = pl.sh;
@@ -494,10 +508,6 @@ cudaError_t launch_k(const Plan& pl, const Args& a, const GmParams& p, CUtensorM
                                                      pl.with_bias ? a.ws_bias : nullptr, p, device_error_word());
   return cudaGetLastError();
 }
-
-// Warp groups: 2 (512 threads) when a warp's accumulator tiles (R x SP x pairs) are at most 8, so its
-// registers stay within the 128 a thread that 512 threads allow; else 1.
-constexpr int groups_of(int tiles) { return tiles <= 8 ? 2 : 1; }
 
 // Chunk pairs a warp: 1, 2 or 4, as many as keep R x SP x pairs <= 24 accumulator tiles.
 template <typename TI, typename TO, int R, int SP>
@@ -561,7 +571,7 @@ Geometry geometry_wgrad_grouped_mma(const Shape& s) {
   // warp's chunk pairs (R x ceil(S/2) x 4 floats each) at most 96 registers
   const int64_t sp = (s.s + 1) / 2;
   if (!((s.r == 1 && s.s == 1) || (s.r == 3 && sp <= 2 && s.s >= 1) || (s.r == 5 && sp <= 3))) return g;
-  const int64_t spk = s.r == 1 ? 1 : s.r == 3 ? 2 : 3;  // the instantiated column pairs
+  const int64_t spk = sp_of(s.r);  // the instantiated column pairs
   if (s.r * spk * pairs_per_warp(s) > 24) return g;
   if (s.ph > s.r - 1 || s.pw > s.s - 1) return g;
   // TMA: rows of at most 256 columns (the dY box adds S - 1), 32-bit coordinates
