@@ -83,6 +83,7 @@ Geometry geometry_of(conv_kernel k, const Shape& s, conv_dir dir) {
     case CONV_KERNEL_WGRAD_GROUPED_TC: return dir == CONV_DIR_WGRAD ? geometry_wgrad_grouped_tc(s) : Geometry{};
     case CONV_KERNEL_WGRAD_TC: return dir == CONV_DIR_WGRAD ? geometry_wgrad_tc(s) : Geometry{};
     case CONV_KERNEL_WGRAD_GROUPED_MMA: return dir == CONV_DIR_WGRAD ? geometry_wgrad_grouped_mma(s) : Geometry{};
+    case CONV_KERNEL_FFMA: return geometry_ffma(s, dir);
     case CONV_KERNEL_DGRAD_DEPTHWISE: return dir == CONV_DIR_DGRAD ? geometry_dgrad_depthwise(s) : Geometry{};
     case CONV_KERNEL_DGRAD_GROUPED_TC: return dir == CONV_DIR_DGRAD ? geometry_dgrad_grouped_tc(s) : Geometry{};
     case CONV_KERNEL_WGRAD_DEPTHWISE: return dir == CONV_DIR_WGRAD ? geometry_wgrad_depthwise(s) : Geometry{};
@@ -136,15 +137,16 @@ conv_status choose_kernel(const Shape& s, conv_dir dir, conv_kernel* kernel, Geo
   static const conv_kernel wgrad_order[] = {CONV_KERNEL_WGRAD_1X1_TF32X3,  CONV_KERNEL_WGRAD_1X1_FFMA,
                                             CONV_KERNEL_WGRAD_DEPTHWISE,    CONV_KERNEL_WGRAD_GROUPED_MMA,
                                             CONV_KERNEL_WGRAD_GROUPED_TC,   CONV_KERNEL_WGRAD_TC,
-                                            CONV_KERNEL_WGRAD_GROUPED,      CONV_KERNEL_GENERIC};
+                                            CONV_KERNEL_FFMA,               CONV_KERNEL_WGRAD_GROUPED,
+                                            CONV_KERNEL_GENERIC};
   // The cluster form of the forward is reached only through the override:
   // on the 3x3 small-M layer it measured slower than the two-stage form.
   static const conv_kernel fwd_order[] = {CONV_KERNEL_FWD_TC, CONV_KERNEL_FWD_DEPTHWISE, CONV_KERNEL_FWD_GROUPED_TC,
-                                          CONV_KERNEL_GENERIC};
+                                          CONV_KERNEL_FFMA, CONV_KERNEL_GENERIC};
   static const conv_kernel dgrad_order[] = {CONV_KERNEL_DGRAD_TC, CONV_KERNEL_DGRAD_DEPTHWISE,
-                                            CONV_KERNEL_DGRAD_GROUPED_TC, CONV_KERNEL_GENERIC};
+                                            CONV_KERNEL_DGRAD_GROUPED_TC, CONV_KERNEL_FFMA, CONV_KERNEL_GENERIC};
   const conv_kernel* order = dir == CONV_DIR_WGRAD ? wgrad_order : dir == CONV_DIR_FWD ? fwd_order : dgrad_order;
-  const int count = dir == CONV_DIR_WGRAD ? 8 : dir == CONV_DIR_FWD ? 4 : 4;
+  const int count = dir == CONV_DIR_WGRAD ? 9 : 5;
   for (int i = 0; i < count; ++i) {
     Geometry g = geometry_of(order[i], s, dir);
     if (g.ok) {
@@ -344,6 +346,7 @@ conv_status run(const conv_problem* prob, conv_dir dir, const void* x, const voi
       case CONV_KERNEL_WGRAD_GROUPED_TC: err = launch_wgrad_grouped_tc(plan, a); break;
       case CONV_KERNEL_WGRAD_TC: err = launch_wgrad_tc(plan, a); break;
       case CONV_KERNEL_WGRAD_GROUPED_MMA: err = launch_wgrad_grouped_mma(plan, a); break;
+      case CONV_KERNEL_FFMA: err = launch_ffma(plan, a); break;
       case CONV_KERNEL_DGRAD_DEPTHWISE: err = launch_dgrad_depthwise(plan, a); break;
       case CONV_KERNEL_DGRAD_GROUPED_TC: err = launch_dgrad_grouped_tc(plan, a); break;
       case CONV_KERNEL_WGRAD_DEPTHWISE: err = launch_wgrad_depthwise(plan, a); break;
@@ -552,7 +555,7 @@ conv_status conv_wgrad_bias_static_ws(const conv_problem* p, const void* x, cons
 
 
 conv_status conv_set_kernel_override(int32_t kernel) {
-  if (kernel < CONV_KERNEL_AUTO || kernel > CONV_KERNEL_WGRAD_GROUPED_MMA) return CONV_ERR_INVALID_ARG;
+  if (kernel < CONV_KERNEL_AUTO || kernel > CONV_KERNEL_FFMA) return CONV_ERR_INVALID_ARG;
   g_kernel_override = kernel;
   return CONV_OK;
 }

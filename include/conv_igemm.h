@@ -130,11 +130,15 @@ typedef enum conv_kernel {
   CONV_KERNEL_DGRAD_GROUPED_TC = 14, /* stride-1 16-bit grouped data gradient (Cg = Kg dividing 128,
                                         C % 128 = 0): the block-diagonal grouped forward over dY
                                         with the turned filter written into the workspace */
-  CONV_KERNEL_WGRAD_GROUPED_MMA = 15 /* 16-bit grouped weight gradient (Cg = Kg in 2..32, C % 64 = 0,
+  CONV_KERNEL_WGRAD_GROUPED_MMA = 15, /* 16-bit grouped weight gradient (Cg = Kg in 2..32, C % 64 = 0,
                                         unit stride and dilation, 1x1, 3 x (1..4) or 5 x (1..6)
                                         filters): warp-level m16n8k16 MMAs over input columns with
                                         the filter column applied as a shift of dY, so every product
                                         is a gradient element (8 or more channels per group) */
+  CONV_KERNEL_FFMA = 16              /* fp32, one group, C and K multiples of 4: implicit-GEMM FFMA
+                                        tiles (128 x 128, 8 x 8 a thread) for the forward, the
+                                        stride-1 data gradient (the turned problem, filter read in
+                                        place) and the weight gradient (+ bias gradient) */
 } conv_kernel;
 
 /* What a call with these arguments would run. */

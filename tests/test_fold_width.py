@@ -66,9 +66,13 @@ def test_planner_folds_when_only_the_folded_problem_has_a_fast_kernel():
     # 4x4 stride 4, C = 16: folded by 4
     p = Problem(n=2, h=32, w=32, c=16, k=128, r=4, s=4, stride_h=4, stride_w=4, in_dtype=BF16, out_dtype=BF16)
     assert fw(p)["kernel_name"] == "fwd_tc" and fw(p)["fold_width"] == 4
-    # a 1x2 W-stride-2 weight gradient in fp32 becomes a 1x1 one
-    p = Problem(n=2, h=8, w=16, c=64, k=64, r=1, s=2, stride_w=2)
+    # a 1x2 W-stride-2 weight gradient in fp32 with 18 channels (no FFMA tiles: not a multiple of 4)
+    # becomes a 1x1 one of 36 channels
+    p = Problem(n=2, h=8, w=64, c=18, k=64, r=1, s=2, stride_w=2)
     assert fw(p, DIR_WGRAD)["kernel_name"] == "wgrad_1x1_tf32x3" and fw(p, DIR_WGRAD)["fold_width"] == 2
+    # with 64 channels the FFMA tiles take it as given: no fold
+    p = Problem(n=2, h=8, w=16, c=64, k=64, r=1, s=2, stride_w=2)
+    assert fw(p, DIR_WGRAD)["kernel_name"] == "ffma" and fw(p, DIR_WGRAD)["fold_width"] == 1
     # and its data gradient (16-bit) becomes stride 1
     p = Problem(n=2, h=8, w=16, c=64, k=128, r=1, s=2, stride_w=2, in_dtype=BF16, out_dtype=BF16)
     assert fw(p, DIR_DGRAD)["kernel_name"] == "dgrad_tc" and fw(p, DIR_DGRAD)["fold_width"] == 2

@@ -593,7 +593,7 @@ def test_empty_batch_every_direction(shape):
     (dict(n=2, h=16, w=16, c=32, k=128, r=2, s=2, stride_h=2, stride_w=2), cig.DIR_FWD, (BF16, BF16), "fwd_tc"),
     (dict(n=3, h=20, w=24, c=16, k=256, r=4, s=4, stride_h=4, stride_w=4), cig.DIR_FWD, (F16, F32), "fwd_tc"),
     (dict(n=2, h=9, w=16, c=32, k=136, r=3, s=2, stride_w=2, pad_h=1), cig.DIR_FWD, (BF16, BF16), "fwd_tc"),
-    (dict(n=2, h=8, w=16, c=64, k=64, r=1, s=2, stride_w=2), cig.DIR_WGRAD, (F32, F32), "wgrad_1x1_tf32x3"),
+    (dict(n=2, h=8, w=64, c=18, k=64, r=1, s=2, stride_w=2), cig.DIR_WGRAD, (F32, F32), "wgrad_1x1_tf32x3"),
     (dict(n=2, h=8, w=16, c=64, k=128, r=1, s=2, stride_w=2), cig.DIR_DGRAD, (BF16, BF16), "dgrad_tc"),
 ], ids=["2x2s2", "4x4s4", "3x2ws2", "wgrad1x2", "dgrad1x2"])
 def test_width_fold(shape, direction, dt, kernel):
@@ -610,3 +610,51 @@ def test_width_fold(shape, direction, dt, kernel):
     else:
         check_dgrad(p, 21, ["auto", "generic"], [-1, 1, 2])
     assert cig.device_errors() == 0
+
+
+# ------------------------------------------------------------- fp32 FFMA tiles
+
+FFMA_SHAPES = [
+    dict(n=2, h=9, w=11, c=20, k=36, r=3, s=3, pad_h=1, pad_w=1),                   # channel tails in a step and a tile
+    dict(n=3, h=13, w=10, c=16, k=132, r=3, s=2, stride_h=2, stride_w=1, pad_h=1, dil_h=2),  # strided, dilated
+    dict(n=1, h=17, w=19, c=64, k=64, r=5, s=5, pad_h=2, pad_w=2),
+    dict(n=2, h=12, w=12, c=136, k=8, r=1, s=1),                                   # pointwise, ragged M
+    dict(n=1, h=20, w=21, c=8, k=260, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1),  # 3 N tiles
+]
+
+
+@pytest.mark.parametrize("shape", FFMA_SHAPES)
+def test_ffma_fp32_all_directions(shape):
+    """fp32 implicit-GEMM FFMA tiles: forward, data gradient (stride 1; else generic) and weight gradient with
+    its bias gradient, against the oracle at the fp32 tolerance, automatic, pinned and maximal degrees."""
+    p = cig.Problem(**shape)
+    assert cig.describe_plan(p, cig.DIR_FWD, -1)["kernel_name"] == "ffma"
+    assert cig.describe_plan(p, cig.DIR_WGRAD, -1)["kernel_name"] in ("ffma", "wgrad_1x1_tf32x3", "wgrad_1x1_ffma")
+    check_fwd(p, 17, ["ffma"], [-1, 1, 3, "max"])
+    check_wgrad(p, 17, ["ffma"], [-1, 1, 3, "max"], bias=True)
+    check_wgrad(p, 17, ["ffma"], [2], bias=False)
+    if p.stride_h == 1 and p.stride_w == 1:
+        assert cig.describe_plan(p, cig.DIR_DGRAD, -1)["kernel_name"] == "ffma"
+        check_dgrad(p, 17, ["ffma"], [-1, 1, 3, "max"])
+    x, w = inputs(p, 17, direction=cig.DIR_FWD)
+    assert torch.equal(run_fwd(p, x, w, 3), run_fwd(p, x, w, 3))
+    assert cig.device_errors() == 0
+
+
+def test_ffma_fp32_exact_on_small_integers():
+    """Small-integer inputs keep every fp32 product and partial sum exact, so every degree gives exactly the
+    oracle's value in all three directions."""
+    p = cig.Problem(n=2, h=10, w=9, c=24, k=40, r=3, s=3, pad_h=1, pad_w=1)
+    orc = oracle.get()
+    x, w = inputs(p, 18, "integer", -3, 3, cig.DIR_FWD)
+    dy, _ = inputs(p, 18, "integer", -3, 3, cig.DIR_DGRAD)
+    cig.set_kernel_override("ffma")
+    try:
+        for sk in (-1, 1, 2, 5):
+            assert np.array_equal(run_fwd(p, x, w, sk).double().numpy(), orc.fwd(oproblem(p), x, w)), sk
+            assert np.array_equal(run_dgrad(p, dy, w, sk).double().numpy(), orc.dgrad(oproblem(p), dy, w)), sk
+            dw, db = run_wgrad(p, x, dy, sk, True)
+            assert np.array_equal(dw.double().numpy(), orc.wgrad(oproblem(p), x, dy)), sk
+            assert np.array_equal(db.double().numpy(), orc.bgrad(oproblem(p), dy)), sk
+    finally:
+        cig.set_kernel_override("auto")

@@ -347,8 +347,9 @@ def test_dense_wgrad_tensor_core_selection():
                  out_dtype=BF16)
     info = wg(g2)
     assert info["kernel_name"] == "wgrad_tc" and info["tiles"] == 2 * 9
-    # not taken: fp32, fewer than 64 channels, channels not a multiple of 8, groups with Kg = 64
-    assert wg(Problem(n=4, h=16, w=16, c=128, k=256, r=3, s=3, pad_h=1, pad_w=1))["kernel_name"] == "generic"
+    # not taken: fp32 (the FFMA tiles take it), fewer than 64 channels, channels not a multiple of 8,
+    # groups with Kg = 64
+    assert wg(Problem(n=4, h=16, w=16, c=128, k=256, r=3, s=3, pad_h=1, pad_w=1))["kernel_name"] == "ffma"
     for c, k in ((32, 128), (128, 32), (100, 128)):
         p = Problem(n=2, h=8, w=8, c=c, k=k, r=3, s=3, pad_h=1, pad_w=1, in_dtype=BF16, out_dtype=BF16)
         assert wg(p)["kernel_name"] == "generic", (c, k)
@@ -363,3 +364,21 @@ def test_dense_wgrad_tensor_core_selection():
     strided = Problem(n=1, h=12, w=12, c=128, k=128, groups=8, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1,
                       in_dtype=F16, out_dtype=F16)
     assert wg(strided)["kernel_name"] == "wgrad_grouped_tc"
+
+
+def test_fp32_ffma_tiles_selection():
+    """fp32 problems with one group and channel counts that are multiples of 4 take the FFMA implicit-GEMM
+    tiles in every direction (the data gradient at stride 1); others keep the generic kernel."""
+    p = Problem(n=4, h=16, w=16, c=128, k=256, r=3, s=3, pad_h=1, pad_w=1)
+    for d, tiles in ((DIR_FWD, 8 * 2), (cig.DIR_DGRAD, 8 * 1), (DIR_WGRAD, 2 * 1 * 9)):
+        info = cig.describe_plan(p, d, -1, sm_count=SMS)
+        assert info["kernel_name"] == "ffma" and info["tiles"] == tiles and info["ctas"] <= SMS, (d, info)
+    strided = Problem(n=2, h=9, w=9, c=16, k=16, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1)
+    assert cig.describe_plan(strided, cig.DIR_DGRAD, -1, sm_count=SMS)["kernel_name"] == "generic"
+    assert cig.describe_plan(strided, DIR_FWD, -1, sm_count=SMS)["kernel_name"] == "ffma"
+    for bad in (Problem(n=2, h=8, w=8, c=6, k=8, r=3, s=3), Problem(n=2, h=8, w=8, c=8, k=8, r=3, s=3, groups=2),
+                Problem(n=2, h=8, w=8, c=8, k=6, r=3, s=3)):
+        assert cig.describe_plan(bad, DIR_FWD, -1, sm_count=SMS)["kernel_name"] == "generic"
+    # 16-bit inputs never take the fp32 tiles
+    b = Problem(n=2, h=8, w=8, c=8, k=8, r=3, s=3, in_dtype=BF16, out_dtype=BF16)
+    assert cig.describe_plan(b, DIR_FWD, -1, sm_count=SMS)["kernel_name"] != "ffma"
