@@ -45,6 +45,10 @@ struct FfParams {
   int32_t R, S, sh, sw, ph, pw, dh, dw;
   int32_t cblocks;     // ceil(C / 16) (forward, data gradient)
   int32_t split;
+  // fused forward epilogue (unsplit only): y = min(max(acc + bias[k], ep_lo), ep_hi)
+  const float* ep_bias;
+  float ep_lo, ep_hi;
+  int32_t ep;
 };
 
 // One operand tile's loads for a step: 2 float4 a thread, staged in registers.
@@ -223,8 +227,16 @@ __global__ void __launch_bounds__(kThreads, 1) ffma_igemm_kernel(FfParams fp) {
       const int64_t n = n0 + h * 64 + tx * 4;
       if (n >= fp.N) continue;
       const int64_t row = DIR == kWgrad ? (m * taps + tap) * fp.N : m * fp.N;
-      *reinterpret_cast<float4*>(dst + row + n) =
-          make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
+      float4 v = make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
+      if (DIR == kFwd && fp.ep) {  // bias + clamp on the fp32 sum (the forward runs unsplit then)
+        const float4 b = fp.ep_bias ? make_float4(fp.ep_bias[n], fp.ep_bias[n + 1], fp.ep_bias[n + 2], fp.ep_bias[n + 3])
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        v.x = fminf(fmaxf(v.x + b.x, fp.ep_lo), fp.ep_hi);
+        v.y = fminf(fmaxf(v.y + b.y, fp.ep_lo), fp.ep_hi);
+        v.z = fminf(fmaxf(v.z + b.z, fp.ep_lo), fp.ep_hi);
+        v.w = fminf(fmaxf(v.w + b.w, fp.ep_lo), fp.ep_hi);
+      }
+      *reinterpret_cast<float4*>(dst + row + n) = v;
     }
   }
   if (do_bias && t < kT && m0 + t < fp.M) {
@@ -304,6 +316,11 @@ cudaError_t launch_ffma(const Plan& p, const Args& a) {
   if (p.dir == CONV_DIR_FWD) {
     fp.a = static_cast<const float*>(a.x);
     fp.b = static_cast<const float*>(a.b);
+    if (a.ep && a.ws) return cudaErrorInvalidValue;  // the epilogue runs unsplit only
+    fp.ep = a.ep ? 1 : 0;
+    fp.ep_bias = static_cast<const float*>(a.ep_bias);
+    fp.ep_lo = a.ep_lo;
+    fp.ep_hi = a.ep_hi;
     ffma_igemm_kernel<kFwd><<<(unsigned)ctas, kThreads, 0, a.stream>>>(fp);
   } else if (p.dir == CONV_DIR_DGRAD) {
     fp.a = static_cast<const float*>(a.x);  // dY
