@@ -73,6 +73,10 @@ WORKLOADS = {
     "grp3x3_dgrad_f16_g64": (dict(n=64, h=28, w=28, c=512, k=512, r=3, s=3, pad_h=1, pad_w=1, groups=64,
                                   in_dtype=2, out_dtype=2), "dgrad", "normal", (0.0, 1.0), 4,
                              "grouped 3x3 dgrad fp16 NHWC N=64 H=W=28 C=K=512 groups=64 (8 ch/group)"),
+    "fwd3x3_f32_n16_c256": (dict(n=16, h=56, w=56, c=256, k=256, r=3, s=3, pad_h=1, pad_w=1), "fwd", "normal",
+                            (0.0, 1.0), 9, "3x3 fwd fp32 NHWC N=16 H=W=56 C=K=256 pad 1 (FFMA tiles)"),
+    "wgrad3x3_f32_n16_c256": (dict(n=16, h=56, w=56, c=256, k=256, r=3, s=3, pad_h=1, pad_w=1), "wgrad", "normal",
+                              (0.0, 1.0), 9, "3x3 wgrad+db fp32 NHWC N=16 H=W=56 C=K=256 pad 1 (FFMA tiles)"),
     "grp3x3_fwd_f16_g64": (dict(n=64, h=28, w=28, c=512, k=512, r=3, s=3, pad_h=1, pad_w=1, groups=64,
                                 in_dtype=2, out_dtype=2), "fwd", "normal", (0.0, 1.0), 4,
                            "grouped 3x3 fwd fp16 NHWC N=64 H=W=28 C=K=512 groups=64 (8 ch/group)"),
@@ -344,7 +348,7 @@ def time_oracle(p, direction, dist, args, seed, target_s: float):
 # headline and reported under "per_config", each at its own automatic plan.
 PER_CONFIG = ["wgrad1x1_f32_n4", "fwd3x3_bf16_n1", "dgrad3x3_bf16_n1", "dw7x7_wgrad_bf16", "dw7x7_dgrad_bf16",
               "grp3x3_wgrad_f16_g64", "grp3x3_wgrad_f16_g128", "grp3x3_dgrad_f16_g64", "fwd3x3_bf16_n64_c256",
-              "dgrad3x3_bf16_n64_c256", "wgrad3x3_bf16_n64_c256"]
+              "dgrad3x3_bf16_n64_c256", "wgrad3x3_bf16_n64_c256", "fwd3x3_f32_n16_c256", "wgrad3x3_f32_n16_c256"]
 # The split-K degrees swept on the small-M layer (auto first).
 SWEEP = {"fwd3x3_bf16_n1": [-1, 1, 2, 4, 8, 16, 32]}
 
@@ -360,7 +364,8 @@ def roofline_for(kname, p, direction, flops, in_bytes, stage1_ms, pk, sms):
         bound = "tensor" if flops / in_bytes > pk["bf16"] * 1e12 / (pk["hbm"] * 1e9) else "hbm"
     elif kname in ("fwd_grouped_tc", "wgrad_grouped_tc", "dgrad_grouped_tc"):
         bound = "tensor_blockdiag"
-    elif kname in ("wgrad_depthwise", "wgrad_grouped", "fwd_depthwise", "dgrad_depthwise") or kname == "generic":
+    elif kname in ("wgrad_depthwise", "wgrad_grouped", "fwd_depthwise", "dgrad_depthwise", "ffma") or \
+            kname == "generic":
         bound = "alu"
     else:
         bound = "hbm"

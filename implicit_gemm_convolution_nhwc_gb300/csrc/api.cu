@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include "conv_internal.h"
+#include "kernel_entry.h"
 
 namespace cig {
 namespace {

@@ -15,6 +15,7 @@
 // Grouped and depthwise data gradients at stride 1 take the same identity
 // with the groups kept (below, and the grouped one in grouped_tc.cu).
 #include "common.cuh"
+#include "../kernel_entry.h"
 
 namespace cig {
 

@@ -29,6 +29,7 @@
 #include <type_traits>
 
 #include "dw_ring.cuh"
+#include "../kernel_entry.h"
 
 namespace cig {
 namespace {

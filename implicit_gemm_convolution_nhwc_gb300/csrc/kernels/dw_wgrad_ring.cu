@@ -38,6 +38,7 @@
 // bytes, and the tile goes out as contiguous fp32 to slab sigma of the
 // workspace or, unsplit, rounded into dW / db.
 #include "dw_ring.cuh"
+#include "../kernel_entry.h"
 
 namespace cig {
 namespace {

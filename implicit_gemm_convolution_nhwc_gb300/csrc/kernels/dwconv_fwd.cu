@@ -17,6 +17,7 @@
 // Reduction depth R*S is small, so there is no split-K: one launch, and the
 // fused forward epilogue (bias + clamp) applies in the store.
 #include "common.cuh"
+#include "../kernel_entry.h"
 
 namespace cig {
 namespace {

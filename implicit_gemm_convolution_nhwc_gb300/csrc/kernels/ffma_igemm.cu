@@ -17,6 +17,7 @@
 // through registers, and each thread accumulates an 8 x 8 block with
 // float4 shared loads (16 FMAs per load).
 #include "common.cuh"
+#include "../kernel_entry.h"
 
 namespace cig {
 namespace {

@@ -12,6 +12,7 @@
 // before it adds any of them, so every warp keeps a batch of independent
 // loads in flight; the adds still happen strictly in slice order.
 #include "common.cuh"
+#include "../kernel_entry.h"
 
 namespace cig {
 namespace {

@@ -34,6 +34,7 @@
 //
 // Warp roles: 0 TMA producer, 1 MMA issuer, 2 TMEM owner, 4-7 epilogue.
 #include "tc_store.cuh"
+#include "../kernel_entry.h"
 
 namespace cig {
 namespace {

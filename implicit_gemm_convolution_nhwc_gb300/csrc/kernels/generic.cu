@@ -5,6 +5,7 @@
 // of a slice is deterministic. These are the correctness floor under the fast
 // kernels, not a fast path.
 #include "common.cuh"
+#include "../kernel_entry.h"
 
 namespace cig {
 namespace {

@@ -12,6 +12,7 @@
 // (16 for 8 channels per group), which the tensor pipe still does faster than
 // the FP32 pipe does the useful part.
 #include "common.cuh"
+#include "../kernel_entry.h"
 
 namespace cig {
 namespace {

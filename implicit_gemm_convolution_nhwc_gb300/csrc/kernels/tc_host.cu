@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "tc_common.cuh"
+#include "../kernel_entry.h"
 
 namespace cig {
 

@@ -15,6 +15,7 @@
 // warp's shared loads of a row are contiguous. The bias is summed from the
 // dY stage already in shared memory (k = tid % 64, 8 rows per thread).
 #include "common.cuh"
+#include "../kernel_entry.h"
 
 namespace cig {
 namespace {

@@ -36,6 +36,7 @@
 // issuer, 2 TMEM owner, 4-11 converters, which also drain the accumulators
 // and run the epilogue.
 #include "tc_common.cuh"
+#include "../kernel_entry.h"
 
 namespace cig {
 namespace {

@@ -29,6 +29,7 @@
 // implicit-GEMM convolution on gfx1250", "Two-stage split-K") or, with one
 // slice, straight to dW / db.
 #include "common.cuh"
+#include "../kernel_entry.h"
 
 namespace cig {
 namespace {

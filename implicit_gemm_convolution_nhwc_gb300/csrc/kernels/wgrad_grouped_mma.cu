@@ -31,6 +31,7 @@
 // belongs to one warp and one lane: no reduction across warps, and the sums
 // run in a fixed order (deterministic).
 #include "dw_ring.cuh"
+#include "../kernel_entry.h"
 
 namespace cig {
 namespace {

@@ -23,6 +23,7 @@
 #include <type_traits>
 
 #include "tc_common.cuh"
+#include "../kernel_entry.h"
 
 namespace cig {
 namespace {

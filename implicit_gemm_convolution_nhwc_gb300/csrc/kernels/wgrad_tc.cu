@@ -32,6 +32,7 @@
 #include <type_traits>
 
 #include "tc_store.cuh"
+#include "../kernel_entry.h"
 
 namespace cig {
 namespace {
