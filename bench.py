@@ -560,6 +560,7 @@ def per_config(dev, sms, pk, steps, warmup):
                               if k in roof}}
         if "useful_frac_of_fp32_pipe" in roof:
             entry["roofline"]["useful_frac_of_fp32_pipe"] = roof["useful_frac_of_fp32_pipe"]
+        entry["roofline"]["traffic"] = recorded_traffic(kname, name)
         wl.free()
         for req in SWEEP.get(name, []):
             sw = Workload(name, dev, sms, split_k=req)
