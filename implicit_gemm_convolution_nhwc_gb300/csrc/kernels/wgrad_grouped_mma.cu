@@ -74,10 +74,21 @@ struct RingShape {
   int d = 0, tr = 0;
 };
 
+int warp_groups(const Shape& s);
+
 // The most rows a step (up to 8: the per-step bookkeeping is paid once per
-// step) with the deepest ring that fits, at least one step ahead and one of
-// slack.
+// step) that still lets the loads run two steps ahead with two of slack, a
+// multiple of the warp groups (which split a step's rows evenly); else the
+// most rows with the deepest ring that fits, at least one step ahead and one
+// of slack. With one step of 7 rows ahead the warps waited for their rows for
+// a quarter of the loop.
 RingShape ring_shape(const Shape& s) {
+  const int ng = warp_groups(s);
+  for (int tr = kMaxTR; tr >= ng; --tr) {
+    if (tr % ng != 0) continue;
+    for (int d = kMaxDepth; d >= 4; --d)
+      if (ring_smem(s, d, tr) <= kSmemLimit) return RingShape{d, tr};
+  }
   for (int tr = kMaxTR; tr >= 1; --tr)
     for (int d = kMaxDepth; d >= 2; --d)
       if (ring_smem(s, d, tr) <= kSmemLimit) return RingShape{d, tr};
@@ -450,8 +461,12 @@ __global__ void __launch_bounds__(256 * NG, 1)
   // sp is row m = lane / 4 + 8 (e / 2) (filter column 2 sp + m / 8, output
   // channel m % 8 of the k chunk) and column n = 2 (lane % 4) + e % 2 (input
   // channel n of the c chunk).
-  const int64_t Cg = p.Cg;
-  const int64_t E = p.C * R * p.S * Cg;  // dW elements (C = K)
+  // Cg divides 64 (a power of two), so the CTA's first channel is a group
+  // boundary: group membership and the channel within the group follow from
+  // the channel indices within the CTA by masks (no 64-bit divisions).
+  const int32_t cgm = p.Cg - 1;
+  const int64_t E = p.C * R * p.S * (int64_t)p.Cg;  // dW elements (C = K)
+  float* slab = ws ? ws + (int64_t)sigma * E : nullptr;
 #pragma unroll
   for (int i = 0; i < CPW; ++i)
 #pragma unroll
@@ -462,11 +477,11 @@ __global__ void __launch_bounds__(256 * NG, 1)
         for (int e = 0; e < 4; ++e) {
           const int m = (lane >> 2) + 8 * (e >> 1), n = 2 * (lane & 3) + (e & 1);
           const int s = 2 * sp + (m >> 3);
-          const int64_t k = cb * kCB + kch * 8 + (m & 7);
-          const int64_t c = cb * kCB + cch[i] * 8 + n;
-          if (!ok || s >= p.S || k / Cg != c / Cg) continue;
-          const int64_t dst = ((k * R + r) * p.S + s) * Cg + (c % Cg);
-          if (ws) ws[(int64_t)sigma * E + dst] = acc[i][r][sp][e];
+          const int32_t kl = kch * 8 + (m & 7), cl = cch[i] * 8 + n;  // within the CTA's 64 channels
+          if (!ok || s >= p.S || ((kl ^ cl) & ~cgm) != 0) continue;
+          const int64_t k = cb * kCB + kl;
+          const int64_t dst = ((k * R + r) * p.S + s) * p.Cg + (cl & cgm);
+          if (ws) slab[dst] = acc[i][r][sp][e];
           else store_out(out + dst, acc[i][r][sp][e]);
         }
   if ((db || ws_bias) && (lane & 3) == 0 && ok) {
