@@ -30,6 +30,8 @@
 // diagonal blocks are kept) and the bias sum of chunk w. Each output element
 // belongs to one warp and one lane: no reduction across warps, and the sums
 // run in a fixed order (deterministic).
+#include <type_traits>
+
 #include "dw_ring.cuh"
 #include "../kernel_entry.h"
 
@@ -95,7 +97,7 @@ RingShape ring_shape(const Shape& s) {
   return RingShape{};
 }
 
-int ahead_of_depth(int d) { return d >= 4 ? d - 2 : 1; }
+int ahead_of_depth(int d) { return d >= 4 ? d - 1 : 1; }
 
 struct Ring {
   const CUtensorMap* tm_x;
@@ -106,8 +108,8 @@ struct Ring {
   uint64_t* empty;
   int32_t* siss;  // wrap count of the last step loaded into each step slot (-1: none)
   volatile uint32_t* abort_flag;
-  // per step slot and row: the input-ring slot of the row's first input row, + 65536 when the row
-  // starts a new input-row sequence (the run's first row or an image's first row)
+  // per step slot and row: the shared address of the ring slot of the row's last input row, + 1
+  // when the row starts a new input-row sequence (the run's first row or an image's first row)
   int32_t* rowinfo;
   unsigned* err;
   uint32_t rowX, rowD, txX, txD;
@@ -128,8 +130,10 @@ __device__ bool issue_step(const Ring& g, const GmParams& p, RowPos a, StepPos s
   }
   {  // the rows' input slots, published by the arrive below (release) to the warps that wait on it
     RowPos b = a;
+    const uint32_t xbase = smem_u32(g.xring);
     for (int32_t j = 0; j < rows; ++j, b.advance(R, p))
-      g.rowinfo[st.ss * p.TR + j] = b.xs + (b.fresh(R) == R ? 65536 : 0);
+      g.rowinfo[st.ss * p.TR + j] =
+          (int32_t)(xbase + (uint32_t)b.slot(R - 1, p) * g.rowX + (b.fresh(R) == R ? 1u : 0u));
   }
   uint64_t* bar = &g.full[st.ss];
   mbar_arrive_expect_tx(bar, bytes);
@@ -169,20 +173,6 @@ __device__ __forceinline__ void mma16816<__half>(float (&d)[4], const uint32_t (
   asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
                : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
-// A pair of 16-bit values widened to fp32.
-template <typename T>
-__device__ __forceinline__ float2 widen(uint32_t v);
-template <>
-__device__ __forceinline__ float2 widen<__nv_bfloat16>(uint32_t v) {
-  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
-}
-template <>
-__device__ __forceinline__ float2 widen<__half>(uint32_t v) {
-  __half2 h;
-  memcpy(&h, &v, sizeof(h));
-  return __half22float2(h);
 }
 
 // The c chunk of pair i of the warp that owns k chunk w (every pair of a warp
@@ -269,23 +259,25 @@ __global__ void __launch_bounds__(256 * NG, 1)
 #pragma unroll
   for (int i = 0; i < CPW; ++i) cch[i] = c_chunk_of(wl, i, p.Cg);
   const int mi = lane >> 3, arow = (mi >> 1) * 8 + (lane & 7), brow = lane & 15;
-  // aoff: the x4 load of a pair; aoff1: the x2 load of a single (last, odd-S) filter column, lanes
-  // 0..15 giving its input columns 0..15
-  uint32_t aoff[SP], aoff1[SP], boff[CPW];
+  // aoff: the x4 load of a pair (a single last column, S odd, fills both halves)
+  uint32_t aoff[SP], boff[CPW];
 #pragma unroll
   for (int sp = 0; sp < SP; ++sp) {
     const int s = 2 * sp + (mi & 1);
     const int pix = arow + p.S - 1 - (s < p.S ? s : p.S - 1);  // dY slot pixel = input column + S - 1 - s
     aoff[sp] = chunk_addr(0u, pix, kch);
-    aoff1[sp] = chunk_addr(0u, brow + p.S - 1 - (2 * sp < p.S ? 2 * sp : p.S - 1), kch);
   }
 #pragma unroll
   for (int i = 0; i < CPW; ++i) boff[i] = chunk_addr(0u, brow, cch[i]);
   // The bias of chunk wl comes from the A fragments of filter column pw (a
-  // real tap): its window is dY columns 0 .. 16 US - 1, each once, zero past
-  // Wo. Thread (g = lane / 4, t = lane % 4) holds output channel g at pixels
-  // 2t, 2t + 1 (register bh) and 2t + 8, 2t + 9 (register 2 + bh) of each step.
+  // real tap), whose window is dY columns 0 .. 16 US - 1, each once, zero past
+  // Wo: one more MMA a row with a B of ones sums them over the 16 columns
+  // (every column of the result is that sum). Thread (g = lane / 4) holds
+  // row g (filter column 2 bsp, output channel g) in register 0 and row g + 8
+  // (column 2 bsp + 1) in register 2.
   const int bsp = p.pw / 2, bh = p.pw % 2;
+  const uint32_t one2 = std::is_same<TI, __half>::value ? 0x3C003C00u : 0x3F803F80u;  // two 1.0s
+  const uint32_t ones[2] = {one2, one2};
   float acc[CPW][R][SP][4];
 #pragma unroll
   for (int i = 0; i < CPW; ++i)
@@ -295,7 +287,7 @@ __global__ void __launch_bounds__(256 * NG, 1)
       for (int sp = 0; sp < SP; ++sp)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[i][r][sp][e] = 0.f;
-  float2 bacc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  float bacc[4] = {0.f, 0.f, 0.f, 0.f};
   const uint32_t dring_u32 = smem_u32(g.dring), xring_u32 = smem_u32(g.xring);
 
   StepPos sc{0, 0u};
@@ -342,20 +334,17 @@ __global__ void __launch_bounds__(256 * NG, 1)
           if (j0 + jj >= j1) break;
           const int32_t j = j0 + jj;
           const int32_t inf = info[jj];
-          const int32_t xs = inf & 0xffff;
-          auto xslot = [&](int r) {
-            const int32_t sl = xs + r >= p.RX ? xs + r - p.RX : xs + r;
-            return xring_u32 + (uint32_t)sl * g.rowX + uo;
-          };
-          if (jj == 0 || (inf >> 16) != 0) {  // a fresh window
+          const uint32_t xlast = (uint32_t)inf & ~1u;  // the window's last input row
+          if (jj == 0 || (inf & 1) != 0) {  // a fresh window: rows R - 1 - r before the last, in the ring
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-              const uint32_t xa = xslot(r);
+              int32_t xa = (int32_t)xlast - (R - 1 - r) * (int32_t)g.rowX;
+              if (xa < (int32_t)xring_u32) xa += p.RX * (int32_t)g.rowX;
 #pragma unroll
-              for (int i = 0; i < CPW; ++i) ldsm_x2_t(xa + boff[i], bw[i][r]);
+              for (int i = 0; i < CPW; ++i) ldsm_x2_t((uint32_t)xa + uo + boff[i], bw[i][r]);
             }
           } else {  // slide by one input row
-            const uint32_t xa = xslot(R - 1);
+            const uint32_t xa = xlast + uo;
 #pragma unroll
             for (int i = 0; i < CPW; ++i) {
 #pragma unroll
@@ -369,31 +358,16 @@ __global__ void __launch_bounds__(256 * NG, 1)
           const uint32_t dslot = dring_u32 + (uint32_t)((sc.ss * p.TR + j) * g.rowD) + uo;
           uint32_t af[SP][4];
 #pragma unroll
-          for (int sp = 0; sp < SP; ++sp) {
-            if (2 * sp + 1 < p.S) {
-              ldsm_x4_t(dslot + aoff[sp], af[sp]);
-            } else {  // a single filter column: rows 8..15 repeat rows 0..7 (not stored)
-              uint32_t h2[2];
-              ldsm_x2_t(dslot + aoff1[sp], h2);
-              af[sp][0] = af[sp][1] = h2[0];
-              af[sp][2] = af[sp][3] = h2[1];
-            }
-          }
+          for (int sp = 0; sp < SP; ++sp) ldsm_x4_t(dslot + aoff[sp], af[sp]);
 #pragma unroll
           for (int i = 0; i < CPW; ++i)
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
               for (int sp = 0; sp < SP; ++sp) mma16816<TI>(acc[i][r][sp], af[sp], bw[i][r]);
-          uint32_t lo = 0u, hi = 0u;  // the bias column's registers, chosen by selects (no local memory)
 #pragma unroll
-          for (int sp = 0; sp < SP; ++sp)
-            if (sp == bsp) {
-              lo = bh ? af[sp][1] : af[sp][0];
-              hi = bh ? af[sp][3] : af[sp][2];
-            }
-          bacc[0] = __fadd2_rn(bacc[0], widen<TI>(lo));
-          bacc[1] = __fadd2_rn(bacc[1], widen<TI>(hi));
+          for (int sp = 0; sp < SP; ++sp)  // the pair holding filter column pw (a select, no local memory)
+            if (sp == bsp) mma16816<TI>(bacc, af[sp], ones);
         }
       }
     }
@@ -416,11 +390,8 @@ __global__ void __launch_bounds__(256 * NG, 1)
   __syncthreads();
   const bool ok = *g.abort_flag == 0u;
 
-  // the bias partial sums of output channel lane / 4 of chunk wl: the lane's four pixels a step, then
-  // the four lanes of the channel, in a fixed order
-  float bsum = (bacc[0].x + bacc[0].y) + (bacc[1].x + bacc[1].y);
-  bsum += __shfl_xor_sync(0xffffffffu, bsum, 1);
-  bsum += __shfl_xor_sync(0xffffffffu, bsum, 2);
+  // the bias partial sum of output channel lane / 4 of chunk wl (every lane of the channel holds it)
+  float bsum = bh ? bacc[2] : bacc[0];
   if (NG > 1) {
     // groups 1.. hand their sums to group 0 through shared memory (over the
     // ring), which adds them in group order
