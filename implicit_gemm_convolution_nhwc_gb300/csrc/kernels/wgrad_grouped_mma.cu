@@ -102,6 +102,8 @@ int ahead_of_depth(int d) { return d >= 4 ? d - 1 : 1; }
 struct Ring {
   const CUtensorMap* tm_x;
   const CUtensorMap* tm_dy;
+  const CUtensorMap* tm_xt;   // boxes of TR input rows (TR consecutive ring slots)
+  const CUtensorMap* tm_dyt;  // boxes of TR dY rows (a whole step slot)
   uint8_t* xring;
   uint8_t* dring;
   uint64_t* full;
@@ -112,35 +114,48 @@ struct Ring {
   // when the row starts a new input-row sequence (the run's first row or an image's first row)
   int32_t* rowinfo;
   unsigned* err;
-  uint32_t rowX, rowD, txX, txD;
+  uint32_t rowX, rowD, txX, txD, txXT, txDT;
   int32_t c0;
 };
 
 // Loads a step: the dY rows of its `rows` output rows (the first at row
 // position a) and the input rows they are the first to read, all landing on
 // the step slot's full mbarrier, once every warp is done with the slot's
-// previous step. False: the wait gave up.
+// previous step. False: the wait gave up. A full step within one image loads
+// its dY rows as one box of TR rows, and, when each row adds one input row
+// and their ring slots do not wrap, its input rows as one more: two copies a
+// step instead of 2 TR (issuing each copy costs the issuing warp a few
+// hundred cycles).
 template <int R>
 __device__ bool issue_step(const Ring& g, const GmParams& p, RowPos a, StepPos st, int32_t rows) {
   if (st.sw > 0 && !mbar_wait(&g.empty[st.ss], (st.sw - 1u) & 1u, g.abort_flag, g.err)) return false;
-  uint32_t bytes = 0;
-  {
-    RowPos b = a;
-    for (int32_t j = 0; j < rows; ++j, b.advance(R, p)) bytes += g.txD + (uint32_t)b.fresh(R) * g.txX;
-  }
+  const bool dblk = rows == p.TR && a.ho + p.TR <= p.Ho;
+  const int32_t s0 = a.slot(R - 1, p);
+  const bool xblk = dblk && !a.first && a.ho != 0 && s0 + p.TR <= p.RX;
+  uint32_t bytes = (dblk ? g.txDT : 0u) + (xblk ? g.txXT : 0u);
   {  // the rows' input slots, published by the arrive below (release) to the warps that wait on it
     RowPos b = a;
     const uint32_t xbase = smem_u32(g.xring);
-    for (int32_t j = 0; j < rows; ++j, b.advance(R, p))
+    for (int32_t j = 0; j < rows; ++j, b.advance(R, p)) {
+      if (!dblk) bytes += g.txD;
+      if (!xblk) bytes += (uint32_t)b.fresh(R) * g.txX;
       g.rowinfo[st.ss * p.TR + j] =
           (int32_t)(xbase + (uint32_t)b.slot(R - 1, p) * g.rowX + (b.fresh(R) == R ? 1u : 0u));
+    }
   }
   uint64_t* bar = &g.full[st.ss];
   mbar_arrive_expect_tx(bar, bytes);
-  for (int32_t j = 0; j < rows; ++j, a.advance(R, p)) {
-    tma_load_4d(g.dring + ((size_t)st.ss * p.TR + j) * g.rowD, g.tm_dy, g.c0, p.pw - p.S + 1, a.ho, a.n, bar);
-    for (int r = R - a.fresh(R); r < R; ++r)
-      tma_load_4d(g.xring + (size_t)a.slot(r, p) * g.rowX, g.tm_x, g.c0, 0, a.ho - p.ph + r, a.n, bar);
+  if (dblk)
+    tma_load_4d(g.dring + (size_t)st.ss * p.TR * g.rowD, g.tm_dyt, g.c0, p.pw - p.S + 1, a.ho, a.n, bar);
+  if (xblk) tma_load_4d(g.xring + (size_t)s0 * g.rowX, g.tm_xt, g.c0, 0, a.ho - p.ph + R - 1, a.n, bar);
+  if (!dblk || !xblk) {
+    for (int32_t j = 0; j < rows; ++j, a.advance(R, p)) {
+      if (!dblk)
+        tma_load_4d(g.dring + ((size_t)st.ss * p.TR + j) * g.rowD, g.tm_dy, g.c0, p.pw - p.S + 1, a.ho, a.n, bar);
+      if (!xblk)
+        for (int r = R - a.fresh(R); r < R; ++r)
+          tma_load_4d(g.xring + (size_t)a.slot(r, p) * g.rowX, g.tm_x, g.c0, 0, a.ho - p.ph + r, a.n, bar);
+    }
   }
   g.siss[st.ss] = (int32_t)st.sw;
   return true;
@@ -199,6 +214,7 @@ struct Frags {
 template <typename TI, typename TO, int R, int SP, int CPW, int NG>
 __global__ void __launch_bounds__(256 * NG, 1)
     wgrad_grouped_mma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
+                             const __grid_constant__ CUtensorMap tm_xt, const __grid_constant__ CUtensorMap tm_dyt,
                              TO* out, float* ws, TO* db, float* ws_bias, GmParams p, unsigned* err) {
   constexpr int kT = 256 * NG;          // threads
   constexpr int kW = kT / 32;           // warps
@@ -207,10 +223,14 @@ __global__ void __launch_bounds__(256 * NG, 1)
   Ring g;
   g.tm_x = &tm_x;
   g.tm_dy = &tm_dy;
+  g.tm_xt = &tm_xt;
+  g.tm_dyt = &tm_dyt;
   g.rowX = (uint32_t)p.XP * 128u;
   g.rowD = (uint32_t)p.DP * 128u;
   g.txX = (uint32_t)(p.US * 16) * 128u;
   g.txD = (uint32_t)(p.US * 16 + p.S - 1) * 128u;
+  g.txXT = (uint32_t)p.TR * g.txX;  // the TR-row boxes: input rows US * 16 pixels, dY rows the slot's DP
+  g.txDT = (uint32_t)p.TR * g.rowD;
   g.xring = smem;
   g.dring = smem + (size_t)p.RX * g.rowX;
   g.full = reinterpret_cast<uint64_t*>(g.dring + (size_t)p.RS * p.TR * g.rowD);
@@ -237,6 +257,8 @@ __global__ void __launch_bounds__(256 * NG, 1)
     mbar_fence_init();
     tma_prefetch(&tm_x);
     tma_prefetch(&tm_dy);
+    tma_prefetch(&tm_xt);
+    tma_prefetch(&tm_dyt);
     // The first `ahead` steps load into fresh slots.
     RowPos a{0, (int32_t)(q_b % p.Ho), (int32_t)(q_b / p.Ho), true};
     StepPos st{0, 0u};
@@ -475,22 +497,27 @@ int warp_groups(const Shape& s) { return groups_of((int)(s.r * sp_of(s.r) * pair
 template <typename TI, typename TO, int R, int SP, int CPW, int NG>
 cudaError_t launch_k(const Plan& pl, const Args& a, const GmParams& p, CUtensorMapDataType dt, size_t smem) {
   const Shape& s = pl.sh;
-  CUtensorMap tm_x, tm_dy;
+  CUtensorMap tm_x, tm_dy, tm_xt, tm_dyt;
   const uint64_t x_dims[4] = {(uint64_t)s.c, (uint64_t)s.w, (uint64_t)s.h, (uint64_t)s.n};
   const uint64_t x_strides[3] = {(uint64_t)s.c * 2u, (uint64_t)(s.w * s.c) * 2u, (uint64_t)(s.h * s.w * s.c) * 2u};
   const uint32_t x_box[4] = {(uint32_t)kCB, (uint32_t)(p.US * 16), 1u, 1u};
   const uint64_t y_dims[4] = {(uint64_t)s.k, (uint64_t)s.wo, (uint64_t)s.ho, (uint64_t)s.n};
   const uint64_t y_strides[3] = {(uint64_t)s.k * 2u, (uint64_t)(s.wo * s.k) * 2u, (uint64_t)(s.ho * s.wo * s.k) * 2u};
   const uint32_t y_box[4] = {(uint32_t)kCB, (uint32_t)(p.US * 16 + s.s - 1), 1u, 1u};
+  // the same tensors in boxes of TR rows: TR ring slots of input rows, a whole dY step slot (DP pixels a row)
+  const uint32_t xt_box[4] = {(uint32_t)kCB, (uint32_t)(p.US * 16), (uint32_t)p.TR, 1u};
+  const uint32_t yt_box[4] = {(uint32_t)kCB, (uint32_t)p.DP, (uint32_t)p.TR, 1u};
   if (!encode_tmap(&tm_x, dt, 4, a.x, x_dims, x_strides, x_box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tmap(&tm_dy, dt, 4, a.b, y_dims, y_strides, y_box, CU_TENSOR_MAP_SWIZZLE_128B))
+      !encode_tmap(&tm_dy, dt, 4, a.b, y_dims, y_strides, y_box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap(&tm_xt, dt, 4, a.x, x_dims, x_strides, xt_box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap(&tm_dyt, dt, 4, a.b, y_dims, y_strides, yt_box, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   auto kern = wgrad_grouped_mma_kernel<TI, TO, R, SP, CPW, NG>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const int64_t ctas = pl.geo.tiles * pl.split;
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<(unsigned)ctas, 256 * NG, smem, a.stream>>>(tm_x, tm_dy, static_cast<TO*>(a.out), a.ws,
+  kern<<<(unsigned)ctas, 256 * NG, smem, a.stream>>>(tm_x, tm_dy, tm_xt, tm_dyt, static_cast<TO*>(a.out), a.ws,
                                                      pl.with_bias ? static_cast<TO*>(a.db) : nullptr,
                                                      pl.with_bias ? a.ws_bias : nullptr, p, device_error_word());
   return cudaGetLastError();
