@@ -133,12 +133,15 @@ __device__ bool issue_step(const Ring& g, const GmParams& p, RowPos a, StepPos s
   const int32_t s0 = a.slot(R - 1, p);
   const bool xblk = dblk && !a.first && a.ho != 0 && s0 + p.TR <= p.RX;
   uint32_t bytes = (dblk ? g.txDT : 0u) + (xblk ? g.txXT : 0u);
-  {  // the rows' input slots, published by the arrive below (release) to the warps that wait on it
+  // the rows' input slots, published by the arrive below (release) to the warps that wait on it
+  const uint32_t xbase = smem_u32(g.xring);
+  if (xblk) {  // consecutive slots, none starting a window
+    for (int32_t j = 0; j < rows; ++j) g.rowinfo[st.ss * p.TR + j] = (int32_t)(xbase + (uint32_t)(s0 + j) * g.rowX);
+  } else {
     RowPos b = a;
-    const uint32_t xbase = smem_u32(g.xring);
     for (int32_t j = 0; j < rows; ++j, b.advance(R, p)) {
       if (!dblk) bytes += g.txD;
-      if (!xblk) bytes += (uint32_t)b.fresh(R) * g.txX;
+      bytes += (uint32_t)b.fresh(R) * g.txX;
       g.rowinfo[st.ss * p.TR + j] =
           (int32_t)(xbase + (uint32_t)b.slot(R - 1, p) * g.rowX + (b.fresh(R) == R ? 1u : 0u));
     }
@@ -321,11 +324,12 @@ __global__ void __launch_bounds__(256 * NG, 1)
   // its image and row, and its first input row's index in the slice's input-row
   // sequence (R rows for the slice's first row and for each image start, one
   // more for every other row), which modulo RX is its ring slot.
-  const int32_t n_b = (int32_t)(q_b / p.Ho);
+  // (32-bit arithmetic: N * Ho < 2^31 is a condition of the kernel.)
+  const uint32_t ho_u = (uint32_t)p.Ho, n_b = (uint32_t)q_b / ho_u;
   auto row_pos = [&](int64_t qq) {
-    const int32_t n = (int32_t)(qq / p.Ho), ho = (int32_t)(qq - (int64_t)n * p.Ho);
-    const int64_t seq = (qq - q_b) + (int64_t)(R - 1) * (n - n_b);
-    return RowPos{(int32_t)(seq % p.RX), ho, n, qq == q_b};
+    const uint32_t n = (uint32_t)qq / ho_u, ho = (uint32_t)qq - n * ho_u;
+    const uint32_t seq = (uint32_t)(qq - q_b) + (uint32_t)(R - 1) * (n - n_b);
+    return RowPos{(int32_t)(seq % (uint32_t)p.RX), (int32_t)ho, (int32_t)n, qq == q_b};
   };
 
   for (int64_t q = q_b; q < q_e; q += p.TR) {
@@ -396,7 +400,6 @@ __global__ void __launch_bounds__(256 * NG, 1)
 
     __syncwarp();
     if (lane == 0) mbar_arrive(&g.empty[sc.ss]);
-    __syncwarp();
     sc.advance(p);
   }
   signal_dependents();
@@ -591,6 +594,7 @@ Geometry geometry_wgrad_grouped_mma(const Shape& s) {
   // TMA: rows of at most 256 columns (the dY box adds S - 1), 32-bit coordinates
   if ((s.w + 15) / 16 * 16 + s.s - 1 > 256 || s.wo > s.w + 2 * s.pw) return g;
   if (s.n > 0x7fffffffLL || s.h + s.r > 0x7fffffffLL) return g;
+  if (s.n * s.ho > 0x7fffffffLL) return g;  // the issuing lane places rows in 32-bit arithmetic
   const RingShape rs = ring_shape(s);
   if (rs.d < 1) return g;
   // two warp groups add their sums through shared memory over the ring's rows
