@@ -95,7 +95,9 @@ typedef struct conv_problem {
  * request alone (never from timing), so a degree and a workspace size
  * resolved ahead of a call hold for that call. Automatic choice never takes
  * CONV_KERNEL_FWD_TC_CLUSTER (on the 3x3 small-M layer it measured slower than
- * the two-stage form); the override selects it. */
+ * the two-stage form) nor CONV_KERNEL_WGRAD_DEPTHWISE_MMA (on the 7x7 layer it
+ * measured slower than CONV_KERNEL_WGRAD_DEPTHWISE); the override selects
+ * them. */
 typedef enum conv_kernel {
   CONV_KERNEL_AUTO = 0,
   CONV_KERNEL_GENERIC = 1,           /* direct, CUDA cores: any shape and type */
@@ -135,10 +137,16 @@ typedef enum conv_kernel {
                                         filters): warp-level m16n8k16 MMAs over input columns with
                                         the filter column applied as a shift of dY, so every product
                                         is a gradient element (8 or more channels per group) */
-  CONV_KERNEL_FFMA = 16              /* fp32, one group, C and K multiples of 4: implicit-GEMM FFMA
+  CONV_KERNEL_FFMA = 16,             /* fp32, one group, C and K multiples of 4: implicit-GEMM FFMA
                                         tiles (128 x 128, 8 x 8 a thread) for the forward, the
                                         stride-1 data gradient (the turned problem, filter read in
                                         place) and the weight gradient (+ bias gradient) */
+  CONV_KERNEL_WGRAD_DEPTHWISE_MMA = 17 /* 16-bit depthwise weight gradient (filters up to 7 x 7, unit
+                                        stride and dilation, rows of at most 64 input and output
+                                        columns, C % 8 = 0): per channel and output row, warp-level
+                                        m16n8k16 MMAs of the filter rows' input rows against dY
+                                        shifted by each filter column (a Toeplitz operand), rows
+                                        transposed in shared memory; the bias from a row of ones */
 } conv_kernel;
 
 /* What a call with these arguments would run. */

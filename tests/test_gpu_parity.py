@@ -449,7 +449,40 @@ def test_config4_depthwise_full():
     p = cig.Problem(n=32, h=56, w=56, c=384, k=384, r=7, s=7, pad_h=3, pad_w=3, groups=384,
                     in_dtype=BF16, out_dtype=BF16)
     assert cig.describe_plan(p, cig.DIR_WGRAD, -1)["kernel_name"] == "wgrad_depthwise"
-    check_wgrad(p, 3, ["auto"], [-1, 1, 7], bias=False)
+    check_wgrad(p, 3, ["auto", "wgrad_depthwise_mma"], [-1, 1, 7], bias=False)
+    check_wgrad(p, 3, ["auto"], [-1], bias=True)
+    x, dy = inputs(p, 3)
+    a, b = run_wgrad(p, x, dy, -1, True), run_wgrad(p, x, dy, -1, True)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    assert cig.device_errors() == 0
+
+
+@pytest.mark.parametrize("shape", [
+    dict(n=2, h=14, w=14, c=64, r=7, s=7, pad_h=3, pad_w=3),
+    dict(n=3, h=13, w=17, c=128, r=5, s=5, pad_h=2, pad_w=2),     # two 16-column chunks
+    dict(n=2, h=9, w=33, c=72, r=3, s=3),                          # three chunks, no padding, 8-channel tail
+    dict(n=2, h=11, w=58, c=96, r=7, s=7, pad_h=6, pad_w=6),      # Wo = 64 > W: bias columns past the input
+    dict(n=1, h=7, w=64, c=64, r=7, s=7, pad_h=3, pad_w=3),       # the widest rows
+    dict(n=3, h=5, w=9, c=8, r=3, s=5, pad_h=1, pad_w=2),         # one warp's channels, non-square filter
+    dict(n=4, h=3, w=16, c=64, r=1, s=1),                          # pointwise, one chunk
+    dict(n=2, h=6, w=20, c=40, r=7, s=3, pad_h=5, pad_w=1),       # fewer input rows than filter rows
+    dict(n=5, h=2, w=5, c=16, r=2, s=4, pad_h=1, pad_w=3),        # even filter sizes, rows spanning images
+])
+@pytest.mark.parametrize("dt", [(BF16, BF16), (BF16, F32), (F16, F16)], ids=lambda d: f"{d[0]}{d[1]}")
+def test_depthwise_mma(shape, dt):
+    """The depthwise MMA weight gradient (Toeplitz dY operand, rows transposed in shared memory) against
+    the oracle at several degrees, with the bias gradient; reruns bit-identical."""
+    shp = dict(shape, k=shape["c"], groups=shape["c"])
+    p = cig.Problem(**shp, in_dtype=dt[0], out_dtype=dt[1])
+    check_wgrad(p, 9, ["wgrad_depthwise_mma"], [-1, 1, 4, "max"], bias=True)
+    x, dy = inputs(p, 9)
+    cig.set_kernel_override("wgrad_depthwise_mma")
+    try:
+        assert cig.describe_plan(p, cig.DIR_WGRAD, -1)["kernel_name"] == "wgrad_depthwise_mma"
+        a, b = run_wgrad(p, x, dy, 3, True), run_wgrad(p, x, dy, 3, True)
+    finally:
+        cig.set_kernel_override("auto")
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
     assert cig.device_errors() == 0
 
 

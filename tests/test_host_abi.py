@@ -324,6 +324,31 @@ def test_depthwise_ring_selection():
 SUPPLEMENT = Problem(n=64, h=56, w=56, c=256, k=256, r=3, s=3, pad_h=1, pad_w=1, in_dtype=BF16, out_dtype=BF16)
 
 
+def test_depthwise_mma_wgrad_admission():
+    """Which depthwise weight gradients the MMA kernel (reached through the override only: it measured
+    slower than the ring kernel) takes: 16-bit, filters up to 7 x 7 (any R, S), unit stride and
+    dilation, pad <= F - 1, rows of at most 64 input and output columns, C % 8 == 0; 64 channels a CTA,
+    split-K over the (n, ho) rows. Automatic choice keeps the ring kernel."""
+    wg = lambda p: cig.describe_plan(p, DIR_WGRAD, -1, sm_count=SMS)  # noqa: E731
+    assert wg(CONFIG4)["kernel_name"] == "wgrad_depthwise"
+    cig.set_kernel_override("wgrad_depthwise_mma")
+    try:
+        info = wg(CONFIG4)
+        assert info["kernel_name"] == "wgrad_depthwise_mma" and info["tiles"] == 6 and info["ctas_per_sm"] == 1
+        assert info["reduction_blocks"] == 32 * 56 and info["ctas"] == 6 * info["split_k"] <= SMS
+        for p in (dw(r=3, s=5, pad_h=1, pad_w=2), dw(r=1, s=1, pad_h=0, pad_w=0), dw(w=64), dw(w=58, pad_w=6),
+                  dw(c=8), dw(in_dtype=F16, out_dtype=F32)):
+            assert wg(p)["kernel_name"] == "wgrad_depthwise_mma", p
+        # rows past 64 columns (input or output), a 9-wide filter, padding F, stride or dilation 2, fp32
+        # inputs, C % 8 != 0: not this kernel
+        for p in (dw(w=65), dw(w=59, pad_w=6), dw(r=9, s=9, pad_h=4, pad_w=4), dw(r=3, s=3, pad_h=1, pad_w=3),
+                  dw(stride_w=2), dw(dil_h=2), dw(in_dtype=F32, out_dtype=F32), dw(c=12)):
+            with pytest.raises(RuntimeError):
+                wg(p)
+    finally:
+        cig.set_kernel_override("auto")
+
+
 def test_dense_wgrad_tensor_core_selection():
     """Which weight gradients the dense tensor-core kernel takes (16-bit, one group or Cg % 64 == 0 with
     Kg % 128 == 0, C and K >= 64 and multiples of 8), and its tiling: 256 output channels x up to 256
