@@ -65,7 +65,10 @@ struct Tile {
   static_assert(MS == 1 || MS == 2, "M sub-tiles");
   static_assert(kTmemCols <= 512, "TMEM columns");
   static_assert(kBM * kLD * 4 <= kStages * kStage, "staged partial tile must fit in the ring");
-  static_assert(2 * kBM * 128 + BN * 4 <= kStages * kStage, "epilogue staging and bias must fit in the ring");
+  // epilogue staging buffers (16 KB each, up to 8) and the bias, over the idle ring
+  static constexpr int kEpiBufs =
+      (kStages * kStage - BN * 4) / (kBM * 128) < 8 ? (kStages * kStage - BN * 4) / (kBM * 128) : 8;
+  static_assert(kEpiBufs >= 2, "epilogue staging and bias must fit in the ring");
 };
 
 struct FwdParams {
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
       uint8_t* stage = smem;  // the ring is idle: every copy landed, every MMA completed
       // The epilogue's bias for the tile's BN channels, as fp32 in shared memory
       // past the two staging buffers (0 beyond K or without a bias).
-      float* sbias = reinterpret_cast<float*>(smem + 2 * kBM * 128);
+      float* sbias = reinterpret_cast<float*>(smem + T::kEpiBufs * kBM * 128);
       if (!ws && fp.ep) {
         const TO* bias = static_cast<const TO*>(fp.ep_bias);
         for (int i = threadIdx.x - 128; i < BN; i += 128)
@@ -291,11 +294,12 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
         const int32_t pz = ws ? (int32_t)(sigma * fp.N + img) : (int32_t)img;
         auto store = [&](const void* buf, int32_t x) { tma_store_3d(&tm_y, buf, x, py, pz); };
         if (ws)
-          store_rows_tma<float>(trow + (uint32_t)(h * BN), stage, BN, (int32_t)k0, (int32_t)fp.K, m, nblk > 0,
-                                threadIdx.x == 128, ok, store);
+          store_rows_tma<float, T::kEpiBufs>(trow + (uint32_t)(h * BN), stage, BN, (int32_t)k0, (int32_t)fp.K, m,
+                                             nblk > 0, threadIdx.x == 128, ok, store);
         else
-          store_rows_tma<TO>(trow + (uint32_t)(h * BN), stage, BN, (int32_t)k0, (int32_t)fp.K, m, nblk > 0,
-                             threadIdx.x == 128, ok, store, sbias, fp.ep_lo, fp.ep_hi, fp.ep != 0);
+          store_rows_tma<TO, T::kEpiBufs>(trow + (uint32_t)(h * BN), stage, BN, (int32_t)k0, (int32_t)fp.K, m,
+                                          nblk > 0, threadIdx.x == 128, ok, store, sbias, fp.ep_lo, fp.ep_hi,
+                                          fp.ep != 0);
       }
     }
   }

@@ -39,16 +39,19 @@ __device__ __forceinline__ uint4 pack16<__half>(const float* v) {
 // [0, ncols) of their rows: thread m owns tensor-memory lane m (trow already
 // carries the warp's lane offset). For each 128-byte column chunk (32 fp32 or
 // 64 16-bit values) the thread writes its 128 bytes into a 128B-swizzled
-// staging buffer (8 conflict-free 16-byte stores; two 16 KB buffers at
-// `stage`, alternating), and the leader thread stores the chunk as one TMA
+// staging buffer (8 conflict-free 16-byte stores; NBUF 16 KB buffers at
+// `stage`, in turn), and the leader thread stores the chunk as one TMA
 // box through store(buf, x), where x = x0 + chunk * (values per chunk) is the
 // innermost coordinate; the tensor map clips the box at the tensor's bounds.
 // Only chunks that start below x_end are stored (each then commits exactly
 // one bulk group, which the buffer-reuse wait counts on). With ep, the bias
 // (fp32 in shared memory, one per column) is added and the value clamped to
 // [ep_lo, ep_hi] before the rounding. Few instructions per thread: with one
-// CTA per SM these four warps issue every one of them.
-template <typename TE, typename StoreFn>
+// CTA per SM these four warps issue every one of them. With two buffers a
+// chunk waited for the store of the chunk before last to finish reading its
+// buffer (the 128 KB fp32 partial tile of a split-K CTA took ~2.5 us); more
+// buffers keep more stores in flight.
+template <typename TE, int NBUF = 2, typename StoreFn>
 __device__ __forceinline__ void store_rows_tma(uint32_t trow, uint8_t* stage, int ncols, int32_t x0, int32_t x_end,
                                                int m, bool have_acc, bool leader, bool do_store, StoreFn store,
                                                const float* ep_bias = nullptr, float ep_lo = 0.f, float ep_hi = 0.f,
@@ -58,9 +61,9 @@ __device__ __forceinline__ void store_rows_tma(uint32_t trow, uint8_t* stage, in
   const int nch = min(ncols / CW, (x_end - x0 + CW - 1) / CW);
 #pragma unroll 1
   for (int c = 0; c < nch; ++c) {
-    uint8_t* buf = stage + (c & 1) * (128 * 128);
-    if (c >= 2) {  // the store that last read this buffer (chunk c - 2) must be done reading
-      if (leader) bulk_wait_read<1>();
+    uint8_t* buf = stage + (c % NBUF) * (128 * 128);
+    if (c >= NBUF) {  // the store that last read this buffer (chunk c - NBUF) must be done reading
+      if (leader) bulk_wait_read<NBUF - 1>();
       named_bar_sync(1, 128);
     }
     float v[CW];
