@@ -40,6 +40,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxStages = 8;
 constexpr int kStageBudget = 64 * 1024;  // bytes of one ring stage at most
+constexpr int kEpiBufs = 4;               // epilogue staging buffers of 16 KB (the ring is at least 118 KB)
 constexpr size_t kSmemMax = 232448;      // dynamic shared memory a CTA may use (227 KB)
 
 // A pair of 16-bit values (one 32-bit word, the lower one first) widened to fp32.
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     signal_dependents();
     tc_fence_after();
     const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
-    uint8_t* stage = smem;  // the ring is idle: every copy landed, every MMA completed
+    uint8_t* stage = smem;  // the ring is idle: every copy landed, every MMA completed (kEpiBufs x 16 KB)
     const int32_t kend = (int32_t)(grp * wp.Kg + wp.Kg);  // this group's channels end here
 #pragma unroll 1
     for (int h = 0; h < wp.MS; ++h) {
@@ -258,16 +259,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the box {chunk, 1 tap, 128 output channels, 1} at (c, tap, k, slab), clipped at Cg and K
       auto store = [&](const void* buf, int32_t x) { tma_store_4d(&tm_out, buf, x, tap, kr, split ? sigma : 0); };
       if (split)
-        store_rows_tma<float>(trow + (uint32_t)(h * wp.BN), stage, wp.BN, c0, wp.Cg, m, nblk > 0,
-                              threadIdx.x == 128, ok, store);
+        store_rows_tma<float, kEpiBufs>(trow + (uint32_t)(h * wp.BN), stage, wp.BN, c0, wp.Cg, m, nblk > 0,
+                                        threadIdx.x == 128, ok, store);
       else
-        store_rows_tma<TO>(trow + (uint32_t)(h * wp.BN), stage, wp.BN, c0, wp.Cg, m, nblk > 0, threadIdx.x == 128,
-                           ok, store);
+        store_rows_tma<TO, kEpiBufs>(trow + (uint32_t)(h * wp.BN), stage, wp.BN, c0, wp.Cg, m, nblk > 0,
+                                     threadIdx.x == 128, ok, store);
     }
     if (do_bias) {
       // The partial sums [phase][chunk][8] after the staging buffers (the ring is idle), then
       // channel j of this CTA's 8 cc channels adds its nph phases in order (deterministic).
-      float* red = reinterpret_cast<float*>(smem + 2 * 128 * 128);
+      float* red = reinterpret_cast<float*>(smem + kEpiBufs * 128 * 128);
       if (ph0 < nph) {
         float* mine = red + (ph0 * cc + t % cc) * 8;
 #pragma unroll
