@@ -19,7 +19,8 @@ KERNELS = {"auto": 0, "generic": 1, "wgrad_1x1_ffma": 2, "wgrad_1x1_tf32x3": 3, 
            "wgrad_depthwise": 5, "wgrad_grouped": 6, "fwd_tc_cluster": 7, "dgrad_tc": 8,
            "fwd_depthwise": 9, "fwd_grouped_tc": 10, "wgrad_grouped_tc": 11, "wgrad_tc": 12,
            "dgrad_depthwise": 13, "dgrad_grouped_tc": 14, "wgrad_grouped_mma": 15,
-           "ffma": 16, "wgrad_depthwise_mma": 17}
+           "ffma": 16, "wgrad_depthwise_mma": 17,
+           "fwd_grouped_mma": 18, "dgrad_grouped_mma": 19}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 STATUS = ["CONV_OK", "CONV_ERR_INVALID_ARG", "CONV_ERR_UNSUPPORTED", "CONV_ERR_WORKSPACE_TOO_SMALL",
           "CONV_ERR_OVERFLOW", "CONV_ERR_ALIGNMENT", "CONV_ERR_CUDA"]

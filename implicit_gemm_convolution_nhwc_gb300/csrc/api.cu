@@ -86,6 +86,8 @@ Geometry geometry_of(conv_kernel k, const Shape& s, conv_dir dir) {
     case CONV_KERNEL_WGRAD_GROUPED_MMA: return dir == CONV_DIR_WGRAD ? geometry_wgrad_grouped_mma(s) : Geometry{};
     case CONV_KERNEL_FFMA: return geometry_ffma(s, dir);
     case CONV_KERNEL_WGRAD_DEPTHWISE_MMA: return dir == CONV_DIR_WGRAD ? geometry_wgrad_depthwise_mma(s) : Geometry{};
+    case CONV_KERNEL_FWD_GROUPED_MMA: return dir == CONV_DIR_FWD ? geometry_fwd_grouped_mma(s) : Geometry{};
+    case CONV_KERNEL_DGRAD_GROUPED_MMA: return dir == CONV_DIR_DGRAD ? geometry_dgrad_grouped_mma(s) : Geometry{};
     case CONV_KERNEL_DGRAD_DEPTHWISE: return dir == CONV_DIR_DGRAD ? geometry_dgrad_depthwise(s) : Geometry{};
     case CONV_KERNEL_DGRAD_GROUPED_TC: return dir == CONV_DIR_DGRAD ? geometry_dgrad_grouped_tc(s) : Geometry{};
     case CONV_KERNEL_WGRAD_DEPTHWISE: return dir == CONV_DIR_WGRAD ? geometry_wgrad_depthwise(s) : Geometry{};
@@ -146,12 +148,14 @@ conv_status choose_kernel(const Shape& s, conv_dir dir, conv_kernel* kernel, Geo
   // the depthwise weight gradient's MMA form: bound by shared-memory traffic
   // (0.65 bytes a useful multiply-add), it measured slower than the CUDA-core
   // ring kernel on the 7x7 layer.
-  static const conv_kernel fwd_order[] = {CONV_KERNEL_FWD_TC, CONV_KERNEL_FWD_DEPTHWISE, CONV_KERNEL_FWD_GROUPED_TC,
-                                          CONV_KERNEL_FFMA, CONV_KERNEL_GENERIC};
-  static const conv_kernel dgrad_order[] = {CONV_KERNEL_DGRAD_TC, CONV_KERNEL_DGRAD_DEPTHWISE,
-                                            CONV_KERNEL_DGRAD_GROUPED_TC, CONV_KERNEL_FFMA, CONV_KERNEL_GENERIC};
+  static const conv_kernel fwd_order[] = {CONV_KERNEL_FWD_TC,         CONV_KERNEL_FWD_DEPTHWISE,
+                                          CONV_KERNEL_FWD_GROUPED_MMA, CONV_KERNEL_FWD_GROUPED_TC,
+                                          CONV_KERNEL_FFMA,            CONV_KERNEL_GENERIC};
+  static const conv_kernel dgrad_order[] = {CONV_KERNEL_DGRAD_TC,         CONV_KERNEL_DGRAD_DEPTHWISE,
+                                            CONV_KERNEL_DGRAD_GROUPED_MMA, CONV_KERNEL_DGRAD_GROUPED_TC,
+                                            CONV_KERNEL_FFMA,              CONV_KERNEL_GENERIC};
   const conv_kernel* order = dir == CONV_DIR_WGRAD ? wgrad_order : dir == CONV_DIR_FWD ? fwd_order : dgrad_order;
-  const int count = dir == CONV_DIR_WGRAD ? 9 : 5;
+  const int count = dir == CONV_DIR_WGRAD ? 9 : 6;
   for (int i = 0; i < count; ++i) {
     Geometry g = geometry_of(order[i], s, dir);
     if (g.ok) {
@@ -353,6 +357,8 @@ conv_status run(const conv_problem* prob, conv_dir dir, const void* x, const voi
       case CONV_KERNEL_WGRAD_GROUPED_MMA: err = launch_wgrad_grouped_mma(plan, a); break;
       case CONV_KERNEL_FFMA: err = launch_ffma(plan, a); break;
       case CONV_KERNEL_WGRAD_DEPTHWISE_MMA: err = launch_wgrad_depthwise_mma(plan, a); break;
+      case CONV_KERNEL_FWD_GROUPED_MMA: err = launch_fwd_grouped_mma(plan, a); break;
+      case CONV_KERNEL_DGRAD_GROUPED_MMA: err = launch_dgrad_grouped_mma(plan, a); break;
       case CONV_KERNEL_DGRAD_DEPTHWISE: err = launch_dgrad_depthwise(plan, a); break;
       case CONV_KERNEL_DGRAD_GROUPED_TC: err = launch_dgrad_grouped_tc(plan, a); break;
       case CONV_KERNEL_WGRAD_DEPTHWISE: err = launch_wgrad_depthwise(plan, a); break;
@@ -561,7 +567,7 @@ conv_status conv_wgrad_bias_static_ws(const conv_problem* p, const void* x, cons
 
 
 conv_status conv_set_kernel_override(int32_t kernel) {
-  if (kernel < CONV_KERNEL_AUTO || kernel > CONV_KERNEL_WGRAD_DEPTHWISE_MMA) return CONV_ERR_INVALID_ARG;
+  if (kernel < CONV_KERNEL_AUTO || kernel > CONV_KERNEL_DGRAD_GROUPED_MMA) return CONV_ERR_INVALID_ARG;
   g_kernel_override = kernel;
   return CONV_OK;
 }

@@ -22,6 +22,8 @@ Geometry geometry_wgrad_grouped_tc(const Shape& s);
 Geometry geometry_wgrad_tc(const Shape& s);
 Geometry geometry_wgrad_grouped_mma(const Shape& s);
 Geometry geometry_wgrad_depthwise_mma(const Shape& s);
+Geometry geometry_fwd_grouped_mma(const Shape& s);
+Geometry geometry_dgrad_grouped_mma(const Shape& s);
 Geometry geometry_ffma(const Shape& s, conv_dir dir);
 // The forward tensor-core kernel on a channel-block problem: output tile of
 // channels [k0, k0 + 128) reads input channels [k0, k0 + 128) of X (full C
@@ -52,6 +54,8 @@ cudaError_t launch_wgrad_grouped_tc(const Plan& p, const Args& a);
 cudaError_t launch_wgrad_tc(const Plan& p, const Args& a);
 cudaError_t launch_wgrad_grouped_mma(const Plan& p, const Args& a);
 cudaError_t launch_wgrad_depthwise_mma(const Plan& p, const Args& a);
+cudaError_t launch_fwd_grouped_mma(const Plan& p, const Args& a);
+cudaError_t launch_dgrad_grouped_mma(const Plan& p, const Args& a);
 cudaError_t launch_ffma(const Plan& p, const Args& a);
 cudaError_t launch_dgrad_depthwise(const Plan& p, const Args& a);
 cudaError_t launch_dgrad_grouped_tc(const Plan& p, const Args& a);

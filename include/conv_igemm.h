@@ -141,12 +141,20 @@ typedef enum conv_kernel {
                                         tiles (128 x 128, 8 x 8 a thread) for the forward, the
                                         stride-1 data gradient (the turned problem, filter read in
                                         place) and the weight gradient (+ bias gradient) */
-  CONV_KERNEL_WGRAD_DEPTHWISE_MMA = 17 /* 16-bit depthwise weight gradient (filters up to 7 x 7, unit
+  CONV_KERNEL_WGRAD_DEPTHWISE_MMA = 17, /* 16-bit depthwise weight gradient (filters up to 7 x 7, unit
                                         stride and dilation, rows of at most 64 input and output
                                         columns, C % 8 = 0): per channel and output row, warp-level
                                         m16n8k16 MMAs of the filter rows' input rows against dY
                                         shifted by each filter column (a Toeplitz operand), rows
-                                        transposed in shared memory; the bias from a row of ones */
+                                        transposed in shared memory; the bias summed from the
+                                        transposed dY rows */
+  CONV_KERNEL_FWD_GROUPED_MMA = 18,  /* 16-bit grouped forward (Cg = Kg = 4 or 8, C % 64 = 0, unit stride
+                                        and dilation, 1x1 / 3x3 / 5x5 filters, Wo <= 64): per output
+                                        row and 16 columns, warp-level m16n8k16 MMAs over pairs of taps
+                                        with the tap as a pixel shift of X and the group's filter in
+                                        registers; unsplit, fused epilogue supported */
+  CONV_KERNEL_DGRAD_GROUPED_MMA = 19 /* the stride-1 grouped data gradient on the same kernel: the
+                                        forward over dY with the turned filter read in place */
 } conv_kernel;
 
 /* What a call with these arguments would run. */

@@ -199,11 +199,11 @@ def test_depthwise_7x7_forward_full_sampled_images():
 @pytest.mark.parametrize("groups", [64, 128], ids=["cpg8", "cpg4"])
 def test_grouped_3x3_forward_full_sampled_images(groups):
     """Grouped 3x3 forward fp16, N=64, 28x28, C=K=512 (the grouped configuration's forward
-    twin), auto (block-diagonal tensor-core blocks): images 0 and 63 against the oracle."""
+    twin), auto (the grouped warp-MMA kernel): images 0 and 63 against the oracle."""
     n, hw, c = 64, 28, 512
     p = cig.Problem(n=n, h=hw, w=hw, c=c, k=c, r=3, s=3, pad_h=1, pad_w=1, groups=groups,
                     in_dtype=cig.F16, out_dtype=cig.F16)
-    assert cig.describe_plan(p, cig.DIR_FWD, -1)["kernel_name"] == "fwd_grouped_tc"
+    assert cig.describe_plan(p, cig.DIR_FWD, -1)["kernel_name"] == "fwd_grouped_mma"
     x = synth.tensor((n, hw, hw, c), torch.float16, "normal", 0.0, 1.0, 4, synth.X_ID)
     w = synth.tensor((c, 3, 3, c // groups), torch.float16, "normal", 0.0, 1.0, 4, synth.W_ID)
     y = torch.empty((n, hw, hw, c), dtype=torch.float16, device="cuda")
@@ -243,7 +243,7 @@ def test_grouped_3x3_dgrad_full(groups):
     n, hw, c = 64, 28, 512
     p = cig.Problem(n=n, h=hw, w=hw, c=c, k=c, r=3, s=3, pad_h=1, pad_w=1, groups=groups,
                     in_dtype=cig.F16, out_dtype=cig.F16)
-    assert cig.describe_plan(p, cig.DIR_DGRAD, -1)["kernel_name"] == "dgrad_grouped_tc"
+    assert cig.describe_plan(p, cig.DIR_DGRAD, -1)["kernel_name"] == "dgrad_grouped_mma"
     dy = synth.tensor((n, hw, hw, c), torch.float16, "normal", 0.0, 1.0, 4, synth.DY_ID)
     w = synth.tensor((c, 3, 3, c // groups), torch.float16, "normal", 0.0, 1.0, 4, synth.W_ID)
     dx = torch.empty((n, hw, hw, c), dtype=torch.float16, device="cuda")

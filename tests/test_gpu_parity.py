@@ -276,9 +276,10 @@ def test_forward_depthwise(shape, dt):
 ])
 @pytest.mark.parametrize("dt", [(BF16, BF16), (F16, F32), (F16, F16)], ids=lambda d: f"{d[0]}{d[1]}")
 def test_forward_grouped_tc(shape, dt):
-    """Grouped forwards as block-diagonal dense 128-channel blocks on the tensor cores."""
+    """Grouped forwards as block-diagonal dense 128-channel blocks on the tensor cores (automatic choice
+    for 4 or 8 channels per group at stride 1: the warp-MMA kernel)."""
     p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
-    assert cig.describe_plan(p, cig.DIR_FWD, -1)["kernel_name"] == "fwd_grouped_tc"
+    assert cig.describe_plan(p, cig.DIR_FWD, -1)["kernel_name"] in ("fwd_grouped_tc", "fwd_grouped_mma")
     check_fwd(p, 14, ["fwd_grouped_tc", "generic"], [-1, 1, 3])
     check_fwd(p, 14, ["fwd_grouped_tc"], ["max"])
     assert cig.device_errors() == 0
@@ -305,7 +306,8 @@ def run_fwd_ep(p, x, w, bias, lo, hi, split_k=-1):
     dict(n=1, h=14, w=14, c=256, k=256, r=3, s=3, pad_h=1, pad_w=1),          # 128 x 256 tiles; conv_fwd would split
     dict(n=2, h=9, w=11, c=12, k=8, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1),  # generic
     dict(n=2, h=13, w=17, c=96, k=96, groups=96, r=7, s=7, pad_h=3, pad_w=3),             # depthwise kernel
-    dict(n=2, h=10, w=12, c=128, k=128, groups=16, r=3, s=3, pad_h=1, pad_w=1),           # grouped, tensor cores
+    dict(n=2, h=10, w=12, c=128, k=128, groups=16, r=3, s=3, pad_h=1, pad_w=1),           # grouped, warp MMAs
+    dict(n=2, h=8, w=8, c=128, k=128, groups=64, r=5, s=5, pad_h=2, pad_w=2),             # grouped, tensor cores
 ])
 @pytest.mark.parametrize("dt", [(BF16, BF16), (F16, F32), (F32, F32)], ids=lambda d: f"{d[0]}{d[1]}")
 def test_forward_fused_epilogue(shape, dt):
@@ -435,9 +437,33 @@ def test_dgrad_grouped_tc(shape, dt):
     filter in the group blocks."""
     p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
     info = cig.describe_plan(p, cig.DIR_DGRAD, -1)
-    assert info["kernel_name"] == "dgrad_grouped_tc" and info["workspace_bytes"] > 0
-    check_dgrad(p, 14, ["auto"], [-1, 1, 2, "max"])
+    assert info["kernel_name"] in ("dgrad_grouped_tc", "dgrad_grouped_mma")
+    check_dgrad(p, 14, ["auto", "dgrad_grouped_tc"], [-1, 1, 2, "max"])
     check_dgrad(p, 14, ["generic"], [1])
+    assert cig.device_errors() == 0
+
+
+@pytest.mark.parametrize("shape", [
+    dict(n=2, h=10, w=13, c=128, k=128, groups=16, r=3, s=3, pad_h=1, pad_w=1),   # cpg 8, two channel blocks
+    dict(n=3, h=9, w=9, c=64, k=64, groups=16, r=3, s=3, pad_h=1, pad_w=1),       # cpg 4
+    dict(n=1, h=12, w=40, c=64, k=64, groups=8, r=3, s=3),                         # no padding, 3 column tiles
+    dict(n=2, h=7, w=9, c=128, k=128, groups=32, r=5, s=5, pad_h=2, pad_w=2),     # cpg 4, 5x5
+    dict(n=2, h=6, w=17, c=64, k=64, groups=8, r=1, s=1),                          # pointwise
+    dict(n=1, h=5, w=64, c=64, k=64, groups=8, r=3, s=3, pad_h=2, pad_w=1),       # widest rows, Ho > H
+    dict(n=5, h=3, w=6, c=64, k=64, groups=16, r=5, s=5, pad_h=4, pad_w=4),       # pad F - 1: rows past the image
+])
+@pytest.mark.parametrize("dt", [(F16, F16), (BF16, F32), (BF16, BF16)], ids=lambda d: f"{d[0]}{d[1]}")
+def test_grouped_mma_forward_and_dgrad(shape, dt):
+    """The grouped warp-MMA kernel (taps as pixel shifts, the group's filter in registers, unsplit):
+    the forward and, on the turned problem with the filter read in place, the stride-1 data gradient,
+    against the oracle; reruns bit-identical."""
+    p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
+    assert cig.describe_plan(p, cig.DIR_FWD, -1)["kernel_name"] == "fwd_grouped_mma"
+    assert cig.describe_plan(p, cig.DIR_DGRAD, -1)["kernel_name"] == "dgrad_grouped_mma"
+    check_fwd(p, 16, ["auto"], [-1, 1])
+    check_dgrad(p, 16, ["auto"], [-1, 1])
+    x, w = inputs(p, 16, direction=cig.DIR_FWD)
+    assert torch.equal(run_fwd(p, x, w, -1), run_fwd(p, x, w, -1))
     assert cig.device_errors() == 0
 
 

@@ -193,10 +193,15 @@ def test_dgrad_plans():
                       in_dtype=BF16, out_dtype=BF16)
     info = cig.describe_plan(strided, cig.DIR_DGRAD, 1, sm_count=SMS)
     assert info["kernel_name"] == "generic" and info["workspace_bytes"] == 0
-    # grouped (Cg = Kg dividing 128) and depthwise data gradients at stride 1 take the turned-filter forwards
+    # grouped and depthwise data gradients at stride 1 take the turned-filter forwards: 4 or 8 channels
+    # per group the MMA kernel (filter read in place, unsplit), else (Cg = Kg dividing 128) the
+    # block-diagonal one (the turned block-diagonal filter in the workspace)
     info = cig.describe_plan(CONFIG5A, cig.DIR_DGRAD, -1, sm_count=SMS)
+    assert (info["kernel_name"], info["split_k"], info["workspace_bytes"]) == ("dgrad_grouped_mma", 1, 0)
+    cpg2 = Problem(n=2, h=8, w=8, c=128, k=128, r=5, s=5, pad_h=2, pad_w=2, groups=64, in_dtype=F16, out_dtype=F16)
+    info = cig.describe_plan(cpg2, cig.DIR_DGRAD, -1, sm_count=SMS)
     assert info["kernel_name"] == "dgrad_grouped_tc"
-    assert info["workspace_bytes"] == r256(CONFIG5A.c * 9 * 128 * 2)  # the turned block-diagonal filter
+    assert info["workspace_bytes"] == r256(cpg2.c * 25 * 128 * 2)  # the turned block-diagonal filter
     info = cig.describe_plan(CONFIG4, cig.DIR_DGRAD, -1, sm_count=SMS)
     assert (info["kernel_name"], info["split_k"], info["workspace_bytes"]) == ("dgrad_depthwise", 1, 0)
     strided_dw = Problem(n=2, h=9, w=9, c=64, k=64, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1,
@@ -347,6 +352,34 @@ def test_depthwise_mma_wgrad_admission():
                 wg(p)
     finally:
         cig.set_kernel_override("auto")
+
+
+def test_grouped_mma_forward_selection():
+    """Which grouped forwards (and stride-1 data gradients) the MMA kernel takes: 16-bit, Cg = Kg = 4 or
+    8, C % 64 == 0, unit stride and dilation, 1x1 / 3x3 / 5x5 filters with pad <= F - 1, at most 64
+    output columns; unsplit, about two CTAs per SM over the 64-channel blocks, no workspace."""
+    fw = lambda p: cig.describe_plan(p, DIR_FWD, -1, sm_count=SMS)  # noqa: E731
+    dg = lambda p: cig.describe_plan(p, cig.DIR_DGRAD, -1, sm_count=SMS)  # noqa: E731
+
+    def grp(**kw):
+        base = dict(n=2, h=12, w=14, c=128, k=128, r=3, s=3, pad_h=1, pad_w=1, groups=16, in_dtype=F16,
+                    out_dtype=F16)
+        base.update(kw)
+        return Problem(**base)
+    for p in (CONFIG5A, CONFIG5B, grp(), grp(groups=32), grp(r=1, s=1, pad_h=0, pad_w=0), grp(r=5, s=5, pad_h=2),
+              grp(w=64), grp(in_dtype=BF16, out_dtype=F32)):
+        info = fw(p)
+        assert (info["kernel_name"], info["split_k"], info["workspace_bytes"]) == ("fwd_grouped_mma", 1, 0), p
+        assert info["ctas"] <= 2 * SMS + p.c // 64 and info["ctas_per_sm"] == 2
+        assert dg(p)["kernel_name"] == "dgrad_grouped_mma", p
+    info = fw(CONFIG5A)
+    assert info["ctas"] == 304  # 8 channel blocks x 38 runs of (n, ho) rows (a multiple of the step)
+    # 2 or 16 channels per group, C % 64 != 0, stride 2, a 7x7 filter, 65 output columns, fp32: not this
+    # kernel (the data gradient at stride 2 is not a forward)
+    for p in (grp(groups=64), grp(groups=8), grp(c=96, k=96, groups=12), grp(stride_h=2, stride_w=2),
+              grp(r=7, s=7, pad_h=3, pad_w=3), grp(w=65), grp(in_dtype=F32, out_dtype=F32)):
+        assert fw(p)["kernel_name"] != "fwd_grouped_mma", p
+    assert dg(grp(r=3, s=3, pad_h=1, pad_w=1, dil_h=2, dil_w=2))["kernel_name"] != "dgrad_grouped_mma"
 
 
 def test_dense_wgrad_tensor_core_selection():
