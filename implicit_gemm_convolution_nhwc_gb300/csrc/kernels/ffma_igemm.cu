@@ -26,6 +26,7 @@ constexpr int kThreads = 256;
 constexpr int kT = 128;      // tile rows and columns
 constexpr int kBK = 16;      // reduction elements a step
 constexpr int kLD = kT + 4;  // shared row stride (floats)
+constexpr int kCtasPerSm = 2;  // 2 x 256 threads x 128 registers fill the register file
 
 enum { kFwd = 0, kDgrad = 1, kWgrad = 2 };
 
@@ -44,6 +45,7 @@ struct FfParams {
   // the forward-form problem: input [N][H][W][C], output [N][Ho][Wo][K], filter R x S
   int64_t H, W, C, Ho, Wo, K;
   int32_t R, S, sh, sw, ph, pw, dh, dw;
+  DivU32 div_wo, div_ho;  // weight gradient: pixel -> (n, ho, wo)
   int32_t cblocks;     // ceil(C / 16) (forward, data gradient)
   int32_t split;
   // fused forward epilogue (unsplit only): y = min(max(acc + bias[k], ep_lo), ep_hi)
@@ -58,7 +60,7 @@ struct Stage {
 };
 
 template <int DIR>
-__global__ void __launch_bounds__(kThreads, 1) ffma_igemm_kernel(FfParams fp) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) ffma_igemm_kernel(FfParams fp) {
   __shared__ __align__(16) float As[2][kBK][kLD];
   __shared__ __align__(16) float Bs[2][kBK][kLD];
   const int t = threadIdx.x;
@@ -79,24 +81,17 @@ __global__ void __launch_bounds__(kThreads, 1) ffma_igemm_kernel(FfParams fp) {
   // gradient: W[k][tap'][c] for step row t / 32 (+ 8), columns n0 + 4 (t % 32) (straight).
   // Weight gradient A: dY pixel t / 32 (+ 8) of the step, channels m0 + 4 (t % 32) (straight); B: X at
   // that pixel shifted by the tap, channels n0 + 4 (t % 32) (straight).
-  int64_t pn[2], pho[2], pwo[2];  // forward-form pixels of this thread's A rows (fwd / dgrad) or B rows (wgrad)
+  // Spatial index arithmetic runs in 32 bits (the host admits only shapes where it cannot overflow).
+  int32_t pn[2], pho[2], pwo[2];  // forward / data gradient: the forward-form pixels of this thread's A rows
   bool pok[2];
   if (DIR != kWgrad) {
     for (int i = 0; i < 2; ++i) {
       const int64_t m = m0 + t / 4 + 64 * i;
       pok[i] = m < fp.M;
       const int64_t mm = pok[i] ? m : 0;
-      pwo[i] = mm % fp.Wo;
-      pho[i] = (mm / fp.Wo) % fp.Ho;
-      pn[i] = mm / (fp.Wo * fp.Ho);
-    }
-  } else {
-    for (int i = 0; i < 2; ++i) {
-      const int64_t p = b0 * kBK + t / 32 + 8 * i;
-      pwo[i] = p % fp.Wo;
-      pho[i] = (p / fp.Wo) % fp.Ho;
-      pn[i] = p / (fp.Wo * fp.Ho);
-      pok[i] = true;
+      pwo[i] = (int32_t)(mm % fp.Wo);
+      pho[i] = (int32_t)((mm / fp.Wo) % fp.Ho);
+      pn[i] = (int32_t)(mm / (fp.Wo * fp.Ho));
     }
   }
   const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -108,7 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffma_igemm_kernel(FfParams fp) {
       const int32_t r = rs / fp.S, s = rs % fp.S;
       const int64_t c = c0 + 4 * (t % 4);
       for (int i = 0; i < 2; ++i) {
-        const int64_t hi = pho[i] * fp.sh + r * fp.dh - fp.ph, wi = pwo[i] * fp.sw + s * fp.dw - fp.pw;
+        const int32_t hi = pho[i] * fp.sh + r * fp.dh - fp.ph, wi = pwo[i] * fp.sw + s * fp.dw - fp.pw;
         const bool in = pok[i] && c < fp.C && hi >= 0 && hi < fp.H && wi >= 0 && wi < fp.W;
         sa.v[i] = in ? *reinterpret_cast<const float4*>(fp.a + ((pn[i] * fp.H + hi) * fp.W + wi) * fp.C + c) : zero4;
       }
@@ -129,21 +124,16 @@ __global__ void __launch_bounds__(kThreads, 1) ffma_igemm_kernel(FfParams fp) {
     } else {
       const int64_t k = m0 + 4 * (t % 32), c = n0 + 4 * (t % 32);
       for (int i = 0; i < 2; ++i) {
-        const int64_t p = blk * kBK + t / 32 + 8 * i;
-        const bool pin = p < fp.P;
-        sa.v[i] = pin && k < fp.M ? *reinterpret_cast<const float4*>(fp.a + p * fp.K + k) : zero4;
-        const int64_t hi = pho[i] * fp.sh + tr * fp.dh - fp.ph, wi = pwo[i] * fp.sw + ts * fp.dw - fp.pw;
+        // pixel p of the step -> (n, ho, wo), no state kept across steps
+        const uint32_t p = (uint32_t)blk * kBK + t / 32 + 8 * i;
+        const bool pin = p < (uint32_t)fp.P;
+        sa.v[i] = pin && k < fp.M ? *reinterpret_cast<const float4*>(fp.a + (int64_t)p * fp.K + k) : zero4;
+        const uint32_t q = fp.div_wo.div(p), n = fp.div_ho.div(q);
+        const int32_t wo = (int32_t)(p - q * fp.div_wo.d), ho = (int32_t)(q - n * fp.div_ho.d);
+        const int32_t hi = ho * fp.sh + tr * fp.dh - fp.ph, wi = wo * fp.sw + ts * fp.dw - fp.pw;
         const bool in = pin && c < fp.N && hi >= 0 && hi < fp.H && wi >= 0 && wi < fp.W;
-        sb.v[i] = in ? *reinterpret_cast<const float4*>(fp.b + ((pn[i] * fp.H + hi) * fp.W + wi) * fp.C + c) : zero4;
-        // the next step's pixel: 16 further on
-        pwo[i] += kBK;
-        while (pwo[i] >= fp.Wo) {
-          pwo[i] -= fp.Wo;
-          if (++pho[i] == fp.Ho) {
-            pho[i] = 0;
-            ++pn[i];
-          }
-        }
+        sb.v[i] = in ? *reinterpret_cast<const float4*>(fp.b + (((int64_t)n * fp.H + hi) * fp.W + wi) * fp.C + c)
+                     : zero4;
       }
     }
   };
@@ -252,6 +242,13 @@ bool admissible(const Shape& s, conv_dir dir) {
   if (dir == CONV_DIR_DGRAD && (s.sh != 1 || s.sw != 1 || s.ph > s.dh * (s.r - 1) || s.pw > s.dw * (s.s - 1)))
     return false;
   if (s.r * s.s > 0x7fffffffLL || (s.c + kBK - 1) / kBK * s.r * s.s > 0x7fffffffLL) return false;
+  // The kernel's spatial index arithmetic is 32-bit: in the forward form, hi = ho*sh + r*dh - ph
+  // lies in [-ph, H + ph), so H + 2 ph (and likewise W + 2 pw) and the image count must stay below
+  // 2^31; the weight gradient's pixel index (up to P + 15) too.
+  const Shape f = dir == CONV_DIR_DGRAD ? dgrad_as_forward(s) : s;
+  const int64_t lim = 0x7fffffffLL;
+  if (f.n >= lim || f.h + 2 * f.ph >= lim || f.w + 2 * f.pw >= lim) return false;
+  if (dir == CONV_DIR_WGRAD && s.n * s.ho * s.wo + kBK >= lim) return false;
   return true;
 }
 
@@ -281,7 +278,7 @@ Geometry geometry_ffma(const Shape& s, conv_dir dir) {
   int64_t M, N, blocks, tiles;
   extents(s, dir, &M, &N, &blocks, &tiles);
   g.ok = true;
-  g.ctas_per_sm = 1;
+  g.ctas_per_sm = kCtasPerSm;
   g.tiles = tiles;
   g.blocks = blocks;
   return g;
@@ -312,6 +309,10 @@ cudaError_t launch_ffma(const Plan& p, const Args& a) {
   }
   fp.cblocks = (int32_t)((fp.C + kBK - 1) / kBK);
   fp.P = s.n * s.ho * s.wo;
+  if (p.dir == CONV_DIR_WGRAD) {
+    fp.div_wo = DivU32((uint32_t)s.wo);
+    fp.div_ho = DivU32((uint32_t)s.ho);
+  }
   const int64_t ctas = tiles * p.split;
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (p.dir == CONV_DIR_FWD) {

@@ -679,6 +679,7 @@ FFMA_SHAPES = [
     dict(n=1, h=17, w=19, c=64, k=64, r=5, s=5, pad_h=2, pad_w=2),
     dict(n=2, h=12, w=12, c=136, k=8, r=1, s=1),                                   # pointwise, ragged M
     dict(n=1, h=20, w=21, c=8, k=260, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1),  # 3 N tiles
+    dict(n=5, h=7, w=1, c=12, k=20, r=3, s=1, pad_h=1),                            # Wo = 1: steps span images
 ]
 
 

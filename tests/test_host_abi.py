@@ -430,7 +430,8 @@ def test_fp32_ffma_tiles_selection():
     p = Problem(n=4, h=16, w=16, c=128, k=256, r=3, s=3, pad_h=1, pad_w=1)
     for d, tiles in ((DIR_FWD, 8 * 2), (cig.DIR_DGRAD, 8 * 1), (DIR_WGRAD, 2 * 1 * 9)):
         info = cig.describe_plan(p, d, -1, sm_count=SMS)
-        assert info["kernel_name"] == "ffma" and info["tiles"] == tiles and info["ctas"] <= SMS, (d, info)
+        assert info["kernel_name"] == "ffma" and info["tiles"] == tiles and info["ctas_per_sm"] == 2, (d, info)
+        assert info["ctas"] <= 2 * SMS, (d, info)
     strided = Problem(n=2, h=9, w=9, c=16, k=16, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1)
     assert cig.describe_plan(strided, cig.DIR_DGRAD, -1, sm_count=SMS)["kernel_name"] == "generic"
     assert cig.describe_plan(strided, DIR_FWD, -1, sm_count=SMS)["kernel_name"] == "ffma"
