@@ -351,6 +351,15 @@ PER_CONFIG = ["wgrad1x1_f32_n4", "fwd3x3_bf16_n1", "dgrad3x3_bf16_n1", "dw7x7_wg
               "dgrad3x3_bf16_n64_c256", "wgrad3x3_bf16_n64_c256", "fwd3x3_f32_n16_c256", "wgrad3x3_f32_n16_c256"]
 # The split-K degrees swept on the small-M layer (auto first).
 SWEEP = {"fwd3x3_bf16_n1": [-1, 1, 2, 4, 8, 16, 32]}
+# The fold on slabs far larger than L2: the dense forward at a pinned degree,
+# whose stage 2 reads S fp32 slabs of the whole output from HBM.
+FOLD_HBM = [("fwd3x3_bf16_n64_c256", 4)]
+
+
+def fold_bytes(split, out, db):
+    """Bytes the fold moves: S fp32 slabs read, the output (and db) written once."""
+    e = out.numel() + (db.numel() if db is not None else 0)
+    return split * e * 4 + e * out.element_size()
 
 
 def roofline_for(kname, p, direction, flops, in_bytes, stage1_ms, pk, sms):
@@ -570,6 +579,20 @@ def per_config(dev, sms, pk, steps, warmup):
                  "stage1_ms": round(statistics.mean(s1_s), 5)})
             sw.free()
         out[name] = entry
+        torch.cuda.empty_cache()
+    for name, deg in FOLD_HBM:
+        wl = Workload(name, dev, sms, split_k=deg)
+        _, _, s2 = wl.time(steps, warmup)
+        f_ms = statistics.mean(s2)
+        fb = fold_bytes(wl.plan["split_k"], wl.out, wl.db)
+        gbs = fb / (f_ms * 1e-3) / 1e9
+        out[f"fold:{name}@S{deg}"] = {
+            "workload": f"stage 2 alone of {wl.desc}, degree {wl.plan['split_k']}: "
+                        f"{wl.plan['split_k']} fp32 slabs of {wl.out.numel()} elements, larger than L2",
+            "kernel": "fold", "fold_ms": round(f_ms, 5), "bytes": fb,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+                         "frac": round(gbs / pk["hbm"], 4)}}
+        wl.free()
         torch.cuda.empty_cache()
     sampler.mark(False)
     out["clocks"] = sampler.stop()

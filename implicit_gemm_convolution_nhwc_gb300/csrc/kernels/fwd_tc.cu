@@ -58,8 +58,17 @@ struct Tile {
   static constexpr int kB = BN * 128;              // B tile bytes (BN rows x 128 B)
   static constexpr int kStage = MS * kA + kB;      // MS A tiles (M sub-tiles) share one B tile
   static constexpr int kStages = (BN == 256 && MS == 1) ? 4 : 3;
-  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + 256;
   static constexpr uint32_t kTmemCols = BN * MS;   // one fp32 accumulator per M sub-tile
+  // 256-wide tiles (one CTA per SM) run persistent: a CTA takes unit after
+  // unit, its ring streaming on across them, the epilogue staging in its own
+  // two 16 KB buffers (+ the bias); with two accumulators in TMEM (when they
+  // fit) a unit's epilogue overlaps the next unit's MMAs.
+  static constexpr bool kPersist = BN == 256;
+  static constexpr int kOwnEpiBufs = 2;
+  static constexpr int kOwnEpi = kPersist ? kOwnEpiBufs * kBM * 128 + BN * 4 : 0;
+  static constexpr int kAccs = kPersist && 2 * kTmemCols <= 512 ? 2 : 1;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + kOwnEpi + 256;
+  static_assert(kSmem <= 227 * 1024, "shared memory");
   static constexpr int kLD = BN + 4;                // staged partial tile row stride, floats (conflict-free float4s)
   static_assert(BN == 128 || BN == 256, "tile width");
   static_assert(MS == 1 || MS == 2, "M sub-tiles");
@@ -122,51 +131,101 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
   using T = Tile<BN, MS>;
   constexpr int kStages = T::kStages, kStage = T::kStage, kB = T::kB, kLD = T::kLD;
   constexpr uint32_t kTmemCols = T::kTmemCols;
+  constexpr bool kPersist = T::kPersist && !CL;
+  constexpr int NACC = T::kAccs;  // TMEM accumulators (2: a unit's epilogue overlaps the next unit's MMAs)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * kStage);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * kStage + T::kOwnEpi);
   uint64_t* empty = full + kStages;
   uint64_t* tmem_full = empty + kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_full + 1);
+  uint64_t* tmem_empty = tmem_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_empty + 2);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   constexpr uint32_t IDESC = mma_idesc(FMT, 0u, BMN ? 1u : 0u, (uint32_t)BN, (uint32_t)kBM);
   constexpr uint32_t kAtom = 64u * 128u;  // one MN-major B atom: 64 reduction rows of 128 bytes
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // Two-stage form: CTA = sigma * tiles + tile. Cluster form: the S CTAs of
-  // a tile are consecutive, sigma = rank in the cluster.
-  const int64_t tile = CL ? (int64_t)(blockIdx.x / (uint32_t)fp.split) : (int64_t)(blockIdx.x % fp.tiles);
-  const int32_t sigma = CL ? (int32_t)cluster_ctarank() : (int32_t)(blockIdx.x / fp.tiles);
-  const int64_t tn = tile % fp.tiles_n;
-  const int64_t tm = tile / fp.tiles_n;
-  const int64_t img = tm / fp.tiles_m_per_img;
-  const int64_t ho0 = (tm % fp.tiles_m_per_img) * fp.TR * MS;  // sub-tile h starts at row ho0 + h * TR
-  const int64_t k0 = tn * BN;
-  const int64_t b0 = slice_begin(fp.blocks, fp.split, sigma);
-  const int64_t nblk = slice_begin(fp.blocks, fp.split, sigma + 1) - b0;
+  // Work units (tile, slice sigma). Two-stage form: unit = sigma * tiles +
+  // tile; a persistent CTA takes units blockIdx.x, blockIdx.x + gridDim.x,
+  // ... (else the grid has one CTA per unit). Cluster form: one unit a CTA,
+  // the S CTAs of a tile consecutive, sigma = rank in the cluster.
+  const int64_t units = CL ? (int64_t)gridDim.x : fp.tiles * fp.split;
+  const int64_t ustride = (int64_t)gridDim.x;
+  struct Unit {
+    int64_t img, ho0, k0, b0, nblk;
+    int32_t sigma;
+  };
+  auto unit_of = [&](int64_t u) {
+    Unit w;
+    const int64_t tile = CL ? u / fp.split : u % fp.tiles;
+    w.sigma = CL ? (int32_t)cluster_ctarank() : (int32_t)(u / fp.tiles);
+    const int64_t tn = tile % fp.tiles_n, tm = tile / fp.tiles_n;
+    w.img = tm / fp.tiles_m_per_img;
+    w.ho0 = (tm % fp.tiles_m_per_img) * fp.TR * MS;  // sub-tile h starts at row ho0 + h * TR
+    w.k0 = tn * BN;
+    w.b0 = slice_begin(fp.blocks, fp.split, w.sigma);
+    w.nblk = slice_begin(fp.blocks, fp.split, w.sigma + 1) - w.b0;
+    return w;
+  };
+  const int64_t u_first = blockIdx.x;
   const uint32_t tx = (uint32_t)(MS * fp.TR * fp.Wo * 128 + kB);
 
-  // Producer state (thread 0): the ring stage and its round's parity, and
-  // the next block's (r, s, c-block), all advanced by increments.
+  // Producer state (every lane of warp 0, kept in step): the ring stage and
+  // its round's parity, the unit and block being loaded, and that block's
+  // (r, s, c-block), all advanced by increments.
   int ps = 0;
   uint32_t pph = 0;
-  int32_t cb = 0, rs = 0, r = 0, sx = 0;
-  int64_t it = 0;
   const int32_t cblocks = (int32_t)fp.cblocks, cg = (int32_t)fp.Cg, sf = (int32_t)fp.S_f;
+  int64_t pu = u_first, pj = 0, it = 0;
+  Unit pw = unit_of(pu);
+  int32_t cb, rs, r, sx;
+  auto unit_start = [&]() {
+    pj = 0;
+    cb = (int32_t)(pw.b0 % fp.cblocks);
+    rs = (int32_t)(pw.b0 / fp.cblocks);
+    r = rs / sf;
+    sx = rs % sf;
+  };
+  unit_start();
+  // true while a block is left to load (moving on past finished units)
+  auto pending = [&]() {
+    while (pj >= pw.nblk) {
+      pu += ustride;
+      if (pu >= units) return false;
+      pw = unit_of(pu);
+      unit_start();
+    }
+    return true;
+  };
+  // A block's loads go out as ONE warp-wide 4-D TMA instruction, lane i
+  // issuing box i: lanes 0..MS-1 the A sub-tiles, the next lanes the B
+  // box(es), rather than one thread issuing them in turn.
+  constexpr int kLoads = MS + (BMN ? BN / 64 : 1);
   auto issue = [&]() {
     uint8_t* st = smem + (size_t)ps * kStage;
-    mbar_arrive_expect_tx(&full[ps], tx);
-#pragma unroll
-    for (int h = 0; h < MS; ++h)  // a sub-tile past the image reads zeros (and is not stored)
-      tma_load_4d(st + h * kA, &tm_x, (fp.a_coff ? (int32_t)k0 : 0) + cb * kBK, sx * fp.dw - fp.pw,
-                  (int32_t)(ho0 + h * fp.TR) * fp.sh + r * fp.dh - fp.ph, (int32_t)img, &full[ps]);
-    if (BMN) {
-#pragma unroll
-      for (int j = 0; j < BN / 64; ++j)
-        tma_load_3d(st + MS * kA + j * kAtom, &tm_w, (int32_t)k0 + 64 * j, fp.taps - 1 - rs, cb * kBK, &full[ps]);
-    } else {
-      tma_load_2d(st + MS * kA, &tm_w, rs * cg + cb * kBK, (int32_t)k0, &full[ps]);
+    if (lane == 0) mbar_arrive_expect_tx(&full[ps], tx);
+    if (lane < kLoads) {
+      const bool is_a = lane < MS;
+      const int j = lane - MS;  // B piece
+      const int32_t a_c0 = (fp.a_coff ? (int32_t)pw.k0 : 0) + cb * kBK;
+      const int32_t a_c2 = (int32_t)(pw.ho0 + lane * fp.TR) * fp.sh + r * fp.dh - fp.ph;
+      const CUtensorMap* map = is_a ? &tm_x : &tm_w;
+      uint8_t* dst = is_a ? st + lane * kA : st + MS * kA + (BMN ? j * (int)kAtom : 0);
+      int32_t c0, c1, c2;
+      if (BMN) {
+        c0 = is_a ? a_c0 : (int32_t)pw.k0 + 64 * j;
+        c1 = is_a ? sx * fp.dw - fp.pw : fp.taps - 1 - rs;
+        c2 = is_a ? a_c2 : cb * kBK;
+      } else {
+        c0 = is_a ? a_c0 : rs * cg + cb * kBK;
+        c1 = is_a ? sx * fp.dw - fp.pw : (int32_t)pw.k0;
+        c2 = is_a ? a_c2 : 0;
+      }
+      // a sub-tile past the image reads zeros (and is not stored)
+      tma_load_4d(dst, map, c0, c1, c2, is_a ? (int32_t)pw.img : 0, &full[ps]);
     }
+    ++pj;
+    ++it;
     if (++cb == cblocks) {
       cb = 0;
       ++rs;
@@ -186,21 +245,23 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(tmem_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tmem_full[i], 1);
+      mbar_init(&tmem_empty[i], 1);
+    }
     *abort_flag = 0u;
     mbar_fence_init();
     tma_prefetch(&tm_x);
     tma_prefetch(&tm_w);
-    cb = (int32_t)(b0 % fp.cblocks);
-    rs = (int32_t)(b0 / fp.cblocks);
-    r = rs / sf;
-    sx = rs % sf;
+  }
+  if (warp == 0) {
+    __syncwarp();  // the barriers are initialised
     // The first ring of loads goes out before the CTA-wide sync (which waits
     // for the TMEM allocation), so its latency overlaps the set-up.
-    for (; it < nblk && it < kStages; ++it) issue();
+    while (it < kStages && pending()) issue();
   }
   if (warp == 2) {
-    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_alloc(tmem_slot, kTmemCols * NACC);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -209,103 +270,148 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) {
-      for (; it < nblk; ++it) {
-        if (!mbar_wait(&empty[ps], pph ^ 1u, abort_flag, err)) break;
-        issue();
-      }
+    while (pending()) {
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&empty[ps], pph ^ 1u, abort_flag, err);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      issue();
+    }
+    if (lane == 0)
       for (int64_t q = it > kStages ? it - kStages : 0; q < it; ++q)
         mbar_wait(&full[q % kStages], (uint32_t)(q / kStages) & 1u, nullptr, err);
-    }
+    __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t base = smem_u32(smem);
       int s = 0;
       uint32_t ph = 0;
-      for (int64_t j = 0; j < nblk; ++j) {
-        if (!mbar_wait(&full[s], ph, abort_flag, err)) break;
+      bool live = true;  // false once a wait gave up: the units left only signal their (empty) accumulators
+      int64_t i = 0;
+      for (int64_t u = u_first; u < units; u += ustride, ++i) {
+        const int64_t nblk = unit_of(u).nblk;
+        const int buf = (int)(i % NACC);
+        const uint32_t use = (uint32_t)(i / NACC);
+        // the epilogue has drained this accumulator's previous unit
+        if (live && use > 0 && !mbar_wait(&tmem_empty[buf], (use - 1u) & 1u, abort_flag, err)) live = false;
         tc_fence_after();
-        const uint32_t a = base + (uint32_t)(s * kStage), b = a + MS * kA;
+        const uint32_t dacc = tmem + (uint32_t)buf * kTmemCols;
+        bool any = false;
+        for (int64_t j = 0; live && j < nblk; ++j) {
+          if (!mbar_wait(&full[s], ph, abort_flag, err)) {
+            live = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a = base + (uint32_t)(s * kStage), b = a + MS * kA;
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          // K-major SW128: 8-row groups 1024 B apart; a K step of 16 elements is
-          // a 32-byte advance inside the swizzled 128-byte row. MN-major SW128
-          // (BMN): atoms kAtom apart, 8-row groups 1024 B apart; a K step of 16
-          // rows is 2048 B.
-          const uint64_t bd =
-              BMN ? smem_desc_sw128(b + 2048u * kk, kAtom, 1024) : smem_desc_sw128(b + 32u * kk, 16, 1024);
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // K-major SW128: 8-row groups 1024 B apart; a K step of 16 elements is
+            // a 32-byte advance inside the swizzled 128-byte row. MN-major SW128
+            // (BMN): atoms kAtom apart, 8-row groups 1024 B apart; a K step of 16
+            // rows is 2048 B.
+            const uint64_t bd =
+                BMN ? smem_desc_sw128(b + 2048u * kk, kAtom, 1024) : smem_desc_sw128(b + 32u * kk, 16, 1024);
 #pragma unroll
-          for (int h = 0; h < MS; ++h)
-            mma_f16(tmem + (uint32_t)(h * BN), smem_desc_sw128(a + (uint32_t)(h * kA) + 32u * kk, 16, 1024), bd,
-                    IDESC, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int h = 0; h < MS; ++h)
+              mma_f16(dacc + (uint32_t)(h * BN), smem_desc_sw128(a + (uint32_t)(h * kA) + 32u * kk, 16, 1024), bd,
+                      IDESC, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&empty[s]);
+          any = true;
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
-        mma_commit(&empty[s]);
-        if (++s == kStages) {
-          s = 0;
-          ph ^= 1u;
-        }
+        if (any) mma_commit(&tmem_full[buf]);
+        else mbar_arrive(&tmem_full[buf]);
       }
-      if (nblk > 0) mma_commit(tmem_full);
-      else mbar_arrive(tmem_full);
     }
   } else if (warp >= 4) {
-    const bool ok = mbar_wait(tmem_full, 0u, nullptr, err) && *abort_flag == 0u;
-    if (!CL) signal_dependents();
-    tc_fence_after();
     const int q = warp - 4;
     const int m = 32 * q + lane;  // tile row = output pixel within the tile
-    if (CL) {
-      // Stage this slice's partial tile: row m at part + m * kLD (the ring is
-      // idle: every copy landed and every MMA that read it has completed).
-      float* part = reinterpret_cast<float*>(smem) + m * kLD;
+    int64_t i = 0;
+    for (int64_t u = u_first; u < units; u += ustride, ++i) {
+      const Unit w = unit_of(u);
+      const int buf = (int)(i % NACC);
+      const uint32_t use = (uint32_t)(i / NACC);
+      const bool ok = mbar_wait(&tmem_full[buf], use & 1u, nullptr, err) && *abort_flag == 0u;
+      if (!CL && u + ustride >= units) signal_dependents();
+      tc_fence_after();
+      const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)buf * kTmemCols;
+      if (CL) {
+        // Stage this slice's partial tile: row m at part + m * kLD (the ring is
+        // idle: every copy landed and every MMA that read it has completed).
+        float* part = reinterpret_cast<float*>(smem) + m * kLD;
 #pragma unroll 1
-      for (int j = 0; j < BN / 32; ++j) {
-        float v[32];
-        if (nblk > 0) {
-          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32u * j, v);
-        } else {
+        for (int j = 0; j < BN / 32; ++j) {
+          float v[32];
+          if (w.nblk > 0) {
+            tmem_ld32(trow + 32u * j, v);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            for (int c = 0; c < 32; ++c) v[c] = 0.f;
+          }
+#pragma unroll
+          for (int c = 0; c < 32; c += 4)
+            *reinterpret_cast<float4*>(part + 32 * j + c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
         }
-#pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(part + 32 * j + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-      }
-    } else {
-      // Y (or slab sigma of the workspace, fp32) as [N (x S)][Ho*Wo][K], one
-      // M sub-tile (accumulator columns h * BN ..) after the other.
-      const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
-      uint8_t* stage = smem;  // the ring is idle: every copy landed, every MMA completed
-      // The epilogue's bias for the tile's BN channels, as fp32 in shared memory
-      // past the two staging buffers (0 beyond K or without a bias).
-      float* sbias = reinterpret_cast<float*>(smem + T::kEpiBufs * kBM * 128);
-      if (!ws && fp.ep) {
-        const TO* bias = static_cast<const TO*>(fp.ep_bias);
-        for (int i = threadIdx.x - 128; i < BN; i += 128)
-          sbias[i] = bias && k0 + i < fp.K ? to_f32(bias[k0 + i]) : 0.f;
-        named_bar_sync(1, 128);
-      }
+      } else {
+        // Y (or slab sigma of the workspace, fp32) as [N (x S)][Ho*Wo][K], one
+        // M sub-tile (accumulator columns h * BN ..) after the other. Staging:
+        // the CTA's last unit (or only one) uses the idle ring, up to 8 16 KB
+        // buffers (every copy landed, every MMA completed); earlier units of a
+        // persistent CTA use its own two, as the ring keeps loading. The
+        // epilogue's bias for the unit's BN channels, fp32 in shared memory
+        // past the staging buffers (0 beyond K or without a bias).
+        const bool in_ring = !kPersist || u + ustride >= units;
+        uint8_t* stage = in_ring ? smem : smem + (size_t)kStages * kStage;
+        float* sbias = reinterpret_cast<float*>(stage + (in_ring ? T::kEpiBufs : T::kOwnEpiBufs) * kBM * 128);
+        if (!ws && fp.ep) {
+          const TO* bias = static_cast<const TO*>(fp.ep_bias);
+          for (int c = threadIdx.x - 128; c < BN; c += 128)
+            sbias[c] = bias && w.k0 + c < fp.K ? to_f32(bias[w.k0 + c]) : 0.f;
+          named_bar_sync(1, 128);
+        }
 #pragma unroll 1
-      for (int h = 0; h < MS; ++h) {
-        const int64_t hrow = ho0 + h * fp.TR;
-        if (hrow >= fp.Ho) break;  // a sub-tile past the image (uniform over the 128 threads)
-        const int32_t py = (int32_t)(hrow * fp.Wo);
-        // the box {chunk, TR*Wo pixels, 1} at (channel, first pixel, image), clipped at K and Ho*Wo
-        const int32_t pz = ws ? (int32_t)(sigma * fp.N + img) : (int32_t)img;
-        auto store = [&](const void* buf, int32_t x) { tma_store_3d(&tm_y, buf, x, py, pz); };
-        if (ws)
-          store_rows_tma<float, T::kEpiBufs>(trow + (uint32_t)(h * BN), stage, BN, (int32_t)k0, (int32_t)fp.K, m,
-                                             nblk > 0, threadIdx.x == 128, ok, store);
-        else
-          store_rows_tma<TO, T::kEpiBufs>(trow + (uint32_t)(h * BN), stage, BN, (int32_t)k0, (int32_t)fp.K, m,
-                                          nblk > 0, threadIdx.x == 128, ok, store, sbias, fp.ep_lo, fp.ep_hi,
-                                          fp.ep != 0);
+        for (int h = 0; h < MS; ++h) {
+          const int64_t hrow = w.ho0 + h * fp.TR;
+          if (hrow >= fp.Ho) break;  // a sub-tile past the image (uniform over the 128 threads)
+          const int32_t py = (int32_t)(hrow * fp.Wo);
+          // the box {chunk, TR*Wo pixels, 1} at (channel, first pixel, image), clipped at K and Ho*Wo
+          const int32_t pz = ws ? (int32_t)(w.sigma * fp.N + w.img) : (int32_t)w.img;
+          auto store = [&](const void* sb, int32_t x) { tma_store_3d(&tm_y, sb, x, py, pz); };
+          const uint32_t acc = trow + (uint32_t)(h * BN);
+          const bool lead = threadIdx.x == 128;
+          if (ws) {
+            if (in_ring)
+              store_rows_tma<float, T::kEpiBufs>(acc, stage, BN, (int32_t)w.k0, (int32_t)fp.K, m, w.nblk > 0, lead,
+                                                 ok, store);
+            else
+              store_rows_tma<float, T::kOwnEpiBufs>(acc, stage, BN, (int32_t)w.k0, (int32_t)fp.K, m, w.nblk > 0,
+                                                    lead, ok, store);
+          } else {
+            if (in_ring)
+              store_rows_tma<TO, T::kEpiBufs>(acc, stage, BN, (int32_t)w.k0, (int32_t)fp.K, m, w.nblk > 0, lead, ok,
+                                              store, sbias, fp.ep_lo, fp.ep_hi, fp.ep != 0);
+            else
+              store_rows_tma<TO, T::kOwnEpiBufs>(acc, stage, BN, (int32_t)w.k0, (int32_t)fp.K, m, w.nblk > 0, lead,
+                                                 ok, store, sbias, fp.ep_lo, fp.ep_hi, fp.ep != 0);
+          }
+        }
       }
+      // every TMEM read of this unit is done: the accumulator is free again
+      tc_fence_before();
+      named_bar_sync(1, 128);
+      if (threadIdx.x == 128) mbar_arrive(&tmem_empty[buf]);
     }
   }
 
   tc_fence_before();
   if (CL) {
+    const Unit w0 = unit_of(u_first);  // the cluster form's single unit
+    const int32_t sigma = w0.sigma;
+    const int64_t ho0 = w0.ho0, img = w0.img, k0 = w0.k0;
     cluster_sync();  // every slice's partial tile is staged
     const int S = fp.split;
     const int r0 = (sigma * kBM) / S, r1 = ((sigma + 1) * kBM) / S;
@@ -340,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
   __syncthreads();
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, kTmemCols * NACC);
   }
 }
 
@@ -364,11 +470,11 @@ int tile_bn(const Shape& s, bool cluster) { return !cluster && s.k >= 256 ? 256 
 // Output rows of an M sub-tile.
 int64_t tile_rows(const Shape& s) { return kBM / s.wo < s.ho ? kBM / s.wo : s.ho; }
 
-// M sub-tiles per CTA: 2 for 256-wide tiles when the grid still has at least
-// 512 such double tiles (over three waves of one CTA per SM here), else 1:
-// the small-M layers keep their many split-K CTAs, and mid-sized grids keep
-// finer waves (a 3x3 stride-2 layer with 256 double tiles measured slower
-// than with 512 single ones).
+// M sub-tiles per CTA: 2 for 256-wide tiles when the grid has at least 512
+// such double tiles, else 1: the small-M layers keep their many split-K
+// units, and mid-sized grids keep single tiles, whose two TMEM accumulators
+// let a unit's epilogue overlap the next unit's MMAs (a 3x3 stride-2 layer
+// with 256 double tiles measured 39.3 us, with 512 single ones 38.0 us).
 int tile_ms(const Shape& s, bool cluster) {
   if (cluster || tile_bn(s, false) != 256) return 1;
   const int64_t tr = tile_rows(s);
@@ -424,17 +530,21 @@ cudaError_t launch_typed(const Plan& p, const Args& a, CUtensorMapDataType dt, b
   const uint32_t x_estr[4] = {1u, (uint32_t)s.sw, (uint32_t)s.sh, 1u};
   if (!encode_tmap(&tm_x, dt, 4, a.x, x_dims, x_strides, x_box, CU_TENSOR_MAP_SWIZZLE_128B, x_estr))
     return cudaErrorInvalidValue;
+  // The filter maps are 4-D (trailing dimensions of extent 1) so that a
+  // block's A and B boxes go out through one 4-D copy instruction.
   if (BMN) {  // the filter [C'][R*S][K']: boxes of 64 output channels x 1 tap x 64 reduction channels
-    const uint64_t w_dims[3] = {(uint64_t)s.k, (uint64_t)(s.r * s.s), (uint64_t)s.cg};
-    const uint64_t w_strides[2] = {(uint64_t)s.k * 2u, (uint64_t)(s.r * s.s * s.k) * 2u};
-    const uint32_t w_box[3] = {64u, 1u, (uint32_t)kBK};
-    if (!encode_tmap(&tm_w, dt, 3, a.b, w_dims, w_strides, w_box, CU_TENSOR_MAP_SWIZZLE_128B))
+    const uint64_t w_dims[4] = {(uint64_t)s.k, (uint64_t)(s.r * s.s), (uint64_t)s.cg, 1u};
+    const uint64_t w_strides[3] = {(uint64_t)s.k * 2u, (uint64_t)(s.r * s.s * s.k) * 2u,
+                                   (uint64_t)(s.r * s.s * s.k * s.cg) * 2u};
+    const uint32_t w_box[4] = {64u, 1u, (uint32_t)kBK, 1u};
+    if (!encode_tmap(&tm_w, dt, 4, a.b, w_dims, w_strides, w_box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   } else {  // W [K][R*S*Cg]: boxes of 64 reduction elements x BN output channels
-    const uint64_t w_dims[2] = {(uint64_t)(s.r * s.s * s.cg), (uint64_t)s.k};
-    const uint64_t w_strides[1] = {(uint64_t)(s.r * s.s * s.cg) * 2u};
-    const uint32_t w_box[2] = {(uint32_t)kBK, (uint32_t)BN};
-    if (!encode_tmap(&tm_w, dt, 2, a.b, w_dims, w_strides, w_box, CU_TENSOR_MAP_SWIZZLE_128B))
+    const uint64_t w_dims[4] = {(uint64_t)(s.r * s.s * s.cg), (uint64_t)s.k, 1u, 1u};
+    const uint64_t w_strides[3] = {(uint64_t)(s.r * s.s * s.cg) * 2u, (uint64_t)(s.r * s.s * s.cg * s.k) * 2u,
+                                   (uint64_t)(s.r * s.s * s.cg * s.k) * 2u};
+    const uint32_t w_box[4] = {(uint32_t)kBK, (uint32_t)BN, 1u, 1u};
+    if (!encode_tmap(&tm_w, dt, 4, a.b, w_dims, w_strides, w_box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
   // Output map of the two-stage form's epilogue: the slabs (fp32) under
@@ -460,8 +570,12 @@ cudaError_t launch_typed(const Plan& p, const Args& a, CUtensorMapDataType dt, b
     auto kern = fwd_tc_kernel<TO, FMT, false, BN, MS, BMN>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
+    // The persistent form: at most one CTA per SM, each taking every
+    // gridDim-th unit; otherwise one CTA per unit.
+    const int sms = current_sm_count() > 0 ? current_sm_count() : 148;
+    const int64_t grid = Tile<BN, MS>::kPersist && ctas > sms ? sms : ctas;
     // Slab sigma starts at ws + sigma * E; the kernel indexes pixels within it.
-    kern<<<(unsigned)ctas, kThreads, smem, a.stream>>>(tm_x, tm_w, tm_y, static_cast<TO*>(a.out), a.ws, fp,
+    kern<<<(unsigned)grid, kThreads, smem, a.stream>>>(tm_x, tm_w, tm_y, static_cast<TO*>(a.out), a.ws, fp,
                                                       device_error_word());
     return cudaGetLastError();
   }

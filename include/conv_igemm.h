@@ -165,7 +165,9 @@ typedef struct conv_plan_info {
   int32_t ctas_per_sm;       /* resident stage-1 CTAs per SM the policy assumes */
   int64_t tiles;             /* output tiles of stage 1 */
   int64_t reduction_blocks;  /* reduction blocks; a pinned degree may not exceed it */
-  int64_t ctas;              /* stage-1 CTAs = tiles * S */
+  int64_t ctas;              /* stage-1 work units = tiles * S (one CTA each; the 256-wide
+                                tensor-core forward runs them on at most one persistent CTA
+                                per SM) */
   uint64_t workspace_bytes;  /* bytes the call needs (0 without stage 2, except the grouped
                                 forward's block-diagonal filter) */
   int32_t max_split;         /* largest degree a pinned request may ask of this kernel */
