@@ -30,6 +30,27 @@ constexpr int kCtasPerSm = 2;  // 2 x 256 threads x 128 registers fill the regis
 
 enum { kFwd = 0, kDgrad = 1, kWgrad = 2 };
 
+// Division of n < 2^31 by a divisor d in [1, 2^31] fixed at launch, as a
+// multiply-high and a shift (Granlund and Montgomery, "Division by Invariant
+// Integers using Multiplication", 1994, section 4): with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1, floor(n / d) = (mulhi(m, n) + n) >> l;
+// n < 2^31 keeps the sum inside 32 bits.
+struct DivU32 {
+  uint32_t d = 1, m = 1, l = 0;
+  DivU32() = default;
+  explicit DivU32(uint32_t dv) : d(dv) {
+    while ((1ull << l) < dv) ++l;
+    m = (uint32_t)((((1ull << 32) * ((1ull << l) - dv)) / dv) + 1);
+  }
+  __host__ __device__ __forceinline__ uint32_t div(uint32_t n) const {
+#ifdef __CUDA_ARCH__
+    return (__umulhi(m, n) + n) >> l;
+#else
+    return (uint32_t)((((uint64_t)m * n) >> 32) + n) >> l;
+#endif
+  }
+};
+
 struct FfParams {
   const float* a;  // forward: X; data gradient: dY; weight gradient: dY
   const float* b;  // forward and data gradient: W; weight gradient: X
