@@ -32,7 +32,8 @@
 // workspace and no fold launch. A second cluster barrier keeps every CTA (and
 // its shared memory) alive until its peers have read it.
 //
-// Warp roles: 0 TMA producer, 1 MMA issuer, 2 TMEM owner, 4-7 epilogue.
+// Warp roles: 0 TMA producer, 1 MMA issuer, 2 TMEM owner, 4-7 epilogue (and
+// 8-11, a second epilogue group, in the persistent form).
 #include "tc_store.cuh"
 #include "../kernel_entry.h"
 
@@ -40,6 +41,9 @@ namespace cig {
 namespace {
 
 constexpr int kThreads = 256;
+// The persistent form has two epilogue groups of four warps (warps 4-7 and
+// 8-11), which share each unit's column chunks.
+constexpr int kThreadsPersist = 384;
 constexpr int kBM = 128;
 constexpr int kBK = 64;                     // channels per reduction block (128 bytes of 16-bit)
 constexpr int kA = kBM * 128;               // A tile bytes (128 rows x 128 B)
@@ -125,7 +129,7 @@ __device__ __forceinline__ void store4<__half>(__half* dst, float4 v) {
 // W'[c][r'][s'][k] = W[k][R-1-r'][S-1-s'][c]. Each stage then holds BN / 64
 // atoms of 64 output channels x 64 reduction rows (128B-swizzled, 8 KB apart).
 template <typename TO, uint32_t FMT, bool CL, int BN, int MS, bool BMN = false>
-__global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
+__global__ void __launch_bounds__(BN == 256 ? kThreadsPersist : kThreads, BN == 256 ? 1 : 2)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                   const __grid_constant__ CUtensorMap tm_y, TO* out, float* ws, FwdParams fp, unsigned* err) {
   using T = Tile<BN, MS>;
@@ -155,14 +159,17 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
     int64_t img, ho0, k0, b0, nblk;
     int32_t sigma;
   };
+  // (units, tiles and their factors fit 32 bits: the host launches at most
+  // 2^31 - 1 units; 32-bit divisions keep this off the loads' critical path)
   auto unit_of = [&](int64_t u) {
     Unit w;
-    const int64_t tile = CL ? u / fp.split : u % fp.tiles;
-    w.sigma = CL ? (int32_t)cluster_ctarank() : (int32_t)(u / fp.tiles);
-    const int64_t tn = tile % fp.tiles_n, tm = tile / fp.tiles_n;
-    w.img = tm / fp.tiles_m_per_img;
-    w.ho0 = (tm % fp.tiles_m_per_img) * fp.TR * MS;  // sub-tile h starts at row ho0 + h * TR
-    w.k0 = tn * BN;
+    const uint32_t u32 = (uint32_t)u, nt = (uint32_t)fp.tiles, ntn = (uint32_t)fp.tiles_n;
+    const uint32_t tile = CL ? u32 / (uint32_t)fp.split : u32 % nt;
+    w.sigma = CL ? (int32_t)cluster_ctarank() : (int32_t)(u32 / nt);
+    const uint32_t tn = tile % ntn, tm = tile / ntn, tmi = (uint32_t)fp.tiles_m_per_img;
+    w.img = tm / tmi;
+    w.ho0 = (int64_t)(tm % tmi) * fp.TR * MS;  // sub-tile h starts at row ho0 + h * TR
+    w.k0 = (int64_t)tn * BN;
     w.b0 = slice_begin(fp.blocks, fp.split, w.sigma);
     w.nblk = slice_begin(fp.blocks, fp.split, w.sigma + 1) - w.b0;
     return w;
@@ -181,8 +188,8 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
   int32_t cb, rs, r, sx;
   auto unit_start = [&]() {
     pj = 0;
-    cb = (int32_t)(pw.b0 % fp.cblocks);
-    rs = (int32_t)(pw.b0 / fp.cblocks);
+    cb = (int32_t)((uint32_t)pw.b0 % (uint32_t)cblocks);
+    rs = (int32_t)((uint32_t)pw.b0 / (uint32_t)cblocks);
     r = rs / sf;
     sx = rs % sf;
   };
@@ -203,7 +210,6 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
   constexpr int kLoads = MS + (BMN ? BN / 64 : 1);
   auto issue = [&]() {
     uint8_t* st = smem + (size_t)ps * kStage;
-    if (lane == 0) mbar_arrive_expect_tx(&full[ps], tx);
     if (lane < kLoads) {
       const bool is_a = lane < MS;
       const int j = lane - MS;  // B piece
@@ -240,6 +246,12 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
     }
   };
 
+  // A full barrier's one arrival (with the stage's byte count) is made ahead
+  // of its loads: here for the first round, then by the MMA thread as soon
+  // as it has seen the previous round's bytes land. The producer only waits
+  // for a free stage and issues its copies (an expect-tx just before the
+  // copies on the same barrier cost the issuing thread several hundred
+  // cycles a block).
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
@@ -247,10 +259,11 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tmem_full[i], 1);
-      mbar_init(&tmem_empty[i], 1);
+      mbar_init(&tmem_empty[i], kPersist ? 2 : 1);  // one arrival per epilogue group
     }
     *abort_flag = 0u;
     mbar_fence_init();
+    for (int i = 0; i < kStages; ++i) mbar_arrive_expect_tx(&full[i], tx);
     tma_prefetch(&tm_x);
     tma_prefetch(&tm_w);
   }
@@ -301,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
             live = false;
             break;
           }
+          mbar_arrive_expect_tx(&full[s], tx);  // arms the stage's next round
           tc_fence_after();
           const uint32_t a = base + (uint32_t)(s * kStage), b = a + MS * kA;
 #pragma unroll
@@ -328,7 +342,9 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
       }
     }
   } else if (warp >= 4) {
-    const int q = warp - 4;
+    constexpr int NG = kPersist ? 2 : 1;  // epilogue groups of four warps
+    const int g = NG == 2 ? (warp - 4) / 4 : 0;
+    const int q = warp % 4;       // TMEM lane quarter of the warp
     const int m = 32 * q + lane;  // tile row = output pixel within the tile
     int64_t i = 0;
     for (int64_t u = u_first; u < units; u += ustride, ++i) {
@@ -364,46 +380,64 @@ __global__ void __launch_bounds__(kThreads, BN == 256 ? 1 : 2)
         // persistent CTA use its own two, as the ring keeps loading. The
         // epilogue's bias for the unit's BN channels, fp32 in shared memory
         // past the staging buffers (0 beyond K or without a bias).
+        // With two groups, group g takes the chunks g, g + 2, ... through its
+        // half of the buffers.
         const bool in_ring = !kPersist || u + ustride >= units;
-        uint8_t* stage = in_ring ? smem : smem + (size_t)kStages * kStage;
-        float* sbias = reinterpret_cast<float*>(stage + (in_ring ? T::kEpiBufs : T::kOwnEpiBufs) * kBM * 128);
+        const int nbufs = in_ring ? T::kEpiBufs : T::kOwnEpiBufs;
+        uint8_t* stage0 = in_ring ? smem : smem + (size_t)kStages * kStage;
+        uint8_t* stage = stage0 + (size_t)g * (nbufs / NG) * kBM * 128;
+        float* sbias = reinterpret_cast<float*>(stage0 + (size_t)nbufs * kBM * 128);
         if (!ws && fp.ep) {
           const TO* bias = static_cast<const TO*>(fp.ep_bias);
-          for (int c = threadIdx.x - 128; c < BN; c += 128)
+          named_bar_sync(NG == 2 ? 3 : 1, 128 * NG);  // every group is done with the previous unit's bias
+          for (int c = threadIdx.x - 128; c < BN; c += 128 * NG)
             sbias[c] = bias && w.k0 + c < fp.K ? to_f32(bias[w.k0 + c]) : 0.f;
-          named_bar_sync(1, 128);
+          named_bar_sync(NG == 2 ? 3 : 1, 128 * NG);
         }
+        // Sub-tiles inside the image (a sub-tile past it is not stored); each
+        // group releases the accumulator after its last read of the last one,
+        // and waits for global completion of its stores only at the CTA's
+        // last unit.
+        const int nsub = (int)((fp.Ho - w.ho0 + fp.TR - 1) / fp.TR) < MS ? (int)((fp.Ho - w.ho0 + fp.TR - 1) / fp.TR)
+                                                                           : MS;
+        const bool last_unit = !kPersist || u + ustride >= units;
 #pragma unroll 1
-        for (int h = 0; h < MS; ++h) {
+        for (int h = 0; h < nsub; ++h) {
           const int64_t hrow = w.ho0 + h * fp.TR;
-          if (hrow >= fp.Ho) break;  // a sub-tile past the image (uniform over the 128 threads)
+          uint64_t* rel = kPersist && h == nsub - 1 ? &tmem_empty[buf] : nullptr;
           const int32_t py = (int32_t)(hrow * fp.Wo);
           // the box {chunk, TR*Wo pixels, 1} at (channel, first pixel, image), clipped at K and Ho*Wo
           const int32_t pz = ws ? (int32_t)(w.sigma * fp.N + w.img) : (int32_t)w.img;
           auto store = [&](const void* sb, int32_t x) { tma_store_3d(&tm_y, sb, x, py, pz); };
           const uint32_t acc = trow + (uint32_t)(h * BN);
-          const bool lead = threadIdx.x == 128;
+          const bool lead = threadIdx.x == 128 + 128 * g;
+          const bool epi = !ws && fp.ep != 0;
           if (ws) {
             if (in_ring)
-              store_rows_tma<float, T::kEpiBufs>(acc, stage, BN, (int32_t)w.k0, (int32_t)fp.K, m, w.nblk > 0, lead,
-                                                 ok, store);
+              store_rows_tma<float, T::kEpiBufs / NG>(acc, stage, BN, (int32_t)w.k0, (int32_t)fp.K, m, w.nblk > 0,
+                                                      lead, ok, store, nullptr, 0.f, 0.f, false, g, NG, 1 + g, rel,
+                                                      last_unit);
             else
-              store_rows_tma<float, T::kOwnEpiBufs>(acc, stage, BN, (int32_t)w.k0, (int32_t)fp.K, m, w.nblk > 0,
-                                                    lead, ok, store);
+              store_rows_tma<float, T::kOwnEpiBufs / NG>(acc, stage, BN, (int32_t)w.k0, (int32_t)fp.K, m,
+                                                         w.nblk > 0, lead, ok, store, nullptr, 0.f, 0.f, false, g,
+                                                         NG, 1 + g, rel, last_unit);
           } else {
             if (in_ring)
-              store_rows_tma<TO, T::kEpiBufs>(acc, stage, BN, (int32_t)w.k0, (int32_t)fp.K, m, w.nblk > 0, lead, ok,
-                                              store, sbias, fp.ep_lo, fp.ep_hi, fp.ep != 0);
+              store_rows_tma<TO, T::kEpiBufs / NG>(acc, stage, BN, (int32_t)w.k0, (int32_t)fp.K, m, w.nblk > 0,
+                                                   lead, ok, store, sbias, fp.ep_lo, fp.ep_hi, epi, g, NG, 1 + g, rel,
+                                                   last_unit);
             else
-              store_rows_tma<TO, T::kOwnEpiBufs>(acc, stage, BN, (int32_t)w.k0, (int32_t)fp.K, m, w.nblk > 0, lead,
-                                                 ok, store, sbias, fp.ep_lo, fp.ep_hi, fp.ep != 0);
+              store_rows_tma<TO, T::kOwnEpiBufs / NG>(acc, stage, BN, (int32_t)w.k0, (int32_t)fp.K, m, w.nblk > 0,
+                                                      lead, ok, store, sbias, fp.ep_lo, fp.ep_hi, epi, g, NG, 1 + g,
+                                                      rel, last_unit);
           }
         }
       }
-      // every TMEM read of this unit is done: the accumulator is free again
-      tc_fence_before();
-      named_bar_sync(1, 128);
-      if (threadIdx.x == 128) mbar_arrive(&tmem_empty[buf]);
+      if (!kPersist) {  // every TMEM read of the unit is done: the accumulator is free again
+        tc_fence_before();
+        named_bar_sync(1, 128);
+        if (threadIdx.x == 128) mbar_arrive(&tmem_empty[buf]);
+      }
     }
   }
 
@@ -575,7 +609,8 @@ cudaError_t launch_typed(const Plan& p, const Args& a, CUtensorMapDataType dt, b
     const int sms = current_sm_count() > 0 ? current_sm_count() : 148;
     const int64_t grid = Tile<BN, MS>::kPersist && ctas > sms ? sms : ctas;
     // Slab sigma starts at ws + sigma * E; the kernel indexes pixels within it.
-    kern<<<(unsigned)grid, kThreads, smem, a.stream>>>(tm_x, tm_w, tm_y, static_cast<TO*>(a.out), a.ws, fp,
+    kern<<<(unsigned)grid, BN == 256 ? kThreadsPersist : kThreads, smem, a.stream>>>(tm_x, tm_w, tm_y,
+                                                                                      static_cast<TO*>(a.out), a.ws, fp,
                                                       device_error_word());
     return cudaGetLastError();
   }

@@ -50,21 +50,31 @@ __device__ __forceinline__ uint4 pack16<__half>(const float* v) {
 // CTA per SM these four warps issue every one of them. With two buffers a
 // chunk waited for the store of the chunk before last to finish reading its
 // buffer (the 128 KB fp32 partial tile of a split-K CTA took ~2.5 us); more
-// buffers keep more stores in flight.
+// buffers keep more stores in flight. Several groups of four warps may share
+// the columns: group g takes chunks g, g + c_step, ... through its own
+// buffers, leader and named barrier bar_id. With tmem_release, the leader
+// arrives on that barrier once every thread of the group has read its last
+// accumulator column (the accumulator may then be overwritten while the
+// stores still run); with wait_global false the call returns once the
+// stores have read the staging buffers, not once they reached global memory.
 template <typename TE, int NBUF = 2, typename StoreFn>
 __device__ __forceinline__ void store_rows_tma(uint32_t trow, uint8_t* stage, int ncols, int32_t x0, int32_t x_end,
                                                int m, bool have_acc, bool leader, bool do_store, StoreFn store,
                                                const float* ep_bias = nullptr, float ep_lo = 0.f, float ep_hi = 0.f,
-                                               bool ep = false) {
+                                               bool ep = false, int c_first = 0, int c_step = 1,
+                                               uint32_t bar_id = 1, uint64_t* tmem_release = nullptr,
+                                               bool wait_global = true) {
   constexpr int CW = 128 / (int)sizeof(TE);  // values per 128-byte chunk
   constexpr int VPU = 16 / (int)sizeof(TE);  // values per 16-byte unit
   const int nch = min(ncols / CW, (x_end - x0 + CW - 1) / CW);
+  int i = 0;  // this group's chunk count
+  if (tmem_release && c_first >= nch && leader) mbar_arrive(tmem_release);  // no chunk for this group
 #pragma unroll 1
-  for (int c = 0; c < nch; ++c) {
-    uint8_t* buf = stage + (c % NBUF) * (128 * 128);
-    if (c >= NBUF) {  // the store that last read this buffer (chunk c - NBUF) must be done reading
+  for (int c = c_first; c < nch; c += c_step, ++i) {
+    uint8_t* buf = stage + (i % NBUF) * (128 * 128);
+    if (i >= NBUF) {  // the store that last read this buffer (this group's chunk i - NBUF) must be done reading
       if (leader) bulk_wait_read<NBUF - 1>();
-      named_bar_sync(1, 128);
+      named_bar_sync(bar_id, 128);
     }
     float v[CW];
 #pragma unroll
@@ -94,14 +104,20 @@ __device__ __forceinline__ void store_rows_tma(uint32_t trow, uint8_t* stage, in
       st_shared_v4(row + ((u ^ (m & 7)) << 4), pk.x, pk.y, pk.z, pk.w);
     }
     fence_proxy_async_smem();
-    named_bar_sync(1, 128);
+    const bool last = c + c_step >= nch;
+    if (tmem_release && last) tc_fence_before();
+    named_bar_sync(bar_id, 128);
+    if (leader && tmem_release && last) mbar_arrive(tmem_release);
     if (leader && do_store) {
       store(buf, x0 + c * CW);
       bulk_commit();
     }
   }
-  if (leader) bulk_wait<0>();
-  named_bar_sync(1, 128);  // the staging buffers are free again for a next call
+  if (leader) {
+    if (wait_global) bulk_wait<0>();
+    else bulk_wait_read<0>();
+  }
+  named_bar_sync(bar_id, 128);  // the staging buffers are free again for a next call
 }
 
 // TMA tensor store of a 4-D box from shared memory (clipped at the tensor's
