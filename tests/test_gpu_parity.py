@@ -341,6 +341,37 @@ def test_forward_fused_epilogue(shape, dt):
     assert cig.device_errors() == 0
 
 
+# ------------------------------------------------------- persistent forward
+
+
+@pytest.mark.parametrize("dt", [(BF16, BF16), (F16, F32)], ids=lambda d: f"{d[0]}{d[1]}")
+def test_persistent_forward_units(dt):
+    """The 256-wide tensor-core forward runs persistent: with more work units than SMs a CTA takes several
+    (tile, slice) units in turn, its two TMEM accumulators alternating and its two epilogue groups sharing
+    each unit's column chunks. K = 320 leaves the last channel tile a single 64-channel chunk (the second
+    epilogue group stores nothing there). Every element against the oracle at pinned degrees 3 and 4 (168
+    and 224 units), unsplit, with the data gradient of the layer with C and K swapped (the same forward form);
+    then 168 unsplit units with the fused
+    bias + ReLU, which a CTA reloads per unit."""
+    p = cig.Problem(n=4, h=28, w=28, c=64, k=320, r=3, s=3, pad_h=1, pad_w=1, in_dtype=dt[0], out_dtype=dt[1])
+    info = cig.describe_plan(p, cig.DIR_FWD, 4)
+    assert info["kernel_name"] == "fwd_tc" and info["ctas"] == 56 * 4, info  # 28 row tiles x 2 channel tiles x 4
+    check_fwd(p, 31, ["auto"], [-1, 1, 3, 4], "normal", 0.0, 0.05)
+    pd = cig.Problem(n=4, h=28, w=28, c=320, k=64, r=3, s=3, pad_h=1, pad_w=1, in_dtype=dt[0], out_dtype=dt[1])
+    assert cig.describe_plan(pd, cig.DIR_DGRAD, 4)["kernel_name"] == "dgrad_tc"
+    check_dgrad(pd, 32, ["auto"], [-1, 1, 3, 4], "normal", 0.0, 0.05)
+    p12 = cig.Problem(n=12, h=28, w=28, c=64, k=320, r=3, s=3, pad_h=1, pad_w=1, in_dtype=dt[0], out_dtype=dt[1])
+    assert cig.describe_plan(p12, cig.DIR_FWD, 1)["ctas"] == 168
+    x, w = inputs(p12, 33, "normal", 0.0, 0.05, cig.DIR_FWD)
+    bias = synth.tensor((p12.k,), TORCH_DT[p12.out_dtype], "normal", 0.0, 0.1, 33, synth.BIAS_ID)
+    orc = oracle.get()
+    ref = orc.fwd_epilogue(oproblem(p12), x, w, bias, 0.0, INF)
+    scale = np.abs(orc.fwd_epilogue(oproblem(p12), x, w, bias)).max()
+    got = run_fwd_ep(p12, x, w, bias, 0.0, INF, 1).double().numpy()
+    assert np.abs(got - ref).max() / scale <= tol(p12)
+    assert cig.device_errors() == 0
+
+
 # ------------------------------------------------------------- data gradient
 
 
