@@ -12,10 +12,14 @@
 // input positions the tile's outputs read through tap (r, s): coordinates
 // outside the image read zeros, which is exactly the zero padding, and the
 // box lands as TR*Wo rows of 128 bytes in the 128B-swizzled K-major layout
-// the MMA reads. B is a 2-D box {64, BN} of W viewed as [K][R*S*C].
+// the MMA reads. B is a box {64, BN} of W viewed as [K][R*S*C].
+//
+// Work units are (tile, slice) pairs. The 256-wide two-stage form runs
+// persistent: at most one CTA per SM, each taking units in turn with its ring
+// streaming on across them (see Tile).
 //
 // Split-K ("feat(rocke): split-K forward implicit-GEMM convolution on
-// gfx1250", "Two-stage split-K"): CTA (tile, sigma) reduces the blocks of
+// gfx1250", "Two-stage split-K"): unit (tile, sigma) reduces the blocks of
 // slice sigma and stores its fp32 partial tile into slab sigma of the
 // workspace, every element written once; the fold kernel sums the slabs in
 // slice order and rounds into Y. With one slice the epilogue rounds straight
