@@ -441,3 +441,13 @@ def test_fp32_ffma_tiles_selection():
     # 16-bit inputs never take the fp32 tiles
     b = Problem(n=2, h=8, w=8, c=8, k=8, r=3, s=3, in_dtype=BF16, out_dtype=BF16)
     assert cig.describe_plan(b, DIR_FWD, -1, sm_count=SMS)["kernel_name"] != "ffma"
+    # the tiles' spatial index arithmetic is 32-bit: a row whose padded width reaches 2^31, or a weight
+    # gradient with 2^31 - 16 output pixels or more, keeps the generic kernel (no memory is touched here)
+    wide = Problem(n=1, h=1, w=2**31 - 2, c=4, k=4, r=1, s=3, pad_w=1)
+    for d in (DIR_FWD, DIR_WGRAD):
+        assert cig.describe_plan(wide, d, -1, sm_count=SMS)["kernel_name"] == "generic", d
+    narrower = Problem(n=1, h=1, w=2**31 - 4, c=4, k=4, r=1, s=3, pad_w=1)  # W + 2 pw = 2^31 - 2
+    assert cig.describe_plan(narrower, DIR_FWD, -1, sm_count=SMS)["kernel_name"] == "ffma"
+    many = Problem(n=2**16, h=2**7, w=2**8 - 1, c=4, k=4)  # 2^31 - 2^23 output pixels: still 32-bit
+    assert cig.describe_plan(many, DIR_WGRAD, -1, sm_count=SMS)["kernel_name"] in ("ffma", "wgrad_1x1_tf32x3",
+                                                                                   "wgrad_1x1_ffma")
