@@ -749,3 +749,48 @@ def test_ffma_fp32_exact_on_small_integers():
             assert np.array_equal(db.double().numpy(), orc.bgrad(oproblem(p), dy)), sk
     finally:
         cig.set_kernel_override("auto")
+
+
+# ------------------------------------------------------------- staged calls
+
+STAGED = [  # (problem, direction): kernels with and without a fold, every direction
+    (dict(n=1, h=14, w=14, c=256, k=512, r=3, s=3, pad_h=1, pad_w=1, in_dtype=BF16, out_dtype=BF16), cig.DIR_FWD),
+    (dict(n=4, h=28, w=28, c=64, k=320, r=3, s=3, pad_h=1, pad_w=1, in_dtype=BF16, out_dtype=BF16), cig.DIR_FWD),
+    (dict(n=1, h=14, w=14, c=512, k=256, r=3, s=3, pad_h=1, pad_w=1, in_dtype=F16, out_dtype=F32), cig.DIR_DGRAD),
+    (dict(n=2, h=16, w=16, c=64, k=128, r=3, s=3, pad_h=1, pad_w=1, in_dtype=BF16, out_dtype=BF16), cig.DIR_WGRAD),
+    (dict(n=2, h=12, w=12, c=16, k=32, r=3, s=3, pad_h=1, pad_w=1), cig.DIR_WGRAD),                     # fp32 FFMA
+    (dict(n=2, h=20, w=20, c=64, k=64, groups=64, r=7, s=7, pad_h=3, pad_w=3, in_dtype=BF16, out_dtype=BF16),
+     cig.DIR_WGRAD),                                                                                   # depthwise
+]
+
+
+@pytest.mark.parametrize("case", STAGED, ids=lambda c: f"{c[1]}-{c[0]['c']}x{c[0]['k']}")
+def test_staged_calls_equal_one_call(case):
+    """conv_stage1 then conv_stage2 with the same arguments is the one call, bit for bit (same kernels, same
+    degree), at the automatic degree, degree 1 (stage 2 enqueues nothing) and a pinned degree with a fold."""
+    shape, d = case
+    p = cig.Problem(**shape)
+    a, b = inputs(p, 41, "normal", 0.0, 0.05, d)
+    a, b = a.cuda(), b.cuda()
+    ho, wo = p.out_hw
+    odt = TORCH_DT[p.out_dtype]
+    n_out = {cig.DIR_FWD: p.n * ho * wo * p.k, cig.DIR_DGRAD: p.n * p.h * p.w * p.c,
+             cig.DIR_WGRAD: p.k * p.r * p.s * (p.c // p.groups)}[d]
+    bias = d == cig.DIR_WGRAD
+    for sk in (-1, 1, 2):
+        ws = cig.workspace(p, d, sk, bias)
+        one, db1 = torch.empty(n_out, dtype=odt, device="cuda"), torch.empty(p.k, dtype=odt, device="cuda")
+        two, db2 = torch.full((n_out,), float("nan"), dtype=odt, device="cuda"), torch.full((p.k,), float("nan"), dtype=odt, device="cuda")
+        if d == cig.DIR_FWD:
+            cig.conv_fwd(p, a, b, one, ws, sk)
+        elif d == cig.DIR_DGRAD:
+            cig.conv_dgrad(p, a, b, one, ws, sk)
+        else:
+            cig.conv_wgrad_bias(p, a, b, one, db1, ws, sk)
+        cig.conv_stage1(p, d, a, b, two, db2 if bias else None, ws, sk)
+        cig.conv_stage2(p, d, two, db2 if bias else None, ws, sk)
+        torch.cuda.synchronize()
+        assert torch.equal(one.view(torch.uint8), two.view(torch.uint8)), (d, sk)
+        if bias:
+            assert torch.equal(db1.view(torch.uint8), db2.view(torch.uint8)), (d, sk)
+    assert cig.device_errors() == 0
