@@ -794,3 +794,64 @@ def test_staged_calls_equal_one_call(case):
         if bias:
             assert torch.equal(db1.view(torch.uint8), db2.view(torch.uint8)), (d, sk)
     assert cig.device_errors() == 0
+
+
+# ------------------------------------------------------------- CUDA graphs
+
+
+@pytest.mark.parametrize("case", STAGED, ids=lambda c: f"{c[1]}-{c[0]['c']}x{c[0]['k']}")
+def test_calls_capture_into_a_cuda_graph(case):
+    """A call (stage 1 and the fold, PDL-linked) captured into a CUDA graph replays to the eager result, bit
+    for bit, at a pinned degree with a fold; the graph replays again after the inputs change in place."""
+    shape, d = case
+    p = cig.Problem(**shape)
+    a, b = inputs(p, 43, "normal", 0.0, 0.05, d)
+    a, b = a.cuda(), b.cuda()
+    ho, wo = p.out_hw
+    odt = TORCH_DT[p.out_dtype]
+    n_out = {cig.DIR_FWD: p.n * ho * wo * p.k, cig.DIR_DGRAD: p.n * p.h * p.w * p.c,
+             cig.DIR_WGRAD: p.k * p.r * p.s * (p.c // p.groups)}[d]
+    bias = d == cig.DIR_WGRAD
+    sk = 2
+    ws = cig.workspace(p, d, sk, bias)
+    out = torch.empty(n_out, dtype=odt, device="cuda")
+    db = torch.empty(p.k, dtype=odt, device="cuda") if bias else None
+
+    def call():
+        if d == cig.DIR_FWD:
+            cig.conv_fwd(p, a, b, out, ws, sk)
+        elif d == cig.DIR_DGRAD:
+            cig.conv_dgrad(p, a, b, out, ws, sk)
+        else:
+            cig.conv_wgrad_bias(p, a, b, out, db, ws, sk)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()  # warm-up outside the capture (module, attributes, tensor maps)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    eager_db = db.clone() if bias else None
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    for trial in range(2):
+        out.fill_(float("nan"))
+        if bias:
+            db.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.uint8), eager.view(torch.uint8)), trial
+        if bias:
+            assert torch.equal(db.view(torch.uint8), eager_db.view(torch.uint8)), trial
+    # new inputs in place: the replay computes on them
+    a.mul_(-1)
+    g.replay()
+    torch.cuda.synchronize()
+    flipped = out.clone()
+    a.mul_(-1)
+    call()
+    torch.cuda.synchronize()
+    assert torch.equal(flipped.float(), -out.float()), "replay on negated inputs"
+    assert cig.device_errors() == 0
