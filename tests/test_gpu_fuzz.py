@@ -1,7 +1,8 @@
 """Seeded random shapes through every path the planner picks, against the oracle: forward and data
 gradient (tensor-core tiles, persistent or not, block-diagonal, generic), weight gradient (dense 16-bit
 tensor cores, fp32 FFMA tiles, grouped warp MMAs, depthwise rings, generic), at the automatic degree and
-pinned ones. The shapes are drawn from a fixed seed, so every run tests the same ones."""
+pinned ones; then grouped, depthwise, dilated and fp32 forwards and data gradients. The shapes are drawn
+from fixed seeds, so every run tests the same ones."""
 import random
 
 import pytest
@@ -62,6 +63,40 @@ def _wgrad_shapes(count, seed):
     return out
 
 
+def _other_fwd_shapes(count, seed):
+    """Grouped (4 or 8 channels a group: warp MMAs; 16 to 64: block-diagonal tiles), depthwise, dilated
+    16-bit and fp32 problems."""
+    rnd = random.Random(seed)
+    out = []
+    kinds = ["grouped_mma", "grouped_tc", "depthwise", "dilated16", "fp32"]
+    while len(out) < count:
+        kind = kinds[len(out) % len(kinds)]
+        st, dil = 1, 1
+        dt = rnd.choice([(cig.BF16, cig.BF16), (cig.F16, cig.F16), (cig.BF16, cig.F32)])
+        if kind == "grouped_mma":
+            cg, g, r = rnd.choice([4, 8]), rnd.choice([16, 32, 64]), rnd.choice([1, 3, 5])
+            c = k = cg * g
+        elif kind == "grouped_tc":
+            cg, g, r = rnd.choice([16, 32, 64]), rnd.choice([2, 4, 8]), rnd.choice([3, 5])
+            c = k = cg * g
+        elif kind == "depthwise":
+            c = k = g = rnd.choice([32, 64, 96, 128])
+            r, st = rnd.choice([3, 5, 7]), rnd.choice([1, 1, 2])
+        elif kind == "dilated16":
+            c, k, g, r, dil = rnd.choice([64, 128]), rnd.choice([128, 256]), 1, 3, rnd.choice([2, 3])
+        else:
+            c, k, g, r = rnd.choice([8, 24, 64]), rnd.choice([16, 40, 128]), 1, rnd.choice([1, 3])
+            st, dil, dt = rnd.choice([1, 2]), rnd.choice([1, 2]), (cig.F32, cig.F32)
+        ph = rnd.randint(0, dil * (r - 1))
+        pw = rnd.randint(0, dil * (r - 1))
+        p = cig.Problem(n=rnd.choice([1, 2, 4]), h=rnd.choice([8, 13, 16, 21]), w=rnd.choice([8, 11, 16, 24]), c=c, k=k,
+                        r=r, s=r, stride_h=st, stride_w=st, pad_h=ph, pad_w=pw, dil_h=dil, dil_w=dil, groups=g,
+                        in_dtype=dt[0], out_dtype=dt[1])
+        if min(p.out_hw) > 0 and p.flops() <= FLOP_CAP:
+            out.append(p)
+    return out
+
+
 def _top(p, direction, bias=False):
     """The largest degree a pinned request may take on this problem's kernel."""
     return cig.describe_plan(p, direction, -1, bias)["max_split"]
@@ -100,4 +135,23 @@ def test_fuzz_wgrad(i):
         if sk <= top:
             dw, db = run_wgrad(p, x, dy, sk, True)
             assert relerr(dw, ref) <= tol(p) and relerr(db, bref) <= tol(p), (p, sk)
+    assert cig.device_errors() == 0
+
+
+@pytest.mark.parametrize("i", range(30))
+def test_fuzz_other_forward_and_dgrad(i):
+    p = _other_fwd_shapes(30, 13)[i]
+    orc = oracle.get()
+    x, w = inputs(p, 350 + i, "normal", 0.0, 0.05, cig.DIR_FWD)
+    ref = orc.fwd(oproblem(p), x, w)
+    top = _top(p, cig.DIR_FWD)
+    for sk in (-1, 1, 2):
+        if sk <= top:
+            assert relerr(run_fwd(p, x, w, sk), ref) <= tol(p), (p, sk)
+    dy, w2 = inputs(p, 450 + i, "normal", 0.0, 0.05, cig.DIR_DGRAD)
+    dref = orc.dgrad(oproblem(p), dy, w2)
+    top = _top(p, cig.DIR_DGRAD)
+    for sk in (-1, 2):
+        if sk <= top:
+            assert relerr(run_dgrad(p, dy, w2, sk), dref) <= tol(p), (p, sk)
     assert cig.device_errors() == 0
