@@ -1,6 +1,6 @@
 // Epilogue of the tensor-core kernels: a 128-row fp32 accumulator in tensor
 // memory goes out through shared memory and TMA tensor stores, optionally
-// with a bias + clamp applied to the fp32 values before the one rounding.
+// with a bias added to the fp32 values and the result clamped.
 #pragma once
 
 #include <cstring>
@@ -35,6 +35,35 @@ __device__ __forceinline__ uint4 pack16<__half>(const float* v) {
   return r;
 }
 
+// Packed 16-bit values clamped to [lo, hi] (packed the same way); a NaN
+// becomes lo, as with fminf(fmaxf(x, lo), hi).
+template <typename TE>
+__device__ __forceinline__ uint4 clamp16(uint4 x, uint4 lo, uint4 hi);
+template <>
+__device__ __forceinline__ uint4 clamp16<__nv_bfloat16>(uint4 x, uint4 lo, uint4 hi) {
+  __nv_bfloat162 v[4], l[4], h[4];
+  memcpy(v, &x, 16);
+  memcpy(l, &lo, 16);
+  memcpy(h, &hi, 16);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __hmin2(__hmax2(v[i], l[i]), h[i]);
+  memcpy(&x, v, 16);
+  return x;
+}
+template <>
+__device__ __forceinline__ uint4 clamp16<__half>(uint4 x, uint4 lo, uint4 hi) {
+  __half2 v[4], l[4], h[4];
+  memcpy(v, &x, 16);
+  memcpy(l, &lo, 16);
+  memcpy(h, &hi, 16);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __hmin2(__hmax2(v[i], l[i]), h[i]);
+  memcpy(&x, v, 16);
+  return x;
+}
+template <>
+__device__ __forceinline__ uint4 clamp16<float>(uint4 x, uint4, uint4) { return x; }
+
 // The 128 epilogue threads (named barrier 1) store the accumulator columns
 // [0, ncols) of their rows: thread m owns tensor-memory lane m (trow already
 // carries the warp's lane offset). For each 128-byte column chunk (32 fp32 or
@@ -46,7 +75,8 @@ __device__ __forceinline__ uint4 pack16<__half>(const float* v) {
 // Only chunks that start below x_end are stored (each then commits exactly
 // one bulk group, which the buffer-reuse wait counts on). With ep, the bias
 // (fp32 in shared memory, one per column) is added and the value clamped to
-// [ep_lo, ep_hi] before the rounding. Few instructions per thread: with one
+// [ep_lo, ep_hi] (fp32 outputs before the rounding, 16-bit ones after it).
+// Few instructions per thread: with one
 // CTA per SM these four warps issue every one of them. With two buffers a
 // chunk waited for the store of the chunk before last to finish reading its
 // buffer (the 128 KB fp32 partial tile of a split-K CTA took ~2.5 us); more
@@ -67,6 +97,17 @@ __device__ __forceinline__ void store_rows_tma(uint32_t trow, uint8_t* stage, in
   constexpr int CW = 128 / (int)sizeof(TE);  // values per 128-byte chunk
   constexpr int VPU = 16 / (int)sizeof(TE);  // values per 16-byte unit
   const int nch = min(ncols / CW, (x_end - x0 + CW - 1) / CW);
+  // 16-bit outputs are clamped after the rounding, with packed min/max
+  // against the rounded bounds: the same values, as rounding to nearest is
+  // monotone (and a NaN still becomes ep_lo).
+  constexpr bool k16 = sizeof(TE) == 2;
+  uint4 lo16 = {}, hi16 = {};
+  if (k16 && ep) {
+    const float lo8[8] = {ep_lo, ep_lo, ep_lo, ep_lo, ep_lo, ep_lo, ep_lo, ep_lo};
+    const float hi8[8] = {ep_hi, ep_hi, ep_hi, ep_hi, ep_hi, ep_hi, ep_hi, ep_hi};
+    lo16 = pack16<TE>(lo8);
+    hi16 = pack16<TE>(hi8);
+  }
   int i = 0;  // this group's chunk count
   if (tmem_release && c_first >= nch && leader) mbar_arrive(tmem_release);  // no chunk for this group
 #pragma unroll 1
@@ -91,16 +132,25 @@ __device__ __forceinline__ void store_rows_tma(uint32_t trow, uint8_t* stage, in
 #pragma unroll
       for (int i = 0; i < CW; i += 4) {
         const float4 b = b4[i / 4];
-        v[i] = fminf(fmaxf(v[i] + b.x, ep_lo), ep_hi);
-        v[i + 1] = fminf(fmaxf(v[i + 1] + b.y, ep_lo), ep_hi);
-        v[i + 2] = fminf(fmaxf(v[i + 2] + b.z, ep_lo), ep_hi);
-        v[i + 3] = fminf(fmaxf(v[i + 3] + b.w, ep_lo), ep_hi);
+        const float2 lo = __fadd2_rn(make_float2(v[i], v[i + 1]), make_float2(b.x, b.y));
+        const float2 hi = __fadd2_rn(make_float2(v[i + 2], v[i + 3]), make_float2(b.z, b.w));
+        v[i] = lo.x;
+        v[i + 1] = lo.y;
+        v[i + 2] = hi.x;
+        v[i + 3] = hi.y;
+        if (!k16) {
+          v[i] = fminf(fmaxf(v[i], ep_lo), ep_hi);
+          v[i + 1] = fminf(fmaxf(v[i + 1], ep_lo), ep_hi);
+          v[i + 2] = fminf(fmaxf(v[i + 2], ep_lo), ep_hi);
+          v[i + 3] = fminf(fmaxf(v[i + 3], ep_lo), ep_hi);
+        }
       }
     }
     uint8_t* row = buf + m * 128;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const uint4 pk = pack16<TE>(v + u * VPU);
+      uint4 pk = pack16<TE>(v + u * VPU);
+      if (k16 && ep) pk = clamp16<TE>(pk, lo16, hi16);
       st_shared_v4(row + ((u ^ (m & 7)) << 4), pk.x, pk.y, pk.z, pk.w);
     }
     fence_proxy_async_smem();
