@@ -230,9 +230,12 @@ conv_status conv_wgrad(const conv_problem* p, const void* x, const void* dy, voi
                        uint64_t ws_bytes, int32_t split_k, void* stream);
 
 /* A fused forward epilogue: y = min(max(conv(x, w) + bias[k], lo), hi),
- * applied to the fp32 accumulator before the one rounding into out_dtype
- * [P2 "Review follow-ups": bias / ReLU / clamp are the non-identity
- * epilogues]. bias is [k] in out_dtype, or NULL for none; ReLU is
+ * with the bias added to the fp32 accumulator and one rounding into
+ * out_dtype [P2 "Review follow-ups": bias / ReLU / clamp are the
+ * non-identity epilogues]. The clamp gives the values it would give before
+ * the rounding (the tensor-core forward clamps 16-bit outputs after it,
+ * against the rounded bounds: rounding to nearest is monotone); a NaN sum
+ * becomes lo (the identity epilogue leaves it NaN). bias is [k] in out_dtype, or NULL for none; ReLU is
  * {lo = 0, hi = +inf}; {-inf, +inf} with no bias is the identity. lo <= hi,
  * neither NaN. */
 typedef struct conv_epilogue {

@@ -309,7 +309,7 @@ def run_fwd_ep(p, x, w, bias, lo, hi, split_k=-1):
     dict(n=2, h=10, w=12, c=128, k=128, groups=16, r=3, s=3, pad_h=1, pad_w=1),           # grouped, warp MMAs
     dict(n=2, h=8, w=8, c=128, k=128, groups=64, r=5, s=5, pad_h=2, pad_w=2),             # grouped, tensor cores
 ])
-@pytest.mark.parametrize("dt", [(BF16, BF16), (F16, F32), (F32, F32)], ids=lambda d: f"{d[0]}{d[1]}")
+@pytest.mark.parametrize("dt", [(BF16, BF16), (F16, F16), (F16, F32), (F32, F32)], ids=lambda d: f"{d[0]}{d[1]}")
 def test_forward_fused_epilogue(shape, dt):
     """Bias / ReLU / clamp fused into the unsplit forward ("feat(rocke): split-K forward
     implicit-GEMM convolution on gfx1250", "Review follow-ups"), against the oracle."""
@@ -317,7 +317,10 @@ def test_forward_fused_epilogue(shape, dt):
     x, w = inputs(p, 21, "normal", 0.0, 0.05, cig.DIR_FWD)
     bias = synth.tensor((p.k,), TORCH_DT[p.out_dtype], "normal", 0.0, 0.1, 21, synth.BIAS_ID)
     orc = oracle.get()
-    for use_bias, lo, hi in [(True, 0.0, INF), (True, -INF, INF), (False, 0.0, INF), (True, -0.05, 0.03)]:
+    # the last bounds lie past fp16's range: 16-bit outputs are clamped after the rounding, against
+    # the rounded (here infinite) bounds
+    for use_bias, lo, hi in [(True, 0.0, INF), (True, -INF, INF), (False, 0.0, INF), (True, -0.05, 0.03),
+                             (True, -7e4, 7e4)]:
         b = bias if use_bias else None
         ref = orc.fwd_epilogue(oproblem(p), x, w, b, lo, hi)
         # bias and clamp are exact; the error is the sum's, so it is measured against the
@@ -340,6 +343,31 @@ def test_forward_fused_epilogue(shape, dt):
     assert err.value.status == 1
     assert cig.device_errors() == 0
 
+
+
+@pytest.mark.parametrize("shape", [
+    dict(n=2, h=10, w=12, c=128, k=136, r=3, s=3, pad_h=1, pad_w=1),          # tensor cores
+    dict(n=2, h=9, w=11, c=12, k=8, r=3, s=3, stride_h=2, stride_w=2, pad_h=1, pad_w=1),  # generic
+    dict(n=2, h=13, w=17, c=96, k=96, groups=96, r=7, s=7, pad_h=3, pad_w=3),             # depthwise kernel
+    dict(n=2, h=10, w=12, c=128, k=128, groups=16, r=3, s=3, pad_h=1, pad_w=1),           # grouped, warp MMAs
+])
+@pytest.mark.parametrize("dt", [(BF16, BF16), (F16, F16), (BF16, F32)], ids=lambda d: f"{d[0]}{d[1]}")
+def test_forward_fused_epilogue_nan_becomes_lo(shape, dt):
+    """A NaN in X makes NaN sums; a non-identity epilogue turns each into lo, as fminf(fmaxf(nan, lo), hi)
+    does, in every kernel (the tensor-core forward clamps 16-bit outputs after the rounding)."""
+    p = cig.Problem(**shape, in_dtype=dt[0], out_dtype=dt[1])
+    x, w = inputs(p, 23, "normal", 0.0, 0.05, cig.DIR_FWD)
+    x[1, 4, 5, 3] = float("nan")
+    bias = synth.tensor((p.k,), TORCH_DT[p.out_dtype], "normal", 0.0, 0.1, 23, synth.BIAS_ID)
+    ref = oracle.get().fwd_epilogue(oproblem(p), x, w, bias, -0.05, 0.03)
+    nan = np.isnan(ref)
+    assert nan.any() and not nan.all()
+    got = run_fwd_ep(p, x, w, bias, -0.05, 0.03).double().numpy()
+    lo = torch.tensor(-0.05, dtype=TORCH_DT[p.out_dtype]).double().item()
+    assert (got[nan] == lo).all()
+    scale = np.abs(np.nan_to_num(oracle.get().fwd_epilogue(oproblem(p), x, w, bias))).max()
+    assert np.abs(got[~nan] - ref[~nan]).max() / scale <= tol(p)
+    assert cig.device_errors() == 0
 
 # ------------------------------------------------------- persistent forward
 
