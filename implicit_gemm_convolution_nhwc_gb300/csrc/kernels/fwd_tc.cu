@@ -110,6 +110,17 @@ struct FwdParams {
   int32_t ep;
 };
 
+// True when the phase with this parity has completed (never suspends).
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 template <typename TO>
 __device__ __forceinline__ void store4(TO* dst, float4 v);
 template <>
@@ -141,6 +152,11 @@ __global__ void __launch_bounds__(BN == 256 ? kThreadsPersist : kThreads, BN == 
   constexpr uint32_t kTmemCols = T::kTmemCols;
   constexpr bool kPersist = T::kPersist && !CL;
   constexpr int NACC = T::kAccs;  // TMEM accumulators (2: a unit's epilogue overlaps the next unit's MMAs)
+  // One accumulator of two M sub-tiles: the epilogue frees each sub-tile on its
+  // own (tmem_empty[h]), so the next unit's sub-tile 0 MMAs start while
+  // sub-tile 1 is still being read; its sub-tile 1 MMAs follow, for up to
+  // kStages held blocks.
+  constexpr bool kSplitRelease = kPersist && NACC == 1 && MS == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * kStage + T::kOwnEpi);
@@ -304,15 +320,34 @@ __global__ void __launch_bounds__(BN == 256 ? kThreadsPersist : kThreads, BN == 
       uint32_t ph = 0;
       bool live = true;  // false once a wait gave up: the units left only signal their (empty) accumulators
       int64_t i = 0;
+      // The MMAs of one block (ring stage st, the unit's block jb) into sub-tile h.
+      auto block_mmas = [&](int st, int64_t jb, int h, uint32_t dacc) {
+        const uint32_t a = base + (uint32_t)(st * kStage), b = a + MS * kA;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          // K-major SW128: 8-row groups 1024 B apart; a K step of 16 elements is
+          // a 32-byte advance inside the swizzled 128-byte row. MN-major SW128
+          // (BMN): atoms kAtom apart, 8-row groups 1024 B apart; a K step of 16
+          // rows is 2048 B.
+          const uint64_t bd =
+              BMN ? smem_desc_sw128(b + 2048u * kk, kAtom, 1024) : smem_desc_sw128(b + 32u * kk, 16, 1024);
+          mma_f16(dacc + (uint32_t)(h * BN), smem_desc_sw128(a + (uint32_t)(h * kA) + 32u * kk, 16, 1024), bd,
+                  IDESC, (jb > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
       for (int64_t u = u_first; u < units; u += ustride, ++i) {
         const int64_t nblk = unit_of(u).nblk;
         const int buf = (int)(i % NACC);
         const uint32_t use = (uint32_t)(i / NACC);
-        // the epilogue has drained this accumulator's previous unit
+        // the epilogue has drained this accumulator's previous unit (with one
+        // accumulator of two sub-tiles: its first sub-tile; the second is
+        // waited for below, while the first one's MMAs run)
         if (live && use > 0 && !mbar_wait(&tmem_empty[buf], (use - 1u) & 1u, abort_flag, err)) live = false;
         tc_fence_after();
         const uint32_t dacc = tmem + (uint32_t)buf * kTmemCols;
         bool any = false;
+        bool h1 = !kSplitRelease || use == 0;  // sub-tile 1 of the accumulator is free
+        int pend = 0;  // blocks before this one whose sub-tile 1 MMAs wait for it (their stages stay held)
         for (int64_t j = 0; live && j < nblk; ++j) {
           if (!mbar_wait(&full[s], ph, abort_flag, err)) {
             live = false;
@@ -320,25 +355,50 @@ __global__ void __launch_bounds__(BN == 256 ? kThreadsPersist : kThreads, BN == 
           }
           mbar_arrive_expect_tx(&full[s], tx);  // arms the stage's next round
           tc_fence_after();
-          const uint32_t a = base + (uint32_t)(s * kStage), b = a + MS * kA;
+          if (!kSplitRelease) {
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            // K-major SW128: 8-row groups 1024 B apart; a K step of 16 elements is
-            // a 32-byte advance inside the swizzled 128-byte row. MN-major SW128
-            // (BMN): atoms kAtom apart, 8-row groups 1024 B apart; a K step of 16
-            // rows is 2048 B.
-            const uint64_t bd =
-                BMN ? smem_desc_sw128(b + 2048u * kk, kAtom, 1024) : smem_desc_sw128(b + 32u * kk, 16, 1024);
-#pragma unroll
-            for (int h = 0; h < MS; ++h)
-              mma_f16(dacc + (uint32_t)(h * BN), smem_desc_sw128(a + (uint32_t)(h * kA) + 32u * kk, 16, 1024), bd,
-                      IDESC, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int h = 0; h < MS; ++h) block_mmas(s, j, h, dacc);
+            mma_commit(&empty[s]);
+          } else {
+            block_mmas(s, j, 0, dacc);
+            if (!h1) h1 = mbar_test(&tmem_empty[1], (use - 1u) & 1u);
+            if (!h1 && pend + 1 == kStages) {  // every stage is held: sub-tile 1 must be free now
+              if (!mbar_wait(&tmem_empty[1], (use - 1u) & 1u, abort_flag, err)) {
+                live = false;
+                break;
+              }
+              h1 = true;
+            }
+            if (h1) {
+              tc_fence_after();
+              for (int t = pend; t > 0; --t) {  // the held blocks first, in order
+                const int st = (s - t + kStages) % kStages;
+                block_mmas(st, j - t, 1, dacc);
+                mma_commit(&empty[st]);
+              }
+              block_mmas(s, j, 1, dacc);
+              mma_commit(&empty[s]);
+              pend = 0;
+            } else {
+              ++pend;
+            }
           }
-          mma_commit(&empty[s]);
           any = true;
           if (++s == kStages) {
             s = 0;
             ph ^= 1u;
+          }
+        }
+        if (kSplitRelease && live && pend > 0) {  // a unit of fewer blocks than stages
+          if (!mbar_wait(&tmem_empty[1], (use - 1u) & 1u, abort_flag, err)) {
+            live = false;
+          } else {
+            tc_fence_after();
+            for (int t = pend; t > 0; --t) {
+              const int st = (s - t + kStages) % kStages;
+              block_mmas(st, nblk - t, 1, dacc);
+              mma_commit(&empty[st]);
+            }
           }
         }
         if (any) mma_commit(&tmem_full[buf]);
@@ -399,7 +459,8 @@ __global__ void __launch_bounds__(BN == 256 ? kThreadsPersist : kThreads, BN == 
           named_bar_sync(NG == 2 ? 3 : 1, 128 * NG);
         }
         // Sub-tiles inside the image (a sub-tile past it is not stored); each
-        // group releases the accumulator after its last read of the last one,
+        // group releases the accumulator after its last read of the last one
+        // (of each one, with kSplitRelease; a sub-tile past the image at once),
         // and waits for global completion of its stores only at the CTA's
         // last unit.
         const int nsub = (int)((fp.Ho - w.ho0 + fp.TR - 1) / fp.TR) < MS ? (int)((fp.Ho - w.ho0 + fp.TR - 1) / fp.TR)
@@ -408,7 +469,7 @@ __global__ void __launch_bounds__(BN == 256 ? kThreadsPersist : kThreads, BN == 
 #pragma unroll 1
         for (int h = 0; h < nsub; ++h) {
           const int64_t hrow = w.ho0 + h * fp.TR;
-          uint64_t* rel = kPersist && h == nsub - 1 ? &tmem_empty[buf] : nullptr;
+          uint64_t* rel = kSplitRelease ? &tmem_empty[h] : kPersist && h == nsub - 1 ? &tmem_empty[buf] : nullptr;
           const int32_t py = (int32_t)(hrow * fp.Wo);
           // the box {chunk, TR*Wo pixels, 1} at (channel, first pixel, image), clipped at K and Ho*Wo
           const int32_t pz = ws ? (int32_t)(w.sigma * fp.N + w.img) : (int32_t)w.img;
@@ -436,6 +497,7 @@ __global__ void __launch_bounds__(BN == 256 ? kThreadsPersist : kThreads, BN == 
                                                       rel, last_unit);
           }
         }
+        if (kSplitRelease && nsub < 2 && threadIdx.x == 128 + 128 * g) mbar_arrive(&tmem_empty[1]);
       }
       if (!kPersist) {  // every TMEM read of the unit is done: the accumulator is free again
         tc_fence_before();

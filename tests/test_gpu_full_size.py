@@ -174,6 +174,46 @@ def test_two_m_subtiles_with_a_partial_second(direction):
     assert cig.device_errors() == 0
 
 
+@pytest.mark.parametrize("direction", ["fwd", "fwd_bias_relu", "dgrad"])
+def test_two_m_subtiles_the_last_pair_single(direction):
+    """128 images of 28x28 (K = C = 256, 3x3, pad 1, bf16): 512 double tiles of two M sub-tiles of 4
+    output rows, over 152 persistent CTAs (the accumulator of a unit freed one sub-tile at a time); each
+    image's last double tile holds rows 24..27 only, so its second sub-tile lies past the image.
+    Images 0, 1 and 127 against the oracle as N=1 problems."""
+    n, hw, c, k = 128, 28, 256, 256
+    p = cig.Problem(n=n, h=hw, w=hw, c=c, k=k, r=3, s=3, pad_h=1, pad_w=1, in_dtype=cig.BF16, out_dtype=cig.BF16)
+    p1 = cig.Problem(n=1, h=hw, w=hw, c=c, k=k, r=3, s=3, pad_h=1, pad_w=1, in_dtype=cig.BF16, out_dtype=cig.BF16)
+    w = synth.tensor((k, 3, 3, c), torch.bfloat16, "normal", 0.0, 0.05, 9, synth.W_ID)
+    bias = synth.tensor((k,), torch.bfloat16, "normal", 0.0, 0.1, 9, synth.BIAS_ID)
+    orc = oracle.get()
+    if direction != "dgrad":
+        info = cig.describe_plan(p, cig.DIR_FWD, -1)
+        assert info["kernel_name"] == "fwd_tc" and info["tiles"] == 4 * n and info["split_k"] == 1, info
+        a = synth.tensor((n, hw, hw, c), torch.bfloat16, "normal", 0.0, 0.05, 9, synth.X_ID)
+        out = torch.empty((n, hw, hw, k), dtype=torch.bfloat16, device="cuda")
+        if direction == "fwd":
+            cig.conv_fwd(p, a.cuda(), w.cuda(), out, cig.workspace(p, cig.DIR_FWD, -1, False), -1)
+        else:
+            cig.conv_fwd_epilogue(p, a.cuda(), w.cuda(), out, bias.cuda(), 0.0, float("inf"), None, -1)
+    else:
+        info = cig.describe_plan(p, cig.DIR_DGRAD, -1)
+        assert info["kernel_name"] == "dgrad_tc" and info["tiles"] == 4 * n and info["split_k"] == 1, info
+        a = synth.tensor((n, hw, hw, k), torch.bfloat16, "normal", 0.0, 0.05, 9, synth.DY_ID)
+        out = torch.empty((n, hw, hw, c), dtype=torch.bfloat16, device="cuda")
+        cig.conv_dgrad(p, a.cuda(), w.cuda(), out, cig.workspace(p, cig.DIR_DGRAD, -1, False), -1)
+    torch.cuda.synchronize()
+    got = out.cpu()
+    for i in (0, 1, 127):
+        if direction == "fwd":
+            ref = orc.fwd(oproblem(p1), a[i:i + 1], w)
+        elif direction == "fwd_bias_relu":
+            ref = orc.fwd_epilogue(oproblem(p1), a[i:i + 1], w, bias, 0.0, float("inf"))
+        else:
+            ref = orc.dgrad(oproblem(p1), a[i:i + 1], w)
+        e = relerr(got[i:i + 1], ref)
+        assert e <= 1e-2, f"{direction} image {i}: err {e:.3e}"
+    assert cig.device_errors() == 0
+
 def test_depthwise_7x7_forward_full_sampled_images():
     """Depthwise 7x7 forward bf16, N=32, 56x56, C=K=384, pad 3 (the depthwise configuration's
     forward twin), auto: images 0, 17 and 31 against the oracle as N=1 problems."""
