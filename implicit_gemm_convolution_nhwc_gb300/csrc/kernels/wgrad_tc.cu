@@ -207,7 +207,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------- TMA producer
-    if (lane == 0) {
+    // Every lane keeps the block position; lane 0 waits for a free stage and
+    // arms its full barrier, then lane j issues box j (dY atoms first, then X):
+    // one warp-wide instruction instead of MA + NA copies in turn from one
+    // thread, each of which costs the issuing thread a few hundred cycles.
+    {
       int s = 0;
       uint32_t ph = 0;
       const int64_t per_img = wp.hblocks * wp.wblocks;
@@ -216,15 +220,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t wb = b0 % wp.wblocks;
       int64_t it = 0;
       for (; it < nblk; ++it) {
-        if (it >= stages && !mbar_wait(&empty[s], ph ^ 1u, abort_flag, err)) break;
+        bool ok = true;
+        if (lane == 0) {
+          if (it >= stages) ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, err);
+          if (ok) mbar_arrive_expect_tx(&full[s], tx);
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         uint8_t* st = smem + (size_t)s * stage_bytes;
         const int32_t ho0 = (int32_t)(hb * wp.TR), wo0 = (int32_t)(wb * wp.BW);
-        mbar_arrive_expect_tx(&full[s], tx);
-        for (int j = 0; j < MA; ++j)  // dY: the block's pixels x output channels k0 + 64 j ..
-          tma_load_4d(st + j * AS, &tm_dy, k0 + 64 * j, wo0, ho0, (int32_t)n, &full[s]);
-        for (int j = 0; j < NA; ++j)  // X through tap (rr, ss): the same pixels' inputs, channels xc0 + 64 j ..
-          tma_load_4d(st + (MA + j) * AS, &tm_x, xc0 + 64 * j, wo0 * wp.sw + ss * wp.dw - wp.pw,
+        if (lane < MA)  // dY: the block's pixels x output channels k0 + 64 lane ..
+          tma_load_4d(st + lane * AS, &tm_dy, k0 + 64 * lane, wo0, ho0, (int32_t)n, &full[s]);
+        else if (lane < MA + NA)  // X through tap (rr, ss): the same pixels' inputs, channels xc0 + 64 (lane - MA) ..
+          tma_load_4d(st + lane * AS, &tm_x, xc0 + 64 * (lane - MA), wo0 * wp.sw + ss * wp.dw - wp.pw,
                       ho0 * wp.sh + rr * wp.dh - wp.ph, (int32_t)n, &full[s]);
+        __syncwarp();
         if (++wb == wp.wblocks) {
           wb = 0;
           if (++hb == wp.hblocks) {
@@ -238,8 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // No copy may still be in flight when the CTA exits.
-      for (int64_t q = it > stages ? it - stages : 0; q < it; ++q)
-        mbar_wait(&full[q % stages], (uint32_t)(q / stages) & 1u, nullptr, err);
+      if (lane == 0)
+        for (int64_t q = it > stages ? it - stages : 0; q < it; ++q)
+          mbar_wait(&full[q % stages], (uint32_t)(q / stages) & 1u, nullptr, err);
+      __syncwarp();
     }
   } else if (warp == 1) {
     // ---------------------------------------------------- MMA issuer
