@@ -20,8 +20,8 @@
 // slot has one full mbarrier, on which the step's dY rows and the input rows
 // it is the first to read all land, and one empty mbarrier, on which every
 // warp arrives when done with the step. The loads of step S + ahead are
-// issued at step S by lane 0 of warp S mod 8, so the issuing work rotates
-// over the warps; every wait is bounded. The rings hold `slack` steps more
+// issued at step S by warp S mod 8, one lane a box, so the issuing work
+// rotates over the warps; every wait is bounded. The rings hold `slack` steps more
 // than the loads in flight need, so an issue at step S only reuses slots that
 // steps before S - slack used: the warps may drift apart by that many steps
 // before an issuing warp waits for the slowest one.
@@ -153,6 +153,40 @@ __device__ bool issue_step(const Ring& g, const RingParams& p, RowPos a, StepPos
   return true;
 }
 
+// issue_step by a whole warp: lane 0 waits for the slot and arms its full
+// barrier, then lane b issues box b of the step (its rows in order, each dY
+// row followed by the input rows it is the first to read), so the issuing
+// warp pays for one copy instruction rather than one per box. Every lane
+// must call it, with the same arguments. False: the wait gave up.
+template <int F>
+__device__ bool issue_step_warp(const Ring& g, const RingParams& p, RowPos a, StepPos st, int32_t rows) {
+  const int lane = threadIdx.x & 31;
+  uint32_t bytes = 0;
+  {
+    RowPos b = a;
+    for (int32_t j = 0; j < rows; ++j, b.advance(F, p)) bytes += g.txD + (uint32_t)b.fresh(F) * g.rowX;
+  }
+  uint64_t* bar = &g.full[st.ss];
+  bool ok = true;
+  if (lane == 0) {
+    if (st.sw > 0) ok = mbar_wait(&g.empty[st.ss], (st.sw - 1u) & 1u, g.abort_flag, g.err);
+    if (ok) mbar_arrive_expect_tx(bar, bytes);
+  }
+  if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+  int box = 0;
+  for (int32_t j = 0; j < rows; ++j, a.advance(F, p)) {
+    if ((box++ & 31) == lane)
+      tma_load_4d(g.dring + ((size_t)st.ss * p.TR + j) * g.rowD + (size_t)(F - 1) * 128, g.tm_dy, g.c0, 0, a.ho, a.n,
+                  bar);
+    for (int r = F - a.fresh(F); r < F; ++r)
+      if ((box++ & 31) == lane)
+        tma_load_4d(g.xring + (size_t)a.slot(r, p) * g.rowX, g.tm_x, g.c0, 0, a.ho - p.ph + r, a.n, bar);
+  }
+  if (lane == 0) g.siss[st.ss] = (int32_t)st.sw;
+  __syncwarp();
+  return true;
+}
+
 // One column sweep of a warp over NROWS output rows of one image (NROWS = 2:
 // rows ho and ho + 1, which share all but one of their input rows): dY row j
 // at dy0[j] (column c at dy0[j] + c * 128), input row i of the first row at
@@ -236,11 +270,8 @@ __device__ __forceinline__ void run_warp(const Ring& g, const RingParams& p, int
 
   for (int64_t q = q_b; q < q_e; q += p.TR) {
     const int32_t rows = q_e - q < p.TR ? (int32_t)(q_e - q) : p.TR;
-    if (warp == issuer && lane == 0 && qa < q_e)
-      issue_step<F>(g, p, la, sl, q_e - qa < p.TR ? (int32_t)(q_e - qa) : p.TR);
-    // Lanes that spin on an mbarrier can hold up a divergent lane of the same
-    // warp; reconverge before any of them waits.
-    __syncwarp();
+    if (warp == issuer && qa < q_e)
+      issue_step_warp<F>(g, p, la, sl, q_e - qa < p.TR ? (int32_t)(q_e - qa) : p.TR);
     for (int32_t j = 0; j < p.TR && qa < q_e; ++j, ++qa) la.advance(F, p);
     sl.advance(p);
     issuer = (issuer + 1) & (kWarps - 1);
