@@ -16,8 +16,8 @@
 // columns}, zero fill outside the image and past C; see dw_ring.cuh). A step
 // slot has one full mbarrier, on which the input rows the step is the first
 // to read all land, and one empty mbarrier, on which every warp arrives when
-// done with the step; the loads of step S + 1 are issued at step S by lane 0
-// of warp S mod 8, and every wait is bounded.
+// done with the step; the loads of step S + 1 are issued at step S by warp
+// S mod 8, one lane a box, and every wait is bounded.
 //
 // A lane holds all F*F taps of its two adjacent channels as packed fp32 pairs
 // and walks its row's input columns u left to right: column u meets output
@@ -138,6 +138,35 @@ __device__ bool issue_step(const FwdRing& g, const FwdRingParams& p, RowPos a, S
   return true;
 }
 
+// issue_step by a whole warp: lane 0 waits for the slot and arms its full
+// barrier, then lane b issues box b (the rows' new input rows in order), so
+// the issuing warp pays for one copy instruction rather than one per row.
+// Every lane must call it, with the same arguments. False: the wait gave up.
+template <int F>
+__device__ bool issue_step_warp(const FwdRing& g, const FwdRingParams& p, RowPos a, StepPos st, int32_t rows) {
+  const int lane = threadIdx.x & 31;
+  uint32_t nrows = 0;
+  {
+    RowPos b = a;
+    for (int32_t j = 0; j < rows; ++j, b.advance(F, p)) nrows += (uint32_t)b.fresh(F);
+  }
+  uint64_t* bar = &g.full[st.ss];
+  bool ok = true;
+  if (lane == 0) {
+    if (st.sw > 0) ok = mbar_wait(&g.empty[st.ss], (st.sw - 1u) & 1u, g.abort_flag, g.err);
+    if (ok) mbar_arrive_expect_tx(bar, nrows * g.rowX);
+  }
+  if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+  int box = 0;
+  for (int32_t j = 0; j < rows; ++j, a.advance(F, p))
+    for (int r = F - a.fresh(F); r < F; ++r)
+      if ((box++ & 31) == lane)
+        tma_load_4d(g.xring + (size_t)a.slot(r, p) * g.rowX, g.tm_x, g.c0, 0, a.ho - p.ph + r, a.n, bar);
+  if (lane == 0) g.siss[st.ss] = (int32_t)st.sw;
+  __syncwarp();
+  return true;
+}
+
 // One output row: input row r at xs[r] (column u at xs[r] + u * 128), outputs
 // to yrow[wo * C]. Column u adds tap (r, s) into output u + pw - s; output
 // slot (wo - pw + F - 1) mod F, so at column u0 + t (u0 a multiple of F)
@@ -250,14 +279,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   for (int64_t q = q_b; q < q_e; q += kTR) {
     const int64_t qa = q + kTR;  // first row of step S + 1
-    if (warp == issuer && lane == 0 && qa < q_e) {
+    if (warp == issuer && qa < q_e) {
       StepPos sl = sc;
       sl.advance(p);
-      issue_step<F>(g, p, la, sl, q_e - qa < kTR ? (int32_t)(q_e - qa) : kTR);
+      issue_step_warp<F>(g, p, la, sl, q_e - qa < kTR ? (int32_t)(q_e - qa) : kTR);
     }
-    // Lanes that spin on an mbarrier can hold up a divergent lane of the same
-    // warp; reconverge before any of them waits.
-    __syncwarp();
     for (int i = 0; i < kTR; ++i) la.advance(F, p);
     issuer = (issuer + 1) & (kWarps - 1);
 
